@@ -1,0 +1,198 @@
+"""Thin ctypes binding of libhymba.so (include/hymba.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.  There is no
+fallback: if the shared library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int32, c_size_t, c_uint32, c_void_p
+from typing import Dict, Optional
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libhymba.so")
+
+HYMBA_OK = 0
+HYMBA_ERR_INVALID = 1
+HYMBA_ERR_UNSUPPORTED = 2
+HYMBA_ERR_WORKSPACE = 3
+HYMBA_ERR_CUDA = 4
+HYMBA_ERR_TIMEOUT = 5
+HYMBA_ERR_RANGE = 6
+
+HYMBA_F32 = 0
+HYMBA_BF16 = 1
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [
+        ("batch", c_int32), ("n_tokens", c_int32), ("n_meta", c_int32), ("d_model", c_int32),
+        ("n_q_heads", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32), ("v_head_dim", c_int32),
+        ("d_inner", c_int32), ("d_state", c_int32), ("d_conv", c_int32), ("dt_rank", c_int32),
+        ("window", c_int32), ("kv_shared", c_int32), ("residual", c_int32), ("dtype", c_int32),
+        ("rope_theta", c_float), ("eps", c_float), ("wait_limit_us", c_uint32), ("reserved", c_int32 * 3),
+    ]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("W_in", "W_out", "W_x", "W_dt", "dt_bias", "A_log", "D", "conv_w",
+                                        "conv_b", "beta1", "beta2")]
+
+
+class KV(ctypes.Structure):
+    _fields_ = [("k", c_void_p), ("v", c_void_p)]
+
+
+class Cache(ctypes.Structure):
+    _fields_ = [("k_ring", c_void_p), ("v_ring", c_void_p), ("k_meta", c_void_p), ("v_meta", c_void_p),
+                ("ssm_state", c_void_p), ("conv_state", c_void_p), ("pos", c_void_p), ("cap", c_int32),
+                ("reserved", c_int32)]
+
+
+WEIGHT_NAMES = [f[0] for f in LayerWeights._fields_]
+CACHE_NAMES = ["k_ring", "v_ring", "k_meta", "v_meta", "ssm_state", "conv_state", "pos"]
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libhymba.so once; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m hybrid_attention_ssm_fwd_b300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    P = POINTER
+    L.hymba_abi_version.restype = c_int32
+    L.hymba_status_str.argtypes = [c_int32]
+    L.hymba_status_str.restype = c_char_p
+    L.hymba_layer_fwd_workspace.argtypes = [P(LayerDesc)]
+    L.hymba_layer_fwd_workspace.restype = c_size_t
+    L.hymba_layer_decode_workspace.argtypes = [P(LayerDesc)]
+    L.hymba_layer_decode_workspace.restype = c_size_t
+    L.hymba_layer_fwd.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache), P(KV), P(KV),
+                                  c_void_p, c_size_t, c_void_p, c_void_p]
+    L.hymba_layer_fwd.restype = c_int32
+    L.hymba_layer_decode.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache), P(Cache),
+                                     c_void_p, c_size_t, c_void_p, c_void_p]
+    L.hymba_layer_decode.restype = c_int32
+    L.hymba_test_gemm.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
+                                  c_void_p, c_int32, c_void_p, c_void_p]
+    L.hymba_test_gemm.restype = c_int32
+    L.hymba_test_scan.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    L.hymba_test_scan.restype = c_int32
+    L.hymba_test_attention.argtypes = [c_int32] * 9 + [c_void_p] * 6
+    L.hymba_test_attention.restype = c_int32
+    L.hymba_test_wait_timeout.argtypes = [c_uint32, c_void_p, c_void_p]
+    L.hymba_test_wait_timeout.restype = c_int32
+    _lib = L
+    return L
+
+
+class HymbaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_str(code)} ({code})")
+        self.code = code
+
+
+def status_str(code: int) -> str:
+    return lib().hymba_status_str(code).decode()
+
+
+def _check(code: int, where: str) -> int:
+    if code != HYMBA_OK:
+        raise HymbaError(code, where)
+    return code
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def make_desc(shape, wait_limit_us: int = 0, residual_mode: Optional[int] = None) -> LayerDesc:
+    """LayerDesc from a synth.LayerShape-like object.  residual_mode overrides
+    the shape's flag: 1 adds the layer input, 2 accumulates into y in place."""
+    return LayerDesc(batch=shape.B, n_tokens=shape.T, n_meta=shape.M, d_model=shape.d, n_q_heads=shape.Hq,
+                     n_kv_heads=shape.Hkv, head_dim=shape.dh, v_head_dim=shape.dv, d_inner=shape.di,
+                     d_state=shape.N, d_conv=shape.k, dt_rank=shape.R, window=shape.window,
+                     kv_shared=int(shape.kv_shared),
+                     residual=int(shape.residual) if residual_mode is None else residual_mode,
+                     dtype=HYMBA_BF16 if shape.dtype == "bf16" else HYMBA_F32, rope_theta=shape.rope_theta,
+                     eps=shape.eps, wait_limit_us=wait_limit_us)
+
+
+def make_weights(w: Dict[str, "object"]) -> LayerWeights:
+    return LayerWeights(**{n: _ptr(w[n]) for n in WEIGHT_NAMES})
+
+
+def make_cache(c: Optional[Dict[str, "object"]], cap: int) -> Optional[Cache]:
+    if c is None:
+        return None
+    return Cache(**{n: _ptr(c.get(n)) for n in CACHE_NAMES}, cap=cap, reserved=0)
+
+
+def layer_fwd_workspace(desc: LayerDesc) -> int:
+    return lib().hymba_layer_fwd_workspace(ctypes.byref(desc))
+
+
+def layer_decode_workspace(desc: LayerDesc) -> int:
+    return lib().hymba_layer_decode_workspace(ctypes.byref(desc))
+
+
+def hymba_layer_fwd(desc: LayerDesc, weights: LayerWeights, x, y, ws, cache_out: Optional[Cache] = None,
+                    kv_in: Optional[KV] = None, kv_out: Optional[KV] = None, status=None, stream=None,
+                    check: bool = True) -> int:
+    """Prefill forward through the C ABI (see include/hymba.h)."""
+    rc = lib().hymba_layer_fwd(ctypes.byref(desc), ctypes.byref(weights), _ptr(x), _ptr(y),
+                               ctypes.byref(cache_out) if cache_out is not None else None,
+                               ctypes.byref(kv_in) if kv_in is not None else None,
+                               ctypes.byref(kv_out) if kv_out is not None else None,
+                               _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+    return _check(rc, "hymba_layer_fwd") if check else rc
+
+
+def hymba_layer_decode(desc: LayerDesc, weights: LayerWeights, x_new, y, cache: Cache, ws,
+                       shared_cache: Optional[Cache] = None, status=None, stream=None, check: bool = True) -> int:
+    """One decode step through the C ABI (see include/hymba.h)."""
+    rc = lib().hymba_layer_decode(ctypes.byref(desc), ctypes.byref(weights), _ptr(x_new), _ptr(y),
+                                  ctypes.byref(cache),
+                                  ctypes.byref(shared_cache) if shared_cache is not None else None,
+                                  _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+    return _check(rc, "hymba_layer_decode") if check else rc
+
+
+def hymba_test_gemm(A, B, C, ab_dtype: int, status=None, stream=None) -> int:
+    M, K = A.shape
+    N = B.shape[0]
+    return lib().hymba_test_gemm(M, N, K, ab_dtype, _ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C),
+                                 C.stride(0), _ptr(status), _stream(stream))
+
+
+def hymba_test_scan(u, z, delta, BC, A_log, D, g, h_out=None, stream=None) -> int:
+    B, L, di = delta.shape
+    N = A_log.shape[1]
+    return lib().hymba_test_scan(B, L, di, N, _ptr(u), u.stride(1), _ptr(z), z.stride(1), _ptr(delta),
+                                 _ptr(BC), _ptr(A_log), _ptr(D), _ptr(g), _ptr(h_out), _stream(stream))
+
+
+def hymba_test_attention(Q, K, V, O, M: int, window: int, use_tc: bool, status=None, stream=None) -> int:
+    B, L, Hq, dh = Q.shape
+    Hkv, dv = K.shape[2], V.shape[3]
+    return lib().hymba_test_attention(B, L, M, Hq, Hkv, dh, dv, window, int(use_tc), _ptr(Q), _ptr(K), _ptr(V),
+                                      _ptr(O), _ptr(status), _stream(stream))
+
+
+def hymba_test_wait_timeout(limit_us: int, status, stream=None) -> int:
+    return lib().hymba_test_wait_timeout(limit_us, _ptr(status), _stream(stream))

@@ -1,0 +1,40 @@
+// Kernels specific to the single-token decode step.
+#pragma once
+
+#include "common.cuh"
+
+namespace hy {
+
+// K/V of the new token (columns k_col / v_col of proj [B, ldp]) into slot
+// pos[b] % cap (window > 0) or pos[b] (global) of the ring.
+template <typename TS, typename TC>
+hymba_status kv_append(int B, int Hkv, int dh, int dv, int window, int cap, const TS* proj, long long ldp,
+                       int k_col, int v_col, const int32_t* pos, TC* k_ring, TC* v_ring, cudaStream_t st);
+
+// Attention of one new token per sequence over the meta K/V plus the last
+// min(pos+1, window) ring entries (pos+1 when global).  q: proj rows (head h
+// at h*dh), out [B, ldo] (head h at h*dv).
+template <typename TQ, typename TC>
+hymba_status decode_attention(int B, int M, int Hq, int Hkv, int dh, int dv, int window, int cap,
+                              const TQ* q, long long ldq, const TC* k_meta, const TC* v_meta,
+                              const TC* k_ring, const TC* v_ring, const int32_t* pos, TQ* out, long long ldo,
+                              cudaStream_t st);
+
+// One conv step from the carried tail: u = silu(sum w * [tail, x] + b); the
+// tail is shifted in place to end with x.
+template <typename T>
+hymba_status conv_step(int B, int di, int k, const T* x, long long ldx, const float* w, const float* bias,
+                       float* conv_state, T* u, long long ldu, cudaStream_t st);
+
+enum ReduceEpi : int { RE_XPROJ = 0, RE_F32 = 1 };
+
+// Sums split-K partials part[s][rows][ldp] and applies the epilogue:
+//   RE_XPROJ: col < R -> dtr (fp16, ld ldd), else BC[row, col-R] (fp32, ld ldc)
+//   RE_F32:   C[row, col] = sum (+ bf16 residual) (+ C itself if accumulate)
+hymba_status splitk_reduce(int splits, int rows, int N, const float* part, long long ldp, int epi, int R,
+                           __half* dtr, long long ldd, float* C, long long ldc, const __nv_bfloat16* resid,
+                           long long ld_resid, bool accumulate, cudaStream_t st);
+
+hymba_status pos_increment(int B, int32_t* pos, cudaStream_t st);
+
+}  // namespace hy

@@ -1,0 +1,409 @@
+// Persistent warp-specialised tcgen05 GEMM for sm_103a.
+//
+//   warp 0      TMA producer: 128x64 A tile + BNx64 B tile per stage (128-byte
+//               swizzle), completion counted on the stage's "full" mbarrier.
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (M=128, N=BN,
+//               K=16, fp32 accumulate) into one of two TMEM accumulators and
+//               commits stage releases / accumulator-ready arrivals.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows they own (TMEM
+//               lanes 32*(warp%4) ..), fused epilogue, direct global stores;
+//               then release the accumulator so the next tile's MMAs, which
+//               overlap this epilogue, can reuse it.
+//
+// Tiles are visited in row-major tile order (N fastest) by a static
+// round-robin over CTAs, so the CTAs resident at one time share a few A
+// row-blocks and the weight matrix stays in L2.  Every wait is bounded.
+#include "gemm_tc.cuh"
+
+namespace hy {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int A_BYTES = BM * BK * 2;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int BUDGET = 220 * 1024 - 2048;
+  static constexpr int S0 = BUDGET / STAGE;
+  static constexpr int STAGES = S0 > 8 ? 8 : S0;
+  static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                        : (2 * BN <= 256) ? 256 : 512;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + 512;
+};
+
+struct TileCoord {
+  int m, n, kb0, kb1, split;
+};
+
+HY_DEV TileCoord tile_coord(const GemmParams& p, int t) {
+  TileCoord c;
+  const int mn = p.tiles_m * p.tiles_n;
+  c.split = t / mn;
+  const int r = t - c.split * mn;
+  c.m = r / p.tiles_n;
+  c.n = r - c.m * p.tiles_n;
+  c.kb0 = c.split * p.kb_per_split;
+  c.kb1 = min(p.n_kb, c.kb0 + p.kb_per_split);
+  return c;
+}
+
+// ---- epilogue helpers --------------------------------------------------------
+
+HY_DEV void store_f16x32(__half* dst, const float (&v)[32], int valid) {
+  // valid = number of leading columns inside N (multiple of 8 or >= 32)
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (g * 8 < valid) {
+      uint4 q;
+      q.x = pack_half2(v[g * 8 + 0], v[g * 8 + 1]);
+      q.y = pack_half2(v[g * 8 + 2], v[g * 8 + 3]);
+      q.z = pack_half2(v[g * 8 + 4], v[g * 8 + 5]);
+      q.w = pack_half2(v[g * 8 + 6], v[g * 8 + 7]);
+      *reinterpret_cast<uint4*>(dst + g * 8) = q;
+    }
+  }
+}
+
+HY_DEV void store_f32xn(float* dst, const float* v, int n, int valid) {
+  if (valid >= n && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+    for (int g = 0; g < n; g += 4)
+      *reinterpret_cast<float4*>(dst + g) = make_float4(v[g], v[g + 1], v[g + 2], v[g + 3]);
+  } else {
+    for (int j = 0; j < n; ++j)
+      if (j < valid) dst[j] = v[j];
+  }
+}
+
+HY_DEV bool any_over_half(const float* v, int n) {
+  bool o = false;
+  for (int j = 0; j < n; ++j) o |= !(fabsf(v[j]) <= kHalfMax);
+  return o;
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p, const uint32_t idesc) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int S = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE);
+  // bars: full[S], empty[S], tfull[2], tempty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* rope_tab = reinterpret_cast<float*>(tmem_slot + 4);  // 32 floats
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[S + s]); };
+  auto tfull = [&](int a) { return smem_u32(&bars[2 * S + a]); };
+  auto tempty = [&](int a) { return smem_u32(&bars[2 * S + 2 + a]); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (EPI == EPI_F16 && threadIdx.x < 32) rope_tab[threadIdx.x] = exp2f(threadIdx.x * p.rope_log2_step);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitCtl wc{abort_flag, p.status, p.wait_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      uint32_t it = 0, issued = 0;
+      uint32_t last_par = 0;  // bit s: parity of the last load issued into stage s
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        const TileCoord c = tile_coord(p, t);
+        for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!mbar_wait(empty(s), ph ^ 1, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(full(s), Cfg::STAGE);
+          tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full(s), kb * BK, c.m * BM);
+          tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full(s), kb * BK, c.n * BN);
+          issued |= 1u << s;
+          last_par = (last_par & ~(1u << s)) | (ph << s);
+        }
+      }
+      if (!ok) {  // let the copies already in flight land before the CTA exits
+        for (int s = 0; s < S; ++s)
+          if (issued & (1u << s)) mbar_wait_drain(full(s), (last_par >> s) & 1, 1000000);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, committed = 0, last_par = 0, tcommitted = 0, tlast = 0;
+      bool ok = true;
+      int local = 0;
+      for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++local) {
+        const TileCoord c = tile_coord(p, t);
+        const int a = local & 1;
+        const uint32_t u = (local >> 1) & 1;
+        if (!mbar_wait(tempty(a), u ^ 1, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + a * BN;
+        for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!mbar_wait(full(s), ph, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = sdesc_sw128(smem_u32(sA + s * A_BYTES), 16, 1024);
+          const uint64_t db = sdesc_sw128(smem_u32(sB + s * Cfg::B_BYTES), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
+          tc_commit(empty(s));
+          committed |= 1u << s;
+          last_par = (last_par & ~(1u << s)) | (ph << s);
+        }
+        if (!ok) break;
+        tc_commit(tfull(a));
+        tcommitted |= 1u << a;
+        tlast = (tlast & ~(1u << a)) | (u << a);
+      }
+      if (!ok) {  // wait for issued MMAs before TMEM is released
+        for (int s = 0; s < S; ++s)
+          if (committed & (1u << s)) mbar_wait_drain(empty(s), (last_par >> s) & 1, 1000000);
+        for (int a = 0; a < 2; ++a)
+          if (tcommitted & (1u << a)) mbar_wait_drain(tfull(a), (tlast >> a) & 1, 1000000);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int local = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
+      const TileCoord c = tile_coord(p, t);
+      const int a = local & 1;
+      const uint32_t u = (local >> 1) & 1;
+      const bool got = mbar_wait(tfull(a), u, wc);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int row = c.m * BM + row_in_tile;
+      const bool row_ok = row < p.M;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + a * BN;
+      const int col_tile = c.n * BN;
+      bool over = false;
+
+      if (EPI == EPI_F16 && p.rope_cols > 0 && col_tile < p.rope_cols) {
+        // RoPE: 64-column heads, pair (i, i+32) rotated by pos * inv_freq[i]
+        const int posn = p.pos ? (p.pos_base + p.pos[min(row, p.M - 1)]) : (row % p.rows_per_seq);
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          const int col = col_tile + c0;
+          if (col >= p.N) break;
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tbase + c0, r0);
+          tmem_ld32(tbase + c0 + 32, r1);
+          tc_wait_ld();
+          float v0[32], v1[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v0[j] = __uint_as_float(r0[j]);
+            v1[j] = __uint_as_float(r1[j]);
+          }
+          if (col < p.rope_cols) {
+#pragma unroll 4
+            for (int j = 0; j < 32; ++j) {
+              float sn, cs;
+              sincosf(static_cast<float>(posn) * rope_tab[j], &sn, &cs);
+              const float x1 = v0[j], x2 = v1[j];
+              v0[j] = x1 * cs - x2 * sn;
+              v1[j] = x2 * cs + x1 * sn;
+            }
+          }
+          over |= any_over_half(v0, 32) | any_over_half(v1, 32);
+          if (row_ok) {
+            __half* dst = reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col;
+            store_f16x32(dst, v0, p.N - col);
+            if (col + 32 < p.N) store_f16x32(dst + 32, v1, p.N - col - 32);
+          }
+        }
+      } else {
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          const int col = col_tile + c0;
+          if (col >= p.N) break;
+          const int nv = (c0 + 32 <= BN) ? 32 : 16;
+          float v[32];
+          if (nv == 32) {
+            uint32_t r[32];
+            tmem_ld32(tbase + c0, r);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          } else {
+            uint32_t r[16];
+            tmem_ld16(tbase + c0, r);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+#pragma unroll
+            for (int j = 16; j < 32; ++j) v[j] = 0.f;
+          }
+          const int valid = min(nv, p.N - col);
+          if (!row_ok) continue;
+          if (EPI == EPI_F16) {
+            over |= any_over_half(v, nv);
+            store_f16x32(reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col, v,
+                         valid);
+          } else if (EPI == EPI_XPROJ) {
+            for (int j = 0; j < valid; ++j) {
+              const int cj = col + j;
+              if (cj < p.xproj_R) {
+                over |= !(fabsf(v[j]) <= kHalfMax);
+                reinterpret_cast<__half*>(p.C2)[static_cast<long long>(row) * p.ldc2 + cj] = __float2half_rn(v[j]);
+              } else {
+                reinterpret_cast<float*>(p.C)[static_cast<long long>(row) * p.ldc + (cj - p.xproj_R)] = v[j];
+              }
+            }
+          } else if (EPI == EPI_SOFTPLUS) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < valid) v[j] = softplus_f(v[j] + p.bias[col + j]);
+            store_f32xn(reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col, v, nv,
+                        valid);
+          } else if (EPI == EPI_F32) {
+            if (p.resid) {
+              const __nv_bfloat16* rr = p.resid + static_cast<long long>(row) * p.ld_resid + col;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < valid) v[j] += __bfloat162float(rr[j]);
+            } else if (p.resid_f32) {
+              const float* rr = p.resid_f32 + static_cast<long long>(row) * p.ld_resid + col;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < valid) v[j] += rr[j];
+            }
+            store_f32xn(reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col, v, nv,
+                        valid);
+          } else {  // EPI_PARTIAL
+            float* dst = reinterpret_cast<float*>(p.C) +
+                         (static_cast<long long>(c.split) * p.M + row) * p.ldc + col;
+            store_f32xn(dst, v, nv, valid);
+          }
+        }
+      }
+      if (over) set_status(p.status, HYMBA_ERR_RANGE);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(a));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+template <int BN, int EPI>
+hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                       uint32_t idesc, int grid, cudaStream_t st) {
+  using Cfg = GemmCfg<BN>;
+  auto kern = gemm_tc_kernel<BN, EPI>;
+  static bool attr_done = false;  // benign race: idempotent attribute set
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
+      return HYMBA_ERR_CUDA;
+    attr_done = true;
+  }
+  kern<<<grid, 192, Cfg::SMEM, st>>>(ta, tb, p, idesc);
+  return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
+}
+
+template <int EPI>
+hymba_status launch_epi(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                        uint32_t ab_fmt, int grid, cudaStream_t st) {
+  const uint32_t id = idesc_f16(BM, bn, ab_fmt, false, false);
+  switch (bn) {
+    case 64: return launch_bn<64, EPI>(ta, tb, p, id, grid, st);
+    case 128: return launch_bn<128, EPI>(ta, tb, p, id, grid, st);
+    case 144: return launch_bn<144, EPI>(ta, tb, p, id, grid, st);
+    case 160: return launch_bn<160, EPI>(ta, tb, p, id, grid, st);
+    case 256: return launch_bn<256, EPI>(ta, tb, p, id, grid, st);
+    default: return HYMBA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+int gemm_pick_bn(int N, bool small_m) {
+  if (small_m) return 64;
+  static const int cand[] = {256, 160, 144, 128, 64};
+  int best = 256;
+  long long best_pad = 1LL << 60;
+  for (int bn : cand) {
+    const long long pad = static_cast<long long>((N + bn - 1) / bn) * bn;
+    if (pad < best_pad) {
+      best_pad = pad;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, long long ldb, int epi,
+                     GemmParams p, int bn, int splits, int num_sms, cudaStream_t st) {
+  if (p.M <= 0 || p.N <= 0 || p.K <= 0) return HYMBA_OK;
+  if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) || (lda % 8) ||
+      (ldb % 8) || lda < p.K || ldb < p.K)
+    return HYMBA_ERR_INVALID;
+  if (bn == 0) bn = gemm_pick_bn(p.N, p.M <= BM);
+  const CUtensorMapDataType dt = ab_fmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap ta, tb;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
+    const uint64_t str[1] = {static_cast<uint64_t>(lda) * 2};
+    const uint32_t box[2] = {BK, BM};
+    if (!encode_tmap(&ta, dt, 2, A, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
+    const uint64_t str[1] = {static_cast<uint64_t>(ldb) * 2};
+    const uint32_t box[2] = {BK, static_cast<uint32_t>(bn)};
+    if (!encode_tmap(&tb, dt, 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
+  }
+  p.tiles_m = (p.M + BM - 1) / BM;
+  p.tiles_n = (p.N + bn - 1) / bn;
+  p.n_kb = (p.K + BK - 1) / BK;
+  splits = std::max(1, std::min(splits, p.n_kb));
+  p.kb_per_split = (p.n_kb + splits - 1) / splits;
+  p.splits = (p.n_kb + p.kb_per_split - 1) / p.kb_per_split;
+  p.total_tiles = p.tiles_m * p.tiles_n * p.splits;
+  if (p.splits > 1 && epi != EPI_PARTIAL) return HYMBA_ERR_INVALID;
+  const int grid = std::min(p.total_tiles, std::max(1, num_sms));
+  const uint32_t fmt = ab_fmt == 1 ? 1u : 0u;
+  switch (epi) {
+    case EPI_F16: return launch_epi<EPI_F16>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_XPROJ: return launch_epi<EPI_XPROJ>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_F32: return launch_epi<EPI_F32>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_PARTIAL: return launch_epi<EPI_PARTIAL>(bn, ta, tb, p, fmt, grid, st);
+    default: return HYMBA_ERR_INVALID;
+  }
+}
+
+}  // namespace hy

@@ -1,0 +1,587 @@
+// C ABI of the hybrid-head layer: argument validation, workspace planning and
+// the launch sequence of prefill and decode on one stream.
+//
+// Prefill (paper "Hymba: A Hybrid-head Architecture for Small Language
+// Models", section 2.1 eq. 3), bf16 path:
+//   in_proj (tcgen05 GEMM, RoPE fused) -> proj [rows, P_in] fp16
+//   attention branch: flash attention over meta + window -> att fp16
+//   SSM branch: conv+SiLU -> u; x_proj (tcgen05) -> dt fp16, B/C fp32;
+//               dt_proj (tcgen05, softplus fused) -> delta fp32;
+//               selective scan + gate -> g fp16 (final state -> cache)
+//   fuse: s = beta1 rms(att) + beta2 rms(g)  -> fp16
+//   out_proj (tcgen05, residual fused) -> Y fp32
+#include <algorithm>
+#include <cstring>
+
+#include "attn_tc.cuh"
+#include "common.cuh"
+#include "decode.cuh"
+#include "gemm_tc.cuh"
+#include "scan.cuh"
+#include "simt.cuh"
+
+using namespace hy;
+
+namespace {
+
+struct Dims {
+  int B, T, M, L, d, Hq, Hkv, dh, dv, di, N, k, R, W, kv_shared, residual, dtype;
+  float theta, eps;
+  uint64_t wait_ns;
+  long long rows;
+  int P_in, k_col, v_col, x_col, z_col, Rp, xo;  // xo = R + 2N
+};
+
+bool is_flag(int v) { return v == 0 || v == 1; }
+
+hymba_status check_desc(const hymba_layer_desc* d, bool decode, Dims* o) {
+  if (!d) return HYMBA_ERR_INVALID;
+  for (int r : d->reserved)
+    if (r != 0) return HYMBA_ERR_INVALID;
+  if (d->batch < 1 || d->n_tokens < 1 || d->n_meta < 0 || d->d_model < 1 || d->n_q_heads < 1 ||
+      d->n_kv_heads < 1 || d->head_dim < 2 || (d->head_dim & 1) || d->v_head_dim < 1 || d->d_inner < 1 ||
+      d->d_state < 1 || d->d_state > 64 || d->d_conv < 1 || d->d_conv > 8 || d->dt_rank < 1 || d->window < 0 ||
+      !is_flag(d->kv_shared) || d->residual < 0 || d->residual > 2 || !(d->eps >= 0.f) || !(d->rope_theta >= 0.f))
+    return HYMBA_ERR_INVALID;
+  if (d->dtype != HYMBA_F32 && d->dtype != HYMBA_BF16) return HYMBA_ERR_INVALID;
+  if (d->n_q_heads % d->n_kv_heads != 0) return HYMBA_ERR_INVALID;
+  if (static_cast<long long>(d->n_q_heads) * d->v_head_dim != d->d_inner) return HYMBA_ERR_INVALID;
+  if (decode && d->n_tokens != 1) return HYMBA_ERR_INVALID;
+  if (d->v_head_dim > 256) return HYMBA_ERR_UNSUPPORTED;
+  Dims& x = *o;
+  x.B = d->batch;
+  x.T = d->n_tokens;
+  x.M = d->n_meta;
+  x.L = decode ? 1 : d->n_meta + d->n_tokens;
+  x.d = d->d_model;
+  x.Hq = d->n_q_heads;
+  x.Hkv = d->n_kv_heads;
+  x.dh = d->head_dim;
+  x.dv = d->v_head_dim;
+  x.di = d->d_inner;
+  x.N = d->d_state;
+  x.k = d->d_conv;
+  x.R = d->dt_rank;
+  x.W = d->window;
+  x.kv_shared = d->kv_shared;
+  x.residual = d->residual;
+  x.dtype = d->dtype;
+  x.theta = d->rope_theta;
+  x.eps = d->eps;
+  x.wait_ns = static_cast<uint64_t>(d->wait_limit_us ? d->wait_limit_us : 2000000u) * 1000ull;
+  x.rows = static_cast<long long>(x.B) * x.L;
+  const long long kvw = x.kv_shared ? 0 : static_cast<long long>(x.Hkv) * (x.dh + x.dv);
+  const long long pin = static_cast<long long>(x.Hq) * x.dh + kvw + 2LL * x.di;
+  if (pin > (1 << 30) || x.rows > (1LL << 31) - 1 || x.rows * pin > (1LL << 40)) return HYMBA_ERR_INVALID;
+  x.P_in = static_cast<int>(pin);
+  x.k_col = x.Hq * x.dh;
+  x.v_col = x.k_col + x.Hkv * x.dh;
+  x.x_col = x.Hq * x.dh + static_cast<int>(kvw);
+  x.z_col = x.x_col + x.di;
+  x.Rp = (x.R + 7) / 8 * 8;
+  x.xo = x.R + 2 * x.N;
+  if (x.dtype == HYMBA_BF16) {
+    // TMA / vector-store alignment of every column block (8 fp16/bf16 = 16 B)
+    if (x.d % 8 || x.di % 8 || x.dh % 8 || (x.Hkv * x.dh) % 8 || (x.Hkv * x.dv) % 8 || (2 * x.N) % 4)
+      return HYMBA_ERR_UNSUPPORTED;
+  }
+  return HYMBA_OK;
+}
+
+// Workspace plan: byte offsets of each scratch buffer (256-byte aligned).
+struct Plan {
+  size_t proj, u, dtr, bc, delta, att, g, s, wout, wx, wdt, part, total;
+};
+
+constexpr int kDecodeSplitsX = 25;
+constexpr int kDecodeSplitsOut = 5;
+
+Plan plan_ws(const Dims& x, bool decode) {
+  Plan p{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t e = x.dtype == HYMBA_BF16 ? 2 : 4;
+  const size_t r = static_cast<size_t>(x.rows);
+  p.proj = take(r * x.P_in * e);
+  p.u = take(r * x.di * e);
+  p.dtr = take(r * (x.dtype == HYMBA_BF16 ? x.Rp : x.R) * e);
+  p.bc = take(r * 2 * x.N * 4);
+  p.delta = take(r * x.di * 4);
+  p.att = take(r * x.di * e);
+  p.g = take(r * x.di * e);
+  p.s = take(r * x.di * e);
+  if (x.dtype == HYMBA_BF16) {
+    p.wout = take(static_cast<size_t>(x.d) * x.di * 2);
+    p.wx = take(static_cast<size_t>(x.xo) * x.di * 2);
+    p.wdt = take(static_cast<size_t>(x.di) * x.Rp * 2);
+    if (decode) {
+      const size_t w1 = static_cast<size_t>(kDecodeSplitsX) * r * ((x.xo + 15) / 16 * 16);
+      const size_t w2 = static_cast<size_t>(kDecodeSplitsOut) * r * x.d;
+      p.part = take(std::max(w1, w2) * 4);
+    }
+  }
+  p.total = off;
+  return p;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+hymba_status check_weights(const hymba_layer_weights* w, const Dims& x) {
+  if (!w || !w->W_in || !w->W_out || !w->W_x || !w->W_dt || !w->dt_bias || !w->A_log || !w->D || !w->conv_w ||
+      !w->conv_b || !w->beta1 || !w->beta2)
+    return HYMBA_ERR_INVALID;
+  const size_t a = x.dtype == HYMBA_BF16 ? 16 : 4;
+  if (!aligned(w->W_in, a) || !aligned(w->W_out, a) || !aligned(w->W_x, a) || !aligned(w->W_dt, 2) ||
+      !aligned(w->dt_bias, 4) || !aligned(w->A_log, 4) || !aligned(w->D, 4) || !aligned(w->conv_w, 4) ||
+      !aligned(w->conv_b, 4) || !aligned(w->beta1, 4) || !aligned(w->beta2, 4))
+    return HYMBA_ERR_INVALID;
+  return HYMBA_OK;
+}
+
+int num_sms() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+#define TRY(...)                           \
+  do {                                     \
+    hymba_status s_ = (__VA_ARGS__);       \
+    if (s_ != HYMBA_OK) return s_;         \
+  } while (0)
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// ---------------------------------------------------------------------------
+// fp32 path (SIMT)
+// ---------------------------------------------------------------------------
+hymba_status fwd_f32(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const float* X, float* Y,
+                     const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
+                     cudaStream_t st) {
+  float* proj = at<float>(ws, pl.proj);
+  float* u = at<float>(ws, pl.u);
+  float* dtr = at<float>(ws, pl.dtr);
+  float* bc = at<float>(ws, pl.bc);
+  float* delta = at<float>(ws, pl.delta);
+  float* att = at<float>(ws, pl.att);
+  float* g = at<float>(ws, pl.g);
+  float* s = at<float>(ws, pl.s);
+  const int rows = static_cast<int>(x.rows);
+  const float* Win = static_cast<const float*>(w->W_in);
+  TRY(gemm_simt<float>(rows, x.P_in, x.d, X, x.d, Win, x.d, SE_STORE, proj, x.P_in, nullptr, 0, 0, nullptr,
+                       nullptr, 0, st));
+  if (x.theta > 0) {
+    TRY(rope_simt<float>(proj, x.P_in, rows, 0, x.Hq, x.dh, x.theta, x.L, nullptr, 0, st));
+    if (!x.kv_shared) TRY(rope_simt<float>(proj, x.P_in, rows, x.k_col, x.Hkv, x.dh, x.theta, x.L, nullptr, 0, st));
+  }
+  const float* Kp = x.kv_shared ? static_cast<const float*>(kv_in->k) : proj + x.k_col;
+  const float* Vp = x.kv_shared ? static_cast<const float*>(kv_in->v) : proj + x.v_col;
+  const long long ldk = x.kv_shared ? static_cast<long long>(x.Hkv) * x.dh : x.P_in;
+  const long long ldv = x.kv_shared ? static_cast<long long>(x.Hkv) * x.dv : x.P_in;
+  if (kv_out) {
+    TRY(copy2d<float, float>(Kp, ldk, static_cast<float*>(kv_out->k), static_cast<long long>(x.Hkv) * x.dh, x.rows,
+                             x.Hkv * x.dh, st));
+    TRY(copy2d<float, float>(Vp, ldv, static_cast<float*>(kv_out->v), static_cast<long long>(x.Hkv) * x.dv, x.rows,
+                             x.Hkv * x.dv, st));
+  }
+  TRY(attention_simt<float>(x.B, x.L, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, proj, x.P_in, Kp, ldk, Vp, ldv, att,
+                            x.di, st));
+  TRY(conv_silu<float, float>(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, st));
+  TRY(gemm_simt<float>(rows, x.xo, x.di, u, x.di, static_cast<const float*>(w->W_x), x.di, SE_XPROJ, bc, 2 * x.N,
+                       dtr, x.R, x.R, nullptr, nullptr, 0, st));
+  TRY(gemm_simt<float>(rows, x.di, x.R, dtr, x.R, static_cast<const float*>(w->W_dt), x.R, SE_SOFTPLUS, delta,
+                       x.di, nullptr, 0, 0, w->dt_bias, nullptr, 0, st));
+  float* h_out = cache_out ? cache_out->ssm_state : nullptr;
+  TRY(scan_simt<float>(x.B, x.L, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, x.di, bc, bc + x.N, 2 * x.N,
+                       w->A_log, w->D, g, x.di, nullptr, h_out, st));
+  TRY(fuse_norm<float>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  TRY(gemm_simt<float>(rows, x.d, x.di, s, x.di, static_cast<const float*>(w->W_out), x.di, SE_RESID, Y, x.d,
+                       nullptr, 0, 0, nullptr, x.residual == 1 ? X : x.residual == 2 ? Y : nullptr, x.d, st));
+  if (cache_out) {
+    TRY(emit_cache<float, float>(x.B, x.L, x.M, x.T, cache_out->cap, x.Hkv, x.dh, x.dv, x.di, x.k,
+                                 x.kv_shared ? nullptr : Kp, ldk, Vp, ldv, proj + x.x_col, x.P_in,
+                                 static_cast<float*>(cache_out->k_ring), static_cast<float*>(cache_out->v_ring),
+                                 static_cast<float*>(cache_out->k_meta), static_cast<float*>(cache_out->v_meta),
+                                 cache_out->conv_state, st));
+  }
+  return HYMBA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 path (tensor cores)
+// ---------------------------------------------------------------------------
+GemmParams gp(int M, int N, int K, int32_t* status, uint64_t wait_ns) {
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.rows_per_seq = 1;
+  p.status = status;
+  p.wait_ns = wait_ns;
+  return p;
+}
+
+hymba_status convert_weights(const Dims& x, const Plan& pl, const hymba_layer_weights* w, void* ws,
+                             cudaStream_t st) {
+  TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_out), x.di, at<__half>(ws, pl.wout),
+                                    x.di, x.d, x.di, st));
+  TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_x), x.di, at<__half>(ws, pl.wx), x.di,
+                                    x.xo, x.di, st));
+  TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_dt), x.R, at<__half>(ws, pl.wdt), x.Rp,
+                                    x.di, x.R, st));
+  return HYMBA_OK;
+}
+
+hymba_status in_proj_bf16(const Dims& x, const void* X, const hymba_layer_weights* w, __half* proj, int rows,
+                          const int32_t* pos, int pos_base, int rows_per_seq, int32_t* status, int sms,
+                          cudaStream_t st) {
+  GemmParams p = gp(rows, x.P_in, x.d, status, x.wait_ns);
+  p.C = proj;
+  p.ldc = x.P_in;
+  const bool fused_rope = x.theta > 0 && x.dh == 64;
+  if (fused_rope) {
+    p.rope_cols = x.Hq * x.dh + (x.kv_shared ? 0 : x.Hkv * x.dh);
+    p.rope_log2_step = -2.0f / x.dh * log2f(x.theta);
+  }
+  p.rows_per_seq = rows_per_seq;
+  p.pos = pos;
+  p.pos_base = pos_base;
+  TRY(gemm_tc(1, X, x.d, w->W_in, x.d, EPI_F16, p, 0, 1, sms, st));
+  if (x.theta > 0 && !fused_rope) {
+    TRY(rope_simt<__half>(proj, x.P_in, rows, 0, x.Hq, x.dh, x.theta, rows_per_seq, pos, pos_base, st));
+    if (!x.kv_shared)
+      TRY(rope_simt<__half>(proj, x.P_in, rows, x.k_col, x.Hkv, x.dh, x.theta, rows_per_seq, pos, pos_base, st));
+  }
+  return HYMBA_OK;
+}
+
+hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const void* X, float* Y,
+                      const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
+                      int32_t* status, cudaStream_t st) {
+  const int sms = num_sms();
+  const int rows = static_cast<int>(x.rows);
+  __half* proj = at<__half>(ws, pl.proj);
+  __half* u = at<__half>(ws, pl.u);
+  __half* dtr = at<__half>(ws, pl.dtr);
+  float* bc = at<float>(ws, pl.bc);
+  float* delta = at<float>(ws, pl.delta);
+  __half* att = at<__half>(ws, pl.att);
+  __half* g = at<__half>(ws, pl.g);
+  __half* s = at<__half>(ws, pl.s);
+  TRY(convert_weights(x, pl, w, ws, st));
+  TRY(in_proj_bf16(x, X, w, proj, rows, nullptr, 0, x.L, status, sms, st));
+
+  const __half* Kp = x.kv_shared ? static_cast<const __half*>(kv_in->k) : proj + x.k_col;
+  const __half* Vp = x.kv_shared ? static_cast<const __half*>(kv_in->v) : proj + x.v_col;
+  const long long ldk = x.kv_shared ? static_cast<long long>(x.Hkv) * x.dh : x.P_in;
+  const long long ldv = x.kv_shared ? static_cast<long long>(x.Hkv) * x.dv : x.P_in;
+  if (kv_out) {
+    TRY(copy2d<__half, __half>(Kp, ldk, static_cast<__half*>(kv_out->k), static_cast<long long>(x.Hkv) * x.dh,
+                               x.rows, x.Hkv * x.dh, st));
+    TRY(copy2d<__half, __half>(Vp, ldv, static_cast<__half*>(kv_out->v), static_cast<long long>(x.Hkv) * x.dv,
+                               x.rows, x.Hkv * x.dv, st));
+  }
+  // attention branch
+  if (attn_tc_supported(x.dh, x.dv)) {
+    TRY(attn_tc(x.B, x.L, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, proj, x.P_in, Kp, ldk, Vp, ldv, att, x.di, status,
+                x.wait_ns, sms, st));
+  } else {
+    TRY(attention_simt<__half>(x.B, x.L, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, proj, x.P_in, Kp, ldk, Vp, ldv, att,
+                               x.di, st));
+  }
+  // SSM branch
+  TRY(conv_silu<__half, __half>(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, st));
+  {
+    GemmParams p = gp(rows, x.xo, x.di, status, x.wait_ns);
+    p.C = bc;
+    p.ldc = 2 * x.N;
+    p.C2 = dtr;
+    p.ldc2 = x.Rp;
+    p.xproj_R = x.R;
+    TRY(gemm_tc(0, u, x.di, at<__half>(ws, pl.wx), x.di, EPI_XPROJ, p, 0, 1, sms, st));
+  }
+  {
+    GemmParams p = gp(rows, x.di, x.R, status, x.wait_ns);
+    p.C = delta;
+    p.ldc = x.di;
+    p.bias = w->dt_bias;
+    TRY(gemm_tc(0, dtr, x.Rp, at<__half>(ws, pl.wdt), x.Rp, EPI_SOFTPLUS, p, 0, 1, sms, st));
+  }
+  float* h_out = cache_out ? cache_out->ssm_state : nullptr;
+  TRY(scan_f16(x.B, x.L, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, bc, w->A_log, w->D, g, nullptr, h_out,
+               st));
+  // fuse + out_proj
+  TRY(fuse_norm<__half>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  {
+    GemmParams p = gp(rows, x.d, x.di, status, x.wait_ns);
+    p.C = Y;
+    p.ldc = x.d;
+    p.resid = x.residual == 1 ? static_cast<const __nv_bfloat16*>(X) : nullptr;
+    p.resid_f32 = x.residual == 2 ? Y : nullptr;
+    p.ld_resid = x.d;
+    TRY(gemm_tc(0, s, x.di, at<__half>(ws, pl.wout), x.di, EPI_F32, p, 0, 1, sms, st));
+  }
+  if (cache_out) {
+    TRY(emit_cache<__half, __nv_bfloat16>(
+        x.B, x.L, x.M, x.T, cache_out->cap, x.Hkv, x.dh, x.dv, x.di, x.k, x.kv_shared ? nullptr : Kp, ldk, Vp, ldv,
+        proj + x.x_col, x.P_in, static_cast<__nv_bfloat16*>(cache_out->k_ring),
+        static_cast<__nv_bfloat16*>(cache_out->v_ring), static_cast<__nv_bfloat16*>(cache_out->k_meta),
+        static_cast<__nv_bfloat16*>(cache_out->v_meta), cache_out->conv_state, st));
+  }
+  return HYMBA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// decode
+// ---------------------------------------------------------------------------
+hymba_status decode_f32(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const float* Xn, float* Y,
+                        const hymba_cache* c, const hymba_cache* kvc, void* ws, cudaStream_t st) {
+  float* proj = at<float>(ws, pl.proj);
+  float* u = at<float>(ws, pl.u);
+  float* dtr = at<float>(ws, pl.dtr);
+  float* bc = at<float>(ws, pl.bc);
+  float* delta = at<float>(ws, pl.delta);
+  float* att = at<float>(ws, pl.att);
+  float* g = at<float>(ws, pl.g);
+  float* s = at<float>(ws, pl.s);
+  const int B = x.B;
+  TRY(gemm_simt<float>(B, x.P_in, x.d, Xn, x.d, static_cast<const float*>(w->W_in), x.d, SE_STORE, proj, x.P_in,
+                       nullptr, 0, 0, nullptr, nullptr, 0, st));
+  if (x.theta > 0) {
+    TRY(rope_simt<float>(proj, x.P_in, B, 0, x.Hq, x.dh, x.theta, 1, c->pos, x.M, st));
+    if (!x.kv_shared) TRY(rope_simt<float>(proj, x.P_in, B, x.k_col, x.Hkv, x.dh, x.theta, 1, c->pos, x.M, st));
+  }
+  if (!x.kv_shared)
+    TRY(kv_append<float, float>(B, x.Hkv, x.dh, x.dv, x.W, c->cap, proj, x.P_in, x.k_col, x.v_col, c->pos,
+                                static_cast<float*>(c->k_ring), static_cast<float*>(c->v_ring), st));
+  TRY(decode_attention<float, float>(B, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, kvc->cap, proj, x.P_in,
+                                     static_cast<const float*>(kvc->k_meta), static_cast<const float*>(kvc->v_meta),
+                                     static_cast<const float*>(kvc->k_ring), static_cast<const float*>(kvc->v_ring),
+                                     c->pos, att, x.di, st));
+  TRY(conv_step<float>(B, x.di, x.k, proj + x.x_col, x.P_in, w->conv_w, w->conv_b, c->conv_state, u, x.di, st));
+  TRY(gemm_simt<float>(B, x.xo, x.di, u, x.di, static_cast<const float*>(w->W_x), x.di, SE_XPROJ, bc, 2 * x.N, dtr,
+                       x.R, x.R, nullptr, nullptr, 0, st));
+  TRY(gemm_simt<float>(B, x.di, x.R, dtr, x.R, static_cast<const float*>(w->W_dt), x.R, SE_SOFTPLUS, delta, x.di,
+                       nullptr, 0, 0, w->dt_bias, nullptr, 0, st));
+  TRY(scan_simt<float>(B, 1, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, x.di, bc, bc + x.N, 2 * x.N,
+                       w->A_log, w->D, g, x.di, c->ssm_state, c->ssm_state, st));
+  TRY(fuse_norm<float>(B, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  TRY(gemm_simt<float>(B, x.d, x.di, s, x.di, static_cast<const float*>(w->W_out), x.di, SE_RESID, Y, x.d, nullptr,
+                       0, 0, nullptr, x.residual == 1 ? Xn : x.residual == 2 ? Y : nullptr, x.d, st));
+  return pos_increment(B, c->pos, st);
+}
+
+hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const void* Xn, float* Y,
+                         const hymba_cache* c, const hymba_cache* kvc, void* ws, int32_t* status,
+                         cudaStream_t st) {
+  const int sms = num_sms();
+  const int B = x.B;
+  __half* proj = at<__half>(ws, pl.proj);
+  __half* u = at<__half>(ws, pl.u);
+  __half* dtr = at<__half>(ws, pl.dtr);
+  float* bc = at<float>(ws, pl.bc);
+  float* delta = at<float>(ws, pl.delta);
+  __half* att = at<__half>(ws, pl.att);
+  __half* g = at<__half>(ws, pl.g);
+  __half* s = at<__half>(ws, pl.s);
+  float* part = at<float>(ws, pl.part);
+  TRY(convert_weights(x, pl, w, ws, st));
+  TRY(in_proj_bf16(x, Xn, w, proj, B, c->pos, x.M, 1, status, sms, st));
+  if (!x.kv_shared)
+    TRY(kv_append<__half, __nv_bfloat16>(B, x.Hkv, x.dh, x.dv, x.W, c->cap, proj, x.P_in, x.k_col, x.v_col, c->pos,
+                                         static_cast<__nv_bfloat16*>(c->k_ring),
+                                         static_cast<__nv_bfloat16*>(c->v_ring), st));
+  TRY(decode_attention<__half, __nv_bfloat16>(
+      B, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, kvc->cap, proj, x.P_in, static_cast<const __nv_bfloat16*>(kvc->k_meta),
+      static_cast<const __nv_bfloat16*>(kvc->v_meta), static_cast<const __nv_bfloat16*>(kvc->k_ring),
+      static_cast<const __nv_bfloat16*>(kvc->v_ring), c->pos, att, x.di, st));
+  TRY(conv_step<__half>(B, x.di, x.k, proj + x.x_col, x.P_in, w->conv_w, w->conv_b, c->conv_state, u, x.di, st));
+  {
+    const int ldp = (x.xo + 15) / 16 * 16;
+    GemmParams p = gp(B, x.xo, x.di, status, x.wait_ns);
+    p.C = part;
+    p.ldc = ldp;
+    TRY(gemm_tc(0, u, x.di, at<__half>(ws, pl.wx), x.di, EPI_PARTIAL, p, 0, kDecodeSplitsX, sms, st));
+    const int n_kb = (x.di + 63) / 64;
+    const int kbs = (n_kb + std::min(kDecodeSplitsX, n_kb) - 1) / std::min(kDecodeSplitsX, n_kb);
+    const int splits = (n_kb + kbs - 1) / kbs;
+    TRY(splitk_reduce(splits, B, x.xo, part, ldp, RE_XPROJ, x.R, dtr, x.Rp, bc, 2 * x.N, nullptr, 0, false, st));
+  }
+  {
+    GemmParams p = gp(B, x.di, x.R, status, x.wait_ns);
+    p.C = delta;
+    p.ldc = x.di;
+    p.bias = w->dt_bias;
+    TRY(gemm_tc(0, dtr, x.Rp, at<__half>(ws, pl.wdt), x.Rp, EPI_SOFTPLUS, p, 0, 1, sms, st));
+  }
+  TRY(scan_simt<__half>(B, 1, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, x.di, bc, bc + x.N, 2 * x.N,
+                        w->A_log, w->D, g, x.di, c->ssm_state, c->ssm_state, st));
+  TRY(fuse_norm<__half>(B, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  {
+    GemmParams p = gp(B, x.d, x.di, status, x.wait_ns);
+    p.C = part;
+    p.ldc = x.d;
+    TRY(gemm_tc(0, s, x.di, at<__half>(ws, pl.wout), x.di, EPI_PARTIAL, p, 0, kDecodeSplitsOut, sms, st));
+    const int n_kb = (x.di + 63) / 64;
+    const int sp = std::min(kDecodeSplitsOut, n_kb);
+    const int kbs = (n_kb + sp - 1) / sp;
+    const int splits = (n_kb + kbs - 1) / kbs;
+    TRY(splitk_reduce(splits, B, x.d, part, x.d, RE_F32, 0, nullptr, 0, Y, x.d,
+                      x.residual == 1 ? static_cast<const __nv_bfloat16*>(Xn) : nullptr, x.d, x.residual == 2, st));
+  }
+  return pos_increment(B, c->pos, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t hymba_abi_version(void) { return HYMBA_ABI_VERSION; }
+
+const char* hymba_status_str(hymba_status s) {
+  switch (s) {
+    case HYMBA_OK: return "HYMBA_OK";
+    case HYMBA_ERR_INVALID: return "HYMBA_ERR_INVALID: invalid argument";
+    case HYMBA_ERR_UNSUPPORTED: return "HYMBA_ERR_UNSUPPORTED: shape or option not implemented";
+    case HYMBA_ERR_WORKSPACE: return "HYMBA_ERR_WORKSPACE: workspace too small";
+    case HYMBA_ERR_CUDA: return "HYMBA_ERR_CUDA: CUDA runtime error";
+    case HYMBA_ERR_TIMEOUT: return "HYMBA_ERR_TIMEOUT: a bounded in-kernel wait gave up";
+    case HYMBA_ERR_RANGE: return "HYMBA_ERR_RANGE: fp16 intermediate overflow";
+    default: return "unknown hymba_status";
+  }
+}
+
+size_t hymba_layer_fwd_workspace(const hymba_layer_desc* d) {
+  Dims x;
+  if (check_desc(d, false, &x) != HYMBA_OK) return 0;
+  return plan_ws(x, false).total;
+}
+
+size_t hymba_layer_decode_workspace(const hymba_layer_desc* d) {
+  Dims x;
+  if (check_desc(d, true, &x) != HYMBA_OK) return 0;
+  return plan_ws(x, true).total;
+}
+
+hymba_status hymba_layer_fwd(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_in, float* y,
+                             const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
+                             size_t ws_bytes, int32_t* dev_status, void* stream) {
+  Dims x;
+  TRY(check_desc(d, false, &x));
+  TRY(check_weights(w, x));
+  if (!x_in || !y || !ws) return HYMBA_ERR_INVALID;
+  if ((x.kv_shared != 0) != (kv_in != nullptr)) return HYMBA_ERR_INVALID;
+  if (kv_in && (!kv_in->k || !kv_in->v)) return HYMBA_ERR_INVALID;
+  if (kv_out && (!kv_out->k || !kv_out->v)) return HYMBA_ERR_INVALID;
+  const size_t a = x.dtype == HYMBA_BF16 ? 16 : 4;
+  if (!aligned(x_in, a) || !aligned(y, 16) || !aligned(ws, 256)) return HYMBA_ERR_INVALID;
+  if (kv_in && (!aligned(kv_in->k, a) || !aligned(kv_in->v, a))) return HYMBA_ERR_INVALID;
+  if (cache_out) {
+    if (!cache_out->ssm_state || !cache_out->conv_state || cache_out->reserved != 0) return HYMBA_ERR_INVALID;
+    if (!x.kv_shared) {
+      if (!cache_out->k_ring || !cache_out->v_ring || !cache_out->k_meta || !cache_out->v_meta)
+        return HYMBA_ERR_INVALID;
+      if (cache_out->cap < 1) return HYMBA_ERR_INVALID;
+      if (x.W > 0 ? cache_out->cap < x.W : cache_out->cap < x.T) return HYMBA_ERR_INVALID;
+    }
+  }
+  const Plan pl = plan_ws(x, false);
+  if (ws_bytes < pl.total) return HYMBA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();  // clear a stale error so launch checks below are ours
+  if (x.dtype == HYMBA_F32)
+    return fwd_f32(x, pl, w, static_cast<const float*>(x_in), y, cache_out, kv_in, kv_out, ws, st);
+  return fwd_bf16(x, pl, w, x_in, y, cache_out, kv_in, kv_out, ws, dev_status, st);
+}
+
+hymba_status hymba_layer_decode(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_new,
+                                float* y, const hymba_cache* cache, const hymba_cache* shared_cache, void* ws,
+                                size_t ws_bytes, int32_t* dev_status, void* stream) {
+  Dims x;
+  TRY(check_desc(d, true, &x));
+  TRY(check_weights(w, x));
+  if (!x_new || !y || !ws || !cache) return HYMBA_ERR_INVALID;
+  if ((x.kv_shared != 0) != (shared_cache != nullptr)) return HYMBA_ERR_INVALID;
+  const hymba_cache* kvc = x.kv_shared ? shared_cache : cache;
+  if (!cache->ssm_state || !cache->conv_state || !cache->pos || cache->reserved != 0) return HYMBA_ERR_INVALID;
+  if (!kvc->k_ring || !kvc->v_ring || (x.M > 0 && (!kvc->k_meta || !kvc->v_meta)) || kvc->cap < 1)
+    return HYMBA_ERR_INVALID;
+  if (x.W > 0 && kvc->cap < x.W) return HYMBA_ERR_INVALID;
+  const size_t a = x.dtype == HYMBA_BF16 ? 16 : 4;
+  if (!aligned(x_new, a) || !aligned(y, 16) || !aligned(ws, 256)) return HYMBA_ERR_INVALID;
+  const Plan pl = plan_ws(x, true);
+  if (ws_bytes < pl.total) return HYMBA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  if (x.dtype == HYMBA_F32)
+    return decode_f32(x, pl, w, static_cast<const float*>(x_new), y, cache, kvc, ws, st);
+  return decode_bf16(x, pl, w, x_new, y, cache, kvc, ws, dev_status, st);
+}
+
+// --------------------------------------------------------------------------- tests
+
+hymba_status hymba_test_gemm(int32_t M, int32_t N, int32_t K, int32_t ab_dtype, const void* A, int32_t lda,
+                             const void* B, int32_t ldb, float* C, int32_t ldc, int32_t* dev_status, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || !A || !B || !C || (ab_dtype != 1 && ab_dtype != 2) || ldc < N)
+    return HYMBA_ERR_INVALID;
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.C = C;
+  p.ldc = ldc;
+  p.rows_per_seq = 1;
+  p.status = dev_status;
+  p.wait_ns = 2000000000ull;
+  cudaGetLastError();
+  return gemm_tc(ab_dtype == 1 ? 1 : 0, A, lda, B, ldb, EPI_F32, p, 0, 1, num_sms(),
+                 static_cast<cudaStream_t>(stream));
+}
+
+hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t N, const void* u, int32_t ld_u, const void* z,
+                             int32_t ld_z, const float* delta, const float* BC, const float* A_log, const float* D,
+                             void* g, float* h_out, void* stream) {
+  if (B < 1 || L < 1 || di < 1 || N < 1 || N > 64 || !u || !z || !delta || !BC || !A_log || !D || !g)
+    return HYMBA_ERR_INVALID;
+  cudaGetLastError();
+  return scan_f16(B, L, di, N, static_cast<const __half*>(u), ld_u, static_cast<const __half*>(z), ld_z, delta, BC,
+                  A_log, D, static_cast<__half*>(g), nullptr, h_out, static_cast<cudaStream_t>(stream));
+}
+
+hymba_status hymba_test_attention(int32_t B, int32_t L, int32_t M, int32_t Hq, int32_t Hkv, int32_t dh, int32_t dv,
+                                  int32_t window, int32_t use_tc, const void* Q, const void* K, const void* V,
+                                  void* O, int32_t* dev_status, void* stream) {
+  if (B < 1 || L < 1 || M < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || dh < 1 || dv < 1 || window < 0 || !Q || !K ||
+      !V || !O)
+    return HYMBA_ERR_INVALID;
+  cudaGetLastError();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const __half* q = static_cast<const __half*>(Q);
+  const __half* k = static_cast<const __half*>(K);
+  const __half* v = static_cast<const __half*>(V);
+  __half* o = static_cast<__half*>(O);
+  if (use_tc) {
+    if (!attn_tc_supported(dh, dv)) return HYMBA_ERR_UNSUPPORTED;
+    return attn_tc(B, L, M, Hq, Hkv, dh, dv, window, q, static_cast<long long>(Hq) * dh, k,
+                   static_cast<long long>(Hkv) * dh, v, static_cast<long long>(Hkv) * dv, o,
+                   static_cast<long long>(Hq) * dv, dev_status, 2000000000ull, num_sms(), st);
+  }
+  return attention_simt<__half>(B, L, M, Hq, Hkv, dh, dv, window, q, static_cast<long long>(Hq) * dh, k,
+                                static_cast<long long>(Hkv) * dh, v, static_cast<long long>(Hkv) * dv, o,
+                                static_cast<long long>(Hq) * dv, st);
+}
+
+hymba_status hymba_test_wait_timeout(uint32_t limit_us, int32_t* dev_status, void* stream) {
+  if (!dev_status || limit_us == 0 || limit_us > 10000000u) return HYMBA_ERR_INVALID;
+  cudaGetLastError();
+  return wait_timeout_probe(limit_us, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

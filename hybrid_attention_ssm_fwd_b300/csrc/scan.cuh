@@ -1,0 +1,21 @@
+// Selective scan + gate of the SSM branch (bf16 path: fp16 activations,
+// fp32 delta / B / C / state), and the bounded-wait probe.
+#pragma once
+
+#include "common.cuh"
+
+namespace hy {
+
+// g = (C.h + D u) * silu(z) with h_t = exp(delta_t A) h_{t-1} + delta_t u_t B_t,
+// A = -exp(A_log).  u, z fp16 rows (strides ld_u, ld_z); delta fp32 [B, L, di];
+// BC fp32 [B, L, 2N] = [B | C]; g fp16 [B, L, di]; h0/h_out [B, di, N] fp32
+// (either may be null).
+hymba_status scan_f16(int B, int L, int di, int N, const __half* u, long long ld_u, const __half* z,
+                      long long ld_z, const float* delta, const float* BC, const float* A_log, const float* D,
+                      __half* g, const float* h0, float* h_out, cudaStream_t st);
+
+// One block waits on an mbarrier nothing arrives on, bounded by limit_us,
+// and records HYMBA_ERR_TIMEOUT in *status.
+hymba_status wait_timeout_probe(uint32_t limit_us, int32_t* status, cudaStream_t st);
+
+}  // namespace hy

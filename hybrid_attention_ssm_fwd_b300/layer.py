@@ -1,0 +1,111 @@
+"""PyTorch-facing convenience wrapper around the C ABI.
+
+Holds a layer's device parameters, its descriptor and a workspace, and calls
+hymba_layer_fwd / hymba_layer_decode on the current stream.  Marshalling
+only: the arithmetic is in libhymba.so.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import numpy as np
+import torch
+
+from . import binding as hb
+
+MATRICES = ("W_in", "W_out", "W_x", "W_dt")
+VECTORS = ("dt_bias", "A_log", "D", "conv_w", "conv_b", "beta1", "beta2")
+
+
+def storage_dtype(shape) -> torch.dtype:
+    return torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+
+
+def kv_dtype(shape) -> torch.dtype:
+    """Element type of exported/imported K/V (fp16 on the bf16 path)."""
+    return torch.float16 if shape.dtype == "bf16" else torch.float32
+
+
+def params_to_device(p: Dict[str, np.ndarray], shape, device="cuda") -> Dict[str, torch.Tensor]:
+    """Matrices in the storage dtype, vectors in fp32 (values are already
+    storage-rounded by the generator, so the conversion is exact)."""
+    out = {}
+    dt = storage_dtype(shape)
+    for n in MATRICES:
+        out[n] = torch.from_numpy(np.ascontiguousarray(p[n], dtype=np.float32)).to(device=device, dtype=dt)
+    for n in VECTORS:
+        out[n] = torch.from_numpy(np.ascontiguousarray(p[n], dtype=np.float32)).to(device)
+    return out
+
+
+def tokens_to_device(Xt: np.ndarray, shape, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(Xt, dtype=np.float32)).to(device=device, dtype=storage_dtype(shape))
+
+
+def alloc_cache(shape, cap: int, device="cuda", with_kv: bool = True) -> Dict[str, torch.Tensor]:
+    dt = storage_dtype(shape)
+    c = {
+        "ssm_state": torch.zeros(shape.B, shape.di, shape.N, device=device, dtype=torch.float32),
+        "conv_state": torch.zeros(shape.B, shape.di, max(shape.k - 1, 1), device=device, dtype=torch.float32),
+        "pos": torch.zeros(shape.B, device=device, dtype=torch.int32),
+    }
+    if with_kv:
+        c["k_ring"] = torch.zeros(shape.B, cap, shape.Hkv, shape.dh, device=device, dtype=dt)
+        c["v_ring"] = torch.zeros(shape.B, cap, shape.Hkv, shape.dv, device=device, dtype=dt)
+        c["k_meta"] = torch.zeros(max(shape.M, 1), shape.Hkv, shape.dh, device=device, dtype=dt)
+        c["v_meta"] = torch.zeros(max(shape.M, 1), shape.Hkv, shape.dv, device=device, dtype=dt)
+    return c
+
+
+def cache_to_device(c: Dict[str, np.ndarray], shape, device="cuda") -> Dict[str, torch.Tensor]:
+    dt = storage_dtype(shape)
+    out = {}
+    for n in ("k_ring", "v_ring", "k_meta", "v_meta"):
+        if n in c:
+            out[n] = torch.from_numpy(np.ascontiguousarray(c[n], dtype=np.float32)).to(device=device, dtype=dt)
+    out["ssm_state"] = torch.from_numpy(np.ascontiguousarray(c["ssm_state"], dtype=np.float32)).to(device)
+    out["conv_state"] = torch.from_numpy(np.ascontiguousarray(c["conv_state"], dtype=np.float32)).to(device)
+    out["pos"] = torch.from_numpy(np.ascontiguousarray(c["pos"], dtype=np.int32)).to(device)
+    return out
+
+
+class HymbaLayer:
+    """One hybrid-head layer on one device."""
+
+    def __init__(self, shape, params: Dict[str, torch.Tensor], wait_limit_us: int = 0, decode: bool = False,
+                 residual_mode: Optional[int] = None):
+        self.shape = shape
+        self.params = params
+        self.desc = hb.make_desc(shape, wait_limit_us, residual_mode)
+        self.weights = hb.make_weights(params)
+        dev = params["W_in"].device
+        nbytes = hb.layer_decode_workspace(self.desc) if decode else hb.layer_fwd_workspace(self.desc)
+        if nbytes == 0:
+            raise hb.HymbaError(hb.HYMBA_ERR_INVALID, "workspace query")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def forward(self, x: torch.Tensor, y: Optional[torch.Tensor] = None, cache_out=None, cap: int = 0,
+                kv_in=None, kv_out=None) -> torch.Tensor:
+        s = self.shape
+        if y is None:
+            y = torch.empty(s.B, s.L, s.d, dtype=torch.float32, device=x.device)
+        hb.hymba_layer_fwd(self.desc, self.weights, x, y, self.ws,
+                           cache_out=hb.make_cache(cache_out, cap) if cache_out is not None else None,
+                           kv_in=hb.KV(kv_in[0].data_ptr(), kv_in[1].data_ptr()) if kv_in is not None else None,
+                           kv_out=hb.KV(kv_out[0].data_ptr(), kv_out[1].data_ptr()) if kv_out is not None else None,
+                           status=self.status)
+        return y
+
+    def decode(self, x_new: torch.Tensor, cache: Dict[str, torch.Tensor], cap: int,
+               y: Optional[torch.Tensor] = None, shared_cache=None, shared_cap: int = 0) -> torch.Tensor:
+        s = self.shape
+        if y is None:
+            y = torch.empty(s.B, s.d, dtype=torch.float32, device=x_new.device)
+        hb.hymba_layer_decode(self.desc, self.weights, x_new, y, hb.make_cache(cache, cap), self.ws,
+                              shared_cache=hb.make_cache(shared_cache, shared_cap) if shared_cache else None,
+                              status=self.status)
+        return y
+
+    def check_status(self) -> int:
+        return int(self.status.item())

@@ -1,0 +1,243 @@
+/*
+ * hymba.h -- C ABI of the B300 (sm_103a) forward pass of Hymba's fused
+ * hybrid-head layer.
+ *
+ * The operation ("Hymba: A Hybrid-head Architecture for Small Language
+ * Models", section 2.1, eq. 3):
+ *
+ *     Y = W_out( beta1 * norm(M_attn X~) + beta2 * norm(M_ssm X~) )
+ *
+ * X~ is the input with the M learned meta-token rows prepended (section 2.3).
+ * One shared input projection W_in yields Q, K, V, the SSM input x and the
+ * gate z.  M_attn is causal GQA softmax attention whose key set is the window
+ * of the last `window` tokens (0 = global) united with the meta prefix
+ * (section 2.2).  M_ssm is a causal depthwise conv1d + SiLU followed by the
+ * selective scan
+ *     h_t = exp(delta_t * A) (.) h_{t-1} + delta_t * B_t * u_t,
+ *     y_t = C_t . h_t + D (.) u_t,     g = y (.) silu(z),
+ * with [dt | B | C] = u W_x^T, delta = softplus(dt W_dt^T + dt_bias),
+ * A = -exp(A_log).  norm is RMSNorm over the d_inner channels of a row
+ * (no weight of its own).  Layers can share K/V with the previous layer
+ * (section 2.2), in which case they have no K/V projection.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are dense row-major ("C order") with the shapes given below.
+ *    Pointers named "device" must point to device memory of the current CUDA
+ *    device; the library never dereferences them on the host.
+ *  - The caller owns every buffer.  The library allocates no memory, keeps no
+ *    pointer after a call returns and has no global mutable state; calls on
+ *    different streams are independent.
+ *  - Calls are stream-ordered and asynchronous: inputs must stay valid and
+ *    outputs must not be read until `stream` reaches the call.  `stream` is a
+ *    cudaStream_t passed as void* (NULL = the legacy default stream).
+ *  - Argument errors are detected on the host before anything is launched;
+ *    the call then returns the error code and leaves every buffer untouched.
+ *    No C++ exception crosses the ABI.
+ *  - `dev_status` (may be NULL) is a device int32 that kernels set to a
+ *    nonzero hymba_status when a bounded wait gives up (HYMBA_ERR_TIMEOUT)
+ *    or an fp16 intermediate overflows (HYMBA_ERR_RANGE).  The caller zeroes
+ *    it before the call and reads it afterwards.
+ */
+#ifndef HYMBA_H
+#define HYMBA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HYMBA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define HYMBA_API __attribute__((visibility("default")))
+#else
+#define HYMBA_API
+#endif
+
+typedef enum hymba_status {
+  HYMBA_OK = 0,
+  HYMBA_ERR_INVALID = 1,      /* null pointer, bad shape, misaligned buffer,
+                                 kv_shared/kv_in mismatch                     */
+  HYMBA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (see per-call)     */
+  HYMBA_ERR_WORKSPACE = 3,    /* ws too small (query the *_workspace call)    */
+  HYMBA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed         */
+  HYMBA_ERR_TIMEOUT = 5,      /* asynchronous: a bounded wait gave up         */
+  HYMBA_ERR_RANGE = 6         /* asynchronous: |value| > 65504 in an fp16
+                                 intermediate (bf16 path)                     */
+} hymba_status;
+
+typedef enum hymba_dtype {
+  HYMBA_F32 = 0,   /* fp32 inputs/weights, fp32 SIMT arithmetic throughout   */
+  HYMBA_BF16 = 1   /* bf16 inputs/weights; tensor-core MMAs with fp32
+                      accumulation; intermediate activations stored as fp16;
+                      scan state, delta, B, C, norms and Y in fp32            */
+} hymba_dtype;
+
+/* Shape and flags of one layer call.  L = n_meta + n_tokens.
+ * P_in = n_q_heads*head_dim + (kv_shared ? 0 : n_kv_heads*(head_dim+v_head_dim))
+ *        + 2*d_inner  (rows of W_in).                                       */
+typedef struct hymba_layer_desc {
+  int32_t batch;        /* B >= 1                                            */
+  int32_t n_tokens;     /* T >= 1 real tokens (1 for decode)                 */
+  int32_t n_meta;       /* M >= 0 meta rows at the start of X~               */
+  int32_t d_model;      /* d                                                 */
+  int32_t n_q_heads;    /* Hq; n_q_heads % n_kv_heads == 0                   */
+  int32_t n_kv_heads;   /* Hkv (GQA groups; query head h uses KV head
+                           h / (Hq/Hkv))                                     */
+  int32_t head_dim;     /* dh of Q and K (even)                              */
+  int32_t v_head_dim;   /* dv; n_q_heads * v_head_dim == d_inner             */
+  int32_t d_inner;      /* di, width of both branches                        */
+  int32_t d_state;      /* N                                                 */
+  int32_t d_conv;       /* k, conv width (1..8)                              */
+  int32_t dt_rank;      /* R                                                 */
+  int32_t window;       /* keys incl. self visible in the window; 0 = global */
+  int32_t kv_shared;    /* 1: no K/V projection; K/V come from kv_in (prefill)
+                           or shared_cache (decode)                          */
+  int32_t residual;     /* 0: none; 1: Y += X~ (the layer input, desc.dtype);
+                           2: Y += Y (y holds an fp32 residual stream on
+                           entry and is updated in place)                    */
+  int32_t dtype;        /* hymba_dtype                                       */
+  float rope_theta;     /* RoPE base (rotate-half pairs, absolute positions
+                           counting the meta rows); 0 disables RoPE          */
+  float eps;            /* RMSNorm epsilon (1e-6 in the reference workloads) */
+  uint32_t wait_limit_us; /* bound on any single in-kernel wait; 0 = 2 s     */
+  int32_t reserved[3];  /* must be 0                                         */
+} hymba_layer_desc;
+
+/* Layer parameters (device pointers).  Matrices are in desc.dtype, vectors
+ * are fp32.  W_in rows: [Q (Hq*dh) | K (Hkv*dh) | V (Hkv*dv) | x (di) | z (di)]
+ * (no K/V rows when kv_shared).  W_x rows: [dt (R) | B (N) | C (N)].          */
+typedef struct hymba_layer_weights {
+  const void* W_in;     /* [P_in, d]                                         */
+  const void* W_out;    /* [d, di]                                           */
+  const void* W_x;      /* [R + 2N, di]                                      */
+  const void* W_dt;     /* [di, R]                                           */
+  const float* dt_bias; /* [di]                                              */
+  const float* A_log;   /* [di, N]; A = -exp(A_log)                          */
+  const float* D;       /* [di]                                              */
+  const float* conv_w;  /* [di, k]; tap k-1 multiplies the newest row        */
+  const float* conv_b;  /* [di]                                              */
+  const float* beta1;   /* [di] attention-branch scale                       */
+  const float* beta2;   /* [di] SSM-branch scale                             */
+} hymba_layer_weights;
+
+/* K/V of a layer, post-RoPE, exported for (or imported by) a KV-sharing
+ * consumer.  Element type: fp16 on the HYMBA_BF16 path, fp32 on HYMBA_F32.  */
+typedef struct hymba_kv {
+  void* k;              /* [B, L, Hkv, dh] device                            */
+  void* v;              /* [B, L, Hkv, dv] device                            */
+} hymba_kv;
+
+/* Decode state of one layer (device pointers).  K/V entries are in
+ * desc.dtype (bf16 or fp32), post-RoPE.  Real token number p (0-based, not
+ * counting meta rows) lives in slot p % cap.  A sliding-window layer needs
+ * cap >= window; a global layer needs cap > the largest position it will
+ * reach (no wrap).  A KV-sharing consumer layer's own cache needs only
+ * ssm_state, conv_state and pos (its K/V pointers may be NULL).             */
+typedef struct hymba_cache {
+  void* k_ring;         /* [B, cap, Hkv, dh]                                 */
+  void* v_ring;         /* [B, cap, Hkv, dv]                                 */
+  void* k_meta;         /* [M, Hkv, dh], shared by the batch                 */
+  void* v_meta;         /* [M, Hkv, dv]                                      */
+  float* ssm_state;     /* [B, di, N] fp32                                   */
+  float* conv_state;    /* [B, di, k-1] fp32, oldest row first               */
+  int32_t* pos;         /* [B] real tokens already consumed                  */
+  int32_t cap;          /* ring slots                                        */
+  int32_t reserved;     /* must be 0                                         */
+} hymba_cache;
+
+/* Bytes of scratch memory hymba_layer_fwd needs for `d` (0 on invalid d).  */
+HYMBA_API size_t hymba_layer_fwd_workspace(const hymba_layer_desc* d);
+
+/* Prefill forward of one layer over X~ (paper section 2.1 eq. 3; meta
+ * tokens section 2.3; window / KV sharing section 2.2).
+ *   x        [B, L, d] device, desc.dtype: X~ with the M meta rows first.
+ *            Meta rows must be identical across the batch when cache_out is
+ *            given (the cache keeps one copy of the meta K/V).
+ *   y        [B, L, d] device fp32: Y for every row (meta rows included).
+ *   cache_out (may be NULL) host struct of device buffers receiving the
+ *            decode state: the last min(T, cap) tokens' K/V in their slots,
+ *            meta K/V, final SSM state, conv tail (last k-1 pre-conv x rows)
+ *            and pos = T.  Requires cap >= window (SWA) or cap >= T (global).
+ *            Not allowed with kv_shared except for its ssm/conv/pos fields.
+ *   kv_in    non-NULL exactly when desc.kv_shared: the producer's K/V.
+ *   kv_out   (may be NULL) receives this layer's post-RoPE K/V.
+ *   ws       device scratch of ws_bytes >= hymba_layer_fwd_workspace(d),
+ *            256-byte aligned; contents on entry are ignored.
+ * Supported: HYMBA_F32 any shape (SIMT); HYMBA_BF16 needs d, P_in, d_inner,
+ * Hkv*dh and Hkv*dv multiples of 8 and 16-byte aligned buffers.
+ * Returns HYMBA_OK or a synchronous error code; asynchronous errors go to
+ * dev_status.                                                               */
+HYMBA_API hymba_status hymba_layer_fwd(const hymba_layer_desc* d, const hymba_layer_weights* w,
+                             const void* x, float* y, const hymba_cache* cache_out,
+                             const hymba_kv* kv_in, const hymba_kv* kv_out,
+                             void* ws, size_t ws_bytes, int32_t* dev_status,
+                             void* stream);
+
+/* Bytes of scratch memory hymba_layer_decode needs for `d` (0 on invalid). */
+HYMBA_API size_t hymba_layer_decode_workspace(const hymba_layer_desc* d);
+
+/* One decode step for B sequences (desc.n_tokens must be 1).  The token of
+ * sequence b sits at absolute position M + pos[b]; its K/V go into slot
+ * pos[b] % cap of `cache` (skipped for a kv_shared layer, which reads the
+ * producer's `shared_cache`, already updated for this token); attention sees
+ * the meta K/V plus the last min(pos+1, window) ring entries (pos+1 for a
+ * global layer); ssm_state and conv_state are advanced in place; pos[b] is
+ * incremented at the end.
+ *   x_new    [B, d] device, desc.dtype.      y  [B, d] device fp32.
+ * Positions beyond what the cache can hold are not checked on the device:
+ * the caller keeps pos[b] + 1 <= cap for global layers.                     */
+HYMBA_API hymba_status hymba_layer_decode(const hymba_layer_desc* d, const hymba_layer_weights* w,
+                                const void* x_new, float* y, const hymba_cache* cache,
+                                const hymba_cache* shared_cache, void* ws, size_t ws_bytes,
+                                int32_t* dev_status, void* stream);
+
+/* Human-readable name of a status code (static storage).                    */
+HYMBA_API const char* hymba_status_str(hymba_status s);
+
+/* HYMBA_ABI_VERSION of the built library.                                   */
+HYMBA_API int32_t hymba_abi_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Component entry points used by the parity tests.  Each runs exactly one of
+ * the kernels hymba_layer_fwd uses, on caller buffers, on `stream`.
+ * ------------------------------------------------------------------------- */
+
+/* C[M, N] (fp32, row stride ldc) = A[M, K] . B[N, K]^T on the tcgen05 GEMM
+ * (paper section 2.1: the shared input projection and W_out are these
+ * GEMMs).  ab_dtype 1 = bf16 operands, 2 = fp16 operands.  K-major rows,
+ * 16-byte aligned, lda/ldb (elements) multiples of 8.                        */
+HYMBA_API hymba_status hymba_test_gemm(int32_t M, int32_t N, int32_t K, int32_t ab_dtype,
+                             const void* A, int32_t lda, const void* B, int32_t ldb,
+                             float* C, int32_t ldc, int32_t* dev_status, void* stream);
+
+/* The bf16-path selective scan + gate kernel alone (SSM recurrence of the
+ * hybrid head, section 2.1).  u, z: fp16 [B, L, di] (row strides ld_u, ld_z);
+ * delta: fp32 [B, L, di]; BC: fp32 [B, L, 2N] ([B | C]); A_log [di, N], D [di]
+ * fp32.  g: fp16 [B, L, di] = (C.h + D u) silu(z); h_out [B, di, N] fp32
+ * final state (may be NULL).                                                */
+HYMBA_API hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t N,
+                             const void* u, int32_t ld_u, const void* z, int32_t ld_z,
+                             const float* delta, const float* BC, const float* A_log,
+                             const float* D, void* g, float* h_out, void* stream);
+
+/* The bf16-path attention kernel alone (section 2.2 window + section 2.3 meta
+ * prefix): Q [B, L, Hq, dh], K [B, L, Hkv, dh], V [B, L, Hkv, dv] fp16 ->
+ * O [B, L, Hq*dv] fp16.  use_tc: 1 = tcgen05 flash kernel, 0 = SIMT kernel. */
+HYMBA_API hymba_status hymba_test_attention(int32_t B, int32_t L, int32_t M, int32_t Hq, int32_t Hkv,
+                                  int32_t dh, int32_t dv, int32_t window, int32_t use_tc,
+                                  const void* Q, const void* K, const void* V, void* O,
+                                  int32_t* dev_status, void* stream);
+
+/* Failure-detection check: one block waits on an mbarrier that nothing
+ * arrives on, for at most limit_us, then writes HYMBA_ERR_TIMEOUT to
+ * *dev_status and returns.  No paper counterpart.                           */
+HYMBA_API hymba_status hymba_test_wait_timeout(uint32_t limit_us, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYMBA_H */

@@ -1,0 +1,134 @@
+"""Host-side checks of the C-ABI library, no GPU needed: it loads, exports
+every entry point include/hymba.h declares, and rejects bad arguments
+synchronously before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from hybrid_attention_ssm_fwd_b300 import binding as hb
+from hybrid_attention_ssm_fwd_b300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "hymba.h")).read()
+    return sorted(set(re.findall(r"HYMBA_API\s+[\w\s\*]+?\b(hymba_\w+)\s*\(", text)))
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    L = hb.lib()
+    syms = declared_symbols()
+    assert len(syms) >= 10
+    for name in syms:
+        assert hasattr(L, name), name
+    assert L.hymba_abi_version() == 1
+
+
+def test_status_strings():
+    for code in range(7):
+        assert hb.status_str(code).startswith("HYMBA_")
+    assert "unknown" in hb.status_str(99)
+
+
+def _fake_weights():
+    # 256-aligned fake device addresses: never dereferenced because every
+    # call below fails validation first
+    return hb.LayerWeights(*[0x10000 * (i + 1) for i in range(11)])
+
+
+def _desc(**kw):
+    s = synth.hymba15b_swa(B=2, T=64)
+    d = hb.make_desc(s)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_workspace_query():
+    d = _desc()
+    n = hb.layer_fwd_workspace(d)
+    s = synth.hymba15b_swa(B=2, T=64)
+    rows = s.B * s.L
+    assert n >= rows * s.P_in * 2 + rows * s.di * (2 * 4 + 4)
+    assert hb.layer_decode_workspace(hb.make_desc(synth.hymba15b_decode(B=4))) > 0
+    assert hb.layer_fwd_workspace(_desc(n_q_heads=7)) == 0          # Hq % Hkv != 0
+    assert hb.layer_decode_workspace(_desc()) == 0                  # decode needs n_tokens == 1
+
+
+@pytest.mark.parametrize("field,value", [("batch", 0), ("n_tokens", 0), ("head_dim", 63), ("d_state", 65),
+                                         ("d_conv", 9), ("window", -1), ("kv_shared", 2), ("dtype", 5),
+                                         ("v_head_dim", 64), ("eps", -1.0)])
+def test_invalid_desc_rejected_before_launch(field, value):
+    d = _desc(**{field: value})
+    w = _fake_weights()
+    ws = ctypes.c_void_p(0x100000)
+    rc = hb.lib().hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, None, None, None, ws,
+                                  1 << 40, None, None)
+    assert rc == hb.HYMBA_ERR_INVALID
+
+
+def test_reserved_fields_must_be_zero():
+    d = _desc()
+    d.reserved[1] = 3
+    assert hb.layer_fwd_workspace(d) == 0
+
+
+def test_null_and_misaligned_pointers_rejected():
+    d = _desc()
+    w = _fake_weights()
+    L = hb.lib()
+    big = 1 << 40
+    assert L.hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), None, 0x300000, None, None, None, 0x100000, big,
+                             None, None) == hb.HYMBA_ERR_INVALID
+    assert L.hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), 0x200002, 0x300000, None, None, None, 0x100000, big,
+                             None, None) == hb.HYMBA_ERR_INVALID
+    assert L.hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, None, None, None, 0x100010, big,
+                             None, None) == hb.HYMBA_ERR_INVALID
+    w.W_in = None
+    assert L.hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, None, None, None, 0x100000, big,
+                             None, None) == hb.HYMBA_ERR_INVALID
+
+
+def test_kv_sharing_pairing_enforced():
+    w = _fake_weights()
+    L = hb.lib()
+    kv = hb.KV(0x400000, 0x500000)
+    d = _desc()
+    assert L.hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, None, ctypes.byref(kv), None,
+                             0x100000, 1 << 40, None, None) == hb.HYMBA_ERR_INVALID
+    d = _desc(kv_shared=1)
+    assert L.hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, None, None, None, 0x100000,
+                             1 << 40, None, None) == hb.HYMBA_ERR_INVALID
+
+
+def test_workspace_too_small():
+    d = _desc()
+    w = _fake_weights()
+    need = hb.layer_fwd_workspace(d)
+    rc = hb.lib().hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, None, None, None,
+                                  0x100000, need - 1, None, None)
+    assert rc == hb.HYMBA_ERR_WORKSPACE
+
+
+def test_decode_argument_checks():
+    s = synth.hymba15b_decode(B=4)
+    d = hb.make_desc(s)
+    w = _fake_weights()
+    L = hb.lib()
+    cache = hb.Cache(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 512, 0)   # cap < window
+    rc = L.hymba_layer_decode(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, ctypes.byref(cache), None,
+                              0x100000, 1 << 40, None, None)
+    assert rc == hb.HYMBA_ERR_INVALID
+    cache.cap = 1024
+    cache.pos = None
+    rc = L.hymba_layer_decode(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, ctypes.byref(cache), None,
+                              0x100000, 1 << 40, None, None)
+    assert rc == hb.HYMBA_ERR_INVALID
+
+
+def test_unaligned_bf16_shapes_unsupported():
+    d = _desc(d_model=1604)
+    assert hb.layer_fwd_workspace(d) == 0

@@ -1,0 +1,163 @@
+"""Component parity on the GPU through the C ABI: the tcgen05 GEMM, the scan
+(closed form, special cases, random vs oracle), the attention kernels (the
+uniform-mean pin of the visible set, random vs oracle) and the bounded wait."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from hybrid_attention_ssm_fwd_b300 import binding as hb
+from oracle import hymba_ref as ref
+
+pytestmark = pytest.mark.gpu
+F = np.float64
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 200, 100), (1000, 1600, 3200), (37, 8960, 1600),
+                                   (4500, 144, 96), (128, 64, 8)])
+@pytest.mark.parametrize("ab", [1, 2])
+def test_gemm_tc_matches_fp64(M, N, K, ab):
+    g = torch.Generator().manual_seed(M * 7 + N + K)
+    dt = torch.bfloat16 if ab == 1 else torch.float16
+    A = torch.randn(M, K, generator=g).to(dt)
+    B = (0.05 * torch.randn(N, K, generator=g)).to(dt)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = hb.hymba_test_gemm(A.cuda(), B.cuda(), C, ab, status=st)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ref_c = A.double() @ B.double().T
+    got = C.cpu().double()
+    err = (got - ref_c).abs().max().item()
+    assert err <= 1e-5 * max(1.0, ref_c.abs().max().item()) * math.sqrt(K / 64), err
+
+
+def _scan_inputs(B, L, di, N, seed, u0=None, d0=None, b0=None, c0=None):
+    rng = np.random.default_rng(seed)
+    u = rng.standard_normal((B, L, di)) if u0 is None else np.full((B, L, di), u0)
+    z = rng.standard_normal((B, L, di)) * 2
+    dl = rng.uniform(1e-3, 0.1, (B, L, di)) if d0 is None else np.full((B, L, di), d0)
+    Bm = rng.standard_normal((B, L, N)) if b0 is None else np.full((B, L, N), b0)
+    Cm = rng.standard_normal((B, L, N)) if c0 is None else np.full((B, L, N), c0)
+    A_log = np.log(rng.uniform(1, 16, (di, N)))
+    D = rng.standard_normal(di)
+    # fp16-representable u, z so both sides see the same values
+    u = u.astype(np.float16).astype(F)
+    z = z.astype(np.float16).astype(F)
+    return u, z, dl.astype(np.float32).astype(F), Bm.astype(np.float32).astype(F), Cm.astype(np.float32).astype(F), \
+        A_log.astype(np.float32).astype(F), D.astype(np.float32).astype(F)
+
+
+def _run_scan(u, z, dl, Bm, Cm, A_log, D):
+    B, L, di = u.shape
+    N = Bm.shape[-1]
+    dev = "cuda"
+    tu = torch.from_numpy(u).to(dev, torch.float16)
+    tz = torch.from_numpy(z).to(dev, torch.float16)
+    td = torch.from_numpy(dl).to(dev, torch.float32)
+    bc = torch.from_numpy(np.concatenate([Bm, Cm], -1)).to(dev, torch.float32).contiguous()
+    ta = torch.from_numpy(A_log).to(dev, torch.float32)
+    tD = torch.from_numpy(D).to(dev, torch.float32)
+    g = torch.empty(B, L, di, device=dev, dtype=torch.float16)
+    h = torch.empty(B, di, N, device=dev, dtype=torch.float32)
+    assert hb.hymba_test_scan(tu, tz, td, bc, ta, tD, g, h) == 0
+    torch.cuda.synchronize()
+    return g.float().cpu().numpy().astype(F), h.cpu().numpy().astype(F)
+
+
+def test_scan_closed_form_on_gpu():
+    """Constant u, Delta, B, C with D = 0: the state follows the geometric
+    series exactly, so C.h dominates the output (the case the end-to-end
+    tolerance cannot see)."""
+    B, L, di, N = 2, 700, 64, 16
+    u, z, dl, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 1, u0=0.75, d0=0.05, b0=1.25, c0=-0.5)
+    D[:] = 0
+    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D)
+    A = -np.exp(A_log)
+    a = np.exp(0.05 * A)                                              # [di, N]
+    t = np.arange(L)[:, None, None]
+    ht = 0.05 * 1.25 * 0.75 * (1 - a[None] ** (t + 1)) / (1 - a[None])
+    y = -0.5 * ht.sum(-1)                                             # [L, di]
+    expect_g = y[None] * ref.silu(z)
+    np.testing.assert_allclose(h, np.broadcast_to(ht[-1], h.shape), rtol=2e-5)
+    np.testing.assert_allclose(g, expect_g, rtol=3e-3, atol=1e-3 * np.abs(expect_g).max())
+
+
+def test_scan_special_cases_on_gpu():
+    B, L, di, N = 1, 300, 96, 16
+    u, z, dl, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 2)
+    g, h = _run_scan(u, z, dl, np.zeros_like(Bm), Cm, A_log, D)       # B = 0: y = D u
+    np.testing.assert_allclose(g, D * u * ref.silu(z), rtol=2e-3, atol=1e-3)
+    assert np.all(h == 0)
+
+
+def test_scan_random_matches_oracle():
+    B, L, di, N = 3, 517, 160, 16
+    u, z, dl, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 3)
+    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D)
+    y, hr = ref.selective_scan(u, dl, -np.exp(A_log), Bm, Cm, D)
+    gr = y * ref.silu(z)
+    np.testing.assert_allclose(h, hr, rtol=1e-4, atol=1e-5 * np.abs(hr).max())
+    np.testing.assert_allclose(g, gr, rtol=2e-3, atol=2e-3 * np.abs(gr).max())
+
+
+def _attn_inputs(B, L, Hq, Hkv, dh, dv, seed, zero_q=False, q_scale=1.0):
+    rng = np.random.default_rng(seed)
+    Q = np.zeros((B, L, Hq, dh)) if zero_q else rng.standard_normal((B, L, Hq, dh)) * q_scale
+    K = rng.standard_normal((B, L, Hkv, dh))
+    V = rng.standard_normal((B, L, Hkv, dv))
+    return [a.astype(np.float16).astype(F) for a in (Q, K, V)]
+
+
+def _run_attn(Q, K, V, M, window, use_tc):
+    B, L, Hq, dh = Q.shape
+    dv = V.shape[-1]
+    t = [torch.from_numpy(a).to("cuda", torch.float16).contiguous() for a in (Q, K, V)]
+    O = torch.full((B, L, Hq * dv), float("nan"), device="cuda", dtype=torch.float16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = hb.hymba_test_attention(*t, O, M, window, use_tc, status=st)
+    if rc == hb.HYMBA_ERR_UNSUPPORTED:
+        pytest.skip("tensor-core attention not available for this shape")
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return O.float().cpu().numpy().astype(F)
+
+
+@pytest.mark.parametrize("use_tc", [0, 1])
+@pytest.mark.parametrize("M,window,L", [(128, 1024, 1500), (16, 32, 300), (128, 0, 700), (0, 1, 260),
+                                        (5, 8, 200), (128, 200, 333)])
+def test_attention_uniform_mean_pins_visible_set(use_tc, M, window, L):
+    """Q = 0: every visible score is 0, so each output row is the plain mean
+    of V over meta-union-window; this pins |vis(i)| for every row."""
+    B, Hq, Hkv, dh, dv = 2, 4, 2, 64, 128
+    Q, K, V = _attn_inputs(B, L, Hq, Hkv, dh, dv, 4, zero_q=True)
+    got = _run_attn(Q, K, V, M, window, use_tc)
+    exp = ref.attention(Q, K, V, M, window)
+    np.testing.assert_allclose(got, exp, atol=2e-3, rtol=2e-3)
+
+
+@pytest.mark.parametrize("use_tc", [0, 1])
+@pytest.mark.parametrize("M,window,L,q_scale", [(128, 1024, 1400, 1.0), (128, 0, 600, 1.0), (16, 64, 301, 3.0),
+                                                (3, 0, 129, 6.0)])
+def test_attention_random_matches_oracle(use_tc, M, window, L, q_scale):
+    """Random Q/K/V, including large scores that force the running-max
+    rescale path."""
+    B, Hq, Hkv, dh, dv = 2, 10, 2, 64, 128
+    Q, K, V = _attn_inputs(B, L, Hq, Hkv, dh, dv, 5, q_scale=q_scale)
+    got = _run_attn(Q, K, V, M, window, use_tc)
+    exp = ref.attention(Q, K, V, M, window)
+    np.testing.assert_allclose(got, exp, atol=4e-3 * max(1, np.abs(exp).max()), rtol=1e-2)
+
+
+def test_bounded_wait_reports_timeout():
+    """A wait on a barrier nothing arrives on gives up after its limit and the
+    status word says so; the context stays usable."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert hb.hymba_test_wait_timeout(20000, st) == 0
+    torch.cuda.synchronize()
+    assert st.item() == hb.HYMBA_ERR_TIMEOUT
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum().item()) == 8.0
