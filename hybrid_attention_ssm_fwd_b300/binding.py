@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
     L.hymba_layer_fwd.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache), P(KV), P(KV),
                                   c_void_p, c_size_t, c_void_p, c_void_p]
     L.hymba_layer_fwd.restype = c_int32
+    L.hymba_layer_fwd_events.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache), P(KV),
+                                         P(KV), c_void_p, c_size_t, c_void_p, c_void_p, c_int32, c_void_p]
+    L.hymba_layer_fwd_events.restype = c_int32
     L.hymba_layer_decode.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache), P(Cache),
                                      c_void_p, c_size_t, c_void_p, c_void_p]
     L.hymba_layer_decode.restype = c_int32
@@ -161,6 +164,20 @@ def hymba_layer_fwd(desc: LayerDesc, weights: LayerWeights, x, y, ws, cache_out:
                                ctypes.byref(kv_out) if kv_out is not None else None,
                                _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
     return _check(rc, "hymba_layer_fwd") if check else rc
+
+
+def hymba_layer_fwd_events(desc: LayerDesc, weights: LayerWeights, x, y, ws, events, n_events: int,
+                           cache_out: Optional[Cache] = None, kv_in: Optional[KV] = None,
+                           kv_out: Optional[KV] = None, status=None, stream=None, check: bool = True) -> int:
+    """hymba_layer_fwd that records per-stage CUDA events (``events`` is a
+    ctypes array of cudaEvent_t handles)."""
+    rc = lib().hymba_layer_fwd_events(ctypes.byref(desc), ctypes.byref(weights), _ptr(x), _ptr(y),
+                                      ctypes.byref(cache_out) if cache_out is not None else None,
+                                      ctypes.byref(kv_in) if kv_in is not None else None,
+                                      ctypes.byref(kv_out) if kv_out is not None else None,
+                                      _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), events, n_events,
+                                      _stream(stream))
+    return _check(rc, "hymba_layer_fwd_events") if check else rc
 
 
 def hymba_layer_decode(desc: LayerDesc, weights: LayerWeights, x_new, y, cache: Cache, ws,

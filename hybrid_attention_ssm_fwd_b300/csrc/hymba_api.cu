@@ -154,6 +154,19 @@ int num_sms() {
     if (s_ != HYMBA_OK) return s_;         \
   } while (0)
 
+// Optional per-stage CUDA events (hymba_layer_fwd_events): events[0] before
+// the first launch, events[k] after stage k.
+struct Marks {
+  void* const* ev = nullptr;
+  int n = 0;
+  int i = 0;
+  cudaStream_t st = nullptr;
+  void mark() {
+    if (ev && i < n) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    ++i;
+  }
+};
+
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -164,7 +177,7 @@ T* at(void* ws, size_t off) {
 // ---------------------------------------------------------------------------
 hymba_status fwd_f32(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const float* X, float* Y,
                      const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
-                     cudaStream_t st) {
+                     Marks& mk, cudaStream_t st) {
   float* proj = at<float>(ws, pl.proj);
   float* u = at<float>(ws, pl.u);
   float* dtr = at<float>(ws, pl.dtr);
@@ -175,12 +188,15 @@ hymba_status fwd_f32(const Dims& x, const Plan& pl, const hymba_layer_weights* w
   float* s = at<float>(ws, pl.s);
   const int rows = static_cast<int>(x.rows);
   const float* Win = static_cast<const float*>(w->W_in);
+  mk.mark();
+  mk.mark();  // no weight conversion on this path
   TRY(gemm_simt<float>(rows, x.P_in, x.d, X, x.d, Win, x.d, SE_STORE, proj, x.P_in, nullptr, 0, 0, nullptr,
                        nullptr, 0, st));
   if (x.theta > 0) {
     TRY(rope_simt<float>(proj, x.P_in, rows, 0, x.Hq, x.dh, x.theta, x.L, nullptr, 0, st));
     if (!x.kv_shared) TRY(rope_simt<float>(proj, x.P_in, rows, x.k_col, x.Hkv, x.dh, x.theta, x.L, nullptr, 0, st));
   }
+  mk.mark();
   const float* Kp = x.kv_shared ? static_cast<const float*>(kv_in->k) : proj + x.k_col;
   const float* Vp = x.kv_shared ? static_cast<const float*>(kv_in->v) : proj + x.v_col;
   const long long ldk = x.kv_shared ? static_cast<long long>(x.Hkv) * x.dh : x.P_in;
@@ -191,26 +207,35 @@ hymba_status fwd_f32(const Dims& x, const Plan& pl, const hymba_layer_weights* w
     TRY(copy2d<float, float>(Vp, ldv, static_cast<float*>(kv_out->v), static_cast<long long>(x.Hkv) * x.dv, x.rows,
                              x.Hkv * x.dv, st));
   }
+  mk.mark();
   TRY(attention_simt<float>(x.B, x.L, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, proj, x.P_in, Kp, ldk, Vp, ldv, att,
                             x.di, st));
+  mk.mark();
   TRY(conv_silu<float, float>(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, st));
+  mk.mark();
   TRY(gemm_simt<float>(rows, x.xo, x.di, u, x.di, static_cast<const float*>(w->W_x), x.di, SE_XPROJ, bc, 2 * x.N,
                        dtr, x.R, x.R, nullptr, nullptr, 0, st));
+  mk.mark();
   TRY(gemm_simt<float>(rows, x.di, x.R, dtr, x.R, static_cast<const float*>(w->W_dt), x.R, SE_SOFTPLUS, delta,
                        x.di, nullptr, 0, 0, w->dt_bias, nullptr, 0, st));
+  mk.mark();
   float* h_out = cache_out ? cache_out->ssm_state : nullptr;
   TRY(scan_simt<float>(x.B, x.L, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, x.di, bc, bc + x.N, 2 * x.N,
                        w->A_log, w->D, g, x.di, nullptr, h_out, st));
+  mk.mark();
   TRY(fuse_norm<float>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  mk.mark();
   TRY(gemm_simt<float>(rows, x.d, x.di, s, x.di, static_cast<const float*>(w->W_out), x.di, SE_RESID, Y, x.d,
                        nullptr, 0, 0, nullptr, x.residual == 1 ? X : x.residual == 2 ? Y : nullptr, x.d, st));
+  mk.mark();
   if (cache_out) {
     TRY(emit_cache<float, float>(x.B, x.L, x.M, x.T, cache_out->cap, x.Hkv, x.dh, x.dv, x.di, x.k,
                                  x.kv_shared ? nullptr : Kp, ldk, Vp, ldv, proj + x.x_col, x.P_in,
                                  static_cast<float*>(cache_out->k_ring), static_cast<float*>(cache_out->v_ring),
                                  static_cast<float*>(cache_out->k_meta), static_cast<float*>(cache_out->v_meta),
-                                 cache_out->conv_state, st));
+                                 cache_out->conv_state, cache_out->pos, st));
   }
+  mk.mark();
   return HYMBA_OK;
 }
 
@@ -264,7 +289,7 @@ hymba_status in_proj_bf16(const Dims& x, const void* X, const hymba_layer_weight
 
 hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const void* X, float* Y,
                       const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
-                      int32_t* status, cudaStream_t st) {
+                      int32_t* status, Marks& mk, cudaStream_t st) {
   const int sms = num_sms();
   const int rows = static_cast<int>(x.rows);
   __half* proj = at<__half>(ws, pl.proj);
@@ -275,8 +300,11 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
   __half* att = at<__half>(ws, pl.att);
   __half* g = at<__half>(ws, pl.g);
   __half* s = at<__half>(ws, pl.s);
+  mk.mark();
   TRY(convert_weights(x, pl, w, ws, st));
+  mk.mark();
   TRY(in_proj_bf16(x, X, w, proj, rows, nullptr, 0, x.L, status, sms, st));
+  mk.mark();
 
   const __half* Kp = x.kv_shared ? static_cast<const __half*>(kv_in->k) : proj + x.k_col;
   const __half* Vp = x.kv_shared ? static_cast<const __half*>(kv_in->v) : proj + x.v_col;
@@ -288,6 +316,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     TRY(copy2d<__half, __half>(Vp, ldv, static_cast<__half*>(kv_out->v), static_cast<long long>(x.Hkv) * x.dv,
                                x.rows, x.Hkv * x.dv, st));
   }
+  mk.mark();
   // attention branch
   if (attn_tc_supported(x.dh, x.dv)) {
     TRY(attn_tc(x.B, x.L, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, proj, x.P_in, Kp, ldk, Vp, ldv, att, x.di, status,
@@ -296,8 +325,10 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     TRY(attention_simt<__half>(x.B, x.L, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, proj, x.P_in, Kp, ldk, Vp, ldv, att,
                                x.di, st));
   }
+  mk.mark();
   // SSM branch
   TRY(conv_silu<__half, __half>(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, st));
+  mk.mark();
   {
     GemmParams p = gp(rows, x.xo, x.di, status, x.wait_ns);
     p.C = bc;
@@ -307,6 +338,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     p.xproj_R = x.R;
     TRY(gemm_tc(0, u, x.di, at<__half>(ws, pl.wx), x.di, EPI_XPROJ, p, 0, 1, sms, st));
   }
+  mk.mark();
   {
     GemmParams p = gp(rows, x.di, x.R, status, x.wait_ns);
     p.C = delta;
@@ -314,11 +346,14 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     p.bias = w->dt_bias;
     TRY(gemm_tc(0, dtr, x.Rp, at<__half>(ws, pl.wdt), x.Rp, EPI_SOFTPLUS, p, 0, 1, sms, st));
   }
+  mk.mark();
   float* h_out = cache_out ? cache_out->ssm_state : nullptr;
   TRY(scan_f16(x.B, x.L, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, bc, w->A_log, w->D, g, nullptr, h_out,
-               st));
+               status, x.wait_ns, st));
+  mk.mark();
   // fuse + out_proj
   TRY(fuse_norm<__half>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  mk.mark();
   {
     GemmParams p = gp(rows, x.d, x.di, status, x.wait_ns);
     p.C = Y;
@@ -328,13 +363,15 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     p.ld_resid = x.d;
     TRY(gemm_tc(0, s, x.di, at<__half>(ws, pl.wout), x.di, EPI_F32, p, 0, 1, sms, st));
   }
+  mk.mark();
   if (cache_out) {
     TRY(emit_cache<__half, __nv_bfloat16>(
         x.B, x.L, x.M, x.T, cache_out->cap, x.Hkv, x.dh, x.dv, x.di, x.k, x.kv_shared ? nullptr : Kp, ldk, Vp, ldv,
         proj + x.x_col, x.P_in, static_cast<__nv_bfloat16*>(cache_out->k_ring),
         static_cast<__nv_bfloat16*>(cache_out->v_ring), static_cast<__nv_bfloat16*>(cache_out->k_meta),
-        static_cast<__nv_bfloat16*>(cache_out->v_meta), cache_out->conv_state, st));
+        static_cast<__nv_bfloat16*>(cache_out->v_meta), cache_out->conv_state, cache_out->pos, st));
   }
+  mk.mark();
   return HYMBA_OK;
 }
 
@@ -470,9 +507,10 @@ size_t hymba_layer_decode_workspace(const hymba_layer_desc* d) {
   return plan_ws(x, true).total;
 }
 
-hymba_status hymba_layer_fwd(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_in, float* y,
-                             const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
-                             size_t ws_bytes, int32_t* dev_status, void* stream) {
+static hymba_status layer_fwd_impl(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_in,
+                                   float* y, const hymba_cache* cache_out, const hymba_kv* kv_in,
+                                   const hymba_kv* kv_out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                   void* const* events, int32_t n_events, void* stream) {
   Dims x;
   TRY(check_desc(d, false, &x));
   TRY(check_weights(w, x));
@@ -492,13 +530,31 @@ hymba_status hymba_layer_fwd(const hymba_layer_desc* d, const hymba_layer_weight
       if (x.W > 0 ? cache_out->cap < x.W : cache_out->cap < x.T) return HYMBA_ERR_INVALID;
     }
   }
+  if (n_events < 0 || (n_events > 0 && !events)) return HYMBA_ERR_INVALID;
   const Plan pl = plan_ws(x, false);
   if (ws_bytes < pl.total) return HYMBA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();  // clear a stale error so launch checks below are ours
+  Marks mk;
+  mk.ev = events;
+  mk.n = n_events;
+  mk.st = st;
   if (x.dtype == HYMBA_F32)
-    return fwd_f32(x, pl, w, static_cast<const float*>(x_in), y, cache_out, kv_in, kv_out, ws, st);
-  return fwd_bf16(x, pl, w, x_in, y, cache_out, kv_in, kv_out, ws, dev_status, st);
+    return fwd_f32(x, pl, w, static_cast<const float*>(x_in), y, cache_out, kv_in, kv_out, ws, mk, st);
+  return fwd_bf16(x, pl, w, x_in, y, cache_out, kv_in, kv_out, ws, dev_status, mk, st);
+}
+
+hymba_status hymba_layer_fwd(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_in, float* y,
+                             const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
+                             size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return layer_fwd_impl(d, w, x_in, y, cache_out, kv_in, kv_out, ws, ws_bytes, dev_status, nullptr, 0, stream);
+}
+
+hymba_status hymba_layer_fwd_events(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_in,
+                                    float* y, const hymba_cache* cache_out, const hymba_kv* kv_in,
+                                    const hymba_kv* kv_out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                    void* const* events, int32_t n_events, void* stream) {
+  return layer_fwd_impl(d, w, x_in, y, cache_out, kv_in, kv_out, ws, ws_bytes, dev_status, events, n_events, stream);
 }
 
 hymba_status hymba_layer_decode(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_new,
@@ -552,7 +608,8 @@ hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t N, const 
     return HYMBA_ERR_INVALID;
   cudaGetLastError();
   return scan_f16(B, L, di, N, static_cast<const __half*>(u), ld_u, static_cast<const __half*>(z), ld_z, delta, BC,
-                  A_log, D, static_cast<__half*>(g), nullptr, h_out, static_cast<cudaStream_t>(stream));
+                  A_log, D, static_cast<__half*>(g), nullptr, h_out, nullptr, 2000000000ull,
+                  static_cast<cudaStream_t>(stream));
 }
 
 hymba_status hymba_test_attention(int32_t B, int32_t L, int32_t M, int32_t Hq, int32_t Hkv, int32_t dh, int32_t dv,

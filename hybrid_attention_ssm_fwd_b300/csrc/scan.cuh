@@ -12,7 +12,8 @@ namespace hy {
 // (either may be null).
 hymba_status scan_f16(int B, int L, int di, int N, const __half* u, long long ld_u, const __half* z,
                       long long ld_z, const float* delta, const float* BC, const float* A_log, const float* D,
-                      __half* g, const float* h0, float* h_out, cudaStream_t st);
+                      __half* g, const float* h0, float* h_out, int32_t* status, uint64_t wait_ns,
+                      cudaStream_t st);
 
 // One block waits on an mbarrier nothing arrives on, bounded by limit_us,
 // and records HYMBA_ERR_TIMEOUT in *status.

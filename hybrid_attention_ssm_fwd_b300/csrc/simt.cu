@@ -350,6 +350,11 @@ __global__ void emit_conv_tail_kernel(int B, int L, int di, int k, const TS* __r
   }
 }
 
+__global__ void fill_i32_kernel(int n, int32_t* dst, int32_t v) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = v;
+}
+
 inline hymba_status last_err() {
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
@@ -430,7 +435,9 @@ hymba_status copy2d(const TS* src, long long lds, TD* dst, long long ldd, long l
 template <typename TS, typename TC>
 hymba_status emit_cache(int B, int L, int M, int T, int cap, int Hkv, int dh, int dv, int di, int k,
                         const TS* Kp, long long ldk, const TS* Vp, long long ldv, const TS* xp, long long ldx,
-                        TC* k_ring, TC* v_ring, TC* k_meta, TC* v_meta, float* conv_state, cudaStream_t st) {
+                        TC* k_ring, TC* v_ring, TC* k_meta, TC* v_meta, float* conv_state, int32_t* pos,
+                        cudaStream_t st) {
+  if (pos) fill_i32_kernel<<<(B + 255) / 256, 256, 0, st>>>(B, pos, T);
   const int n_keep = std::min(T, cap);
   if (Kp && k_ring && n_keep > 0) {
     long long n = static_cast<long long>(B) * n_keep * Hkv * dh;
@@ -494,11 +501,11 @@ template hymba_status copy2d<__half, __nv_bfloat16>(const __half*, long long, __
                                                     long long, int, cudaStream_t);
 template hymba_status emit_cache<float, float>(int, int, int, int, int, int, int, int, int, int, const float*,
                                                long long, const float*, long long, const float*, long long,
-                                               float*, float*, float*, float*, float*, cudaStream_t);
+                                               float*, float*, float*, float*, float*, int32_t*, cudaStream_t);
 template hymba_status emit_cache<__half, __nv_bfloat16>(int, int, int, int, int, int, int, int, int, int,
                                                         const __half*, long long, const __half*, long long,
                                                         const __half*, long long, __nv_bfloat16*,
                                                         __nv_bfloat16*, __nv_bfloat16*, __nv_bfloat16*, float*,
-                                                        cudaStream_t);
+                                                        int32_t*, cudaStream_t);
 
 }  // namespace hy

@@ -59,11 +59,12 @@ hymba_status copy2d(const TS* src, long long lds, TD* dst, long long ldd, long l
                     cudaStream_t st);
 
 // Prefill cache emission: ring K/V (last min(T, cap) tokens at slot t % cap),
-// meta K/V (from sequence 0) and the conv tail (last k-1 x rows, fp32).
+// meta K/V (from sequence 0), the conv tail (last k-1 x rows, fp32) and
+// pos[b] = T.
 template <typename TS, typename TC>
 hymba_status emit_cache(int B, int L, int M, int T, int cap, int Hkv, int dh, int dv, int di, int k,
                         const TS* Kp, long long ldk, const TS* Vp, long long ldv, const TS* xp,
                         long long ldx, TC* k_ring, TC* v_ring, TC* k_meta, TC* v_meta,
-                        float* conv_state, cudaStream_t st);
+                        float* conv_state, int32_t* pos, cudaStream_t st);
 
 }  // namespace hy

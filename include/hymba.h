@@ -176,6 +176,21 @@ HYMBA_API hymba_status hymba_layer_fwd(const hymba_layer_desc* d, const hymba_la
                              void* ws, size_t ws_bytes, int32_t* dev_status,
                              void* stream);
 
+/* hymba_layer_fwd that also records CUDA events on `stream` around its
+ * stages, for profiling: events[0] before the first launch and events[k]
+ * after stage k, stages being 1 weight conversion, 2 input projection (+RoPE),
+ * 3 K/V export, 4 attention, 5 conv+SiLU, 6 x_proj, 7 dt_proj+softplus,
+ * 8 selective scan+gate, 9 norm/beta/sum, 10 output projection, 11 cache
+ * emission (HYMBA_FWD_EVENTS events in all; extra events are not recorded,
+ * missing ones are skipped).  events are cudaEvent_t handles created by the
+ * caller; n_events >= 0.  Otherwise identical to hymba_layer_fwd.            */
+#define HYMBA_FWD_EVENTS 12
+HYMBA_API hymba_status hymba_layer_fwd_events(const hymba_layer_desc* d, const hymba_layer_weights* w,
+                                              const void* x, float* y, const hymba_cache* cache_out,
+                                              const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
+                                              size_t ws_bytes, int32_t* dev_status, void* const* events,
+                                              int32_t n_events, void* stream);
+
 /* Bytes of scratch memory hymba_layer_decode needs for `d` (0 on invalid). */
 HYMBA_API size_t hymba_layer_decode_workspace(const hymba_layer_desc* d);
 

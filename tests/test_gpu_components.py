@@ -24,7 +24,14 @@ def test_gemm_tc_matches_fp64(M, N, K, ab):
     B = (0.05 * torch.randn(N, K, generator=g)).to(dt)
     C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = hb.hymba_test_gemm(A.cuda(), B.cuda(), C, ab, status=st)
+    # rows must start on 16 bytes: pad the row stride to a multiple of 8 and
+    # fill the padding with NaN, which the K tail must never read
+    Kp = (K + 7) // 8 * 8
+    Ad = torch.full((M, Kp), float("nan"), dtype=dt, device="cuda")
+    Bd = torch.full((N, Kp), float("nan"), dtype=dt, device="cuda")
+    Ad[:, :K] = A.cuda()
+    Bd[:, :K] = B.cuda()
+    rc = hb.hymba_test_gemm(Ad[:, :K], Bd[:, :K], C, ab, status=st)
     assert rc == 0
     torch.cuda.synchronize()
     assert st.item() == 0
