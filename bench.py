@@ -145,7 +145,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     peaks, peak_src = load_peaks()
-    s = synth.hymba15b_swa(rope_theta=10000.0)
+    s = synth.hymba15b_swa(rope_theta=10000.0, B=args.batch)
     p = synth.make_layer_inputs(s, 1 + rank)
     params = hl.params_to_device(p, s, dev)
     layer = hl.HymbaLayer(s, params)
@@ -229,6 +229,8 @@ def run_ours(args, rank, world, local_rank):
     # free the prefill buffers before the other workloads
     del layer, X, Y, params
     torch.cuda.empty_cache()
+    if args.only_main:
+        return out
     out["e2e"] = run_e2e(args, torch, hb, hl, dev, stream)
     out["decode"] = run_decode(args, torch, hb, hl, dev, stream, peaks, peak_src)
     out["global_prefill"] = run_prefill_extra(args, torch, hb, hl, dev, stream, synth.hymba15b_global(rope_theta=10000.0),
@@ -497,6 +499,9 @@ def main():
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
     ap.add_argument("--ref-sample-tokens", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-main", action="store_true",
+                    help="time only the main prefill workload (used for profiler runs)")
+    ap.add_argument("--batch", type=int, default=8, help="sequences in the main prefill workload")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
