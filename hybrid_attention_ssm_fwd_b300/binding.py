@@ -81,6 +81,9 @@ def lib() -> ctypes.CDLL:
     L.hymba_layer_decode.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache), P(Cache),
                                      c_void_p, c_size_t, c_void_p, c_void_p]
     L.hymba_layer_decode.restype = c_int32
+    L.hymba_layer_decode_static.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache),
+                                            P(Cache), c_void_p, c_void_p]
+    L.hymba_layer_decode_static.restype = c_int32
     L.hymba_test_gemm.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
                                   c_void_p, c_int32, c_void_p, c_void_p]
     L.hymba_test_gemm.restype = c_int32
@@ -188,6 +191,22 @@ def hymba_layer_decode(desc: LayerDesc, weights: LayerWeights, x_new, y, cache: 
                                   ctypes.byref(shared_cache) if shared_cache is not None else None,
                                   _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
     return _check(rc, "hymba_layer_decode") if check else rc
+
+
+STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def hymba_layer_decode_static(desc: LayerDesc, weights: LayerWeights, x_new, y, cache: Cache,
+                              shared_cache: Optional[Cache] = None, status=None, stream=None,
+                              check: bool = True) -> int:
+    """hymba_layer_decode with the library's built-in scratch buffer instead of
+    a workspace, for callers that cannot allocate device memory (see
+    include/hymba.h).  Calls must not overlap on the GPU."""
+    rc = lib().hymba_layer_decode_static(ctypes.byref(desc), ctypes.byref(weights), _ptr(x_new), _ptr(y),
+                                         ctypes.byref(cache),
+                                         ctypes.byref(shared_cache) if shared_cache is not None else None,
+                                         _ptr(status), _stream(stream))
+    return _check(rc, "hymba_layer_decode_static") if check else rc
 
 
 def hymba_test_gemm(A, B, C, ab_dtype: int, status=None, stream=None) -> int:

@@ -12,6 +12,7 @@
 //   out_proj (tcgen05, residual fused) -> Y fp32
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "attn_tc.cuh"
 #include "common.cuh"
@@ -642,3 +643,52 @@ hymba_status hymba_test_wait_timeout(uint32_t limit_us, int32_t* dev_status, voi
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without caller-supplied workspace (hymba_layer_decode_static).
+//
+// For callers that cannot allocate device memory when they run a decode step
+// (a plugin whose host framework owns all device memory, a serving loop whose
+// memory is fully reserved by its cache pool): the scratch is this file-scope
+// device buffer.  Host code must not use the symbol itself as a device
+// address; it fetches the per-device address once with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_decode_scratch[HYMBA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device (looked up on the
+// first call per device, with that device current).
+hymba_status static_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return HYMBA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return HYMBA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return HYMBA_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return HYMBA_OK;
+}
+
+}  // namespace
+
+extern "C" hymba_status hymba_layer_decode_static(const hymba_layer_desc* d, const hymba_layer_weights* w,
+                                                  const void* x_new, float* y, const hymba_cache* cache,
+                                                  const hymba_cache* shared_cache, int32_t* dev_status,
+                                                  void* stream) {
+  const size_t need = hymba_layer_decode_workspace(d);
+  if (need == 0)  // invalid descriptor: report its error without touching the device
+    return hymba_layer_decode(d, w, x_new, y, cache, shared_cache, nullptr, 0, dev_status, stream);
+  if (need > HYMBA_STATIC_SCRATCH_BYTES) return HYMBA_ERR_WORKSPACE;
+  void* ws = nullptr;
+  const hymba_status s = static_scratch(&ws);
+  if (s != HYMBA_OK) return s;
+  return hymba_layer_decode(d, w, x_new, y, cache, shared_cache, ws, HYMBA_STATIC_SCRATCH_BYTES, dev_status, stream);
+}

@@ -209,6 +209,39 @@ HYMBA_API hymba_status hymba_layer_decode(const hymba_layer_desc* d, const hymba
                                 const hymba_cache* shared_cache, void* ws, size_t ws_bytes,
                                 int32_t* dev_status, void* stream);
 
+/* Size of the library's built-in decode scratch buffer (32 MiB), used by
+ * hymba_layer_decode_static.                                                */
+#define HYMBA_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* hymba_layer_decode for callers that cannot allocate device memory.  No
+ * counterpart in the paper: it exists for integration only.
+ *
+ * Some callers cannot call cudaMalloc at the point where they run a decode
+ * step: a plugin inside a host framework that owns all device memory and
+ * hands out none, or a serving loop whose memory is fully reserved by its
+ * KV-cache pool and where cudaMalloc would fail or stall the device.  This
+ * entry point takes the same arguments as hymba_layer_decode minus the
+ * workspace: its scratch lives in one statically sized device buffer that the
+ * library declares (HYMBA_STATIC_SCRATCH_BYTES per GPU that loads the
+ * library, held until the process exits).  It allocates nothing.
+ *   - Shapes whose decode workspace (hymba_layer_decode_workspace) exceeds
+ *     HYMBA_STATIC_SCRATCH_BYTES are rejected with HYMBA_ERR_WORKSPACE before
+ *     anything is launched.  The 1.5B-shaped decode at batch 128 needs about
+ *     23 MiB.
+ *   - The first call on a device looks up that device's address of the
+ *     buffer (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.
+ *   - Every call, on every stream, uses the same buffer: calls whose
+ *     execution overlaps on the GPU race on it and give wrong results.
+ *     Serialise them (one stream, or events).  The buffer keeps the last
+ *     call's contents; the decode step writes every scratch byte it reads, so
+ *     nothing has to start at zero.
+ * Other arguments, errors and effects are those of hymba_layer_decode.       */
+HYMBA_API hymba_status hymba_layer_decode_static(const hymba_layer_desc* d, const hymba_layer_weights* w,
+                                                 const void* x_new, float* y, const hymba_cache* cache,
+                                                 const hymba_cache* shared_cache, int32_t* dev_status,
+                                                 void* stream);
+
 /* Human-readable name of a status code (static storage).                    */
 HYMBA_API const char* hymba_status_str(hymba_status s);
 
