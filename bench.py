@@ -393,6 +393,16 @@ def run_decode(args, torch, hb, hl, dev, stream, peaks, peak_src):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    # per-stage times from one instrumented pass
+    evs = make_events(torch, 12)
+    evp = ctypes_array(evs)
+    for _ in range(3):
+        hb.hymba_layer_decode_events(layer.desc, layer.weights, xn, y, cc, layer.ws, evp, 12, status=layer.status,
+                                     stream=stream)
+    torch.cuda.synchronize()
+    dstages = ["convert", "in_proj", "kv_append", "attention", "conv", "x_proj", "dt_proj", "scan", "fuse_norm",
+               "out_proj", "pos"]
+    stage_us = {nm: round(evs[k].elapsed_time(evs[k + 1]) * 1e3, 2) for k, nm in enumerate(dstages)}
     n = max(10, args.steps * 5)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
@@ -429,7 +439,7 @@ def run_decode(args, torch, hb, hl, dev, stream, peaks, peak_src):
     gbs = nbytes / (best * 1e-6) / 1e9
     return {"workload": "decode step, batch 128, 8192 cached tokens (1024-slot ring + 128 meta), 1.5B shapes",
             "value": round(s.B / (best * 1e-6), 1), "unit": "tokens/s", "us_per_step": round(us, 2),
-            "us_per_step_graph": round(g_us, 2) if isinstance(g_us, float) else g_us,
+            "us_per_step_graph": round(g_us, 2) if isinstance(g_us, float) else g_us, "stage_us": stage_us,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes,
                          "peak_source": f"{peak_src} HBM copy"},

@@ -81,6 +81,9 @@ def lib() -> ctypes.CDLL:
     L.hymba_layer_decode.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache), P(Cache),
                                      c_void_p, c_size_t, c_void_p, c_void_p]
     L.hymba_layer_decode.restype = c_int32
+    L.hymba_layer_decode_events.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache), P(Cache),
+                                            c_void_p, c_size_t, c_void_p, c_void_p, c_int32, c_void_p]
+    L.hymba_layer_decode_events.restype = c_int32
     L.hymba_layer_decode_static.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache),
                                             P(Cache), c_void_p, c_void_p]
     L.hymba_layer_decode_static.restype = c_int32
@@ -90,6 +93,9 @@ def lib() -> ctypes.CDLL:
     L.hymba_test_scan.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     L.hymba_test_scan.restype = c_int32
+    L.hymba_test_scan_fused.argtypes = [c_int32] * 5 + [c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_int32] + \
+        [c_void_p] * 8
+    L.hymba_test_scan_fused.restype = c_int32
     L.hymba_test_attention.argtypes = [c_int32] * 9 + [c_void_p] * 6
     L.hymba_test_attention.restype = c_int32
     L.hymba_test_wait_timeout.argtypes = [c_uint32, c_void_p, c_void_p]
@@ -193,6 +199,18 @@ def hymba_layer_decode(desc: LayerDesc, weights: LayerWeights, x_new, y, cache: 
     return _check(rc, "hymba_layer_decode") if check else rc
 
 
+def hymba_layer_decode_events(desc: LayerDesc, weights: LayerWeights, x_new, y, cache: Cache, ws, events,
+                              n_events: int, shared_cache: Optional[Cache] = None, status=None, stream=None,
+                              check: bool = True) -> int:
+    """hymba_layer_decode that records per-stage CUDA events."""
+    rc = lib().hymba_layer_decode_events(ctypes.byref(desc), ctypes.byref(weights), _ptr(x_new), _ptr(y),
+                                         ctypes.byref(cache),
+                                         ctypes.byref(shared_cache) if shared_cache is not None else None,
+                                         _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), events, n_events,
+                                         _stream(stream))
+    return _check(rc, "hymba_layer_decode_events") if check else rc
+
+
 STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
@@ -221,6 +239,15 @@ def hymba_test_scan(u, z, delta, BC, A_log, D, g, h_out=None, stream=None) -> in
     N = A_log.shape[1]
     return lib().hymba_test_scan(B, L, di, N, _ptr(u), u.stride(1), _ptr(z), z.stride(1), _ptr(delta),
                                  _ptr(BC), _ptr(A_log), _ptr(D), _ptr(g), _ptr(h_out), _stream(stream))
+
+
+def hymba_test_scan_fused(u, z, dtr, W_dt, dt_bias, BC, A_log, D, g, h_out=None, stream=None) -> int:
+    B, L, di = u.shape
+    N = A_log.shape[1]
+    R = W_dt.shape[1]
+    return lib().hymba_test_scan_fused(B, L, di, N, R, _ptr(u), u.stride(1), _ptr(z), z.stride(1), _ptr(dtr),
+                                       dtr.stride(1), _ptr(W_dt), _ptr(dt_bias), _ptr(BC), _ptr(A_log), _ptr(D),
+                                       _ptr(g), _ptr(h_out), _stream(stream))
 
 
 def hymba_test_attention(Q, K, V, O, M: int, window: int, use_tc: bool, status=None, stream=None) -> int:

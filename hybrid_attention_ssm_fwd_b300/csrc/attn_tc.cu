@@ -247,38 +247,42 @@ __global__ void __launch_bounds__(192, 1)
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
         float s[BKV];
+        {
+          uint32_t rr[4][32];
 #pragma unroll
-        for (int c = 0; c < BKV / 32; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(lane_base + sb * BKV + c * 32, rr);
+          for (int c = 0; c < BKV / 32; ++c) tmem_ld32(lane_base + sb * BKV + c * 32, rr[c]);
           tc_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(rr[e]);
+          for (int c = 0; c < BKV / 32; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(rr[c][e]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_SEMPTY0 + sb));
-        // mask + scale
+        // mask (raw scores; the positive scale is applied inside the exp2 below)
         const int k0 = tile_kt(U, t) * BKV;
         const bool full_vis = (k0 + BKV - 1 <= U.q0) && (k0 + BKV <= p.L) &&
                               (p.window == 0 || k0 + BKV <= p.M || (U.qv1 - 1) - max(k0, p.M) < p.window);
-        float mt = -INFINITY;
-        if (full_vis) {
+        if (!full_vis) {
+          // key e of this tile (j = k0 + e) is visible iff e <= hi and (e >= lo or e < ml)
+          const int hi = min(i, p.L - 1) - k0;
+          const int lo = p.window > 0 ? i - p.window + 1 - k0 : -BKV;
+          const int ml = p.M - k0;
 #pragma unroll
           for (int e = 0; e < BKV; ++e) {
-            s[e] *= p.scale_log2;
-            mt = fmaxf(mt, s[e]);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < BKV; ++e) {
-            const int j = k0 + e;
-            const bool vis = (j <= i) && (j < p.L) && (p.window == 0 || i - j < p.window || j < p.M);
-            s[e] = vis ? s[e] * p.scale_log2 : -INFINITY;
-            mt = fmaxf(mt, s[e]);
+            const bool vis = (e <= hi) && (e >= lo || e < ml);
+            s[e] = vis ? s[e] : -INFINITY;
           }
         }
-        // running max: raise it on the first tile, or when the tile exceeds it by > 2^8
+        float mp[8];
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) mp[q8] = s[q8];
+#pragma unroll
+        for (int e = 8; e < BKV; ++e) mp[e & 7] = fmaxf(mp[e & 7], s[e]);
+        const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * p.scale_log2;
+        // running max (log2 units): set on the first tile; raised only when a tile exceeds it by > 2^8
         bool need = (t == 0) ? true : (mt > m_run + kRescaleLog2);
         if (t > 0 && __any_sync(0xffffffffu, need)) {
           const float m_new = fmaxf(m_run, mt);
@@ -303,19 +307,21 @@ __global__ void __launch_bounds__(192, 1)
         } else if (t == 0) {
           m_run = mt;
         }
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
         // P buffer sb is free once PV of tile jt-2 completed
         const bool g3 = mbar_wait(bar(B_PVDONE0 + sb), ((jt >> 1) & 1) ^ 1, wc);
         if (!__all_sync(0xffffffffu, g3)) { ok = false; break; }
         const uint32_t prow = sP + sb * Cfg::P_BYTES + r * 128;
-        float lsum = 0.f;
+        float ls[8];
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) ls[q8] = 0.f;
 #pragma unroll
         for (int c = 0; c < BKV / 8; ++c) {  // 16 chunks of 8 keys (16 bytes)
           float pv[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            pv[e] = ex2_approx(s[c * 8 + e] - m_use);
-            lsum += pv[e];
+            pv[e] = ex2_approx(fmaf(s[c * 8 + e], p.scale_log2, neg_m));
+            ls[e] += pv[e];
           }
           const uint32_t w0 = pack_half2(pv[0], pv[1]), w1 = pack_half2(pv[2], pv[3]);
           const uint32_t w2 = pack_half2(pv[4], pv[5]), w3 = pack_half2(pv[6], pv[7]);
@@ -324,6 +330,7 @@ __global__ void __launch_bounds__(192, 1)
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
                        : "memory");
         }
+        const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         l_run += lsum;
         fence_proxy_async_smem();
         tc_fence_before();

@@ -248,12 +248,61 @@ HY_DEV float silu_f(float v) { return v / (1.0f + __expf(-v)); }
 
 HY_DEV float softplus_f(float v) { return v > 20.0f ? v : log1pf(__expf(v)); }
 
+HY_DEV float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// softplus(v) = ln(1 + e^v) with two SFU operations: for e = e^v < 1/16 the
+// series e - e^2/2 + e^3/3 - e^4/4 (relative error < e^4/5 < 3e-6), otherwise
+// ln2 * log2(1 + e) (1 + e >= 1.0625 keeps the relative error near 1e-6).
+HY_DEV float softplus_fast(float v) {
+  if (v > 15.0f) return v;
+  const float e = ex2_approx(v * 1.4426950408889634f);
+  const float series = e * fmaf(-e, fmaf(-e, fmaf(-e, 0.25f, 0.33333334f), 0.5f), 1.0f);
+  const float lg = lg2_approx(1.0f + e) * 0.6931471805599453f;
+  return e < 0.0625f ? series : lg;
+}
+
 HY_DEV uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
 constexpr float kHalfMax = 65504.0f;
+
+// Packed fp32 pair arithmetic (one f32x2 instruction for two lanes of work).
+HY_DEV uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+HY_DEV float2 up2(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+HY_DEV uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+HY_DEV uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// D(16x8 fp32) += A(16x16 fp16, row) * B(16x8 fp16, col): warp-level MMA for
+// small contractions fused into SIMT kernels.
+HY_DEV void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
 }  // namespace hy
 

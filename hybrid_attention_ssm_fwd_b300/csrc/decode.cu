@@ -125,6 +125,272 @@ __global__ void __launch_bounds__(128) decode_attention_kernel(int B, int M, int
   }
 }
 
+// Split-KV decode attention for bf16 caches.  One CTA per (sequence b, KV
+// group g, key split sp) serves all G = Hq/Hkv query heads of the group, so
+// each K/V row of the cache is read once per step.  Keys 0..M-1 are the meta
+// prefix, keys M.. the visible ring entries (newest first).  Each thread
+// scores whole keys (16-byte K loads); P.V walks the keys with the threads
+// spread over the value dims.  Output: per (b, head, split) the partial
+// max m (log2 units), sum l and unnormalised o[dv], all fp32.
+constexpr int DA_THREADS = 128;
+constexpr int DA_MAXG = 8;
+
+__global__ void __launch_bounds__(DA_THREADS)
+    decode_attn_split_kernel(int M, int Hq, int Hkv, int dh, int dv, int window, int cap, int nsplit,
+                             const __half* __restrict__ q, long long ldq, const __nv_bfloat16* __restrict__ k_meta,
+                             const __nv_bfloat16* __restrict__ v_meta, const __nv_bfloat16* __restrict__ k_ring,
+                             const __nv_bfloat16* __restrict__ v_ring, const int32_t* __restrict__ pos,
+                             float* __restrict__ part) {
+  extern __shared__ float sm[];
+  const int G = Hq / Hkv;
+  const int sp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int p = pos[b];
+  const int n_vis = min(window > 0 ? min(p + 1, window) : p + 1, cap);
+  const int n_keys = M + n_vis;
+  const int per = (n_keys + nsplit - 1) / nsplit;
+  const int k_lo = sp * per, k_hi = min(n_keys, k_lo + per);
+  const int nk = max(0, k_hi - k_lo);
+  float* qs = sm;                       // [G][dh], pre-scaled by log2(e)/sqrt(dh)
+  float* sc = sm + DA_MAXG * 128;       // [G][per]
+  float* red = sc + G * per;            // [2][G][4]
+  const float qscale = 1.4426950408889634f * rsqrtf(static_cast<float>(dh));
+  for (int idx = tid; idx < G * dh; idx += DA_THREADS) {
+    const int hh = idx / dh, e = idx % dh;
+    qs[idx] = __half2float(q[b * ldq + (g * G + hh) * dh + e]) * qscale;
+  }
+  __syncthreads();
+  const long long wk = static_cast<long long>(Hkv) * dh, wv = static_cast<long long>(Hkv) * dv;
+  auto krow = [&](int j) -> const __nv_bfloat16* {
+    if (j < M) return k_meta + j * wk + g * dh;
+    const int rel = j - M;  // 0 = this token
+    const int slot = window > 0 ? (p - rel) % cap : p - rel;
+    return k_ring + (static_cast<long long>(b) * cap + slot) * wk + g * dh;
+  };
+  auto vrow = [&](int j) -> const __nv_bfloat16* {
+    if (j < M) return v_meta + j * wv + g * dv;
+    const int rel = j - M;
+    const int slot = window > 0 ? (p - rel) % cap : p - rel;
+    return v_ring + (static_cast<long long>(b) * cap + slot) * wv + g * dv;
+  };
+  // scores
+  float lmax[DA_MAXG];
+#pragma unroll
+  for (int hh = 0; hh < DA_MAXG; ++hh) lmax[hh] = -INFINITY;
+  for (int kk = tid; kk < nk; kk += DA_THREADS) {
+    const uint4* kr = reinterpret_cast<const uint4*>(krow(k_lo + kk));
+    float acc[DA_MAXG];
+#pragma unroll
+    for (int hh = 0; hh < DA_MAXG; ++hh) acc[hh] = 0.f;
+    for (int c = 0; c < dh / 8; ++c) {
+      const uint4 v = kr[c];
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        const float2 f = __bfloat1622float2(h2[e2]);
+#pragma unroll
+        for (int hh = 0; hh < DA_MAXG; ++hh)
+          if (hh < G) acc[hh] = fmaf(qs[hh * dh + c * 8 + 2 * e2 + 1], f.y, fmaf(qs[hh * dh + c * 8 + 2 * e2], f.x, acc[hh]));
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < DA_MAXG; ++hh)
+      if (hh < G) {
+        sc[hh * per + kk] = acc[hh];
+        lmax[hh] = fmaxf(lmax[hh], acc[hh]);
+      }
+  }
+  // block max per head
+  const int w = tid >> 5, l = tid & 31;
+#pragma unroll
+  for (int hh = 0; hh < DA_MAXG; ++hh) {
+    if (hh >= G) break;
+    float v = lmax[hh];
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (l == 0) red[hh * 4 + w] = v;
+  }
+  __syncthreads();
+  // probabilities and sums
+  float lsum[DA_MAXG];
+  float mh[DA_MAXG];
+#pragma unroll
+  for (int hh = 0; hh < DA_MAXG; ++hh) {
+    lsum[hh] = 0.f;
+    mh[hh] = hh < G ? fmaxf(fmaxf(red[hh * 4], red[hh * 4 + 1]), fmaxf(red[hh * 4 + 2], red[hh * 4 + 3])) : 0.f;
+  }
+  for (int kk = tid; kk < nk; kk += DA_THREADS) {
+#pragma unroll
+    for (int hh = 0; hh < DA_MAXG; ++hh)
+      if (hh < G) {
+        const float e = ex2_approx(sc[hh * per + kk] - mh[hh]);
+        sc[hh * per + kk] = e;
+        lsum[hh] += e;
+      }
+  }
+  float* red2 = red + G * 4;
+#pragma unroll
+  for (int hh = 0; hh < DA_MAXG; ++hh) {
+    if (hh >= G) break;
+    float v = lsum[hh];
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (l == 0) red2[hh * 4 + w] = v;
+  }
+  __syncthreads();
+  // P.V: a thread owns a pair of value dims for one key phase; with dv/2 < 128
+  // pairs the threads split the keys into nkh phases merged through smem
+  const int npairs = dv / 2;
+  const int nkh = max(1, DA_THREADS / npairs);
+  float* ored = red2 + G * 4;  // [nkh][G][dv]
+  for (int pr0 = 0; pr0 < npairs; pr0 += DA_THREADS) {
+    const int pr = pr0 + tid % npairs;
+    const int kh = (npairs >= DA_THREADS) ? 0 : tid / npairs;
+    const bool act = pr < npairs && kh < nkh;
+    const int e = 2 * pr;
+    float o0[DA_MAXG], o1[DA_MAXG];
+#pragma unroll
+    for (int hh = 0; hh < DA_MAXG; ++hh) o0[hh] = o1[hh] = 0.f;
+    if (act) {
+      for (int kk = kh; kk < nk; kk += nkh) {
+        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vrow(k_lo + kk) + e));
+#pragma unroll
+        for (int hh = 0; hh < DA_MAXG; ++hh)
+          if (hh < G) {
+            const float pp = sc[hh * per + kk];
+            o0[hh] = fmaf(pp, v.x, o0[hh]);
+            o1[hh] = fmaf(pp, v.y, o1[hh]);
+          }
+      }
+      if (nkh > 1) {
+#pragma unroll
+        for (int hh = 0; hh < DA_MAXG; ++hh)
+          if (hh < G) {
+            ored[(kh * G + hh) * dv + e] = o0[hh];
+            ored[(kh * G + hh) * dv + e + 1] = o1[hh];
+          }
+      }
+    }
+    if (nkh > 1) {
+      __syncthreads();
+      for (int idx = tid; idx < G * dv; idx += DA_THREADS) {
+        const int hh = idx / dv, ee = idx % dv;
+        float acc = 0.f;
+        for (int q2 = 0; q2 < nkh; ++q2) acc += ored[(q2 * G + hh) * dv + ee];
+        part[((static_cast<long long>(b) * Hq + g * G + hh) * nsplit + sp) * (dv + 2) + 2 + ee] = acc;
+      }
+    } else if (act) {
+#pragma unroll
+      for (int hh = 0; hh < DA_MAXG; ++hh)
+        if (hh < G) {
+          float* dst = part + ((static_cast<long long>(b) * Hq + g * G + hh) * nsplit + sp) * (dv + 2);
+          dst[2 + e] = o0[hh];
+          dst[3 + e] = o1[hh];
+        }
+    }
+  }
+  if (tid < G) {
+    const int hh = tid;
+    float* dst = part + ((static_cast<long long>(b) * Hq + g * G + hh) * nsplit + sp) * (dv + 2);
+    dst[0] = nk > 0 ? mh[hh] : -INFINITY;
+    dst[1] = red2[hh * 4] + red2[hh * 4 + 1] + red2[hh * 4 + 2] + red2[hh * 4 + 3];
+  }
+}
+
+// Merges the splits of each (b, head): o = sum_s 2^(m_s - m) o_s / sum_s 2^(m_s - m) l_s.
+__global__ void decode_attn_combine_kernel(int Hq, int dv, int nsplit, const float* __restrict__ part,
+                                           __half* __restrict__ out, long long ldo) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const float* pp = part + (static_cast<long long>(b) * Hq + h) * nsplit * (dv + 2);
+  float m = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) m = fmaxf(m, pp[s * (dv + 2)]);
+  float den = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float ms = pp[s * (dv + 2)];
+    if (ms != -INFINITY) den += ex2_approx(ms - m) * pp[s * (dv + 2) + 1];
+  }
+  const float inv = 1.0f / den;
+  for (int e = threadIdx.x; e < dv; e += blockDim.x) {
+    float num = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+      const float ms = pp[s * (dv + 2)];
+      if (ms != -INFINITY) num += ex2_approx(ms - m) * pp[s * (dv + 2) + 2 + e];
+    }
+    out[b * ldo + h * dv + e] = __float2half_rn(num * inv);
+  }
+}
+
+// One decode step of the SSM branch with the dt projection fused: per
+// (sequence b, channel c) thread,
+//   delta = softplus(dt[b] . W_dt[c] + bias[c]),  h = exp(delta A) h + delta u B[b],
+//   y = C[b] . h + D u,  g = y silu(z);  the state is updated in place.
+// A block owns 128 channels for DS_BB sequences; the W_dt rows of its
+// channels and the dt / B / C rows of its sequences sit in shared memory.
+constexpr int DS_THREADS = 128;
+constexpr int DS_BB = 8;
+
+template <int N>
+__global__ void __launch_bounds__(DS_THREADS)
+    decode_ssm_step_kernel(int B, int di, int R, const __half* __restrict__ u, long long ldu,
+                           const __half* __restrict__ z, long long ldz, const __half* __restrict__ dtr,
+                           long long ld_dtr, const float* __restrict__ BC, const __nv_bfloat16* __restrict__ W_dt,
+                           const float* __restrict__ dt_bias, const float* __restrict__ A_log,
+                           const float* __restrict__ D, float* __restrict__ state, __half* __restrict__ g,
+                           long long ldg) {
+  extern __shared__ float sm[];
+  float* sW = sm;                           // [DS_THREADS][R + 1]
+  float* sdt = sW + DS_THREADS * (R + 1);   // [DS_BB][R]
+  float* sbc = sdt + DS_BB * R;             // [DS_BB][2N]
+  const int c0 = blockIdx.x * DS_THREADS;
+  const int b0 = blockIdx.y * DS_BB;
+  const int tid = threadIdx.x;
+  for (int idx = tid; idx < DS_THREADS * R; idx += DS_THREADS) {
+    const int cc = idx / R, r = idx % R;
+    sW[cc * (R + 1) + r] = (c0 + cc < di) ? __bfloat162float(W_dt[static_cast<long long>(c0 + cc) * R + r]) : 0.f;
+  }
+  for (int idx = tid; idx < DS_BB * R; idx += DS_THREADS) {
+    const int bb = idx / R, r = idx % R;
+    sdt[idx] = (b0 + bb < B) ? __half2float(dtr[(b0 + bb) * ld_dtr + r]) : 0.f;
+  }
+  for (int idx = tid; idx < DS_BB * 2 * N; idx += DS_THREADS) {
+    const int bb = idx / (2 * N);
+    sbc[idx] = (b0 + bb < B) ? BC[(b0 + bb) * 2 * N + idx % (2 * N)] : 0.f;
+  }
+  __syncthreads();
+  const int c = c0 + tid;
+  if (c >= di) return;
+  float A2[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) A2[n] = -__expf(A_log[c * N + n]) * 1.4426950408889634f;
+  const float bias = dt_bias[c], Dc = D[c];
+  const float* wr = sW + tid * (R + 1);
+  for (int bb = 0; bb < DS_BB; ++bb) {
+    const int b = b0 + bb;
+    if (b >= B) break;
+    float acc = bias;
+    for (int r = 0; r < R; ++r) acc = fmaf(sdt[bb * R + r], wr[r], acc);
+    const float dt = softplus_fast(acc);
+    const float uu = __half2float(u[b * ldu + c]);
+    const float du = dt * uu;
+    float4* hp = reinterpret_cast<float4*>(state + (static_cast<long long>(b) * di + c) * N);
+    float h[N];
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+      const float4 v = hp[q];
+      h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
+    }
+    float y = 0.f;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      h[n] = fmaf(ex2_approx(dt * A2[n]), h[n], du * sbc[bb * 2 * N + n]);
+      y = fmaf(sbc[bb * 2 * N + N + n], h[n], y);
+    }
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) hp[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+    y = fmaf(Dc, uu, y);
+    const float zz = __half2float(z[b * ldz + c]);
+    g[b * ldg + c] = __float2half_rn(y * zz / (1.0f + __expf(-zz)));
+  }
+}
+
 template <typename T>
 __global__ void conv_step_kernel(int B, int di, int k, const T* x, long long ldx, const float* w,
                                  const float* bias, float* conv_state, T* u, long long ldu) {
@@ -204,6 +470,54 @@ hymba_status splitk_reduce(int splits, int rows, int N, const float* part, long 
   const long long n = static_cast<long long>(rows) * N;
   splitk_reduce_kernel<<<static_cast<unsigned>(std::min<long long>((n + 255) / 256, 148 * 8)), 256, 0, st>>>(
       splits, rows, N, part, ldp, epi, R, dtr, ldd, C, ldc, resid, ld_resid, accumulate ? 1 : 0);
+  return last_err();
+}
+
+bool decode_attn_split_supported(int Hq, int Hkv, int dh, int dv) {
+  return Hq / Hkv <= DA_MAXG && dh <= 128 && dh % 8 == 0 && dv % 2 == 0 && dv <= 512;
+}
+
+size_t decode_attn_split_scratch(int B, int Hq, int dv, int nsplit) {
+  return static_cast<size_t>(B) * Hq * nsplit * (dv + 2) * sizeof(float);
+}
+
+hymba_status decode_attention_split(int B, int M, int Hq, int Hkv, int dh, int dv, int window, int cap, int nsplit,
+                                    const __half* q, long long ldq, const __nv_bfloat16* k_meta,
+                                    const __nv_bfloat16* v_meta, const __nv_bfloat16* k_ring,
+                                    const __nv_bfloat16* v_ring, const int32_t* pos, float* part, __half* out,
+                                    long long ldo, int max_keys, cudaStream_t st) {
+  if (!decode_attn_split_supported(Hq, Hkv, dh, dv)) return HYMBA_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  const int per = (max_keys + nsplit - 1) / nsplit;
+  const int nkh = std::max(1, DA_THREADS / (dv / 2));
+  const size_t smem =
+      (DA_MAXG * 128 + static_cast<size_t>(G) * per + 2 * G * 4 + static_cast<size_t>(nkh) * G * dv) * sizeof(float);
+  if (smem > 200 * 1024) return HYMBA_ERR_UNSUPPORTED;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(decode_attn_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
+  decode_attn_split_kernel<<<dim3(nsplit, Hkv, B), DA_THREADS, smem, st>>>(
+      M, Hq, Hkv, dh, dv, window, cap, nsplit, q, ldq, k_meta, v_meta, k_ring, v_ring, pos, part);
+  decode_attn_combine_kernel<<<dim3(Hq, B), 128, 0, st>>>(Hq, dv, nsplit, part, out, ldo);
+  return last_err();
+}
+
+bool decode_ssm_step_supported(int N, int R) { return N == 16 && R <= 256; }
+
+hymba_status decode_ssm_step(int B, int di, int N, int R, const __half* u, long long ldu, const __half* z,
+                             long long ldz, const __half* dtr, long long ld_dtr, const float* BC,
+                             const __nv_bfloat16* W_dt, const float* dt_bias, const float* A_log, const float* D,
+                             float* state, __half* g, long long ldg, cudaStream_t st) {
+  if (!decode_ssm_step_supported(N, R)) return HYMBA_ERR_UNSUPPORTED;
+  const size_t smem = (static_cast<size_t>(DS_THREADS) * (R + 1) + DS_BB * R + DS_BB * 2 * N) * sizeof(float);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(decode_ssm_step_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
+  dim3 grid((di + DS_THREADS - 1) / DS_THREADS, (B + DS_BB - 1) / DS_BB);
+  decode_ssm_step_kernel<16><<<grid, DS_THREADS, smem, st>>>(B, di, R, u, ldu, z, ldz, dtr, ld_dtr, BC, W_dt,
+                                                               dt_bias, A_log, D, state, g, ldg);
   return last_err();
 }
 

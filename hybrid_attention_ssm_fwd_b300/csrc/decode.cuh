@@ -35,6 +35,25 @@ hymba_status splitk_reduce(int splits, int rows, int N, const float* part, long 
                            __half* dtr, long long ldd, float* C, long long ldc, const __nv_bfloat16* resid,
                            long long ld_resid, bool accumulate, cudaStream_t st);
 
+// Split-KV decode attention over bf16 caches (one CTA per sequence, KV group
+// and key split; all query heads of a group share each K/V read), followed by
+// the merge of the splits into out (fp16).  `part` is scratch of
+// decode_attn_split_scratch() bytes; max_keys bounds M + visible ring entries.
+bool decode_attn_split_supported(int Hq, int Hkv, int dh, int dv);
+size_t decode_attn_split_scratch(int B, int Hq, int dv, int nsplit);
+hymba_status decode_attention_split(int B, int M, int Hq, int Hkv, int dh, int dv, int window, int cap, int nsplit,
+                                    const __half* q, long long ldq, const __nv_bfloat16* k_meta,
+                                    const __nv_bfloat16* v_meta, const __nv_bfloat16* k_ring,
+                                    const __nv_bfloat16* v_ring, const int32_t* pos, float* part, __half* out,
+                                    long long ldo, int max_keys, cudaStream_t st);
+
+// Decode step of the SSM branch with the dt projection fused (see decode.cu).
+bool decode_ssm_step_supported(int N, int R);
+hymba_status decode_ssm_step(int B, int di, int N, int R, const __half* u, long long ldu, const __half* z,
+                             long long ldz, const __half* dtr, long long ld_dtr, const float* BC,
+                             const __nv_bfloat16* W_dt, const float* dt_bias, const float* A_log, const float* D,
+                             float* state, __half* g, long long ldg, cudaStream_t st);
+
 hymba_status pos_increment(int B, int32_t* pos, cudaStream_t st);
 
 }  // namespace hy

@@ -67,19 +67,24 @@ HY_DEV void store_f16x32(__half* dst, const float (&v)[32], int valid) {
   }
 }
 
-HY_DEV void store_f32xn(float* dst, const float* v, int n, int valid) {
-  if (valid >= n && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-    for (int g = 0; g < n; g += 4)
+// 32 fp32 values; `valid` leading columns are inside N.  Compile-time
+// indices only, so v stays in registers.
+HY_DEV void store_f32x32(float* dst, const float (&v)[32], int valid) {
+  if (valid >= 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+    for (int g = 0; g < 32; g += 4)
       *reinterpret_cast<float4*>(dst + g) = make_float4(v[g], v[g + 1], v[g + 2], v[g + 3]);
   } else {
-    for (int j = 0; j < n; ++j)
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
       if (j < valid) dst[j] = v[j];
   }
 }
 
-HY_DEV bool any_over_half(const float* v, int n) {
+HY_DEV bool any_over_half(const float (&v)[32]) {
   bool o = false;
-  for (int j = 0; j < n; ++j) o |= !(fabsf(v[j]) <= kHalfMax);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) o |= !(fabsf(v[j]) <= kHalfMax);
   return o;
 }
 
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(192, 1)
             v1[j] = __uint_as_float(r1[j]);
           }
           if (col < p.rope_cols) {
-#pragma unroll 4
+#pragma unroll
             for (int j = 0; j < 32; ++j) {
               float sn, cs;
               sincosf(static_cast<float>(posn) * rope_tab[j], &sn, &cs);
@@ -235,7 +240,7 @@ __global__ void __launch_bounds__(192, 1)
               v1[j] = x2 * cs + x1 * sn;
             }
           }
-          over |= any_over_half(v0, 32) | any_over_half(v1, 32);
+          over |= any_over_half(v0) | any_over_half(v1);
           if (row_ok) {
             __half* dst = reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col;
             store_f16x32(dst, v0, p.N - col);
@@ -266,25 +271,27 @@ __global__ void __launch_bounds__(192, 1)
           const int valid = min(nv, p.N - col);
           if (!row_ok) continue;
           if (EPI == EPI_F16) {
-            over |= any_over_half(v, nv);
+            over |= any_over_half(v);
             store_f16x32(reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col, v,
                          valid);
           } else if (EPI == EPI_XPROJ) {
-            for (int j = 0; j < valid; ++j) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
               const int cj = col + j;
-              if (cj < p.xproj_R) {
-                over |= !(fabsf(v[j]) <= kHalfMax);
-                reinterpret_cast<__half*>(p.C2)[static_cast<long long>(row) * p.ldc2 + cj] = __float2half_rn(v[j]);
-              } else {
-                reinterpret_cast<float*>(p.C)[static_cast<long long>(row) * p.ldc + (cj - p.xproj_R)] = v[j];
+              if (j < valid) {
+                if (cj < p.xproj_R) {
+                  over |= !(fabsf(v[j]) <= kHalfMax);
+                  reinterpret_cast<__half*>(p.C2)[static_cast<long long>(row) * p.ldc2 + cj] = __float2half_rn(v[j]);
+                } else {
+                  reinterpret_cast<float*>(p.C)[static_cast<long long>(row) * p.ldc + (cj - p.xproj_R)] = v[j];
+                }
               }
             }
           } else if (EPI == EPI_SOFTPLUS) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (j < valid) v[j] = softplus_f(v[j] + p.bias[col + j]);
-            store_f32xn(reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col, v, nv,
-                        valid);
+            store_f32x32(reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col, v, valid);
           } else if (EPI == EPI_F32) {
             if (p.resid) {
               const __nv_bfloat16* rr = p.resid + static_cast<long long>(row) * p.ld_resid + col;
@@ -297,12 +304,11 @@ __global__ void __launch_bounds__(192, 1)
               for (int j = 0; j < 32; ++j)
                 if (j < valid) v[j] += rr[j];
             }
-            store_f32xn(reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col, v, nv,
-                        valid);
+            store_f32x32(reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col, v, valid);
           } else {  // EPI_PARTIAL
             float* dst = reinterpret_cast<float*>(p.C) +
                          (static_cast<long long>(c.split) * p.M + row) * p.ldc + col;
-            store_f32xn(dst, v, nv, valid);
+            store_f32x32(dst, v, valid);
           }
         }
       }

@@ -91,8 +91,15 @@ hymba_status check_desc(const hymba_layer_desc* d, bool decode, Dims* o) {
 
 // Workspace plan: byte offsets of each scratch buffer (256-byte aligned).
 struct Plan {
-  size_t proj, u, dtr, bc, delta, att, g, s, wout, wx, wdt, part, total;
+  size_t proj, u, dtr, bc, delta, att, g, s, wout, wx, wdt, part, apart, total;
+  int attn_splits;
 };
+
+// Key splits of the decode attention: enough CTAs for ~4 per SM.
+int decode_attn_splits(const Dims& x) {
+  const int ctas = x.B * x.Hkv;
+  return std::max(1, std::min(16, (4 * 148 + ctas - 1) / ctas));
+}
 
 constexpr int kDecodeSplitsX = 25;
 constexpr int kDecodeSplitsOut = 5;
@@ -111,7 +118,9 @@ Plan plan_ws(const Dims& x, bool decode) {
   p.u = take(r * x.di * e);
   p.dtr = take(r * (x.dtype == HYMBA_BF16 ? x.Rp : x.R) * e);
   p.bc = take(r * 2 * x.N * 4);
-  p.delta = take(r * x.di * 4);
+  // the bf16 prefill computes delta inside the scan when it can
+  const bool fused = x.dtype == HYMBA_BF16 && !decode && scan_fused_supported(x.di, x.N, x.R);
+  p.delta = fused ? 0 : take(r * x.di * 4);
   p.att = take(r * x.di * e);
   p.g = take(r * x.di * e);
   p.s = take(r * x.di * e);
@@ -123,6 +132,8 @@ Plan plan_ws(const Dims& x, bool decode) {
       const size_t w1 = static_cast<size_t>(kDecodeSplitsX) * r * ((x.xo + 15) / 16 * 16);
       const size_t w2 = static_cast<size_t>(kDecodeSplitsOut) * r * x.d;
       p.part = take(std::max(w1, w2) * 4);
+      p.attn_splits = decode_attn_splits(x);
+      p.apart = take(decode_attn_split_scratch(x.B, x.Hq, x.dv, p.attn_splits));
     }
   }
   p.total = off;
@@ -340,17 +351,23 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     TRY(gemm_tc(0, u, x.di, at<__half>(ws, pl.wx), x.di, EPI_XPROJ, p, 0, 1, sms, st));
   }
   mk.mark();
-  {
+  float* h_out = cache_out ? cache_out->ssm_state : nullptr;
+  if (scan_fused_supported(x.di, x.N, x.R)) {
+    // dt projection + softplus run inside the scan (no delta in HBM)
+    mk.mark();
+    TRY(scan_fused_f16(x.B, x.L, x.di, x.N, x.R, u, x.di, proj + x.z_col, x.P_in, dtr, x.Rp,
+                       static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, bc, w->A_log, w->D, g, nullptr, h_out,
+                       status, x.wait_ns, st));
+  } else {
     GemmParams p = gp(rows, x.di, x.R, status, x.wait_ns);
     p.C = delta;
     p.ldc = x.di;
     p.bias = w->dt_bias;
     TRY(gemm_tc(0, dtr, x.Rp, at<__half>(ws, pl.wdt), x.Rp, EPI_SOFTPLUS, p, 0, 1, sms, st));
+    mk.mark();
+    TRY(scan_f16(x.B, x.L, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, bc, w->A_log, w->D, g, nullptr, h_out,
+                 status, x.wait_ns, st));
   }
-  mk.mark();
-  float* h_out = cache_out ? cache_out->ssm_state : nullptr;
-  TRY(scan_f16(x.B, x.L, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, bc, w->A_log, w->D, g, nullptr, h_out,
-               status, x.wait_ns, st));
   mk.mark();
   // fuse + out_proj
   TRY(fuse_norm<__half>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
@@ -417,7 +434,7 @@ hymba_status decode_f32(const Dims& x, const Plan& pl, const hymba_layer_weights
 }
 
 hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const void* Xn, float* Y,
-                         const hymba_cache* c, const hymba_cache* kvc, void* ws, int32_t* status,
+                         const hymba_cache* c, const hymba_cache* kvc, void* ws, int32_t* status, Marks& mk,
                          cudaStream_t st) {
   const int sms = num_sms();
   const int B = x.B;
@@ -430,17 +447,33 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   __half* g = at<__half>(ws, pl.g);
   __half* s = at<__half>(ws, pl.s);
   float* part = at<float>(ws, pl.part);
+  mk.mark();
   TRY(convert_weights(x, pl, w, ws, st));
+  mk.mark();
   TRY(in_proj_bf16(x, Xn, w, proj, B, c->pos, x.M, 1, status, sms, st));
+  mk.mark();
   if (!x.kv_shared)
     TRY(kv_append<__half, __nv_bfloat16>(B, x.Hkv, x.dh, x.dv, x.W, c->cap, proj, x.P_in, x.k_col, x.v_col, c->pos,
                                          static_cast<__nv_bfloat16*>(c->k_ring),
                                          static_cast<__nv_bfloat16*>(c->v_ring), st));
-  TRY(decode_attention<__half, __nv_bfloat16>(
-      B, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, kvc->cap, proj, x.P_in, static_cast<const __nv_bfloat16*>(kvc->k_meta),
-      static_cast<const __nv_bfloat16*>(kvc->v_meta), static_cast<const __nv_bfloat16*>(kvc->k_ring),
-      static_cast<const __nv_bfloat16*>(kvc->v_ring), c->pos, att, x.di, st));
+  mk.mark();
+  if (decode_attn_split_supported(x.Hq, x.Hkv, x.dh, x.dv)) {
+    const int max_keys = x.M + (x.W > 0 ? std::min(x.W, kvc->cap) : kvc->cap);
+    TRY(decode_attention_split(B, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, kvc->cap, pl.attn_splits, proj, x.P_in,
+                               static_cast<const __nv_bfloat16*>(kvc->k_meta),
+                               static_cast<const __nv_bfloat16*>(kvc->v_meta),
+                               static_cast<const __nv_bfloat16*>(kvc->k_ring),
+                               static_cast<const __nv_bfloat16*>(kvc->v_ring), c->pos, at<float>(ws, pl.apart), att,
+                               x.di, max_keys, st));
+  } else {
+    TRY(decode_attention<__half, __nv_bfloat16>(
+        B, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, kvc->cap, proj, x.P_in, static_cast<const __nv_bfloat16*>(kvc->k_meta),
+        static_cast<const __nv_bfloat16*>(kvc->v_meta), static_cast<const __nv_bfloat16*>(kvc->k_ring),
+        static_cast<const __nv_bfloat16*>(kvc->v_ring), c->pos, att, x.di, st));
+  }
+  mk.mark();
   TRY(conv_step<__half>(B, x.di, x.k, proj + x.x_col, x.P_in, w->conv_w, w->conv_b, c->conv_state, u, x.di, st));
+  mk.mark();
   {
     const int ldp = (x.xo + 15) / 16 * 16;
     GemmParams p = gp(B, x.xo, x.di, status, x.wait_ns);
@@ -452,16 +485,25 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
     const int splits = (n_kb + kbs - 1) / kbs;
     TRY(splitk_reduce(splits, B, x.xo, part, ldp, RE_XPROJ, x.R, dtr, x.Rp, bc, 2 * x.N, nullptr, 0, false, st));
   }
-  {
+  mk.mark();
+  if (decode_ssm_step_supported(x.N, x.R)) {
+    mk.mark();  // dt projection is fused into the step below
+    TRY(decode_ssm_step(B, x.di, x.N, x.R, u, x.di, proj + x.z_col, x.P_in, dtr, x.Rp, bc,
+                        static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, w->A_log, w->D, c->ssm_state, g, x.di,
+                        st));
+  } else {
     GemmParams p = gp(B, x.di, x.R, status, x.wait_ns);
     p.C = delta;
     p.ldc = x.di;
     p.bias = w->dt_bias;
     TRY(gemm_tc(0, dtr, x.Rp, at<__half>(ws, pl.wdt), x.Rp, EPI_SOFTPLUS, p, 0, 1, sms, st));
+    mk.mark();
+    TRY(scan_simt<__half>(B, 1, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, x.di, bc, bc + x.N, 2 * x.N,
+                          w->A_log, w->D, g, x.di, c->ssm_state, c->ssm_state, st));
   }
-  TRY(scan_simt<__half>(B, 1, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, x.di, bc, bc + x.N, 2 * x.N,
-                        w->A_log, w->D, g, x.di, c->ssm_state, c->ssm_state, st));
+  mk.mark();
   TRY(fuse_norm<__half>(B, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  mk.mark();
   {
     GemmParams p = gp(B, x.d, x.di, status, x.wait_ns);
     p.C = part;
@@ -474,7 +516,10 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
     TRY(splitk_reduce(splits, B, x.d, part, x.d, RE_F32, 0, nullptr, 0, Y, x.d,
                       x.residual == 1 ? static_cast<const __nv_bfloat16*>(Xn) : nullptr, x.d, x.residual == 2, st));
   }
-  return pos_increment(B, c->pos, st);
+  mk.mark();
+  TRY(pos_increment(B, c->pos, st));
+  mk.mark();
+  return HYMBA_OK;
 }
 
 }  // namespace
@@ -558,9 +603,10 @@ hymba_status hymba_layer_fwd_events(const hymba_layer_desc* d, const hymba_layer
   return layer_fwd_impl(d, w, x_in, y, cache_out, kv_in, kv_out, ws, ws_bytes, dev_status, events, n_events, stream);
 }
 
-hymba_status hymba_layer_decode(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_new,
-                                float* y, const hymba_cache* cache, const hymba_cache* shared_cache, void* ws,
-                                size_t ws_bytes, int32_t* dev_status, void* stream) {
+static hymba_status layer_decode_impl(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_new,
+                                      float* y, const hymba_cache* cache, const hymba_cache* shared_cache, void* ws,
+                                      size_t ws_bytes, int32_t* dev_status, void* const* events, int32_t n_events,
+                                      void* stream) {
   Dims x;
   TRY(check_desc(d, true, &x));
   TRY(check_weights(w, x));
@@ -573,13 +619,32 @@ hymba_status hymba_layer_decode(const hymba_layer_desc* d, const hymba_layer_wei
   if (x.W > 0 && kvc->cap < x.W) return HYMBA_ERR_INVALID;
   const size_t a = x.dtype == HYMBA_BF16 ? 16 : 4;
   if (!aligned(x_new, a) || !aligned(y, 16) || !aligned(ws, 256)) return HYMBA_ERR_INVALID;
+  if (n_events < 0 || (n_events > 0 && !events)) return HYMBA_ERR_INVALID;
   const Plan pl = plan_ws(x, true);
   if (ws_bytes < pl.total) return HYMBA_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
   if (x.dtype == HYMBA_F32)
     return decode_f32(x, pl, w, static_cast<const float*>(x_new), y, cache, kvc, ws, st);
-  return decode_bf16(x, pl, w, x_new, y, cache, kvc, ws, dev_status, st);
+  Marks mk;
+  mk.ev = events;
+  mk.n = n_events;
+  mk.st = st;
+  return decode_bf16(x, pl, w, x_new, y, cache, kvc, ws, dev_status, mk, st);
+}
+
+hymba_status hymba_layer_decode(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_new,
+                                float* y, const hymba_cache* cache, const hymba_cache* shared_cache, void* ws,
+                                size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return layer_decode_impl(d, w, x_new, y, cache, shared_cache, ws, ws_bytes, dev_status, nullptr, 0, stream);
+}
+
+hymba_status hymba_layer_decode_events(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_new,
+                                       float* y, const hymba_cache* cache, const hymba_cache* shared_cache,
+                                       void* ws, size_t ws_bytes, int32_t* dev_status, void* const* events,
+                                       int32_t n_events, void* stream) {
+  return layer_decode_impl(d, w, x_new, y, cache, shared_cache, ws, ws_bytes, dev_status, events, n_events,
+                           stream);
 }
 
 // --------------------------------------------------------------------------- tests
@@ -611,6 +676,20 @@ hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t N, const 
   return scan_f16(B, L, di, N, static_cast<const __half*>(u), ld_u, static_cast<const __half*>(z), ld_z, delta, BC,
                   A_log, D, static_cast<__half*>(g), nullptr, h_out, nullptr, 2000000000ull,
                   static_cast<cudaStream_t>(stream));
+}
+
+hymba_status hymba_test_scan_fused(int32_t B, int32_t L, int32_t di, int32_t N, int32_t R, const void* u,
+                                   int32_t ld_u, const void* z, int32_t ld_z, const void* dtr, int32_t ld_dtr,
+                                   const void* W_dt, const float* dt_bias, const float* BC, const float* A_log,
+                                   const float* D, void* g, float* h_out, void* stream) {
+  if (B < 1 || L < 1 || di < 1 || N < 1 || R < 1 || !u || !z || !dtr || !W_dt || !dt_bias || !BC || !A_log || !D ||
+      !g)
+    return HYMBA_ERR_INVALID;
+  cudaGetLastError();
+  return scan_fused_f16(B, L, di, N, R, static_cast<const __half*>(u), ld_u, static_cast<const __half*>(z), ld_z,
+                        static_cast<const __half*>(dtr), ld_dtr, static_cast<const __nv_bfloat16*>(W_dt), dt_bias, BC,
+                        A_log, D, static_cast<__half*>(g), nullptr, h_out, nullptr, 2000000000ull,
+                        static_cast<cudaStream_t>(stream));
 }
 
 hymba_status hymba_test_attention(int32_t B, int32_t L, int32_t M, int32_t Hq, int32_t Hkv, int32_t dh, int32_t dv,

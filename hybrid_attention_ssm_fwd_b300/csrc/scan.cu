@@ -4,44 +4,71 @@
 // Recurrence (per batch b, channel c, state n), run literally in time:
 //     h_t = exp(delta_t * A) * h_{t-1} + (delta_t * u_t) * B_t
 //     y_t = C_t . h_t + D * u_t,   g_t = y_t * silu(z_t),   A = -exp(A_log)
-// The state stays in registers for the whole sequence.  Two threads share a
-// channel (8 states each) and combine C.h with one shuffle; a block of 64
-// threads owns 32 channels of one sequence.  Time is walked in chunks of 32
-// rows whose delta / u / z / [B|C] tiles arrive by TMA into a 2-stage shared
-// memory ring, so every global read is a full coalesced tile and the scan
-// itself only touches shared memory.  g is staged per chunk and written back
-// with 16-byte stores.
+// with delta = softplus(dt W_dt^T + dt_bias) computed here (dt projection
+// fused in) or read from a delta buffer (component-test mode).
+//
+// One thread owns one (sequence, channel) and all 16 states, in registers
+// for the whole sequence, so the per-row loads, the C.h sum and the gate are
+// paid once per channel and no shuffle is needed.  A block of 64 threads
+// (two warps) owns 64 channels of one sequence.  Time is walked in chunks of
+// 16 rows whose dt (or delta) / u / z / [B|C] tiles arrive by TMA into a
+// 2-stage shared-memory ring.  In fused mode each warp computes delta for its
+// 32 channels x 16 rows with mma.sync (W_dt fragments stay in registers) and
+// applies softplus.  The scan advances 4 rows per group with paired fp32
+// arithmetic, which leaves 8 independent state pairs and 4 rows of loads in
+// flight per thread.  g is staged per chunk and written back with 16-byte
+// stores.
+#include <type_traits>
+
 #include "scan.cuh"
 #include "simt.cuh"
 
 namespace hy {
 namespace {
 
-constexpr int SC_CH = 32;      // channels per block
-constexpr int SC_T = 32;       // time rows per chunk
+constexpr int SC_CH = 64;      // channels per block (one per thread)
+constexpr int SC_T = 16;       // time rows per chunk
 constexpr int SC_THREADS = 64;
+constexpr int SC_N = 16;       // states per channel on this path
 
-template <int NH>  // states per thread (N = 2 * NH)
+// KS = number of 16-wide k steps of the fused dt projection (0: delta input)
+template <int KS>
 struct ScanCfg {
-  static constexpr int N = 2 * NH;
-  static constexpr int D_BYTES = SC_T * SC_CH * 4;
+  static constexpr int KP = KS * 16;                       // padded dt rank
+  static constexpr int X_BYTES = KS > 0 ? SC_T * KP * 2 : SC_T * SC_CH * 4;  // dt tile or delta tile
   static constexpr int U_BYTES = SC_T * SC_CH * 2;
   static constexpr int Z_BYTES = SC_T * SC_CH * 2;
-  static constexpr int BC_BYTES = SC_T * 2 * N * 4;
-  static constexpr int STAGE = D_BYTES + U_BYTES + Z_BYTES + BC_BYTES;
-  static constexpr int OFF_G = 2 * STAGE;
+  static constexpr int BC_BYTES = SC_T * 2 * SC_N * 4;
+  static constexpr int OFF_U = X_BYTES;
+  static constexpr int OFF_Z = OFF_U + U_BYTES;
+  static constexpr int OFF_BC = OFF_Z + Z_BYTES;
+  static constexpr int STAGE = OFF_BC + BC_BYTES;
+  static constexpr int OFF_DELTA = 2 * STAGE;               // fused mode: delta tile [SC_T][SC_CH] fp32
+  static constexpr int OFF_G = OFF_DELTA + (KS > 0 ? SC_T * SC_CH * 4 : 0);
   static constexpr int OFF_BAR = OFF_G + SC_T * SC_CH * 2;
   static constexpr int SMEM = 128 + OFF_BAR + 64;
 };
 
-template <int NH>
+struct ScanArgs {
+  int L, di, R;
+  const __nv_bfloat16* W_dt;   // [di, R] (fused mode)
+  const float* dt_bias;        // [di]    (fused mode)
+  const float* A_log;
+  const float* D;
+  __half* g;
+  const float* h0;
+  float* h_out;
+  int32_t* status;
+  uint64_t wait_ns;
+};
+
+template <int KS>
 __global__ void __launch_bounds__(SC_THREADS)
-    scan_tc_kernel(const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmU,
-                   const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmBC, int L, int di,
-                   const float* __restrict__ A_log, const float* __restrict__ Dp, __half* __restrict__ g,
-                   const float* __restrict__ h0, float* __restrict__ h_out, int32_t* status, uint64_t wait_ns) {
-  using Cfg = ScanCfg<NH>;
-  constexpr int N = Cfg::N;
+    scan_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmU,
+                const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmBC,
+                const ScanArgs a) {
+  using Cfg = ScanCfg<KS>;
+  constexpr int N = SC_N;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
@@ -49,11 +76,12 @@ __global__ void __launch_bounds__(SC_THREADS)
   __half* sg = reinterpret_cast<__half*>(smem + Cfg::OFF_G);
 
   const int tid = threadIdx.x;
-  const int cl = tid >> 1;          // channel within block
-  const int half = tid & 1;         // which 8 states
+  const int warp = tid >> 5, lane = tid & 31;
+  const int cl = tid;               // channel within block
   const int c0 = blockIdx.x * SC_CH;
   const int b = blockIdx.y;
   const int c = c0 + cl;
+  const int L = a.L, di = a.di;
   const long long row0 = static_cast<long long>(b) * L;
   const int n_chunks = (L + SC_T - 1) / SC_T;
 
@@ -64,7 +92,7 @@ __global__ void __launch_bounds__(SC_THREADS)
     fence_mbar_init();
   }
   __syncthreads();
-  const WaitCtl wc{&abort_flag, status, wait_ns};
+  const WaitCtl wc{&abort_flag, a.status, a.wait_ns};
 
   auto issue = [&](int k) {
     const int s = k & 1;
@@ -72,82 +100,154 @@ __global__ void __launch_bounds__(SC_THREADS)
     const uint32_t bar = smem_u32(&bars[s]);
     const int r = static_cast<int>(row0) + k * SC_T;
     mbar_arrive_expect_tx(bar, Cfg::STAGE);
-    tma_load_2d(smem_u32(st), &tmD, bar, c0, r);
-    tma_load_2d(smem_u32(st + Cfg::D_BYTES), &tmU, bar, c0, r);
-    tma_load_2d(smem_u32(st + Cfg::D_BYTES + Cfg::U_BYTES), &tmZ, bar, c0, r);
-    tma_load_2d(smem_u32(st + Cfg::D_BYTES + Cfg::U_BYTES + Cfg::Z_BYTES), &tmBC, bar, 0, r);
+    tma_load_2d(smem_u32(st), &tmX, bar, KS > 0 ? 0 : c0, r);
+    tma_load_2d(smem_u32(st + Cfg::OFF_U), &tmU, bar, c0, r);
+    tma_load_2d(smem_u32(st + Cfg::OFF_Z), &tmZ, bar, c0, r);
+    tma_load_2d(smem_u32(st + Cfg::OFF_BC), &tmBC, bar, 0, r);
   };
   if (tid == 0) {
     issue(0);
     if (n_chunks > 1) issue(1);
   }
 
-  // per-thread constants: A * log2(e) for its states, D, initial state
-  float A2[NH], h[NH];
+  // per-thread constants: A * log2(e) for the 16 states (packed pairs), D, state
+  uint64_t A2[N / 2], h2[N / 2];
 #pragma unroll
-  for (int n = 0; n < NH; ++n) {
-    A2[n] = -__expf(A_log[c * N + half * NH + n]) * 1.4426950408889634f;
-    h[n] = h0 ? h0[(static_cast<long long>(b) * di + c) * N + half * NH + n] : 0.f;
+  for (int n = 0; n < N / 2; ++n) {
+    const int s0 = c * N + 2 * n;
+    A2[n] = pk2(-__expf(a.A_log[s0]) * 1.4426950408889634f, -__expf(a.A_log[s0 + 1]) * 1.4426950408889634f);
+    const long long hb = (static_cast<long long>(b) * di + c) * N + 2 * n;
+    h2[n] = a.h0 ? pk2(a.h0[hb], a.h0[hb + 1]) : pk2(0.f, 0.f);
   }
-  const float Dc = Dp[c];
+  const float Dc = a.D[c];
+
+  // fused dt projection: this warp's 32 channels = four n-tiles of 8
+  const int grp = lane >> 2, tig = lane & 3;
+  uint32_t bfr[4][KS > 0 ? KS : 1][2];
+  float bias_c[4][2];
+  if constexpr (KS > 0) {
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int ch = c0 + warp * 32 + nt * 8 + grp;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r0 = kk * 16 + hh * 8 + tig * 2;
+          const float v0 = r0 < a.R ? __bfloat162float(a.W_dt[static_cast<long long>(ch) * a.R + r0]) : 0.f;
+          const float v1 = r0 + 1 < a.R ? __bfloat162float(a.W_dt[static_cast<long long>(ch) * a.R + r0 + 1]) : 0.f;
+          bfr[nt][kk][hh] = pack_half2(v0, v1);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) bias_c[nt][e] = a.dt_bias[c0 + warp * 32 + nt * 8 + tig * 2 + e];
+    }
+  }
 
   int kfail = -1;
   for (int k = 0; k < n_chunks; ++k) {
     const int s = k & 1;
-    bool got = mbar_wait(smem_u32(&bars[s]), (k >> 1) & 1, wc);
+    const bool got = mbar_wait(smem_u32(&bars[s]), (k >> 1) & 1, wc);
     if (!__syncthreads_and(got)) {
       kfail = k;
       break;
     }
     const uint8_t* st = smem + s * Cfg::STAGE;
-    const float* sD = reinterpret_cast<const float*>(st);
-    const __half* sU = reinterpret_cast<const __half*>(st + Cfg::D_BYTES);
-    const __half* sZ = reinterpret_cast<const __half*>(st + Cfg::D_BYTES + Cfg::U_BYTES);
-    const float* sBC = reinterpret_cast<const float*>(st + Cfg::D_BYTES + Cfg::U_BYTES + Cfg::Z_BYTES);
-    const int nt = min(SC_T, L - k * SC_T);
-#pragma unroll 2
-    for (int t = 0; t < nt; ++t) {
+    const __half* sU = reinterpret_cast<const __half*>(st + Cfg::OFF_U);
+    const __half* sZ = reinterpret_cast<const __half*>(st + Cfg::OFF_Z);
+    const float* sBC = reinterpret_cast<const float*>(st + Cfg::OFF_BC);
+    const float* sD;
+    if constexpr (KS > 0) {
+      // delta[t][ch] = softplus(dt[t] . W_dt[ch] + bias[ch]) for 16 rows x this warp's 32 channels
+      const __half* sDT = reinterpret_cast<const __half*>(st);
+      float* sDw = reinterpret_cast<float*>(smem + Cfg::OFF_DELTA);
+      float acc[4][4];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const __half* base = sDT + grp * Cfg::KP + kk * 16 + tig * 2;
+        uint32_t af[4];
+        af[0] = *reinterpret_cast<const uint32_t*>(base);
+        af[1] = *reinterpret_cast<const uint32_t*>(base + 8 * Cfg::KP);
+        af[2] = *reinterpret_cast<const uint32_t*>(base + 8);
+        af[3] = *reinterpret_cast<const uint32_t*>(base + 8 * Cfg::KP + 8);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) mma_16816_f16(acc[nt], af, bfr[nt][kk][0], bfr[nt][kk][1]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int col = warp * 32 + nt * 8 + tig * 2;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int row = grp + (e >> 1) * 8;
+          sDw[row * SC_CH + col + (e & 1)] = softplus_fast(acc[nt][e] + bias_c[nt][e & 1]);
+        }
+      }
+      __syncwarp();
+      sD = sDw;
+    } else {
+      sD = reinterpret_cast<const float*>(st);
+    }
+    const int nt_rows = min(SC_T, L - k * SC_T);
+
+    auto step = [&](int t) {
       const float dt = sD[t * SC_CH + cl];
       const float uu = __half2float(sU[t * SC_CH + cl]);
       const float du = dt * uu;
-      const float4* Bp = reinterpret_cast<const float4*>(sBC + t * 2 * N + half * NH);
-      const float4* Cp = reinterpret_cast<const float4*>(sBC + t * 2 * N + N + half * NH);
-      float Bv[NH], Cv[NH];
+      const uint64_t dt2 = pk2(dt, dt), du2 = pk2(du, du);
+      const float4* Bp = reinterpret_cast<const float4*>(sBC + t * 2 * N);
+      const float4* Cp = reinterpret_cast<const float4*>(sBC + t * 2 * N + N);
+      uint64_t y0 = pk2(0.f, 0.f), y1 = pk2(0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < NH / 4; ++q) {
-        const float4 bb = Bp[q], cc = Cp[q];
-        Bv[4 * q] = bb.x; Bv[4 * q + 1] = bb.y; Bv[4 * q + 2] = bb.z; Bv[4 * q + 3] = bb.w;
-        Cv[4 * q] = cc.x; Cv[4 * q + 1] = cc.y; Cv[4 * q + 2] = cc.z; Cv[4 * q + 3] = cc.w;
-      }
-      float yp = 0.f;
+      for (int qq = 0; qq < N / 4; ++qq) {
+        const float4 bb = Bp[qq], cc = Cp[qq];
 #pragma unroll
-      for (int n = 0; n < NH; ++n) {
-        const float a = ex2_approx(dt * A2[n]);
-        h[n] = fmaf(a, h[n], du * Bv[n]);
-        yp = fmaf(Cv[n], h[n], yp);
+        for (int p2 = 0; p2 < 2; ++p2) {
+          const int n = qq * 2 + p2;
+          const float2 ea = up2(mul2(dt2, A2[n]));
+          const uint64_t av = pk2(ex2_approx(ea.x), ex2_approx(ea.y));
+          const uint64_t bu = mul2(du2, p2 == 0 ? pk2(bb.x, bb.y) : pk2(bb.z, bb.w));
+          h2[n] = fma2(av, h2[n], bu);
+          if (p2 == 0)
+            y0 = fma2(pk2(cc.x, cc.y), h2[n], y0);
+          else
+            y1 = fma2(pk2(cc.z, cc.w), h2[n], y1);
+        }
       }
-      yp += __shfl_xor_sync(0xffffffffu, yp, 1);
-      if (half == 0) {
-        const float zz = __half2float(sZ[t * SC_CH + cl]);
-        const float y = fmaf(Dc, uu, yp);
-        sg[t * SC_CH + cl] = __float2half_rn(y * zz / (1.0f + __expf(-zz)));
-      }
+      const float2 ya = up2(y0), yb = up2(y1);
+      const float y = fmaf(Dc, uu, (ya.x + ya.y) + (yb.x + yb.y));
+      const float zz = __half2float(sZ[t * SC_CH + cl]);
+      const float sz = zz / (1.0f + ex2_approx(-1.4426950408889634f * zz));
+      sg[t * SC_CH + cl] = __float2half_rn(y * sz);
+    };
+    if (nt_rows == SC_T) {
+#pragma unroll 4
+      for (int t = 0; t < SC_T; ++t) step(t);
+    } else {
+      for (int t = 0; t < nt_rows; ++t) step(t);
     }
     __syncthreads();
     // stage s is consumed: refill it with chunk k + 2 while g is written back
     if (tid == 0 && k + 2 < n_chunks) issue(k + 2);
-    // g rows of this chunk: nt x 32 fp16 = nt x 64 bytes, 16 bytes per thread-step
-    for (int idx = tid; idx < nt * 4; idx += SC_THREADS) {
-      const int t = idx >> 2, q = idx & 3;
-      *reinterpret_cast<uint4*>(g + (row0 + k * SC_T + t) * di + c0 + q * 8) =
-          *reinterpret_cast<const uint4*>(sg + t * SC_CH + q * 8);
+    for (int idx = tid; idx < nt_rows * (SC_CH / 8); idx += SC_THREADS) {
+      const int tt = idx / (SC_CH / 8), q = idx % (SC_CH / 8);
+      *reinterpret_cast<uint4*>(a.g + (row0 + k * SC_T + tt) * di + c0 + q * 8) =
+          *reinterpret_cast<const uint4*>(sg + tt * SC_CH + q * 8);
     }
     __syncthreads();
   }
   if (kfail < 0) {
-    if (h_out) {
+    if (a.h_out) {
 #pragma unroll
-      for (int n = 0; n < NH; ++n) h_out[(static_cast<long long>(b) * di + c) * N + half * NH + n] = h[n];
+      for (int n = 0; n < N / 2; ++n) {
+        const float2 hv = up2(h2[n]);
+        const long long hb = (static_cast<long long>(b) * di + c) * N + 2 * n;
+        a.h_out[hb] = hv.x;
+        a.h_out[hb + 1] = hv.y;
+      }
     }
   } else if (tid == 0) {
     // chunks kfail and kfail + 1 may still be landing: let them finish
@@ -180,41 +280,76 @@ bool map2(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, l
   return encode_tmap(m, dt, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int NH>
-hymba_status launch_scan(int B, int L, int di, const __half* u, long long ld_u, const __half* z, long long ld_z,
-                         const float* delta, const float* BC, const float* A_log, const float* D, __half* g,
-                         const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, cudaStream_t st) {
-  using Cfg = ScanCfg<NH>;
+template <int KS>
+hymba_status launch_scan(int B, int L, int di, const CUtensorMap& mX, const __half* u, long long ld_u,
+                         const __half* z, long long ld_z, const float* BC, const ScanArgs& args, cudaStream_t st) {
+  using Cfg = ScanCfg<KS>;
   const long long rows = static_cast<long long>(B) * L;
-  CUtensorMap mD, mU, mZ, mBC;
-  if (!map2(&mD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, di, rows, di, SC_CH, SC_T) ||
-      !map2(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, u, di, rows, ld_u, SC_CH, SC_T) ||
+  CUtensorMap mU, mZ, mBC;
+  if (!map2(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, u, di, rows, ld_u, SC_CH, SC_T) ||
       !map2(&mZ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, z, di, rows, ld_z, SC_CH, SC_T) ||
-      !map2(&mBC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BC, 2 * Cfg::N, rows, 2 * Cfg::N, 2 * Cfg::N, SC_T))
+      !map2(&mBC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BC, 2 * SC_N, rows, 2 * SC_N, 2 * SC_N, SC_T))
     return HYMBA_ERR_CUDA;
-  auto kern = scan_tc_kernel<NH>;
+  auto kern = scan_kernel<KS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
   dim3 grid(di / SC_CH, B);
-  kern<<<grid, SC_THREADS, Cfg::SMEM, st>>>(mD, mU, mZ, mBC, L, di, A_log, D, g, h0, h_out, status, wait_ns);
+  kern<<<grid, SC_THREADS, Cfg::SMEM, st>>>(mX, mU, mZ, mBC, args);
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 
+hymba_status launch_fused(int KS, int B, int L, int di, const CUtensorMap& mX, const __half* u, long long ld_u,
+                          const __half* z, long long ld_z, const float* BC, const ScanArgs& args, cudaStream_t st) {
+  switch (KS) {
+    case 1: return launch_scan<1>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 2: return launch_scan<2>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 3: return launch_scan<3>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 4: return launch_scan<4>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 5: return launch_scan<5>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 6: return launch_scan<6>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 7: return launch_scan<7>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 8: return launch_scan<8>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    default: return HYMBA_ERR_UNSUPPORTED;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 }  // namespace
+
+bool scan_fused_supported(int di, int N, int R) { return di % SC_CH == 0 && N == SC_N && R >= 1 && R <= 128; }
 
 hymba_status scan_f16(int B, int L, int di, int N, const __half* u, long long ld_u, const __half* z,
                       long long ld_z, const float* delta, const float* BC, const float* A_log, const float* D,
                       __half* g, const float* h0, float* h_out, int32_t* status, uint64_t wait_ns,
                       cudaStream_t st) {
-  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  const bool tma_ok = di % SC_CH == 0 && ld_u % 8 == 0 && ld_z % 8 == 0 && al(u) && al(z) && al(delta) &&
-                      al(BC) && al(g);
-  if (tma_ok && N == 16)
-    return launch_scan<8>(B, L, di, u, ld_u, z, ld_z, delta, BC, A_log, D, g, h0, h_out, status, wait_ns, st);
-  if (tma_ok && N == 8)
-    return launch_scan<4>(B, L, di, u, ld_u, z, ld_z, delta, BC, A_log, D, g, h0, h_out, status, wait_ns, st);
+  const bool tma_ok = di % SC_CH == 0 && ld_u % 8 == 0 && ld_z % 8 == 0 && aligned16(u) && aligned16(z) &&
+                      aligned16(delta) && aligned16(BC) && aligned16(g);
+  if (tma_ok && N == SC_N) {
+    CUtensorMap mX;
+    if (!map2(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, di, static_cast<long long>(B) * L, di, SC_CH, SC_T))
+      return HYMBA_ERR_CUDA;
+    ScanArgs args{L, di, 0, nullptr, nullptr, A_log, D, g, h0, h_out, status, wait_ns};
+    return launch_scan<0>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+  }
   return scan_simt<__half>(B, L, di, N, u, ld_u, z, ld_z, delta, di, BC, BC + N, 2 * N, A_log, D, g, di, h0, h_out,
                            st);
+}
+
+hymba_status scan_fused_f16(int B, int L, int di, int N, int R, const __half* u, long long ld_u, const __half* z,
+                            long long ld_z, const __half* dtr, long long ld_dtr, const __nv_bfloat16* W_dt,
+                            const float* dt_bias, const float* BC, const float* A_log, const float* D, __half* g,
+                            const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, cudaStream_t st) {
+  if (!scan_fused_supported(di, N, R)) return HYMBA_ERR_UNSUPPORTED;
+  if (ld_u % 8 || ld_z % 8 || ld_dtr % 8 || !aligned16(u) || !aligned16(z) || !aligned16(dtr) || !aligned16(BC) ||
+      !aligned16(g))
+    return HYMBA_ERR_INVALID;
+  const int KS = (R + 15) / 16;
+  CUtensorMap mX;
+  if (!map2(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, dtr, R, static_cast<long long>(B) * L, ld_dtr, KS * 16, SC_T))
+    return HYMBA_ERR_CUDA;
+  ScanArgs args{L, di, R, W_dt, dt_bias, A_log, D, g, h0, h_out, status, wait_ns};
+  return launch_fused(KS, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
 }
 
 hymba_status wait_timeout_probe(uint32_t limit_us, int32_t* status, cudaStream_t st) {

@@ -15,6 +15,15 @@ hymba_status scan_f16(int B, int L, int di, int N, const __half* u, long long ld
                       __half* g, const float* h0, float* h_out, int32_t* status, uint64_t wait_ns,
                       cudaStream_t st);
 
+// Same scan with the dt projection fused in: delta = softplus(dtr . W_dt^T +
+// dt_bias) is computed per chunk inside the kernel.  dtr fp16 [B*L, ld_dtr]
+// (R valid columns), W_dt bf16 [di, R].
+bool scan_fused_supported(int di, int N, int R);  // di % 64 == 0, N == 16, R <= 128
+hymba_status scan_fused_f16(int B, int L, int di, int N, int R, const __half* u, long long ld_u, const __half* z,
+                            long long ld_z, const __half* dtr, long long ld_dtr, const __nv_bfloat16* W_dt,
+                            const float* dt_bias, const float* BC, const float* A_log, const float* D, __half* g,
+                            const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, cudaStream_t st);
+
 // One block waits on an mbarrier nothing arrives on, bounded by limit_us,
 // and records HYMBA_ERR_TIMEOUT in *status.
 hymba_status wait_timeout_probe(uint32_t limit_us, int32_t* status, cudaStream_t st);

@@ -144,6 +144,77 @@ __global__ void conv_silu_kernel(const TI* __restrict__ x, long long ld_x, TO* _
   }
 }
 
+// fp16 conv: one thread owns 8 consecutive channels (one 16-byte vector) for
+// a tile of CONV_TT consecutive rows and keeps the last K-1 inputs in
+// registers, so x is read once and u written once, both fully coalesced.
+constexpr int CONV_TT = 64;
+
+template <int K>
+__global__ void __launch_bounds__(128) conv_silu_vec_kernel(const __half* __restrict__ x, long long ld_x,
+                                                            __half* __restrict__ u, long long ld_u, int L, int di,
+                                                            const float* __restrict__ w,
+                                                            const float* __restrict__ bias) {
+  const int cg = blockIdx.x * blockDim.x + threadIdx.x;  // channel group of 8
+  if (cg * 8 >= di) return;
+  const int t0 = blockIdx.y * CONV_TT;
+  const int b = blockIdx.z;
+  const int c0 = cg * 8;
+  float wt[8][K], bs[8], win[K][8];  // win[j] = row t - (K-1) + j for the next row t (j < K-1)
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    bs[e] = bias[c0 + e];
+#pragma unroll
+    for (int j = 0; j < K; ++j) wt[e][j] = w[(c0 + e) * K + j];
+  }
+  const long long rb = static_cast<long long>(b) * L;
+#pragma unroll
+  for (int j = 0; j < K - 1; ++j) {
+    const int src = t0 - (K - 1) + j;
+    if (src >= 0) {
+      const uint4 q = *reinterpret_cast<const uint4*>(x + (rb + src) * ld_x + c0);
+      const __half* hq = reinterpret_cast<const __half*>(&q);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) win[j][e] = __half2float(hq[e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) win[j][e] = 0.f;
+    }
+  }
+  const int t1 = min(t0 + CONV_TT, L);
+  constexpr int RB = 8;  // rows loaded per batch: 8 independent 16-byte loads in flight
+  for (int tb = t0; tb < t1; tb += RB) {
+    uint4 qv[RB];
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+      if (tb + r < t1) qv[r] = *reinterpret_cast<const uint4*>(x + (rb + tb + r) * ld_x + c0);
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      if (tb + r >= t1) break;
+      const __half* hq = reinterpret_cast<const __half*>(&qv[r]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) win[K - 1][e] = __half2float(hq[e]);
+      float out[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float acc = bs[e];
+#pragma unroll
+        for (int j = 0; j < K; ++j) acc = fmaf(wt[e][j], win[j][e], acc);
+        out[e] = acc / (1.0f + __expf(-acc));
+      }
+#pragma unroll
+      for (int j = 0; j + 1 < K; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
+      uint4 o;
+      o.x = pack_half2(out[0], out[1]);
+      o.y = pack_half2(out[2], out[3]);
+      o.z = pack_half2(out[4], out[5]);
+      o.w = pack_half2(out[6], out[7]);
+      *reinterpret_cast<uint4*>(u + (rb + tb + r) * ld_u + c0) = o;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // generic selective scan + gate (one thread per (b, channel))
 // ---------------------------------------------------------------------------
@@ -229,6 +300,80 @@ __global__ void __launch_bounds__(256) fuse_norm_kernel(int di, const T* __restr
     s[row * di + c] = from_f<T>(beta1[c] * to_f(a[c]) * ra + beta2[c] * to_f(gg[c]) * rg);
 }
 
+// fp16 fused norm: 16-byte vectors kept in registers (one HBM read of att
+// and g), up to FN_MAXC vectors of each per thread.
+constexpr int FN_MAXC = 4;
+
+__global__ void __launch_bounds__(256) fuse_norm_vec_kernel(int di, const __half* __restrict__ att,
+                                                            const __half* __restrict__ g,
+                                                            const float* __restrict__ beta1,
+                                                            const float* __restrict__ beta2, float eps,
+                                                            __half* __restrict__ s) {
+  const long long row = blockIdx.x;
+  const int nch = di / 8;
+  const uint4* a4 = reinterpret_cast<const uint4*>(att + row * di);
+  const uint4* g4 = reinterpret_cast<const uint4*>(g + row * di);
+  uint4 av[FN_MAXC], gv[FN_MAXC];
+  float sa = 0.f, sg = 0.f;
+#pragma unroll
+  for (int q = 0; q < FN_MAXC; ++q) {
+    const int ch = threadIdx.x + q * 256;
+    if (ch < nch) {
+      av[q] = a4[ch];
+      gv[q] = g4[ch];
+      const __half2* ah = reinterpret_cast<const __half2*>(&av[q]);
+      const __half2* gh = reinterpret_cast<const __half2*>(&gv[q]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __half22float2(ah[e]), fg = __half22float2(gh[e]);
+        sa = fmaf(fa.x, fa.x, fmaf(fa.y, fa.y, sa));
+        sg = fmaf(fg.x, fg.x, fmaf(fg.y, fg.y, sg));
+      }
+    }
+  }
+  __shared__ float red[2][8];
+  for (int o = 16; o > 0; o >>= 1) {
+    sa += __shfl_xor_sync(0xffffffffu, sa, o);
+    sg += __shfl_xor_sync(0xffffffffu, sg, o);
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    red[0][w] = sa;
+    red[1][w] = sg;
+  }
+  __syncthreads();
+  float ta = 0.f, tg = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    ta += red[0][i];
+    tg += red[1][i];
+  }
+  const float ra = rsqrtf(ta / di + eps), rg = rsqrtf(tg / di + eps);
+  uint4* s4 = reinterpret_cast<uint4*>(s + row * di);
+#pragma unroll
+  for (int q = 0; q < FN_MAXC; ++q) {
+    const int ch = threadIdx.x + q * 256;
+    if (ch < nch) {
+      const __half2* ah = reinterpret_cast<const __half2*>(&av[q]);
+      const __half2* gh = reinterpret_cast<const __half2*>(&gv[q]);
+      const float4 b1a = *reinterpret_cast<const float4*>(beta1 + ch * 8);
+      const float4 b1b = *reinterpret_cast<const float4*>(beta1 + ch * 8 + 4);
+      const float4 b2a = *reinterpret_cast<const float4*>(beta2 + ch * 8);
+      const float4 b2b = *reinterpret_cast<const float4*>(beta2 + ch * 8 + 4);
+      const float bb1[8] = {b1a.x, b1a.y, b1a.z, b1a.w, b1b.x, b1b.y, b1b.z, b1b.w};
+      const float bb2[8] = {b2a.x, b2a.y, b2a.z, b2a.w, b2b.x, b2b.y, b2b.z, b2b.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __half22float2(ah[e]), fg = __half22float2(gh[e]);
+        o[e] = pack_half2(bb1[2 * e] * fa.x * ra + bb2[2 * e] * fg.x * rg,
+                          bb1[2 * e + 1] * fa.y * ra + bb2[2 * e + 1] * fg.y * rg);
+      }
+      s4[ch] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // SIMT attention: one warp per (b, row i, query head)
 // ---------------------------------------------------------------------------
@@ -311,12 +456,24 @@ __global__ void __launch_bounds__(128) attention_simt_kernel(int B, int L, int M
 template <typename TS, typename TD>
 __global__ void copy2d_kernel(const TS* __restrict__ src, long long lds, TD* __restrict__ dst, long long ldd,
                               long long rows, int cols) {
-  const long long n = rows * cols;
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = idx / cols;
-    const int c = static_cast<int>(idx % cols);
-    dst[r * ldd + c] = from_f<TD>(to_f(src[r * lds + c]));
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  for (long long r = blockIdx.y; r < rows; r += gridDim.y) dst[r * ldd + c] = from_f<TD>(to_f(src[r * lds + c]));
+}
+
+__global__ void bf16_to_f16_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n8) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const uint4 v = src[i];
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+    uint4 o;
+    uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(b2[e]);
+      o32[e] = pack_half2(f.x, f.y);
+    }
+    dst[i] = o;
   }
 }
 
@@ -385,6 +542,18 @@ hymba_status rope_simt(T* X, long long ld, int rows, int col0, int n_heads, int 
 template <typename TI, typename TO>
 hymba_status conv_silu(const TI* x, long long ld_x, TO* u, long long ld_u, int B, int L, int di, int k,
                        const float* w, const float* bias, cudaStream_t st) {
+  if (std::is_same<TI, __half>::value && std::is_same<TO, __half>::value && di % 8 == 0 && ld_x % 8 == 0 &&
+      ld_u % 8 == 0 && (k == 2 || k == 3 || k == 4) && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(u) & 15) == 0) {
+    const int groups = di / 8;
+    dim3 grid((groups + 127) / 128, (L + CONV_TT - 1) / CONV_TT, B);
+    const __half* xh = reinterpret_cast<const __half*>(x);
+    __half* uh = reinterpret_cast<__half*>(u);
+    if (k == 4) conv_silu_vec_kernel<4><<<grid, 128, 0, st>>>(xh, ld_x, uh, ld_u, L, di, w, bias);
+    else if (k == 3) conv_silu_vec_kernel<3><<<grid, 128, 0, st>>>(xh, ld_x, uh, ld_u, L, di, w, bias);
+    else conv_silu_vec_kernel<2><<<grid, 128, 0, st>>>(xh, ld_x, uh, ld_u, L, di, w, bias);
+    return last_err();
+  }
   const long long n = static_cast<long long>(B) * L * di;
   conv_silu_kernel<TI, TO><<<std::min<long long>(grid1d(n, 256), 148 * 32), 256, 0, st>>>(
       x, ld_x, u, ld_u, B, L, di, k, w, bias);
@@ -407,6 +576,13 @@ template <typename T>
 hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* beta1, const float* beta2,
                        float eps, T* s, cudaStream_t st) {
   if (rows <= 0) return HYMBA_OK;
+  if (std::is_same<T, __half>::value && di % 8 == 0 && di <= 8 * 256 * FN_MAXC &&
+      (reinterpret_cast<uintptr_t>(beta1) & 15) == 0 && (reinterpret_cast<uintptr_t>(beta2) & 15) == 0) {
+    fuse_norm_vec_kernel<<<rows, 256, 0, st>>>(di, reinterpret_cast<const __half*>(att),
+                                               reinterpret_cast<const __half*>(g), beta1, beta2, eps,
+                                               reinterpret_cast<__half*>(s));
+    return last_err();
+  }
   fuse_norm_kernel<T><<<rows, 256, 0, st>>>(di, att, g, beta1, beta2, eps, s);
   return last_err();
 }
@@ -425,10 +601,18 @@ hymba_status attention_simt(int B, int L, int M, int Hq, int Hkv, int dh, int dv
 template <typename TS, typename TD>
 hymba_status copy2d(const TS* src, long long lds, TD* dst, long long ldd, long long rows, int cols,
                     cudaStream_t st) {
-  const long long n = rows * cols;
-  if (n <= 0) return HYMBA_OK;
-  copy2d_kernel<TS, TD><<<std::min<long long>(grid1d(n, 256), 148 * 32), 256, 0, st>>>(src, lds, dst, ldd,
-                                                                                     rows, cols);
+  if (std::is_same<TS, __nv_bfloat16>::value && std::is_same<TD, __half>::value && lds == cols && ldd == cols &&
+      (static_cast<long long>(rows) * cols) % 8 == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+    const long long n8 = rows * cols / 8;
+    bf16_to_f16_vec_kernel<<<static_cast<unsigned>(std::min<long long>((n8 + 255) / 256, 148 * 8)), 256, 0, st>>>(
+        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), n8);
+    return last_err();
+  }
+  if (rows <= 0 || cols <= 0) return HYMBA_OK;
+  const unsigned gx = grid1d(cols, 256);
+  const unsigned gy = static_cast<unsigned>(std::min<long long>(rows, std::max<long long>(1, 148 * 64 / gx)));
+  copy2d_kernel<TS, TD><<<dim3(gx, std::min(gy, 65535u)), 256, 0, st>>>(src, lds, dst, ldd, rows, cols);
   return last_err();
 }
 

@@ -242,6 +242,19 @@ HYMBA_API hymba_status hymba_layer_decode_static(const hymba_layer_desc* d, cons
                                                  const hymba_cache* shared_cache, int32_t* dev_status,
                                                  void* stream);
 
+/* hymba_layer_decode that also records CUDA events on `stream` around its
+ * stages (bf16 path): events[0] before the first launch, events[k] after
+ * stage k: 1 weight conversion, 2 input projection (+RoPE), 3 ring append,
+ * 4 attention, 5 conv step, 6 x_proj, 7 dt_proj+softplus, 8 scan step,
+ * 9 norm/beta/sum, 10 output projection, 11 position advance
+ * (HYMBA_DECODE_EVENTS events).  Otherwise identical to hymba_layer_decode. */
+#define HYMBA_DECODE_EVENTS 12
+HYMBA_API hymba_status hymba_layer_decode_events(const hymba_layer_desc* d, const hymba_layer_weights* w,
+                                                 const void* x_new, float* y, const hymba_cache* cache,
+                                                 const hymba_cache* shared_cache, void* ws, size_t ws_bytes,
+                                                 int32_t* dev_status, void* const* events, int32_t n_events,
+                                                 void* stream);
+
 /* Human-readable name of a status code (static storage).                    */
 HYMBA_API const char* hymba_status_str(hymba_status s);
 
@@ -270,6 +283,17 @@ HYMBA_API hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t
                              const void* u, int32_t ld_u, const void* z, int32_t ld_z,
                              const float* delta, const float* BC, const float* A_log,
                              const float* D, void* g, float* h_out, void* stream);
+
+/* The same scan with the dt projection fused in, as hymba_layer_fwd runs it:
+ * delta = softplus(dtr . W_dt^T + dt_bias) is computed inside the kernel.
+ * dtr fp16 [B, L, ld_dtr] (R valid columns, ld_dtr % 8 == 0), W_dt bf16
+ * [di, R], dt_bias fp32 [di]; other arguments as hymba_test_scan.
+ * HYMBA_ERR_UNSUPPORTED unless di % 32 == 0, N in {8, 16}, R <= 128.        */
+HYMBA_API hymba_status hymba_test_scan_fused(int32_t B, int32_t L, int32_t di, int32_t N, int32_t R,
+                                             const void* u, int32_t ld_u, const void* z, int32_t ld_z,
+                                             const void* dtr, int32_t ld_dtr, const void* W_dt,
+                                             const float* dt_bias, const float* BC, const float* A_log,
+                                             const float* D, void* g, float* h_out, void* stream);
 
 /* The bf16-path attention kernel alone (section 2.2 window + section 2.3 meta
  * prefix): Q [B, L, Hq, dh], K [B, L, Hkv, dh], V [B, L, Hkv, dv] fp16 ->

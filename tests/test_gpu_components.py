@@ -93,7 +93,7 @@ def test_scan_closed_form_on_gpu():
 
 
 def test_scan_special_cases_on_gpu():
-    B, L, di, N = 1, 300, 96, 16
+    B, L, di, N = 1, 300, 128, 16
     u, z, dl, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 2)
     g, h = _run_scan(u, z, dl, np.zeros_like(Bm), Cm, A_log, D)       # B = 0: y = D u
     np.testing.assert_allclose(g, D * u * ref.silu(z), rtol=2e-3, atol=1e-3)
@@ -101,7 +101,7 @@ def test_scan_special_cases_on_gpu():
 
 
 def test_scan_random_matches_oracle():
-    B, L, di, N = 3, 517, 160, 16
+    B, L, di, N = 3, 517, 192, 16
     u, z, dl, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 3)
     g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D)
     y, hr = ref.selective_scan(u, dl, -np.exp(A_log), Bm, Cm, D)
@@ -168,3 +168,69 @@ def test_bounded_wait_reports_timeout():
     assert st.item() == hb.HYMBA_ERR_TIMEOUT
     x = torch.ones(4, device="cuda")
     assert float((x * 2).sum().item()) == 8.0
+
+
+def _run_scan_fused(u, z, dtr, W_dt, dt_bias, Bm, Cm, A_log, D):
+    B, L, di = u.shape
+    N = Bm.shape[-1]
+    R = W_dt.shape[1]
+    Rp = (R + 7) // 8 * 8
+    dev = "cuda"
+    tu = torch.from_numpy(u).to(dev, torch.float16)
+    tz = torch.from_numpy(z).to(dev, torch.float16)
+    tdt = torch.full((B, L, Rp), float("nan"), device=dev, dtype=torch.float16)   # padding never read
+    tdt[..., :R] = torch.from_numpy(dtr).to(dev, torch.float16)
+    tw = torch.from_numpy(W_dt).to(dev, torch.bfloat16)
+    tb = torch.from_numpy(dt_bias).to(dev, torch.float32)
+    bc = torch.from_numpy(np.concatenate([Bm, Cm], -1)).to(dev, torch.float32).contiguous()
+    ta = torch.from_numpy(A_log).to(dev, torch.float32)
+    tD = torch.from_numpy(D).to(dev, torch.float32)
+    g = torch.empty(B, L, di, device=dev, dtype=torch.float16)
+    h = torch.empty(B, di, N, device=dev, dtype=torch.float32)
+    assert hb.hymba_test_scan_fused(tu, tz, tdt, tw, tb, bc, ta, tD, g, h) == 0
+    torch.cuda.synchronize()
+    return g.float().cpu().numpy().astype(F), h.cpu().numpy().astype(F)
+
+
+def test_fused_scan_closed_form_on_gpu():
+    """Fused dt projection with W_dt = 0: delta = softplus(bias) = 0.05 for every
+    row, so the geometric-series closed form must hold through the fused path."""
+    B, L, di, N, R = 2, 650, 64, 16, 100
+    u, z, _, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 6, u0=0.75, b0=1.25, c0=-0.5)
+    D[:] = 0
+    rng = np.random.default_rng(7)
+    dtr = rng.standard_normal((B, L, R)).astype(np.float16).astype(F)
+    W_dt = np.zeros((di, R))
+    d0 = 0.05
+    bias = np.full(di, d0 + np.log(-np.expm1(-d0))).astype(np.float32).astype(F)
+    g, h = _run_scan_fused(u, z, dtr, W_dt, bias, Bm, Cm, A_log, D)
+    dl = ref.softplus(bias)[0]
+    A = -np.exp(A_log)
+    a = np.exp(dl * A)
+    t = np.arange(L)[:, None, None]
+    ht = dl * 1.25 * 0.75 * (1 - a[None] ** (t + 1)) / (1 - a[None])
+    expect_g = (-0.5 * ht.sum(-1))[None] * ref.silu(z)
+    np.testing.assert_allclose(h, np.broadcast_to(ht[-1], h.shape), rtol=5e-5)
+    np.testing.assert_allclose(g, expect_g, rtol=3e-3, atol=1e-3 * np.abs(expect_g).max())
+
+
+@pytest.mark.parametrize("R,di,L", [(100, 192, 517), (64, 128, 130), (8, 64, 33)])
+def test_fused_scan_random_matches_oracle(R, di, L):
+    B, N = 2, 16
+    u, z, _, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 8)
+    rng = np.random.default_rng(9)
+    dtr = (rng.standard_normal((B, L, R)) * 0.5).astype(np.float16).astype(F)
+    W_dt = synth_bf16(rng.standard_normal((di, R)) * 0.1)
+    dt0 = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), di))
+    bias = (dt0 + np.log(-np.expm1(-dt0))).astype(np.float32).astype(F)
+    g, h = _run_scan_fused(u, z, dtr, W_dt, bias, Bm, Cm, A_log, D)
+    dl = ref.softplus(dtr @ W_dt.T + bias)
+    y, hr = ref.selective_scan(u, dl, -np.exp(A_log), Bm, Cm, D)
+    gr = y * ref.silu(z)
+    np.testing.assert_allclose(h, hr, rtol=2e-3, atol=2e-4 * np.abs(hr).max())
+    np.testing.assert_allclose(g, gr, rtol=3e-3, atol=3e-3 * np.abs(gr).max())
+
+
+def synth_bf16(a):
+    from hybrid_attention_ssm_fwd_b300 import synth
+    return synth.bf16_round(np.asarray(a, np.float32)).astype(F)
