@@ -91,10 +91,10 @@ def lib() -> ctypes.CDLL:
                                   c_void_p, c_int32, c_void_p, c_void_p]
     L.hymba_test_gemm.restype = c_int32
     L.hymba_test_scan.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
-                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]
     L.hymba_test_scan.restype = c_int32
     L.hymba_test_scan_fused.argtypes = [c_int32] * 5 + [c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_int32] + \
-        [c_void_p] * 8
+        [c_void_p] * 7 + [c_int32, c_void_p]
     L.hymba_test_scan_fused.restype = c_int32
     L.hymba_test_attention.argtypes = [c_int32] * 9 + [c_void_p] * 6
     L.hymba_test_attention.restype = c_int32
@@ -234,20 +234,22 @@ def hymba_test_gemm(A, B, C, ab_dtype: int, status=None, stream=None) -> int:
                                  C.stride(0), _ptr(status), _stream(stream))
 
 
-def hymba_test_scan(u, z, delta, BC, A_log, D, g, h_out=None, stream=None) -> int:
+def hymba_test_scan(u, z, delta, BC, A_log, D, g, h_out=None, threads_per_channel=0, stream=None) -> int:
     B, L, di = delta.shape
     N = A_log.shape[1]
     return lib().hymba_test_scan(B, L, di, N, _ptr(u), u.stride(1), _ptr(z), z.stride(1), _ptr(delta),
-                                 _ptr(BC), _ptr(A_log), _ptr(D), _ptr(g), _ptr(h_out), _stream(stream))
+                                 _ptr(BC), _ptr(A_log), _ptr(D), _ptr(g), _ptr(h_out), threads_per_channel,
+                                 _stream(stream))
 
 
-def hymba_test_scan_fused(u, z, dtr, W_dt, dt_bias, BC, A_log, D, g, h_out=None, stream=None) -> int:
+def hymba_test_scan_fused(u, z, dtr, W_dt, dt_bias, BC, A_log, D, g, h_out=None, threads_per_channel=0,
+                          stream=None) -> int:
     B, L, di = u.shape
     N = A_log.shape[1]
     R = W_dt.shape[1]
     return lib().hymba_test_scan_fused(B, L, di, N, R, _ptr(u), u.stride(1), _ptr(z), z.stride(1), _ptr(dtr),
                                        dtr.stride(1), _ptr(W_dt), _ptr(dt_bias), _ptr(BC), _ptr(A_log), _ptr(D),
-                                       _ptr(g), _ptr(h_out), _stream(stream))
+                                       _ptr(g), _ptr(h_out), threads_per_channel, _stream(stream))
 
 
 def hymba_test_attention(Q, K, V, O, M: int, window: int, use_tc: bool, status=None, stream=None) -> int:

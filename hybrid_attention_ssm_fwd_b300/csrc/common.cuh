@@ -244,6 +244,12 @@ HY_DEV float ex2_approx(float x) {
   return y;
 }
 
+HY_DEV float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 HY_DEV float silu_f(float v) { return v / (1.0f + __expf(-v)); }
 
 HY_DEV float softplus_f(float v) { return v > 20.0f ? v : log1pf(__expf(v)); }
@@ -286,6 +292,11 @@ HY_DEV float2 up2(uint64_t r) {
 HY_DEV uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+HY_DEV uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 HY_DEV uint64_t mul2(uint64_t a, uint64_t b) {

@@ -33,6 +33,7 @@ __global__ void kv_append_kernel(int B, int Hkv, int dh, int dv, int window, int
     const int b = idx / (wk + wv);
     const int c = idx % (wk + wv);
     const int slot = ring_slot(pos[b], window, cap);
+    if (slot < 0 || slot >= cap) continue;  // a full global cache (or pos < 0): write nothing
     if (c < wk)
       k_ring[(static_cast<long long>(b) * cap + slot) * wk + c] = from_f<TC>(to_f(proj[b * ldp + k_col + c]));
     else
@@ -499,6 +500,12 @@ hymba_status decode_attention_split(int B, int M, int Hq, int Hkv, int dh, int d
     return HYMBA_ERR_CUDA;
   decode_attn_split_kernel<<<dim3(nsplit, Hkv, B), DA_THREADS, smem, st>>>(
       M, Hq, Hkv, dh, dv, window, cap, nsplit, q, ldq, k_meta, v_meta, k_ring, v_ring, pos, part);
+  decode_attn_combine_kernel<<<dim3(Hq, B), 128, 0, st>>>(Hq, dv, nsplit, part, out, ldo);
+  return last_err();
+}
+
+hymba_status decode_attn_combine(int B, int Hq, int dv, int nsplit, const float* part, __half* out, long long ldo,
+                                 cudaStream_t st) {
   decode_attn_combine_kernel<<<dim3(Hq, B), 128, 0, st>>>(Hq, dv, nsplit, part, out, ldo);
   return last_err();
 }

@@ -47,6 +47,23 @@ hymba_status decode_attention_split(int B, int M, int Hq, int Hkv, int dh, int d
                                     const __nv_bfloat16* v_ring, const int32_t* pos, float* part, __half* out,
                                     long long ldo, int max_keys, cudaStream_t st);
 
+// Merges per-split partials (m in log2 units, l, unnormalised o[dv]) into
+// out [B, Hq*dv] fp16.
+hymba_status decode_attn_combine(int B, int Hq, int dv, int nsplit, const float* part, __half* out, long long ldo,
+                                 cudaStream_t st);
+
+// Decode attention on persistent TMA-fed warps with mma.sync (see
+// decode_attn.cu): dh == 64, dv in {64, 128}, Hq / Hkv <= 8, bf16 caches.
+// part needs decode_attn_split_scratch(B, Hq, dv, nsplit) bytes; nsplit from
+// decode_attn_tc_splits.
+bool decode_attn_tc_supported(int Hq, int Hkv, int dh, int dv);
+int decode_attn_tc_splits(int B, int Hkv, int num_sms);
+hymba_status decode_attention_tc(int B, int M, int Hq, int Hkv, int dh, int dv, int window, int cap, int nsplit,
+                                 const __half* q, long long ldq, const __nv_bfloat16* k_meta,
+                                 const __nv_bfloat16* v_meta, const __nv_bfloat16* k_ring,
+                                 const __nv_bfloat16* v_ring, const int32_t* pos, float* part, __half* out,
+                                 long long ldo, int num_sms, int32_t* status, uint64_t wait_ns, cudaStream_t st);
+
 // Decode step of the SSM branch with the dt projection fused (see decode.cu).
 bool decode_ssm_step_supported(int N, int R);
 hymba_status decode_ssm_step(int B, int di, int N, int R, const __half* u, long long ldu, const __half* z,

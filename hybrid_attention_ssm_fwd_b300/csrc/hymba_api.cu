@@ -95,8 +95,11 @@ struct Plan {
   int attn_splits;
 };
 
-// Key splits of the decode attention: enough CTAs for ~4 per SM.
+int num_sms();
+
+// Key splits of the decode attention.
 int decode_attn_splits(const Dims& x) {
+  if (decode_attn_tc_supported(x.Hq, x.Hkv, x.dh, x.dv)) return decode_attn_tc_splits(x.B, x.Hkv, num_sms());
   const int ctas = x.B * x.Hkv;
   return std::max(1, std::min(16, (4 * 148 + ctas - 1) / ctas));
 }
@@ -357,7 +360,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     mk.mark();
     TRY(scan_fused_f16(x.B, x.L, x.di, x.N, x.R, u, x.di, proj + x.z_col, x.P_in, dtr, x.Rp,
                        static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, bc, w->A_log, w->D, g, nullptr, h_out,
-                       status, x.wait_ns, st));
+                       status, x.wait_ns, 0, st));
   } else {
     GemmParams p = gp(rows, x.di, x.R, status, x.wait_ns);
     p.C = delta;
@@ -366,7 +369,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     TRY(gemm_tc(0, dtr, x.Rp, at<__half>(ws, pl.wdt), x.Rp, EPI_SOFTPLUS, p, 0, 1, sms, st));
     mk.mark();
     TRY(scan_f16(x.B, x.L, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, bc, w->A_log, w->D, g, nullptr, h_out,
-                 status, x.wait_ns, st));
+                 status, x.wait_ns, 0, st));
   }
   mk.mark();
   // fuse + out_proj
@@ -457,7 +460,14 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
                                          static_cast<__nv_bfloat16*>(c->k_ring),
                                          static_cast<__nv_bfloat16*>(c->v_ring), st));
   mk.mark();
-  if (decode_attn_split_supported(x.Hq, x.Hkv, x.dh, x.dv)) {
+  if (decode_attn_tc_supported(x.Hq, x.Hkv, x.dh, x.dv)) {
+    TRY(decode_attention_tc(B, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, kvc->cap, pl.attn_splits, proj, x.P_in,
+                            static_cast<const __nv_bfloat16*>(kvc->k_meta),
+                            static_cast<const __nv_bfloat16*>(kvc->v_meta),
+                            static_cast<const __nv_bfloat16*>(kvc->k_ring),
+                            static_cast<const __nv_bfloat16*>(kvc->v_ring), c->pos, at<float>(ws, pl.apart), att,
+                            x.di, sms, status, x.wait_ns, st));
+  } else if (decode_attn_split_supported(x.Hq, x.Hkv, x.dh, x.dv)) {
     const int max_keys = x.M + (x.W > 0 ? std::min(x.W, kvc->cap) : kvc->cap);
     TRY(decode_attention_split(B, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, kvc->cap, pl.attn_splits, proj, x.P_in,
                                static_cast<const __nv_bfloat16*>(kvc->k_meta),
@@ -669,26 +679,28 @@ hymba_status hymba_test_gemm(int32_t M, int32_t N, int32_t K, int32_t ab_dtype, 
 
 hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t N, const void* u, int32_t ld_u, const void* z,
                              int32_t ld_z, const float* delta, const float* BC, const float* A_log, const float* D,
-                             void* g, float* h_out, void* stream) {
-  if (B < 1 || L < 1 || di < 1 || N < 1 || N > 64 || !u || !z || !delta || !BC || !A_log || !D || !g)
+                             void* g, float* h_out, int32_t threads_per_channel, void* stream) {
+  if (B < 1 || L < 1 || di < 1 || N < 1 || N > 64 || !u || !z || !delta || !BC || !A_log || !D || !g ||
+      (threads_per_channel != 0 && threads_per_channel != 1 && threads_per_channel != 2 && threads_per_channel != 4))
     return HYMBA_ERR_INVALID;
   cudaGetLastError();
   return scan_f16(B, L, di, N, static_cast<const __half*>(u), ld_u, static_cast<const __half*>(z), ld_z, delta, BC,
-                  A_log, D, static_cast<__half*>(g), nullptr, h_out, nullptr, 2000000000ull,
+                  A_log, D, static_cast<__half*>(g), nullptr, h_out, nullptr, 2000000000ull, threads_per_channel,
                   static_cast<cudaStream_t>(stream));
 }
 
 hymba_status hymba_test_scan_fused(int32_t B, int32_t L, int32_t di, int32_t N, int32_t R, const void* u,
                                    int32_t ld_u, const void* z, int32_t ld_z, const void* dtr, int32_t ld_dtr,
                                    const void* W_dt, const float* dt_bias, const float* BC, const float* A_log,
-                                   const float* D, void* g, float* h_out, void* stream) {
+                                   const float* D, void* g, float* h_out, int32_t threads_per_channel,
+                                   void* stream) {
   if (B < 1 || L < 1 || di < 1 || N < 1 || R < 1 || !u || !z || !dtr || !W_dt || !dt_bias || !BC || !A_log || !D ||
-      !g)
+      !g || (threads_per_channel != 0 && threads_per_channel != 1 && threads_per_channel != 2 && threads_per_channel != 4))
     return HYMBA_ERR_INVALID;
   cudaGetLastError();
   return scan_fused_f16(B, L, di, N, R, static_cast<const __half*>(u), ld_u, static_cast<const __half*>(z), ld_z,
                         static_cast<const __half*>(dtr), ld_dtr, static_cast<const __nv_bfloat16*>(W_dt), dt_bias, BC,
-                        A_log, D, static_cast<__half*>(g), nullptr, h_out, nullptr, 2000000000ull,
+                        A_log, D, static_cast<__half*>(g), nullptr, h_out, nullptr, 2000000000ull, threads_per_channel,
                         static_cast<cudaStream_t>(stream));
 }
 

@@ -7,17 +7,29 @@
 // with delta = softplus(dt W_dt^T + dt_bias) computed here (dt projection
 // fused in) or read from a delta buffer (component-test mode).
 //
-// One thread owns one (sequence, channel) and all 16 states, in registers
-// for the whole sequence, so the per-row loads, the C.h sum and the gate are
-// paid once per channel and no shuffle is needed.  A block of 64 threads
-// (two warps) owns 64 channels of one sequence.  Time is walked in chunks of
-// 16 rows whose dt (or delta) / u / z / [B|C] tiles arrive by TMA into a
-// 2-stage shared-memory ring.  In fused mode each warp computes delta for its
-// 32 channels x 16 rows with mma.sync (W_dt fragments stay in registers) and
-// applies softplus.  The scan advances 4 rows per group with paired fp32
-// arithmetic, which leaves 8 independent state pairs and 4 rows of loads in
-// flight per thread.  g is staged per chunk and written back with 16-byte
-// stores.
+// Work split.  A block owns CH channels of one sequence and walks the whole
+// sequence in chunks of SC_T rows.  The warps of a block specialise, like
+// the stages of a pipeline, so that the short dependent steps of one role
+// overlap the work of the others:
+//   delta warps (ND)  per chunk: delta for the block's channels x SC_T rows
+//                     (fused mode: mma.sync of the dt tile against W_dt
+//                     fragments kept in shared memory, then softplus;
+//                     otherwise the delta tile itself) and delta*u, as
+//                     (d, d*u) pairs; rows past the end of the sequence get
+//                     d = 0, which leaves the state unchanged;
+//   scan warps        the recurrence, fully unrolled over the chunk.  TPC
+//                     threads share one channel, each holding 16/TPC of its
+//                     states in registers for the whole sequence; their
+//                     partial C.h are summed with shuffles and stored per row;
+//   gate warp (1)     y = C.h + D*u, g = y*silu(z), eight channels of one row
+//                     per lane and one 16-byte store to global memory; its
+//                     lane 0 also issues the TMA loads of the chunk's dt (or
+//                     delta), u, z and [B|C] tiles into an SC_S-stage ring,
+//                     refilling a stage as soon as the gate is done with it
+//                     (the gate is the last reader of every stage).
+// (delta, delta*u) and C.h pass from role to role through double-buffered
+// shared-memory tiles guarded by mbarriers.  TPC is picked on the host from
+// the channels per SM.  Every wait is bounded.
 #include <type_traits>
 
 #include "scan.cuh"
@@ -26,33 +38,51 @@
 namespace hy {
 namespace {
 
-constexpr int SC_CH = 64;      // channels per block (one per thread)
-constexpr int SC_T = 16;       // time rows per chunk
-constexpr int SC_THREADS = 64;
-constexpr int SC_N = 16;       // states per channel on this path
+constexpr int SC_N = 16;  // states per channel on this path
+constexpr int SC_T = 16;  // time rows per chunk
+constexpr int SC_S = 3;   // TMA pipeline stages
+constexpr float kLog2e = 1.4426950408889634f;
 
-// KS = number of 16-wide k steps of the fused dt projection (0: delta input)
-template <int KS>
+// KS = 16-wide k steps of the fused dt projection (0: delta is an input).
+template <int KS, int TPC, int CH>
 struct ScanCfg {
-  static constexpr int KP = KS * 16;                       // padded dt rank
-  static constexpr int X_BYTES = KS > 0 ? SC_T * KP * 2 : SC_T * SC_CH * 4;  // dt tile or delta tile
-  static constexpr int U_BYTES = SC_T * SC_CH * 2;
-  static constexpr int Z_BYTES = SC_T * SC_CH * 2;
+  static constexpr int NWS = CH * TPC / 32;           // scan warps
+  static constexpr int ND = CH >= 64 ? CH / 32 : 1;   // delta warps
+  static constexpr int NW = NWS + ND + 1;             // + gate warp
+  static constexpr int NT = NW * 32;
+  static constexpr int W_DELTA = NWS;                 // first delta warp
+  static constexpr int W_GATE = NWS + ND;
+  static constexpr int CHW = 32 / TPC;                // channels per scan warp
+  static constexpr int NS = SC_N / TPC;               // states per scan thread
+  static constexpr int RPL = SC_T / TPC;              // rows of y each scan thread stores
+  static constexpr int CHD = CH / ND;                 // channels per delta warp
+  static constexpr int NTD = CHD / 8;                 // mma n-tiles per delta warp
+  static constexpr int KP = KS * 16;                  // padded dt rank
+  static constexpr int X_BYTES = KS > 0 ? SC_T * KP * 2 : SC_T * CH * 4;
+  static constexpr int U_BYTES = SC_T * CH * 2;
   static constexpr int BC_BYTES = SC_T * 2 * SC_N * 4;
   static constexpr int OFF_U = X_BYTES;
   static constexpr int OFF_Z = OFF_U + U_BYTES;
-  static constexpr int OFF_BC = OFF_Z + Z_BYTES;
-  static constexpr int STAGE = OFF_BC + BC_BYTES;
-  static constexpr int OFF_DELTA = 2 * STAGE;               // fused mode: delta tile [SC_T][SC_CH] fp32
-  static constexpr int OFF_G = OFF_DELTA + (KS > 0 ? SC_T * SC_CH * 4 : 0);
-  static constexpr int OFF_BAR = OFF_G + SC_T * SC_CH * 2;
-  static constexpr int SMEM = 128 + OFF_BAR + 64;
+  static constexpr int OFF_BC = OFF_Z + U_BYTES;
+  static constexpr int TX_BYTES = OFF_BC + BC_BYTES;  // bytes landing per stage
+  static constexpr int STAGE = (TX_BYTES + 127) / 128 * 128;
+  static constexpr int DU_STR = CH + 4;               // float2 per row of a (d, d*u) tile
+  static constexpr int DU_BYTES = SC_T * DU_STR * 8;
+  static constexpr int Y_BYTES = SC_T * CH * 4;       // C.h [SC_T][CH] fp32
+  static constexpr int W_BYTES = KS > 0 ? (CH / 8) * KS * 32 * 8 : 0;  // W_dt mma fragments
+  static constexpr int OFF_DU = SC_S * STAGE;
+  static constexpr int OFF_Y = OFF_DU + 2 * DU_BYTES;
+  static constexpr int OFF_W = OFF_Y + 2 * Y_BYTES;
+  static constexpr int OFF_BAR = OFF_W + W_BYTES;
+  static constexpr int N_BAR = SC_S + 8;
+  static constexpr int SMEM = 128 + OFF_BAR + N_BAR * 8;
+  static_assert(NWS >= 1 && CHD % 8 == 0 && CH % 8 == 0 && SC_T % TPC == 0, "scan block shape");
 };
 
 struct ScanArgs {
   int L, di, R;
-  const __nv_bfloat16* W_dt;   // [di, R] (fused mode)
-  const float* dt_bias;        // [di]    (fused mode)
+  const __nv_bfloat16* W_dt;  // [di, R] (fused mode)
+  const float* dt_bias;       // [di]    (fused mode)
   const float* A_log;
   const float* D;
   __half* g;
@@ -62,197 +92,293 @@ struct ScanArgs {
   uint64_t wait_ns;
 };
 
-template <int KS>
-__global__ void __launch_bounds__(SC_THREADS)
+HY_DEV void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// softplus(v) = ln(1 + e^v).  For e = e^v < 1/8 the alternating series of
+// ln(1 + e) to the e^6 term (truncation < e^7/7 < 7e-8 relative to the
+// result); above that ln2 * log2(1 + e), where 1 + e >= 1.125 keeps lg2's
+// relative error near 1e-6.  The second branch is taken by the whole warp or
+// skipped, so the common case costs one SFU operation.
+HY_DEV float softplus_scan(float v) {
+  if (v > 15.0f) return v;
+  const float e = ex2_approx(v * kLog2e);
+  float r = e * fmaf(e, fmaf(e, fmaf(e, fmaf(e, fmaf(e, -1.0f / 6, 0.2f), -0.25f), 1.0f / 3), -0.5f), 1.0f);
+  if (e >= 0.125f) r = lg2_approx(1.0f + e) * 0.6931471805599453f;
+  return r;
+}
+
+// y * silu(z) = y * z / (1 + 2^(-z log2 e))
+HY_DEV float gate1(float y, float z) { return y * z * rcp_approx(1.0f + ex2_approx(-kLog2e * z)); }
+
+template <int KS, int TPC, int CH>
+__global__ void __launch_bounds__(ScanCfg<KS, TPC, CH>::NT, 3)
     scan_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmU,
                 const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmBC,
                 const ScanArgs a) {
-  using Cfg = ScanCfg<KS>;
+  using Cfg = ScanCfg<KS, TPC, CH>;
   constexpr int N = SC_N;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+  // full[SC_S] | du_full[2] | du_empty[2] | y_full[2] | y_empty[2]
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto du_full = [&](int i) { return smem_u32(&bars[SC_S + i]); };
+  auto du_empty = [&](int i) { return smem_u32(&bars[SC_S + 2 + i]); };
+  auto y_full = [&](int i) { return smem_u32(&bars[SC_S + 4 + i]); };
+  auto y_empty = [&](int i) { return smem_u32(&bars[SC_S + 6 + i]); };
   __shared__ int abort_flag;
-  __half* sg = reinterpret_cast<__half*>(smem + Cfg::OFF_G);
+  __shared__ int n_issued;  // TMA chunks issued (read after the final barrier)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int cl = tid;               // channel within block
-  const int c0 = blockIdx.x * SC_CH;
+  const int c0 = blockIdx.x * CH;
   const int b = blockIdx.y;
-  const int c = c0 + cl;
   const int L = a.L, di = a.di;
   const long long row0 = static_cast<long long>(b) * L;
   const int n_chunks = (L + SC_T - 1) / SC_T;
 
   if (tid == 0) {
-    mbar_init(smem_u32(&bars[0]), 1);
-    mbar_init(smem_u32(&bars[1]), 1);
+    for (int s = 0; s < SC_S; ++s) mbar_init(full(s), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(du_full(i), Cfg::ND * 32);
+      mbar_init(du_empty(i), Cfg::NWS * 32);
+      mbar_init(y_full(i), Cfg::NWS * 32);
+      mbar_init(y_empty(i), 32);
+    }
     abort_flag = 0;
+    n_issued = 0;
     fence_mbar_init();
   }
   __syncthreads();
   const WaitCtl wc{&abort_flag, a.status, a.wait_ns};
+  auto stage = [&](int k) { return smem + (k % SC_S) * Cfg::STAGE; };
+  auto du_tile = [&](int k) { return reinterpret_cast<float2*>(smem + Cfg::OFF_DU + (k & 1) * Cfg::DU_BYTES); };
+  auto y_tile = [&](int k) { return reinterpret_cast<float*>(smem + Cfg::OFF_Y + (k & 1) * Cfg::Y_BYTES); };
 
-  auto issue = [&](int k) {
-    const int s = k & 1;
-    uint8_t* st = smem + s * Cfg::STAGE;
-    const uint32_t bar = smem_u32(&bars[s]);
-    const int r = static_cast<int>(row0) + k * SC_T;
-    mbar_arrive_expect_tx(bar, Cfg::STAGE);
-    tma_load_2d(smem_u32(st), &tmX, bar, KS > 0 ? 0 : c0, r);
-    tma_load_2d(smem_u32(st + Cfg::OFF_U), &tmU, bar, c0, r);
-    tma_load_2d(smem_u32(st + Cfg::OFF_Z), &tmZ, bar, c0, r);
-    tma_load_2d(smem_u32(st + Cfg::OFF_BC), &tmBC, bar, 0, r);
-  };
-  if (tid == 0) {
-    issue(0);
-    if (n_chunks > 1) issue(1);
-  }
-
-  // per-thread constants: A * log2(e) for the 16 states (packed pairs), D, state
-  uint64_t A2[N / 2], h2[N / 2];
+  if (warp < Cfg::NWS) {
+    // ------------------------------------------------------------ scan warps
+    constexpr int NS = Cfg::NS;
+    const int sub = lane % TPC;
+    const int chl = warp * Cfg::CHW + lane / TPC;
+    const int c = c0 + chl;
+    uint64_t A2[NS / 2], h2[NS / 2];
 #pragma unroll
-  for (int n = 0; n < N / 2; ++n) {
-    const int s0 = c * N + 2 * n;
-    A2[n] = pk2(-__expf(a.A_log[s0]) * 1.4426950408889634f, -__expf(a.A_log[s0 + 1]) * 1.4426950408889634f);
-    const long long hb = (static_cast<long long>(b) * di + c) * N + 2 * n;
-    h2[n] = a.h0 ? pk2(a.h0[hb], a.h0[hb + 1]) : pk2(0.f, 0.f);
-  }
-  const float Dc = a.D[c];
-
-  // fused dt projection: this warp's 32 channels = four n-tiles of 8
-  const int grp = lane >> 2, tig = lane & 3;
-  uint32_t bfr[4][KS > 0 ? KS : 1][2];
-  float bias_c[4][2];
-  if constexpr (KS > 0) {
+    for (int p = 0; p < NS / 2; ++p) {
+      const int s0 = c * N + sub * NS + 2 * p;
+      A2[p] = pk2(-__expf(a.A_log[s0]) * kLog2e, -__expf(a.A_log[s0 + 1]) * kLog2e);
+      const long long hb = (static_cast<long long>(b) * di + c) * N + sub * NS + 2 * p;
+      h2[p] = a.h0 ? pk2(a.h0[hb], a.h0[hb + 1]) : pk2(0.f, 0.f);
+    }
+    bool ok = true;
+    for (int k = 0; k < n_chunks; ++k) {
+      const int i = k & 1;
+      ok = mbar_wait(du_full(i), (k >> 1) & 1, wc) && mbar_wait(y_empty(i), ((k >> 1) & 1) ^ 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      const float2* du_p = du_tile(k) + chl;
+      const float* sBC = reinterpret_cast<const float*>(stage(k) + Cfg::OFF_BC);
+      float* y_p = y_tile(k) + chl;
+      // C.h stays in registers until the chunk is done: no store inside the
+      // loop, so the loads of later rows can be issued early
+      float yr[SC_T];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int ch = c0 + warp * 32 + nt * 8 + grp;
+      for (int t = 0; t < SC_T; ++t) {
+        const float2 q = du_p[t * Cfg::DU_STR];
+        const uint64_t dt2 = pk2(q.x, q.x), du2 = pk2(q.y, q.y);
+        const float4* Bp = reinterpret_cast<const float4*>(sBC + t * 2 * N + sub * NS);
+        const float4* Cp = reinterpret_cast<const float4*>(sBC + t * 2 * N + N + sub * NS);
+        uint64_t y0 = pk2(0.f, 0.f), y1 = pk2(0.f, 0.f);
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
+        for (int qq = 0; qq < NS / 4; ++qq) {
+          const float4 bb = Bp[qq], cc = Cp[qq];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r0 = kk * 16 + hh * 8 + tig * 2;
-          const float v0 = r0 < a.R ? __bfloat162float(a.W_dt[static_cast<long long>(ch) * a.R + r0]) : 0.f;
-          const float v1 = r0 + 1 < a.R ? __bfloat162float(a.W_dt[static_cast<long long>(ch) * a.R + r0 + 1]) : 0.f;
-          bfr[nt][kk][hh] = pack_half2(v0, v1);
+          for (int p2 = 0; p2 < 2; ++p2) {
+            const int p = qq * 2 + p2;
+            const float2 ea = up2(mul2(dt2, A2[p]));
+            const uint64_t av = pk2(ex2_approx(ea.x), ex2_approx(ea.y));
+            const uint64_t bu = mul2(du2, p2 == 0 ? pk2(bb.x, bb.y) : pk2(bb.z, bb.w));
+            h2[p] = fma2(av, h2[p], bu);
+            if (p2 == 0)
+              y0 = fma2(pk2(cc.x, cc.y), h2[p], y0);
+            else
+              y1 = fma2(pk2(cc.z, cc.w), h2[p], y1);
+          }
+        }
+        const float2 ys = up2(add2(y0, y1));
+        yr[t] = ys.x + ys.y;
+      }
+      // sum the TPC partials of each row: a transposing butterfly leaves
+      // lane `sub` with the totals of rows sub*RPL .. sub*RPL + RPL - 1
+#pragma unroll
+      for (int o = TPC / 2, m = SC_T; o >= 1; o >>= 1, m >>= 1) {
+        const bool upper = (sub & o) != 0;
+#pragma unroll
+        for (int j = 0; j < m / 2; ++j) {
+          const float keep = upper ? yr[m / 2 + j] : yr[j];
+          const float send = upper ? yr[j] : yr[m / 2 + j];
+          yr[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
       }
 #pragma unroll
-      for (int e = 0; e < 2; ++e) bias_c[nt][e] = a.dt_bias[c0 + warp * 32 + nt * 8 + tig * 2 + e];
+      for (int j = 0; j < Cfg::RPL; ++j) y_p[(sub * Cfg::RPL + j) * CH] = yr[j];
+      mbar_arrive(du_empty(i));
+      mbar_arrive(y_full(i));
     }
-  }
-
-  int kfail = -1;
-  for (int k = 0; k < n_chunks; ++k) {
-    const int s = k & 1;
-    const bool got = mbar_wait(smem_u32(&bars[s]), (k >> 1) & 1, wc);
-    if (!__syncthreads_and(got)) {
-      kfail = k;
-      break;
-    }
-    const uint8_t* st = smem + s * Cfg::STAGE;
-    const __half* sU = reinterpret_cast<const __half*>(st + Cfg::OFF_U);
-    const __half* sZ = reinterpret_cast<const __half*>(st + Cfg::OFF_Z);
-    const float* sBC = reinterpret_cast<const float*>(st + Cfg::OFF_BC);
-    const float* sD;
-    if constexpr (KS > 0) {
-      // delta[t][ch] = softplus(dt[t] . W_dt[ch] + bias[ch]) for 16 rows x this warp's 32 channels
-      const __half* sDT = reinterpret_cast<const __half*>(st);
-      float* sDw = reinterpret_cast<float*>(smem + Cfg::OFF_DELTA);
-      float acc[4][4];
+    if (ok && a.h_out) {
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const __half* base = sDT + grp * Cfg::KP + kk * 16 + tig * 2;
-        uint32_t af[4];
-        af[0] = *reinterpret_cast<const uint32_t*>(base);
-        af[1] = *reinterpret_cast<const uint32_t*>(base + 8 * Cfg::KP);
-        af[2] = *reinterpret_cast<const uint32_t*>(base + 8);
-        af[3] = *reinterpret_cast<const uint32_t*>(base + 8 * Cfg::KP + 8);
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) mma_16816_f16(acc[nt], af, bfr[nt][kk][0], bfr[nt][kk][1]);
-      }
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int col = warp * 32 + nt * 8 + tig * 2;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = grp + (e >> 1) * 8;
-          sDw[row * SC_CH + col + (e & 1)] = softplus_fast(acc[nt][e] + bias_c[nt][e & 1]);
-        }
-      }
-      __syncwarp();
-      sD = sDw;
-    } else {
-      sD = reinterpret_cast<const float*>(st);
-    }
-    const int nt_rows = min(SC_T, L - k * SC_T);
-
-    auto step = [&](int t) {
-      const float dt = sD[t * SC_CH + cl];
-      const float uu = __half2float(sU[t * SC_CH + cl]);
-      const float du = dt * uu;
-      const uint64_t dt2 = pk2(dt, dt), du2 = pk2(du, du);
-      const float4* Bp = reinterpret_cast<const float4*>(sBC + t * 2 * N);
-      const float4* Cp = reinterpret_cast<const float4*>(sBC + t * 2 * N + N);
-      uint64_t y0 = pk2(0.f, 0.f), y1 = pk2(0.f, 0.f);
-#pragma unroll
-      for (int qq = 0; qq < N / 4; ++qq) {
-        const float4 bb = Bp[qq], cc = Cp[qq];
-#pragma unroll
-        for (int p2 = 0; p2 < 2; ++p2) {
-          const int n = qq * 2 + p2;
-          const float2 ea = up2(mul2(dt2, A2[n]));
-          const uint64_t av = pk2(ex2_approx(ea.x), ex2_approx(ea.y));
-          const uint64_t bu = mul2(du2, p2 == 0 ? pk2(bb.x, bb.y) : pk2(bb.z, bb.w));
-          h2[n] = fma2(av, h2[n], bu);
-          if (p2 == 0)
-            y0 = fma2(pk2(cc.x, cc.y), h2[n], y0);
-          else
-            y1 = fma2(pk2(cc.z, cc.w), h2[n], y1);
-        }
-      }
-      const float2 ya = up2(y0), yb = up2(y1);
-      const float y = fmaf(Dc, uu, (ya.x + ya.y) + (yb.x + yb.y));
-      const float zz = __half2float(sZ[t * SC_CH + cl]);
-      const float sz = zz / (1.0f + ex2_approx(-1.4426950408889634f * zz));
-      sg[t * SC_CH + cl] = __float2half_rn(y * sz);
-    };
-    if (nt_rows == SC_T) {
-#pragma unroll 4
-      for (int t = 0; t < SC_T; ++t) step(t);
-    } else {
-      for (int t = 0; t < nt_rows; ++t) step(t);
-    }
-    __syncthreads();
-    // stage s is consumed: refill it with chunk k + 2 while g is written back
-    if (tid == 0 && k + 2 < n_chunks) issue(k + 2);
-    for (int idx = tid; idx < nt_rows * (SC_CH / 8); idx += SC_THREADS) {
-      const int tt = idx / (SC_CH / 8), q = idx % (SC_CH / 8);
-      *reinterpret_cast<uint4*>(a.g + (row0 + k * SC_T + tt) * di + c0 + q * 8) =
-          *reinterpret_cast<const uint4*>(sg + tt * SC_CH + q * 8);
-    }
-    __syncthreads();
-  }
-  if (kfail < 0) {
-    if (a.h_out) {
-#pragma unroll
-      for (int n = 0; n < N / 2; ++n) {
-        const float2 hv = up2(h2[n]);
-        const long long hb = (static_cast<long long>(b) * di + c) * N + 2 * n;
+      for (int p = 0; p < NS / 2; ++p) {
+        const float2 hv = up2(h2[p]);
+        const long long hb = (static_cast<long long>(b) * di + c) * N + sub * NS + 2 * p;
         a.h_out[hb] = hv.x;
         a.h_out[hb + 1] = hv.y;
       }
     }
-  } else if (tid == 0) {
-    // chunks kfail and kfail + 1 may still be landing: let them finish
-    for (int kk = kfail; kk < min(kfail + 2, n_chunks); ++kk)
-      mbar_wait_drain(smem_u32(&bars[kk & 1]), (kk >> 1) & 1, 1000000);
+  } else if (warp < Cfg::W_GATE) {
+    // ------------------------------------------------------------ delta warps
+    const int dw = warp - Cfg::W_DELTA;
+    const int grp = lane >> 2, tig = lane & 3;
+    const int dc0 = dw * Cfg::CHD;  // first channel of this warp within the block
+    constexpr int NTD = Cfg::NTD;
+    // W_dt as mma B fragments, [n-tile][k-step][lane] x 2 registers, in shared memory
+    uint2* sW = reinterpret_cast<uint2*>(smem + Cfg::OFF_W);
+    float bias_c[NTD][2];
+    if constexpr (KS > 0) {
+#pragma unroll
+      for (int nt = 0; nt < NTD; ++nt) {
+        const int ntg = dw * NTD + nt;
+        const int ch = c0 + ntg * 8 + grp;
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t f[2];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int r0 = kk * 16 + hh * 8 + tig * 2;
+            const float v0 = r0 < a.R ? __bfloat162float(a.W_dt[static_cast<long long>(ch) * a.R + r0]) : 0.f;
+            const float v1 =
+                r0 + 1 < a.R ? __bfloat162float(a.W_dt[static_cast<long long>(ch) * a.R + r0 + 1]) : 0.f;
+            f[hh] = pack_half2(v0, v1);
+          }
+          sW[(ntg * KS + kk) * 32 + lane] = make_uint2(f[0], f[1]);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) bias_c[nt][e] = a.dt_bias[c0 + dc0 + nt * 8 + tig * 2 + e];
+      }
+      __syncwarp();
+    }
+    for (int k = 0; k < n_chunks; ++k) {
+      const int i = k & 1;
+      bool ok = mbar_wait(full(k % SC_S), (k / SC_S) & 1, wc) && mbar_wait(du_empty(i), ((k >> 1) & 1) ^ 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint8_t* st = stage(k);
+      const __half* sU = reinterpret_cast<const __half*>(st + Cfg::OFF_U);
+      float2* du = du_tile(k);
+      const int nt_rows = min(SC_T, L - k * SC_T);
+      if constexpr (KS > 0) {
+        float acc[NTD][4];
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+        const uint32_t abase = smem_u32(st) + ((lane & 15) * Cfg::KP + (lane >> 4) * 8) * 2;
+        const uint2* wf = sW + dw * NTD * KS * 32 + lane;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t af[4];
+          ldsm_x4(abase + kk * 32, af);
+#pragma unroll
+          for (int nt = 0; nt < NTD; ++nt) {
+            const uint2 bw = wf[(nt * KS + kk) * 32];
+            mma_16816_f16(acc[nt], af, bw.x, bw.y);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NTD; ++nt) {
+          const int col = dc0 + nt * 8 + tig * 2;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int row = grp + hh * 8;
+            const float2 uv = __half22float2(*reinterpret_cast<const __half2*>(sU + row * CH + col));
+            float d0 = softplus_scan(acc[nt][2 * hh] + bias_c[nt][0]);
+            float d1 = softplus_scan(acc[nt][2 * hh + 1] + bias_c[nt][1]);
+            if (row >= nt_rows) d0 = d1 = 0.f;
+            *reinterpret_cast<float4*>(du + row * Cfg::DU_STR + col) = make_float4(d0, d0 * uv.x, d1, d1 * uv.y);
+          }
+        }
+      } else {
+        const float* sDl = reinterpret_cast<const float*>(st);
+        for (int idx = lane; idx < SC_T * Cfg::CHD; idx += 32) {
+          const int row = idx / Cfg::CHD, col = dc0 + idx % Cfg::CHD;
+          const float d = row < nt_rows ? sDl[row * CH + col] : 0.f;
+          du[row * Cfg::DU_STR + col] = make_float2(d, d * __half2float(sU[row * CH + col]));
+        }
+      }
+      mbar_arrive(du_full(i));
+    }
+  } else {
+    // ------------------------------------------------------------ gate warp (+ TMA)
+    constexpr int GPR = CH / 8;             // 8-channel groups per row
+    constexpr int ITEMS = SC_T * GPR;       // (row, group) items per chunk
+    const int gq = lane % GPR;
+    float Dg[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) Dg[e] = a.D[c0 + gq * 8 + e];
+    auto issue = [&](int k) {
+      uint8_t* st = stage(k);
+      const uint32_t bar = full(k % SC_S);
+      const int r = static_cast<int>(row0) + k * SC_T;
+      mbar_arrive_expect_tx(bar, Cfg::TX_BYTES);
+      tma_load_2d(smem_u32(st), &tmX, bar, KS > 0 ? 0 : c0, r);
+      tma_load_2d(smem_u32(st + Cfg::OFF_U), &tmU, bar, c0, r);
+      tma_load_2d(smem_u32(st + Cfg::OFF_Z), &tmZ, bar, c0, r);
+      tma_load_2d(smem_u32(st + Cfg::OFF_BC), &tmBC, bar, 0, r);
+    };
+    int issued = 0;
+    if (lane == 0)
+      for (; issued < min(SC_S, n_chunks); ++issued) issue(issued);
+    for (int k = 0; k < n_chunks; ++k) {
+      const int i = k & 1;
+      const bool ok = mbar_wait(y_full(i), (k >> 1) & 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint8_t* st = stage(k);
+      const __half* sU = reinterpret_cast<const __half*>(st + Cfg::OFF_U);
+      const __half* sZ = reinterpret_cast<const __half*>(st + Cfg::OFF_Z);
+      const float* yt = y_tile(k);
+      const int nt_rows = min(SC_T, L - k * SC_T);
+      for (int it = lane; it < ITEMS; it += 32) {
+        const int row = it / GPR;
+        if (row >= nt_rows) break;
+        const float4 ya = *reinterpret_cast<const float4*>(yt + row * CH + gq * 8);
+        const float4 yb = *reinterpret_cast<const float4*>(yt + row * CH + gq * 8 + 4);
+        const float y[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
+        const uint4 uv = *reinterpret_cast<const uint4*>(sU + row * CH + gq * 8);
+        const uint4 zv = *reinterpret_cast<const uint4*>(sZ + row * CH + gq * 8);
+        const __half2* uh = reinterpret_cast<const __half2*>(&uv);
+        const __half2* zh = reinterpret_cast<const __half2*>(&zv);
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 uf = __half22float2(uh[e]), zf = __half22float2(zh[e]);
+          o[e] = pack_half2(gate1(fmaf(Dg[2 * e], uf.x, y[2 * e]), zf.x),
+                            gate1(fmaf(Dg[2 * e + 1], uf.y, y[2 * e + 1]), zf.y));
+        }
+        *reinterpret_cast<uint4*>(a.g + (row0 + k * SC_T + row) * di + c0 + gq * 8) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      __syncwarp();
+      mbar_arrive(y_empty(i));
+      // the gate is the last reader of stage k: refill it with chunk k + SC_S
+      if (lane == 0 && issued < n_chunks) issue(issued++);
+    }
+    if (lane == 0) n_issued = issued;
+  }
+  // After a bounded wait gave up, loads may still be in flight: let the last
+  // stages land before the block exits (no-ops otherwise).
+  __syncthreads();
+  if (warp == Cfg::W_GATE && lane == 0) {
+    const int last = n_issued;
+    for (int j = max(0, last - SC_S); j < last; ++j) mbar_wait_drain(full(j % SC_S), (j / SC_S) & 1, 1000000);
   }
 }
 
@@ -280,57 +406,99 @@ bool map2(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, l
   return encode_tmap(m, dt, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int KS>
+template <int KS, int TPC, int CH>
 hymba_status launch_scan(int B, int L, int di, const CUtensorMap& mX, const __half* u, long long ld_u,
                          const __half* z, long long ld_z, const float* BC, const ScanArgs& args, cudaStream_t st) {
-  using Cfg = ScanCfg<KS>;
+  using Cfg = ScanCfg<KS, TPC, CH>;
   const long long rows = static_cast<long long>(B) * L;
   CUtensorMap mU, mZ, mBC;
-  if (!map2(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, u, di, rows, ld_u, SC_CH, SC_T) ||
-      !map2(&mZ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, z, di, rows, ld_z, SC_CH, SC_T) ||
+  if (!map2(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, u, di, rows, ld_u, CH, SC_T) ||
+      !map2(&mZ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, z, di, rows, ld_z, CH, SC_T) ||
       !map2(&mBC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BC, 2 * SC_N, rows, 2 * SC_N, 2 * SC_N, SC_T))
     return HYMBA_ERR_CUDA;
-  auto kern = scan_kernel<KS>;
+  auto kern = scan_kernel<KS, TPC, CH>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
-  dim3 grid(di / SC_CH, B);
-  kern<<<grid, SC_THREADS, Cfg::SMEM, st>>>(mX, mU, mZ, mBC, args);
+  dim3 grid(di / CH, B);
+  kern<<<grid, Cfg::NT, Cfg::SMEM, st>>>(mX, mU, mZ, mBC, args);
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 
-hymba_status launch_fused(int KS, int B, int L, int di, const CUtensorMap& mX, const __half* u, long long ld_u,
-                          const __half* z, long long ld_z, const float* BC, const ScanArgs& args, cudaStream_t st) {
+// Threads per channel, from the channels each SM gets: the recurrence of one
+// thread is a long chain of dependent steps, so with few channels per SM the
+// states are split over more threads (measured on B300: 16 states per thread
+// from ~300 channels per SM, 8 from ~80, 4 below).
+int pick_tpc(int B, int di, int num_sms) {
+  const long long per_sm = static_cast<long long>(B) * di / num_sms;
+  if (per_sm >= 300) return 1;
+  if (per_sm >= 80) return 2;
+  return 4;
+}
+
+// Channels per block: 64 (one wave of 2-3 blocks per SM at the 1.5B
+// shapes), 16 at four threads per channel so that a small batch still
+// spreads over the SMs.
+int block_channels(int tpc) { return tpc == 4 ? 16 : 64; }
+
+template <int KS>
+hymba_status launch_tpc(int tpc, int B, int L, int di, const CUtensorMap& mX, const __half* u, long long ld_u,
+                        const __half* z, long long ld_z, const float* BC, const ScanArgs& args, cudaStream_t st) {
+  switch (tpc) {
+    case 1: return launch_scan<KS, 1, 64>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 2: return launch_scan<KS, 2, 64>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 4: return launch_scan<KS, 4, 16>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    default: return HYMBA_ERR_UNSUPPORTED;
+  }
+}
+
+hymba_status launch_fused(int KS, int tpc, int B, int L, int di, const CUtensorMap& mX, const __half* u,
+                          long long ld_u, const __half* z, long long ld_z, const float* BC, const ScanArgs& args,
+                          cudaStream_t st) {
   switch (KS) {
-    case 1: return launch_scan<1>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 2: return launch_scan<2>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 3: return launch_scan<3>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 4: return launch_scan<4>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 5: return launch_scan<5>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 6: return launch_scan<6>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 7: return launch_scan<7>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 8: return launch_scan<8>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 1: return launch_tpc<1>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 2: return launch_tpc<2>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 3: return launch_tpc<3>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 4: return launch_tpc<4>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 5: return launch_tpc<5>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 6: return launch_tpc<6>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 7: return launch_tpc<7>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 8: return launch_tpc<8>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
     default: return HYMBA_ERR_UNSUPPORTED;
   }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+int resolve_tpc(int tpc, int B, int di) {
+  if (tpc == 0) {
+    int dev = 0, n = kNumSMsHint;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    tpc = pick_tpc(B, di, n > 0 ? n : kNumSMsHint);
+  }
+  if (tpc != 1 && tpc != 2 && tpc != 4) return -1;
+  if (di % block_channels(tpc) != 0) tpc = 4;  // 16-channel blocks fit any di % 16 == 0
+  return tpc;
+}
+
 }  // namespace
 
-bool scan_fused_supported(int di, int N, int R) { return di % SC_CH == 0 && N == SC_N && R >= 1 && R <= 128; }
+bool scan_fused_supported(int di, int N, int R) { return di % 16 == 0 && N == SC_N && R >= 1 && R <= 128; }
 
 hymba_status scan_f16(int B, int L, int di, int N, const __half* u, long long ld_u, const __half* z,
                       long long ld_z, const float* delta, const float* BC, const float* A_log, const float* D,
-                      __half* g, const float* h0, float* h_out, int32_t* status, uint64_t wait_ns,
+                      __half* g, const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, int tpc,
                       cudaStream_t st) {
-  const bool tma_ok = di % SC_CH == 0 && ld_u % 8 == 0 && ld_z % 8 == 0 && aligned16(u) && aligned16(z) &&
+  const bool tma_ok = di % 16 == 0 && ld_u % 8 == 0 && ld_z % 8 == 0 && aligned16(u) && aligned16(z) &&
                       aligned16(delta) && aligned16(BC) && aligned16(g);
   if (tma_ok && N == SC_N) {
+    tpc = resolve_tpc(tpc, B, di);
+    if (tpc < 0) return HYMBA_ERR_INVALID;
     CUtensorMap mX;
-    if (!map2(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, di, static_cast<long long>(B) * L, di, SC_CH, SC_T))
+    if (!map2(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, di, static_cast<long long>(B) * L, di,
+              block_channels(tpc), SC_T))
       return HYMBA_ERR_CUDA;
     ScanArgs args{L, di, 0, nullptr, nullptr, A_log, D, g, h0, h_out, status, wait_ns};
-    return launch_scan<0>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    return launch_tpc<0>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
   }
   return scan_simt<__half>(B, L, di, N, u, ld_u, z, ld_z, delta, di, BC, BC + N, 2 * N, A_log, D, g, di, h0, h_out,
                            st);
@@ -339,17 +507,20 @@ hymba_status scan_f16(int B, int L, int di, int N, const __half* u, long long ld
 hymba_status scan_fused_f16(int B, int L, int di, int N, int R, const __half* u, long long ld_u, const __half* z,
                             long long ld_z, const __half* dtr, long long ld_dtr, const __nv_bfloat16* W_dt,
                             const float* dt_bias, const float* BC, const float* A_log, const float* D, __half* g,
-                            const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, cudaStream_t st) {
+                            const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, int tpc,
+                            cudaStream_t st) {
   if (!scan_fused_supported(di, N, R)) return HYMBA_ERR_UNSUPPORTED;
   if (ld_u % 8 || ld_z % 8 || ld_dtr % 8 || !aligned16(u) || !aligned16(z) || !aligned16(dtr) || !aligned16(BC) ||
       !aligned16(g))
     return HYMBA_ERR_INVALID;
+  tpc = resolve_tpc(tpc, B, di);
+  if (tpc < 0) return HYMBA_ERR_INVALID;
   const int KS = (R + 15) / 16;
   CUtensorMap mX;
   if (!map2(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, dtr, R, static_cast<long long>(B) * L, ld_dtr, KS * 16, SC_T))
     return HYMBA_ERR_CUDA;
   ScanArgs args{L, di, R, W_dt, dt_bias, A_log, D, g, h0, h_out, status, wait_ns};
-  return launch_fused(KS, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+  return launch_fused(KS, tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
 }
 
 hymba_status wait_timeout_probe(uint32_t limit_us, int32_t* status, cudaStream_t st) {

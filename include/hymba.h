@@ -202,8 +202,9 @@ HYMBA_API size_t hymba_layer_decode_workspace(const hymba_layer_desc* d);
  * global layer); ssm_state and conv_state are advanced in place; pos[b] is
  * incremented at the end.
  *   x_new    [B, d] device, desc.dtype.      y  [B, d] device fp32.
- * Positions beyond what the cache can hold are not checked on the device:
- * the caller keeps pos[b] + 1 <= cap for global layers.                     */
+ * A global layer needs pos[b] + 1 <= cap: a token past a full global cache
+ * is not stored (the write is skipped on the device, never out of bounds)
+ * and attends to the first cap cached entries only.                         */
 HYMBA_API hymba_status hymba_layer_decode(const hymba_layer_desc* d, const hymba_layer_weights* w,
                                 const void* x_new, float* y, const hymba_cache* cache,
                                 const hymba_cache* shared_cache, void* ws, size_t ws_bytes,
@@ -278,22 +279,25 @@ HYMBA_API hymba_status hymba_test_gemm(int32_t M, int32_t N, int32_t K, int32_t 
  * hybrid head, section 2.1).  u, z: fp16 [B, L, di] (row strides ld_u, ld_z);
  * delta: fp32 [B, L, di]; BC: fp32 [B, L, 2N] ([B | C]); A_log [di, N], D [di]
  * fp32.  g: fp16 [B, L, di] = (C.h + D u) silu(z); h_out [B, di, N] fp32
- * final state (may be NULL).                                                */
+ * final state (may be NULL).  threads_per_channel: how many threads share
+ * one channel's states (1, 2 or 4; 0 = the choice hymba_layer_fwd makes).   */
 HYMBA_API hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t N,
                              const void* u, int32_t ld_u, const void* z, int32_t ld_z,
                              const float* delta, const float* BC, const float* A_log,
-                             const float* D, void* g, float* h_out, void* stream);
+                             const float* D, void* g, float* h_out,
+                             int32_t threads_per_channel, void* stream);
 
 /* The same scan with the dt projection fused in, as hymba_layer_fwd runs it:
  * delta = softplus(dtr . W_dt^T + dt_bias) is computed inside the kernel.
  * dtr fp16 [B, L, ld_dtr] (R valid columns, ld_dtr % 8 == 0), W_dt bf16
  * [di, R], dt_bias fp32 [di]; other arguments as hymba_test_scan.
- * HYMBA_ERR_UNSUPPORTED unless di % 32 == 0, N in {8, 16}, R <= 128.        */
+ * HYMBA_ERR_UNSUPPORTED unless di % 16 == 0, N == 16, R <= 128.             */
 HYMBA_API hymba_status hymba_test_scan_fused(int32_t B, int32_t L, int32_t di, int32_t N, int32_t R,
                                              const void* u, int32_t ld_u, const void* z, int32_t ld_z,
                                              const void* dtr, int32_t ld_dtr, const void* W_dt,
                                              const float* dt_bias, const float* BC, const float* A_log,
-                                             const float* D, void* g, float* h_out, void* stream);
+                                             const float* D, void* g, float* h_out,
+                                             int32_t threads_per_channel, void* stream);
 
 /* The bf16-path attention kernel alone (section 2.2 window + section 2.3 meta
  * prefix): Q [B, L, Hq, dh], K [B, L, Hkv, dh], V [B, L, Hkv, dv] fp16 ->

@@ -57,7 +57,7 @@ def _scan_inputs(B, L, di, N, seed, u0=None, d0=None, b0=None, c0=None):
         A_log.astype(np.float32).astype(F), D.astype(np.float32).astype(F)
 
 
-def _run_scan(u, z, dl, Bm, Cm, A_log, D):
+def _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc=0):
     B, L, di = u.shape
     N = Bm.shape[-1]
     dev = "cuda"
@@ -69,19 +69,21 @@ def _run_scan(u, z, dl, Bm, Cm, A_log, D):
     tD = torch.from_numpy(D).to(dev, torch.float32)
     g = torch.empty(B, L, di, device=dev, dtype=torch.float16)
     h = torch.empty(B, di, N, device=dev, dtype=torch.float32)
-    assert hb.hymba_test_scan(tu, tz, td, bc, ta, tD, g, h) == 0
+    assert hb.hymba_test_scan(tu, tz, td, bc, ta, tD, g, h, threads_per_channel=tpc) == 0
     torch.cuda.synchronize()
     return g.float().cpu().numpy().astype(F), h.cpu().numpy().astype(F)
 
 
-def test_scan_closed_form_on_gpu():
+@pytest.mark.parametrize("tpc", [1, 2, 4])
+def test_scan_closed_form_on_gpu(tpc):
     """Constant u, Delta, B, C with D = 0: the state follows the geometric
     series exactly, so C.h dominates the output (the case the end-to-end
-    tolerance cannot see)."""
+    tolerance cannot see).  Every split of the 16 states over 1, 2 or 4
+    threads per channel."""
     B, L, di, N = 2, 700, 64, 16
     u, z, dl, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 1, u0=0.75, d0=0.05, b0=1.25, c0=-0.5)
     D[:] = 0
-    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D)
+    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc)
     A = -np.exp(A_log)
     a = np.exp(0.05 * A)                                              # [di, N]
     t = np.arange(L)[:, None, None]
@@ -100,10 +102,11 @@ def test_scan_special_cases_on_gpu():
     assert np.all(h == 0)
 
 
-def test_scan_random_matches_oracle():
-    B, L, di, N = 3, 517, 192, 16
+@pytest.mark.parametrize("tpc,L", [(1, 517), (2, 517), (4, 517), (2, 3), (4, 18)])
+def test_scan_random_matches_oracle(tpc, L):
+    B, di, N = 3, 192, 16
     u, z, dl, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 3)
-    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D)
+    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc)
     y, hr = ref.selective_scan(u, dl, -np.exp(A_log), Bm, Cm, D)
     gr = y * ref.silu(z)
     np.testing.assert_allclose(h, hr, rtol=1e-4, atol=1e-5 * np.abs(hr).max())
@@ -170,7 +173,7 @@ def test_bounded_wait_reports_timeout():
     assert float((x * 2).sum().item()) == 8.0
 
 
-def _run_scan_fused(u, z, dtr, W_dt, dt_bias, Bm, Cm, A_log, D):
+def _run_scan_fused(u, z, dtr, W_dt, dt_bias, Bm, Cm, A_log, D, tpc=0):
     B, L, di = u.shape
     N = Bm.shape[-1]
     R = W_dt.shape[1]
@@ -187,7 +190,7 @@ def _run_scan_fused(u, z, dtr, W_dt, dt_bias, Bm, Cm, A_log, D):
     tD = torch.from_numpy(D).to(dev, torch.float32)
     g = torch.empty(B, L, di, device=dev, dtype=torch.float16)
     h = torch.empty(B, di, N, device=dev, dtype=torch.float32)
-    assert hb.hymba_test_scan_fused(tu, tz, tdt, tw, tb, bc, ta, tD, g, h) == 0
+    assert hb.hymba_test_scan_fused(tu, tz, tdt, tw, tb, bc, ta, tD, g, h, threads_per_channel=tpc) == 0
     torch.cuda.synchronize()
     return g.float().cpu().numpy().astype(F), h.cpu().numpy().astype(F)
 
@@ -214,8 +217,10 @@ def test_fused_scan_closed_form_on_gpu():
     np.testing.assert_allclose(g, expect_g, rtol=3e-3, atol=1e-3 * np.abs(expect_g).max())
 
 
-@pytest.mark.parametrize("R,di,L", [(100, 192, 517), (64, 128, 130), (8, 64, 33)])
-def test_fused_scan_random_matches_oracle(R, di, L):
+@pytest.mark.parametrize("R,di,L,tpc", [(100, 192, 517, 0), (100, 192, 517, 1), (100, 192, 517, 2),
+                                        (100, 192, 517, 4), (64, 128, 130, 2), (8, 64, 33, 1), (128, 48, 70, 4),
+                                        (17, 64, 1, 2)])
+def test_fused_scan_random_matches_oracle(R, di, L, tpc):
     B, N = 2, 16
     u, z, _, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 8)
     rng = np.random.default_rng(9)
@@ -223,7 +228,7 @@ def test_fused_scan_random_matches_oracle(R, di, L):
     W_dt = synth_bf16(rng.standard_normal((di, R)) * 0.1)
     dt0 = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), di))
     bias = (dt0 + np.log(-np.expm1(-dt0))).astype(np.float32).astype(F)
-    g, h = _run_scan_fused(u, z, dtr, W_dt, bias, Bm, Cm, A_log, D)
+    g, h = _run_scan_fused(u, z, dtr, W_dt, bias, Bm, Cm, A_log, D, tpc)
     dl = ref.softplus(dtr @ W_dt.T + bias)
     y, hr = ref.selective_scan(u, dl, -np.exp(A_log), Bm, Cm, D)
     gr = y * ref.silu(z)

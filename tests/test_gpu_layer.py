@@ -145,3 +145,33 @@ def test_bf16_prefill_then_decode_equals_longer_prefill():
     ys = [layer.decode(hl.tokens_to_device(p["Xt"][:, s0.L + i], sd), cache, cap).cpu().numpy() for i in range(n)]
     yr = ref.layer_fwd(p, p["Xt"], s)["Y"][:, s0.L:]
     assert_bf16_close(np.stack(ys, 1), yr, "bf16 prefill->decode")
+
+
+@pytest.mark.parametrize("kw,cap,pos", [
+    # ring not yet full, exactly full, wrapped into two slot ranges; meta of 16 (a partial chunk)
+    (dict(B=6, T=1, window=64), 64, [0, 5, 62, 63, 64, 500]),
+    # window smaller than the ring, ranges that straddle the ring's end
+    (dict(B=4, T=1, window=40, M=70), 100, [3, 39, 130, 199]),
+    # global layer: the cache holds every token, no wrap
+    (dict(B=3, T=1, window=0, M=0), 300, [0, 150, 299 - 1]),
+    # 1.5B widths: G = 5 query heads per KV head, dv = 128, a 1024-slot ring
+    (dict(B=3, T=1, M=128, d=1600, Hq=25, Hkv=5, di=3200, window=1024), 1024, [1, 1023, 8192]),
+])
+def test_bf16_decode_per_sequence_positions(kw, cap, pos):
+    """Each sequence at its own position: the visible ring slots form one or
+    two ranges of any length, next to a meta prefix that fills a partial
+    chunk or none."""
+    s = small_bf16(**kw)
+    inp = synth.make_decode_inputs(s, 7, cap=cap, pos=0)
+    inp["pos"] = np.asarray(pos, np.int32)
+    cache = hl.cache_to_device(inp, s)
+    layer = hl.HymbaLayer(s, hl.params_to_device(inp, s), decode=True)
+    y = layer.decode(hl.tokens_to_device(inp["x_new"], s), cache, cap).cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.check_status() == 0
+    keys = ("k_ring", "v_ring", "k_meta", "v_meta", "ssm_state", "conv_state", "pos")
+    r = ref.layer_decode(inp, inp["x_new"], {k: inp[k] for k in keys}, s)
+    assert_bf16_close(y, r["y"], f"decode y {pos}")
+    c = cache_np(cache)
+    assert np.all(c["pos"] == np.asarray(pos) + 1)
+    assert_bf16_close(c["k_ring"], r["cache"]["k_ring"], "decode k_ring")
