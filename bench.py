@@ -145,6 +145,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     peaks, peak_src = load_peaks()
+    if args.only_decode:
+        return {"decode": run_decode(args, torch, hb, hl, dev, torch.cuda.current_stream(dev), peaks, peak_src)}
     s = synth.hymba15b_swa(rope_theta=10000.0, B=args.batch)
     p = synth.make_layer_inputs(s, 1 + rank)
     params = hl.params_to_device(p, s, dev)
@@ -512,6 +514,8 @@ def main():
     ap.add_argument("--only-main", action="store_true",
                     help="time only the main prefill workload (used for profiler runs)")
     ap.add_argument("--batch", type=int, default=8, help="sequences in the main prefill workload")
+    ap.add_argument("--only-decode", action="store_true",
+                    help="time only the decode step (used for profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
     L.hymba_test_gemm.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
                                   c_void_p, c_int32, c_void_p, c_void_p]
     L.hymba_test_gemm.restype = c_int32
+    L.hymba_test_conv.argtypes = [c_int32] * 4 + [c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                  c_void_p]
+    L.hymba_test_conv.restype = c_int32
     L.hymba_test_scan.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]
     L.hymba_test_scan.restype = c_int32
@@ -232,6 +235,14 @@ def hymba_test_gemm(A, B, C, ab_dtype: int, status=None, stream=None) -> int:
     N = B.shape[0]
     return lib().hymba_test_gemm(M, N, K, ab_dtype, _ptr(A), A.stride(0), _ptr(B), B.stride(0), _ptr(C),
                                  C.stride(0), _ptr(status), _stream(stream))
+
+
+def hymba_test_conv(x, u, conv_w, conv_b, status=None, stream=None) -> int:
+    """x: fp16 [B, L, ld_x] (the first di columns are used); u: fp16 [B, L, di]."""
+    B, L, di = u.shape
+    k = conv_w.shape[1]
+    return lib().hymba_test_conv(B, L, di, k, _ptr(x), x.stride(1), _ptr(u), _ptr(conv_w), _ptr(conv_b),
+                                 _ptr(status), _stream(stream))
 
 
 def hymba_test_scan(u, z, delta, BC, A_log, D, g, h_out=None, threads_per_channel=0, stream=None) -> int:

@@ -21,7 +21,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhymba.so")
-SOURCES = ["tmap.cu", "gemm_tc.cu", "attn_tc.cu", "scan.cu", "simt.cu", "decode.cu", "decode_attn.cu", "hymba_api.cu"]
+SOURCES = ["tmap.cu", "gemm_tc.cu", "attn_tc.cu", "scan.cu", "simt.cu", "conv.cu", "decode.cu", "decode_attn.cu", "hymba_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

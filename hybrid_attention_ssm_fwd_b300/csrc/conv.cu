@@ -1,0 +1,186 @@
+// Causal depthwise conv1d + SiLU of the SSM branch on the fp16 path
+// ("Hymba: A Hybrid-head Architecture for Small Language Models", section 2.1:
+// the SSM heads' input goes through a short causal convolution before the
+// selective scan):
+//     u[b, t, c] = silu(bias[c] + sum_{j<K} w[c, j] * x[b, t - K + 1 + j, c]),
+// with x = 0 before the first row of each sequence.
+//
+// The step reads x once and writes u once, so it is bound by HBM.  Persistent
+// blocks walk tiles of TT rows x CW channels of one sequence; thread 0 streams
+// each tile, together with its K-1 rows of causal history, into a ring of
+// shared-memory stages with one 3-D TMA load (sequence, row, channel).  The
+// load of a tile that starts at row 0 begins at row -(K-1), which TMA fills
+// with zeros: that is the causal zero padding, and no row of the previous
+// sequence is ever read.  Each thread then computes 8 rows x 8 channels from
+// shared memory and writes 16-byte vectors of u.  Every wait is bounded.
+#include "simt.cuh"
+
+namespace hy {
+namespace {
+
+constexpr int CV_TT = 64;       // rows per tile
+constexpr int CV_CW = 128;      // channels per tile (256-byte rows)
+constexpr int CV_S = 3;         // ring stages
+constexpr int CV_THREADS = 128; // 16 channel groups x 8 row groups
+constexpr int CV_RPT = CV_TT / (CV_THREADS / (CV_CW / 8));  // rows per thread = 8
+
+template <int K>
+struct ConvCfg {
+  static constexpr int ROWS = CV_TT + K - 1;         // rows per stage, history included
+  static constexpr int STAGE = ROWS * CV_CW * 2;     // bytes per stage
+  static constexpr int SMEM = 128 + CV_S * STAGE;    // + mbarriers
+};
+
+template <int K>
+__global__ void __launch_bounds__(CV_THREADS, 3)
+    conv_tma_kernel(const __grid_constant__ CUtensorMap tmX, __half* __restrict__ u, long long ld_u, int B, int L,
+                    int di, const float* __restrict__ w, const float* __restrict__ bias, int32_t* status,
+                    uint64_t wait_ns) {
+  using Cfg = ConvCfg<K>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CV_S * Cfg::STAGE);
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x;
+  const int cg = tid % (CV_CW / 8), rg = tid / (CV_CW / 8);
+  const int n_ct = (di + CV_CW - 1) / CV_CW, n_tt = (L + CV_TT - 1) / CV_TT;
+  const int n_tiles = B * n_tt * n_ct;
+  if (tid == 0) {
+    for (int s = 0; s < CV_S; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl wc{&abort_flag, status, wait_ns};
+  // tile -> (channel tile fastest, then row tile, then sequence)
+  auto issue = [&](int tile, int s) {
+    const int ct = tile % n_ct, rest = tile / n_ct;
+    const int tt = rest % n_tt, b = rest / n_tt;
+    const uint32_t bar = smem_u32(&bars[s]);
+    mbar_arrive_expect_tx(bar, Cfg::STAGE);
+    tma_load_3d(smem_u32(smem + s * Cfg::STAGE), &tmX, bar, ct * CV_CW, tt * CV_TT - (K - 1), b);
+  };
+  int issued = 0;  // tiles issued by this block (thread 0's count)
+  if (tid == 0) {
+    tma_prefetch_desc(&tmX);
+    for (int j = 0; j < CV_S; ++j) {
+      const int tile = blockIdx.x + j * gridDim.x;
+      if (tile < n_tiles) {
+        issue(tile, j);
+        ++issued;
+      }
+    }
+  }
+  int it = 0;
+  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+    const int s = it % CV_S;
+    bool ok = mbar_wait(smem_u32(&bars[s]), (it / CV_S) & 1, wc);
+    if (!__syncthreads_and(ok)) break;
+    const int ct = tile % n_ct, rest = tile / n_ct;
+    const int tt = rest % n_tt, b = rest / n_tt;
+    const int c0 = ct * CV_CW + cg * 8;
+    if (c0 < di) {
+      float wt[8][K], bs[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        bs[e] = __ldg(bias + c0 + e);
+#pragma unroll
+        for (int j = 0; j < K; ++j) wt[e][j] = __ldg(w + (c0 + e) * K + j);
+      }
+      const uint8_t* st = smem + s * Cfg::STAGE + cg * 16;
+      const int r0 = rg * CV_RPT;  // first output row of this thread within the tile
+      float win[K][8];             // win[j] = x row (output row - K + 1 + j)
+#pragma unroll
+      for (int j = 0; j < K - 1; ++j) {
+        const uint4 q = *reinterpret_cast<const uint4*>(st + (r0 + j) * (CV_CW * 2));
+        const __half2* hq = reinterpret_cast<const __half2*>(&q);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(hq[e]);
+          win[j][2 * e] = f.x;
+          win[j][2 * e + 1] = f.y;
+        }
+      }
+      const long long row_base = static_cast<long long>(b) * L + tt * CV_TT;
+#pragma unroll
+      for (int r = 0; r < CV_RPT; ++r) {
+        const uint4 q = *reinterpret_cast<const uint4*>(st + (r0 + r + K - 1) * (CV_CW * 2));
+        const __half2* hq = reinterpret_cast<const __half2*>(&q);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(hq[e]);
+          win[K - 1][2 * e] = f.x;
+          win[K - 1][2 * e + 1] = f.y;
+        }
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float acc = bs[e];
+#pragma unroll
+          for (int j = 0; j < K; ++j) acc = fmaf(wt[e][j], win[j][e], acc);
+          o[e] = acc / (1.0f + __expf(-acc));
+        }
+#pragma unroll
+        for (int j = 0; j + 1 < K; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
+        const int t = tt * CV_TT + r0 + r;
+        if (t < L)
+          *reinterpret_cast<uint4*>(u + (row_base + r0 + r) * ld_u + c0) =
+              make_uint4(pack_half2(o[0], o[1]), pack_half2(o[2], o[3]), pack_half2(o[4], o[5]),
+                         pack_half2(o[6], o[7]));
+      }
+    }
+    __syncthreads();  // every thread is done with stage s
+    if (tid == 0) {
+      const int next = tile + CV_S * gridDim.x;
+      if (next < n_tiles) {
+        issue(next, s);
+        ++issued;
+      }
+    }
+  }
+  // after a wait gave up, let this block's loads in flight land before exit
+  if (tid == 0 && abort_flag)
+    for (int j = max(0, issued - CV_S); j < issued; ++j)
+      mbar_wait_drain(smem_u32(&bars[j % CV_S]), (j / CV_S) & 1, 1000000);
+}
+
+template <int K>
+hymba_status launch_conv(const CUtensorMap& m, __half* u, long long ld_u, int B, int L, int di, const float* w,
+                         const float* bias, int32_t* status, uint64_t wait_ns, int num_sms, cudaStream_t st) {
+  using Cfg = ConvCfg<K>;
+  auto kern = conv_tma_kernel<K>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
+  const long long tiles = static_cast<long long>(B) * ((L + CV_TT - 1) / CV_TT) * ((di + CV_CW - 1) / CV_CW);
+  const int grid = static_cast<int>(std::min<long long>(tiles, 3LL * num_sms));
+  kern<<<grid, CV_THREADS, Cfg::SMEM, st>>>(m, u, ld_u, B, L, di, w, bias, status, wait_ns);
+  return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool conv_tma_supported(int di, int k, long long ld_x, long long ld_u, const void* x, const void* u) {
+  return di % 8 == 0 && k >= 2 && k <= 4 && ld_x % 8 == 0 && ld_u % 8 == 0 &&
+         (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (reinterpret_cast<uintptr_t>(u) & 15) == 0;
+}
+
+hymba_status conv_silu_tma(const __half* x, long long ld_x, __half* u, long long ld_u, int B, int L, int di, int k,
+                           const float* w, const float* bias, int32_t* status, uint64_t wait_ns, int num_sms,
+                           cudaStream_t st) {
+  if (!conv_tma_supported(di, k, ld_x, ld_u, x, u)) return HYMBA_ERR_UNSUPPORTED;
+  if (B < 1 || L < 1) return HYMBA_OK;
+  CUtensorMap m;
+  const uint64_t dims[3] = {static_cast<uint64_t>(di), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
+  const uint64_t str[2] = {static_cast<uint64_t>(ld_x) * 2, static_cast<uint64_t>(ld_x) * 2 * L};
+  const uint32_t box[3] = {static_cast<uint32_t>(CV_CW), static_cast<uint32_t>(CV_TT + k - 1), 1};
+  if (!encode_tmap(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return HYMBA_ERR_CUDA;
+  switch (k) {
+    case 2: return launch_conv<2>(m, u, ld_u, B, L, di, w, bias, status, wait_ns, num_sms, st);
+    case 3: return launch_conv<3>(m, u, ld_u, B, L, di, w, bias, status, wait_ns, num_sms, st);
+    default: return launch_conv<4>(m, u, ld_u, B, L, di, w, bias, status, wait_ns, num_sms, st);
+  }
+}
+
+}  // namespace hy

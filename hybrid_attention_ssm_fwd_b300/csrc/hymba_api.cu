@@ -342,7 +342,11 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
   }
   mk.mark();
   // SSM branch
-  TRY(conv_silu<__half, __half>(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, st));
+  if (conv_tma_supported(x.di, x.k, x.P_in, x.di, proj + x.x_col, u))
+    TRY(conv_silu_tma(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, status, x.wait_ns,
+                      sms, st));
+  else
+    TRY(conv_silu<__half, __half>(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, st));
   mk.mark();
   {
     GemmParams p = gp(rows, x.xo, x.di, status, x.wait_ns);
@@ -675,6 +679,15 @@ hymba_status hymba_test_gemm(int32_t M, int32_t N, int32_t K, int32_t ab_dtype, 
   cudaGetLastError();
   return gemm_tc(ab_dtype == 1 ? 1 : 0, A, lda, B, ldb, EPI_F32, p, 0, 1, num_sms(),
                  static_cast<cudaStream_t>(stream));
+}
+
+hymba_status hymba_test_conv(int32_t B, int32_t L, int32_t di, int32_t k, const void* x, int32_t ld_x, void* u,
+                             const float* conv_w, const float* conv_b, int32_t* dev_status, void* stream) {
+  if (B < 1 || L < 1 || di < 1 || !x || !u || !conv_w || !conv_b || ld_x < di) return HYMBA_ERR_INVALID;
+  if (!conv_tma_supported(di, k, ld_x, di, x, u)) return HYMBA_ERR_UNSUPPORTED;
+  cudaGetLastError();
+  return conv_silu_tma(static_cast<const __half*>(x), ld_x, static_cast<__half*>(u), di, B, L, di, k, conv_w, conv_b,
+                       dev_status, 2000000000ull, num_sms(), static_cast<cudaStream_t>(stream));
 }
 
 hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t N, const void* u, int32_t ld_u, const void* z,

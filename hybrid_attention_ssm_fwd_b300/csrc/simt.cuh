@@ -30,6 +30,13 @@ template <typename TI, typename TO>
 hymba_status conv_silu(const TI* x, long long ld_x, TO* u, long long ld_u, int B, int L, int di, int k,
                        const float* w, const float* bias, cudaStream_t st);
 
+// fp16 conv + SiLU fed by TMA (conv.cu): the same result as conv_silu for
+// k in 2..4, di % 8 == 0, 16-byte aligned x and u, row strides % 8 == 0.
+bool conv_tma_supported(int di, int k, long long ld_x, long long ld_u, const void* x, const void* u);
+hymba_status conv_silu_tma(const __half* x, long long ld_x, __half* u, long long ld_u, int B, int L, int di, int k,
+                           const float* w, const float* bias, int32_t* status, uint64_t wait_ns, int num_sms,
+                           cudaStream_t st);
+
 // Generic selective scan + gate, one thread per (b, channel), N <= 64.
 // delta fp32 [B,L,di]; BC: B at Bm[row*ld_bc + n], C at Cm[row*ld_bc + n].
 // h0 (may be null) initial state, h_out (may be null) final state [B,di,N].

@@ -275,6 +275,17 @@ HYMBA_API hymba_status hymba_test_gemm(int32_t M, int32_t N, int32_t K, int32_t 
                              const void* A, int32_t lda, const void* B, int32_t ldb,
                              float* C, int32_t ldc, int32_t* dev_status, void* stream);
 
+/* The bf16-path causal depthwise conv + SiLU kernel alone (the SSM heads'
+ * short convolution, section 2.1): u[b,t,c] = silu(conv_b[c] + sum_j
+ * conv_w[c,j] x[b, t-k+1+j, c]) with x = 0 before row 0 of each sequence.
+ * x fp16 [B, L, ld_x] (di valid columns), u fp16 [B, L, di]; conv_w [di, k],
+ * conv_b [di] fp32.  HYMBA_ERR_UNSUPPORTED unless di % 8 == 0, 2 <= k <= 4,
+ * ld_x % 8 == 0 and x, u 16-byte aligned.                                    */
+HYMBA_API hymba_status hymba_test_conv(int32_t B, int32_t L, int32_t di, int32_t k,
+                                       const void* x, int32_t ld_x, void* u,
+                                       const float* conv_w, const float* conv_b,
+                                       int32_t* dev_status, void* stream);
+
 /* The bf16-path selective scan + gate kernel alone (SSM recurrence of the
  * hybrid head, section 2.1).  u, z: fp16 [B, L, di] (row strides ld_u, ld_z);
  * delta: fp32 [B, L, di]; BC: fp32 [B, L, 2N] ([B | C]); A_log [di, N], D [di]

@@ -239,3 +239,25 @@ def test_fused_scan_random_matches_oracle(R, di, L, tpc):
 def synth_bf16(a):
     from hybrid_attention_ssm_fwd_b300 import synth
     return synth.bf16_round(np.asarray(a, np.float32)).astype(F)
+
+
+@pytest.mark.parametrize("B,L,di,k,ld_x", [(3, 200, 256, 4, 520), (2, 64, 3200, 4, 3200), (1, 1, 136, 3, 136),
+                                          (4, 131, 24, 2, 40)])
+def test_conv_matches_oracle(B, L, di, k, ld_x):
+    """Causal conv + SiLU of the SSM branch: each sequence starts from zero
+    history (never the previous sequence's rows), ragged row and channel
+    tiles, strided input rows as in the projection buffer."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((B, L, ld_x)).astype(np.float16)
+    w = (rng.standard_normal((di, k)) * 0.5).astype(np.float32)
+    bias = (rng.standard_normal(di) * 0.1).astype(np.float32)
+    tx = torch.from_numpy(x).cuda()
+    u = torch.full((B, L, di), float("nan"), dtype=torch.float16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert hb.hymba_test_conv(tx, u, torch.from_numpy(w).cuda(), torch.from_numpy(bias).cuda(), status) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ur = ref.conv1d_silu(x[:, :, :di].astype(F), w.astype(F), bias.astype(F))
+    got = u.float().cpu().numpy()
+    # fp16 output: half an ulp of |u| plus fp32 accumulation
+    np.testing.assert_allclose(got, ur, rtol=1e-3, atol=1e-3)
