@@ -6,12 +6,13 @@
 // with x = 0 before the first row of each sequence.
 //
 // The step reads x once and writes u once, so it is bound by HBM.  Persistent
-// blocks walk tiles of TT rows x CW channels of one sequence; thread 0 streams
+// blocks own one channel tile (its weights stay in registers) and walk row
+// tiles of TT rows x CW channels of one sequence; thread 0 streams
 // each tile, together with its K-1 rows of causal history, into a ring of
 // shared-memory stages with one 3-D TMA load (sequence, row, channel).  The
 // load of a tile that starts at row 0 begins at row -(K-1), which TMA fills
 // with zeros: that is the causal zero padding, and no row of the previous
-// sequence is ever read.  Each thread then computes 8 rows x 8 channels from
+// sequence is ever read.  Each thread then computes 4 rows x 8 channels from
 // shared memory and writes 16-byte vectors of u.  Every wait is bounded.
 #include "simt.cuh"
 
@@ -21,8 +22,9 @@ namespace {
 constexpr int CV_TT = 64;       // rows per tile
 constexpr int CV_CW = 128;      // channels per tile (256-byte rows)
 constexpr int CV_S = 3;         // ring stages
-constexpr int CV_THREADS = 128; // 16 channel groups x 8 row groups
-constexpr int CV_RPT = CV_TT / (CV_THREADS / (CV_CW / 8));  // rows per thread = 8
+constexpr int CV_THREADS = 256; // 16 channel groups x 16 row groups
+constexpr int CV_RPT = CV_TT / (CV_THREADS / (CV_CW / 8));  // rows per thread = 4
+constexpr float kCvLog2e = 1.4426950408889634f;
 
 template <int K>
 struct ConvCfg {
@@ -32,7 +34,7 @@ struct ConvCfg {
 };
 
 template <int K>
-__global__ void __launch_bounds__(CV_THREADS, 3)
+__global__ void __launch_bounds__(CV_THREADS, 2)
     conv_tma_kernel(const __grid_constant__ CUtensorMap tmX, __half* __restrict__ u, long long ld_u, int B, int L,
                     int di, const float* __restrict__ w, const float* __restrict__ bias, int32_t* status,
                     uint64_t wait_ns) {
@@ -42,8 +44,11 @@ __global__ void __launch_bounds__(CV_THREADS, 3)
   __shared__ int abort_flag;
   const int tid = threadIdx.x;
   const int cg = tid % (CV_CW / 8), rg = tid / (CV_CW / 8);
+  // block -> (channel tile ct, slot j); slot j walks row tiles j, j + per_ct, ...
   const int n_ct = (di + CV_CW - 1) / CV_CW, n_tt = (L + CV_TT - 1) / CV_TT;
-  const int n_tiles = B * n_tt * n_ct;
+  const int per_ct = gridDim.x / n_ct;
+  const int ct = blockIdx.x % n_ct, slot = blockIdx.x / n_ct;
+  const int n_rt = B * n_tt;  // row tiles
   if (tid == 0) {
     for (int s = 0; s < CV_S; ++s) mbar_init(smem_u32(&bars[s]), 1);
     abort_flag = 0;
@@ -51,10 +56,8 @@ __global__ void __launch_bounds__(CV_THREADS, 3)
   }
   __syncthreads();
   const WaitCtl wc{&abort_flag, status, wait_ns};
-  // tile -> (channel tile fastest, then row tile, then sequence)
-  auto issue = [&](int tile, int s) {
-    const int ct = tile % n_ct, rest = tile / n_ct;
-    const int tt = rest % n_tt, b = rest / n_tt;
+  auto issue = [&](int rt, int s) {
+    const int tt = rt % n_tt, b = rt / n_tt;
     const uint32_t bar = smem_u32(&bars[s]);
     mbar_arrive_expect_tx(bar, Cfg::STAGE);
     tma_load_3d(smem_u32(smem + s * Cfg::STAGE), &tmX, bar, ct * CV_CW, tt * CV_TT - (K - 1), b);
@@ -63,29 +66,28 @@ __global__ void __launch_bounds__(CV_THREADS, 3)
   if (tid == 0) {
     tma_prefetch_desc(&tmX);
     for (int j = 0; j < CV_S; ++j) {
-      const int tile = blockIdx.x + j * gridDim.x;
-      if (tile < n_tiles) {
-        issue(tile, j);
+      const int rt = slot + j * per_ct;
+      if (rt < n_rt) {
+        issue(rt, j);
         ++issued;
       }
     }
   }
+  const int c0 = ct * CV_CW + cg * 8;
+  float wt[8][K], bs[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    bs[e] = c0 < di ? __ldg(bias + c0 + e) : 0.f;
+#pragma unroll
+    for (int j = 0; j < K; ++j) wt[e][j] = c0 < di ? __ldg(w + (c0 + e) * K + j) : 0.f;
+  }
   int it = 0;
-  for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+  for (int rt = slot; rt < n_rt; rt += per_ct, ++it) {
     const int s = it % CV_S;
     bool ok = mbar_wait(smem_u32(&bars[s]), (it / CV_S) & 1, wc);
     if (!__syncthreads_and(ok)) break;
-    const int ct = tile % n_ct, rest = tile / n_ct;
-    const int tt = rest % n_tt, b = rest / n_tt;
-    const int c0 = ct * CV_CW + cg * 8;
+    const int tt = rt % n_tt, b = rt / n_tt;
     if (c0 < di) {
-      float wt[8][K], bs[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        bs[e] = __ldg(bias + c0 + e);
-#pragma unroll
-        for (int j = 0; j < K; ++j) wt[e][j] = __ldg(w + (c0 + e) * K + j);
-      }
       const uint8_t* st = smem + s * Cfg::STAGE + cg * 16;
       const int r0 = rg * CV_RPT;  // first output row of this thread within the tile
       float win[K][8];             // win[j] = x row (output row - K + 1 + j)
@@ -117,7 +119,7 @@ __global__ void __launch_bounds__(CV_THREADS, 3)
           float acc = bs[e];
 #pragma unroll
           for (int j = 0; j < K; ++j) acc = fmaf(wt[e][j], win[j][e], acc);
-          o[e] = acc / (1.0f + __expf(-acc));
+          o[e] = acc * rcp_approx(1.0f + ex2_approx(-kCvLog2e * acc));  // silu
         }
 #pragma unroll
         for (int j = 0; j + 1 < K; ++j)
@@ -132,8 +134,8 @@ __global__ void __launch_bounds__(CV_THREADS, 3)
     }
     __syncthreads();  // every thread is done with stage s
     if (tid == 0) {
-      const int next = tile + CV_S * gridDim.x;
-      if (next < n_tiles) {
+      const int next = rt + CV_S * per_ct;
+      if (next < n_rt) {
         issue(next, s);
         ++issued;
       }
@@ -152,8 +154,11 @@ hymba_status launch_conv(const CUtensorMap& m, __half* u, long long ld_u, int B,
   auto kern = conv_tma_kernel<K>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
-  const long long tiles = static_cast<long long>(B) * ((L + CV_TT - 1) / CV_TT) * ((di + CV_CW - 1) / CV_CW);
-  const int grid = static_cast<int>(std::min<long long>(tiles, 3LL * num_sms));
+  // every channel tile gets the same number of blocks (about two per SM in all)
+  const int n_ct = (di + CV_CW - 1) / CV_CW;
+  const long long n_rt = static_cast<long long>(B) * ((L + CV_TT - 1) / CV_TT);
+  const int per_ct = static_cast<int>(std::max(1LL, std::min(n_rt, (2LL * num_sms + n_ct - 1) / n_ct)));
+  const int grid = n_ct * per_ct;
   kern<<<grid, CV_THREADS, Cfg::SMEM, st>>>(m, u, ld_u, B, L, di, w, bias, status, wait_ns);
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }

@@ -374,6 +374,77 @@ __global__ void __launch_bounds__(256) fuse_norm_vec_kernel(int di, const __half
   }
 }
 
+// fp16 fused norm, one warp per row: a lane holds up to FW_V 16-byte vectors
+// of att and of g, all loaded before the first use (one HBM read, many loads
+// in flight), and the two sums of squares are reduced with shuffles only.
+constexpr int FW_V = 16;  // di <= 32 * 8 * FW_V = 4096
+
+__global__ void __launch_bounds__(128) fuse_norm_warp_kernel(int rows, int di, const __half* __restrict__ att,
+                                                             const __half* __restrict__ g,
+                                                             const float* __restrict__ beta1,
+                                                             const float* __restrict__ beta2, float eps,
+                                                             __half* __restrict__ s) {
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int nch = di / 8;
+  const uint4* a4 = reinterpret_cast<const uint4*>(att + row * di);
+  const uint4* g4 = reinterpret_cast<const uint4*>(g + row * di);
+  uint4 av[FW_V], gv[FW_V];
+#pragma unroll
+  for (int q = 0; q < FW_V; ++q) {
+    const int ch = lane + q * 32;
+    if (ch < nch) {
+      av[q] = __ldcs(a4 + ch);  // read once: do not keep in L2
+      gv[q] = __ldcs(g4 + ch);
+    }
+  }
+  float sa = 0.f, sg = 0.f;
+#pragma unroll
+  for (int q = 0; q < FW_V; ++q) {
+    if (lane + q * 32 < nch) {
+      const __half2* ah = reinterpret_cast<const __half2*>(&av[q]);
+      const __half2* gh = reinterpret_cast<const __half2*>(&gv[q]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __half22float2(ah[e]), fg = __half22float2(gh[e]);
+        sa = fmaf(fa.x, fa.x, fmaf(fa.y, fa.y, sa));
+        sg = fmaf(fg.x, fg.x, fmaf(fg.y, fg.y, sg));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sa += __shfl_xor_sync(0xffffffffu, sa, o);
+    sg += __shfl_xor_sync(0xffffffffu, sg, o);
+  }
+  const float ra = rsqrtf(sa / di + eps), rg = rsqrtf(sg / di + eps);
+  uint4* s4 = reinterpret_cast<uint4*>(s + row * di);
+#pragma unroll
+  for (int q = 0; q < FW_V; ++q) {
+    const int ch = lane + q * 32;
+    if (ch < nch) {
+      const __half2* ah = reinterpret_cast<const __half2*>(&av[q]);
+      const __half2* gh = reinterpret_cast<const __half2*>(&gv[q]);
+      const float4 b1a = __ldg(reinterpret_cast<const float4*>(beta1 + ch * 8));
+      const float4 b1b = __ldg(reinterpret_cast<const float4*>(beta1 + ch * 8 + 4));
+      const float4 b2a = __ldg(reinterpret_cast<const float4*>(beta2 + ch * 8));
+      const float4 b2b = __ldg(reinterpret_cast<const float4*>(beta2 + ch * 8 + 4));
+      const float bb1[8] = {b1a.x * ra, b1a.y * ra, b1a.z * ra, b1a.w * ra, b1b.x * ra, b1b.y * ra, b1b.z * ra,
+                            b1b.w * ra};
+      const float bb2[8] = {b2a.x * rg, b2a.y * rg, b2a.z * rg, b2a.w * rg, b2b.x * rg, b2b.y * rg, b2b.z * rg,
+                            b2b.w * rg};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __half22float2(ah[e]), fg = __half22float2(gh[e]);
+        o[e] = pack_half2(fmaf(bb1[2 * e], fa.x, bb2[2 * e] * fg.x), fmaf(bb1[2 * e + 1], fa.y, bb2[2 * e + 1] * fg.y));
+      }
+      s4[ch] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // SIMT attention: one warp per (b, row i, query head)
 // ---------------------------------------------------------------------------
@@ -576,8 +647,16 @@ template <typename T>
 hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* beta1, const float* beta2,
                        float eps, T* s, cudaStream_t st) {
   if (rows <= 0) return HYMBA_OK;
-  if (std::is_same<T, __half>::value && di % 8 == 0 && di <= 8 * 256 * FN_MAXC &&
-      (reinterpret_cast<uintptr_t>(beta1) & 15) == 0 && (reinterpret_cast<uintptr_t>(beta2) & 15) == 0) {
+  const bool vec_ok = std::is_same<T, __half>::value && di % 8 == 0 && (reinterpret_cast<uintptr_t>(beta1) & 15) == 0 &&
+                      (reinterpret_cast<uintptr_t>(beta2) & 15) == 0 && (reinterpret_cast<uintptr_t>(att) & 15) == 0 &&
+                      (reinterpret_cast<uintptr_t>(g) & 15) == 0 && (reinterpret_cast<uintptr_t>(s) & 15) == 0;
+  if (vec_ok && di <= 32 * 8 * FW_V) {
+    fuse_norm_warp_kernel<<<(rows + 3) / 4, 128, 0, st>>>(rows, di, reinterpret_cast<const __half*>(att),
+                                                          reinterpret_cast<const __half*>(g), beta1, beta2, eps,
+                                                          reinterpret_cast<__half*>(s));
+    return last_err();
+  }
+  if (vec_ok && di <= 8 * 256 * FN_MAXC) {
     fuse_norm_vec_kernel<<<rows, 256, 0, st>>>(di, reinterpret_cast<const __half*>(att),
                                                reinterpret_cast<const __half*>(g), beta1, beta2, eps,
                                                reinterpret_cast<__half*>(s));
