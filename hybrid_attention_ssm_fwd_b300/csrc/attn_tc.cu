@@ -3,67 +3,78 @@
 // sliding-window / global attention, section 2.3 meta tokens): query row i
 // sees key j iff j <= i and (window == 0 or i - j < window or j < M).
 //
-// One persistent CTA per SM walks work units (batch, 128-row query tile,
-// query head), heaviest query tiles first.  Per unit only the key tiles that
-// can hold a visible key are visited: the meta tiles and the tiles of the
-// window (all tiles up to the diagonal for a global layer).
+// One persistent CTA per SM walks work units (batch b, 128-row query tile,
+// pair of query heads A and B of one KV group), heaviest query tiles first.
+// Both heads of a unit read the same K/V tiles, so each tile is loaded once
+// for two heads.  Per unit only the 64-key tiles that can hold a visible key
+// are visited: the meta tiles and the tiles of the window (all tiles up to the
+// diagonal for a global layer).
 //
-//   warp 0      TMA: Q tile once per unit; K tiles and V tiles through two
-//               2-stage rings (128-byte swizzle).
-//   warp 1      TMEM owner; one thread issues S = Q K^T (M=128, N=128, K=16
-//               x4) into one of two TMEM S buffers and O += P V (N = dv, K=16
-//               x8, V read MN-major) into the TMEM O accumulator, in the order
-//               S0 S1 PV0 S2 PV1 ... so softmax of tile j overlaps S_{j+1} and
-//               PV_{j-1}.
-//   warps 2..5  softmax, one query row per thread (TMEM lane = row): masked
-//               row max, exp2, row sum, P (fp16) written to shared memory in
-//               the swizzled K-major layout the MMA reads.  The running max is
-//               only raised when a tile's max exceeds it by more than 2^8
-//               (then O is rescaled in TMEM after the previous PV completes);
-//               otherwise P stays <= 2^8, which fp16 and fp32 hold exactly
-//               enough.  At the end of a unit O / l is stored as fp16.
-// Every wait is bounded (see WaitCtl).
+//   warps 0-3  softmax of head A, warps 4-7 softmax of head B: one query row
+//              per thread (TMEM lane = row).  Masked row max, exp2, row sum;
+//              P (fp16) is written back into TMEM over the first half of the
+//              S buffer it came from.  The running max is only raised when a
+//              tile's max exceeds it by more than 2^8 (then O is rescaled in
+//              TMEM), so P stays <= 2^8.  At the end of a unit O / l is stored.
+//   warp 8     TMA: Q of both heads once per unit; K and V tiles through two
+//              6-stage rings (128-byte swizzle).
+//   warps 9,10 one thread each issues the MMAs of head A / head B (warp 9
+//              also owns TMEM).  S is double-buffered per head, so S of tile
+//              t+1 is computed while the softmax works on tile t, and S of tile
+//              t+2 is issued right after P V of tile t (it reuses that buffer):
+//                S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ...   for each head.
+//              S = Q K^T reads Q and K from shared memory; O += P V reads P
+//              from TMEM and V from shared memory.
+// TMEM columns: S_A buffers [0,64) [64,128), S_B buffers [128,192) [192,256),
+// O_A [256, 256+dv), O_B after it.  Every wait is bounded (see WaitCtl).
 #include "attn_tc.cuh"
 
 namespace hy {
 namespace {
 
 constexpr int BQ = 128;        // query rows per unit
-constexpr int BKV = 128;       // keys per tile
+constexpr int BKV = 64;        // keys per tile
 constexpr int DH = 64;         // Q/K head dim handled here
+constexpr int KV_STAGES = 6;   // K and V ring depth
+constexpr int MAX_HU = 128;    // head units (pairs or single heads)
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int NTHREADS = 352;  // 11 warps
+constexpr int W_TMA = 8, W_MMA = 9;  // MMA issuers: warps 9 (head A) and 10 (head B)
 
 struct AttnParams {
-  int B, L, M, Hq, Hkv, dv, window, n_qt, n_units;
+  int B, L, M, Hq, Hkv, dv, window, n_qt, n_hu, n_units;
   float scale_log2;  // log2(e) / sqrt(dh)
   __half* O;
   long long ldo;
   int32_t* status;
   uint64_t wait_ns;
+  int16_t hA[MAX_HU], hB[MAX_HU];  // head unit -> heads (hB = -1: single head)
 };
 
 struct Unit {
-  int b, h, g, q0, qv1;  // qv1 = min(q0 + BQ, L)
-  int n_tiles, meta_last, win_first, split;  // split: tiles [0, split) are 0.., rest start at win_first
+  int b, hA, hB, g, q0, qv1;  // qv1 = min(q0 + BQ, L)
+  int n_tiles, win_first, split;  // split: tiles [0, split) are 0.., rest start at win_first
 };
 
 HY_DEV Unit make_unit(const AttnParams& p, int u) {
   Unit U;
-  U.h = u % p.Hq;
-  const int r = u / p.Hq;
+  const int hu = u % p.n_hu;
+  const int r = u / p.n_hu;
   const int qt = p.n_qt - 1 - (r % p.n_qt);
   U.b = r / p.n_qt;
-  U.g = (U.h * p.Hkv) / p.Hq;
+  U.hA = p.hA[hu];
+  U.hB = p.hB[hu];
+  U.g = (U.hA * p.Hkv) / p.Hq;
   U.q0 = qt * BQ;
   U.qv1 = min(U.q0 + BQ, p.L);
   const int diag = (U.qv1 - 1) / BKV;
-  U.meta_last = p.M > 0 ? (p.M - 1) / BKV : -1;
+  const int meta_last = p.M > 0 ? (p.M - 1) / BKV : -1;
   U.win_first = p.window > 0 ? max(0, U.q0 - p.window + 1) / BKV : 0;
-  if (U.win_first <= U.meta_last + 1) {
+  if (U.win_first <= meta_last + 1) {
     U.n_tiles = diag + 1;
     U.split = U.n_tiles;
   } else {
-    U.split = U.meta_last + 1;
+    U.split = meta_last + 1;
     U.n_tiles = U.split + diag - U.win_first + 1;
   }
   return U;
@@ -73,30 +84,62 @@ HY_DEV int tile_kt(const Unit& U, int t) { return t < U.split ? t : U.win_first 
 
 template <int DV>
 struct AttnCfg {
-  static constexpr int Q_BYTES = BQ * DH * 2;            // 16 KB
-  static constexpr int K_BYTES = BKV * DH * 2;           // 16 KB
-  static constexpr int V_BYTES = BKV * DV * 2;           // 16/32 KB
-  static constexpr int P_BYTES = BQ * BKV * 2;           // 32 KB
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * V_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  static constexpr uint32_t TMEM_COLS = 512;             // S0, S1 (128 each), O (DV)
-  static constexpr uint32_t O_COL = 256;
+  static constexpr int Q_BYTES = BQ * DH * 2;            // 16 KB per head
+  static constexpr int K_BYTES = BKV * DH * 2;           // 8 KB
+  static constexpr int V_BYTES = BKV * DV * 2;           // 8/16 KB
+  static constexpr int OFF_Q = 0;                        // Q_A | Q_B
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + KV_STAGES * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + KV_STAGES * V_BYTES;
+  static constexpr int SMEM = 1024 + OFF_BAR + 512;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // S buffer `buf` of head x, O of head x
+  static HY_DEV uint32_t s_col(int x, uint32_t buf) { return static_cast<uint32_t>(x) * 128u + (buf & 1u) * 64u; }
+  static HY_DEV uint32_t o_col(int x) { return x == 0 ? 256u : 256u + DV; }
 };
 
 // barrier indices
 enum {
-  B_QFULL = 0, B_QEMPTY, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1,
-  B_SFULL0, B_SFULL1, B_SEMPTY0, B_SEMPTY1, B_PFULL0, B_PFULL1, B_PVDONE0, B_PVDONE1, B_OEMPTY, B_COUNT
+  B_QFULL = 0, B_QEMPTY,
+  B_KFULL = 2,                        // [KV_STAGES]
+  B_KEMPTY = B_KFULL + KV_STAGES,     // [KV_STAGES]
+  B_VFULL = B_KEMPTY + KV_STAGES,     // [KV_STAGES]
+  B_VEMPTY = B_VFULL + KV_STAGES,     // [KV_STAGES]
+  B_SFULL = B_VEMPTY + KV_STAGES,     // [head][buffer]
+  B_PFULL = B_SFULL + 4,              // [head][buffer], 4 arrivals (softmax warps)
+  B_PVDONE = B_PFULL + 4,             // [head]
+  B_OEMPTY = B_PVDONE + 2,            // [head], 4 arrivals
+  B_COUNT = B_OEMPTY + 2
 };
 
+HY_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+HY_DEV float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// O += P V with A (P, fp16, 128 x 16 per MMA) read from TMEM.
+HY_DEV void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 template <int DV>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
   using Cfg = AttnCfg<DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -106,160 +149,176 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sQ = smem_u32(smem + Cfg::OFF_Q);
   const uint32_t sK = smem_u32(smem + Cfg::OFF_K);
   const uint32_t sV = smem_u32(smem + Cfg::OFF_V);
-  const uint32_t sP = smem_u32(smem + Cfg::OFF_P);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
-      const bool four = (i == B_SEMPTY0 || i == B_SEMPTY1 || i == B_PFULL0 || i == B_PFULL1 || i == B_OEMPTY);
-      mbar_init(bar(i), four ? 4 : 1);
+      const bool four = (i >= B_PFULL && i < B_PFULL + 4) || i == B_OEMPTY || i == B_OEMPTY + 1;
+      // ring slots and Q are released by both MMA issuers
+      const bool two = i == B_QEMPTY || (i >= B_KEMPTY && i < B_KEMPTY + KV_STAGES) ||
+                       (i >= B_VEMPTY && i < B_VEMPTY + KV_STAGES);
+      mbar_init(bar(i), four ? 4 : two ? 2 : 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+  if (warp == W_MMA) tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, p.status, p.wait_ns};
 
-  if (warp == 0) {
+  if (warp == W_TMA) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       uint32_t kc = 0, uc = 0;
-      uint32_t issued = 0, par = 0;  // bits: Q, K0, K1, V0, V1 outstanding + their parities
       bool ok = true;
       for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
         const Unit U = make_unit(p, u);
         if (!mbar_wait(bar(B_QEMPTY), (uc & 1) ^ 1, wc)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar(B_QFULL), Cfg::Q_BYTES);
-        tma_load_3d(sQ, &tmQ, bar(B_QFULL), U.h * DH, U.q0, U.b);
-        issued |= 1u;
-        par = (par & ~1u) | (uc & 1);
+        mbar_arrive_expect_tx(bar(B_QFULL), (U.hB >= 0 ? 2 : 1) * Cfg::Q_BYTES);
+        tma_load_3d(sQ, &tmQ, bar(B_QFULL), U.hA * DH, U.q0, U.b);
+        if (U.hB >= 0) tma_load_3d(sQ + Cfg::Q_BYTES, &tmQ, bar(B_QFULL), U.hB * DH, U.q0, U.b);
         for (int t = 0; t < U.n_tiles; ++t, ++kc) {
-          const int s = kc & 1;
-          const uint32_t ph = (kc >> 1) & 1;
+          const int s = kc % KV_STAGES;
+          const uint32_t ph = (kc / KV_STAGES) & 1;
           const int k0 = tile_kt(U, t) * BKV;
-          if (!mbar_wait(bar(B_KEMPTY0 + s), ph ^ 1, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(B_KFULL0 + s), Cfg::K_BYTES);
-          tma_load_3d(sK + s * Cfg::K_BYTES, &tmK, bar(B_KFULL0 + s), U.g * DH, k0, U.b);
-          issued |= 2u << s;
-          par = (par & ~(2u << s)) | (ph << (1 + s));
-          if (!mbar_wait(bar(B_VEMPTY0 + s), ph ^ 1, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar(B_VFULL0 + s), Cfg::V_BYTES);
+          if (!mbar_wait(bar(B_KEMPTY + s), ph ^ 1, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(B_KFULL + s), Cfg::K_BYTES);
+          tma_load_3d(sK + s * Cfg::K_BYTES, &tmK, bar(B_KFULL + s), U.g * DH, k0, U.b);
+          if (!mbar_wait(bar(B_VEMPTY + s), ph ^ 1, wc)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar(B_VFULL + s), Cfg::V_BYTES);
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(sV + s * Cfg::V_BYTES + c * (BKV * 128), &tmV, bar(B_VFULL0 + s), U.g * DV + c * 64, k0, U.b);
-          issued |= 8u << s;
-          par = (par & ~(8u << s)) | (ph << (3 + s));
+            tma_load_3d(sV + s * Cfg::V_BYTES + c * (BKV * 128), &tmV, bar(B_VFULL + s), U.g * DV + c * 64, k0, U.b);
         }
       }
+      // after a wait gave up, let the loads this thread issued land before
+      // the CTA exits (each ring slot's recent loads and the last Q load)
       if (!ok) {
-        if (issued & 1u) mbar_wait_drain(bar(B_QFULL), par & 1, 1000000);
-        for (int s = 0; s < 2; ++s) {
-          if (issued & (2u << s)) mbar_wait_drain(bar(B_KFULL0 + s), (par >> (1 + s)) & 1, 1000000);
-          if (issued & (8u << s)) mbar_wait_drain(bar(B_VFULL0 + s), (par >> (3 + s)) & 1, 1000000);
+        for (uint32_t j = (kc >= KV_STAGES ? kc - KV_STAGES : 0); j <= kc; ++j) {
+          mbar_wait_drain(bar(B_KFULL + j % KV_STAGES), (j / KV_STAGES) & 1, 1000000);
+          mbar_wait_drain(bar(B_VFULL + j % KV_STAGES), (j / KV_STAGES) & 1, 1000000);
         }
+        mbar_wait_drain(bar(B_QFULL), uc & 1, 1000000);
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == W_MMA || warp == W_MMA + 1) {
+    // ---------------------------------------------------------------- MMA issuers
+    // warp W_MMA + x issues every MMA of head x; both walk all units and the
+    // K/V/Q ring barriers take one arrival from each (a warp whose head is
+    // absent in a unit only waits and arrives)
     if (lane == 0) {
+      const int x = warp - W_MMA;
       constexpr uint32_t idS = idesc_f16(128, BKV, 0, false, false);
       constexpr uint32_t idPV = idesc_f16(128, DV, 0, false, true);
-      uint32_t kc = 0, jt = 0, uc = 0;
-      uint32_t last_commit_bar = 0xffffffffu, last_commit_par = 0;
+      uint32_t J = 0;           // global tile counter of head x (S buffer = J & 1)
+      uint32_t ju = 0;          // units of head x (OEMPTY phase)
+      uint32_t kc = 0, uc = 0;  // K/V ring position of the unit's first tile; unit count (QFULL phase)
       bool ok = true;
-      auto issue_S = [&](uint32_t j_global, uint32_t kcl) -> bool {
-        const int s = kcl & 1;
-        const int sb = j_global & 1;
-        if (!mbar_wait(bar(B_KFULL0 + s), (kcl >> 1) & 1, wc)) return false;
-        if (!mbar_wait(bar(B_SEMPTY0 + sb), ((j_global >> 1) & 1) ^ 1, wc)) return false;
-        tc_fence_after();
-        const uint64_t dq = sdesc_sw128(sQ, 16, 1024);
-        const uint64_t dk = sdesc_sw128(sK + s * Cfg::K_BYTES, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) tc_mma_f16(tmem + sb * BKV, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
-        tc_commit(bar(B_SFULL0 + sb));
-        tc_commit(bar(B_KEMPTY0 + s));
-        last_commit_bar = B_SFULL0 + sb;
-        last_commit_par = (j_global >> 1) & 1;
-        return true;
+      bool any_commit = false;
+      uint32_t last_bar = 0, last_par = 0;
+      const uint64_t dq = sdesc_sw128(sQ + x * Cfg::Q_BYTES, 16, 1024);
+      auto wait_k = [&](uint32_t kcl) {
+        return mbar_wait(bar(B_KFULL + kcl % KV_STAGES), (kcl / KV_STAGES) & 1, wc);
       };
-      auto issue_PV = [&](uint32_t j_global, uint32_t kcl, bool first) -> bool {
-        const int s = kcl & 1;
-        const int pb = j_global & 1;
-        if (!mbar_wait(bar(B_PFULL0 + pb), (j_global >> 1) & 1, wc)) return false;
-        if (!mbar_wait(bar(B_VFULL0 + s), (kcl >> 1) & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t pbase = sP + pb * Cfg::P_BYTES;
-        const uint32_t vbase = sV + s * Cfg::V_BYTES;
+      auto commit = [&](int b, uint32_t par) {
+        tc_commit(bar(b));
+        any_commit = true;
+        last_bar = b;
+        last_par = par;
+      };
+      // S_x of head-x tile Jt (into buffer Jt & 1) from the K tile at ring position kcl
+      auto issue_S = [&](uint32_t Jt, uint32_t kcl) {
+        const uint64_t dk = sdesc_sw128(sK + (kcl % KV_STAGES) * Cfg::K_BYTES, 16, 1024);
+        const uint32_t d = tmem + Cfg::s_col(x, Jt);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) tc_mma_f16(d, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
+        commit(B_SFULL + 2 * x + (Jt & 1), (Jt >> 1) & 1);
+      };
+      // O_x += P_x(Jt) V for the V tile at ring position kcl
+      auto issue_PV = [&](uint32_t Jt, uint32_t kcl, bool first) {
+        const uint32_t vbase = sV + (kcl % KV_STAGES) * Cfg::V_BYTES;
+        const uint32_t a = tmem + Cfg::s_col(x, Jt);
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk) {
-          const uint64_t da = sdesc_sw128(pbase + (kk >> 2) * (BQ * 128) + (kk & 3) * 32, 16, 1024);
           const uint64_t db = sdesc_sw128(vbase + kk * 16 * 128, BKV * 128, 1024);
-          tc_mma_f16(tmem + Cfg::O_COL, da, db, idPV, (first && kk == 0) ? 0u : 1u);
+          tc_mma_f16_ts(tmem + Cfg::o_col(x), a + kk * 8, db, idPV, (first && kk == 0) ? 0u : 1u);
         }
-        tc_commit(bar(B_PVDONE0 + pb));
-        tc_commit(bar(B_VEMPTY0 + s));
-        last_commit_bar = B_PVDONE0 + pb;
-        last_commit_par = (j_global >> 1) & 1;
-        return true;
+        commit(B_PVDONE + x, Jt & 1);
       };
       for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
         const Unit U = make_unit(p, u);
+        const bool mine = x == 0 || U.hB >= 0;
+        // the first (up to) two S tiles of the unit
         if (!mbar_wait(bar(B_QFULL), uc & 1, wc)) { ok = false; break; }
-        const uint32_t j0 = jt, k0c = kc;
-        if (!issue_S(j0, k0c)) { ok = false; break; }
-        for (int t = 0; t < U.n_tiles; ++t) {
-          if (t + 1 < U.n_tiles) {
-            if (!issue_S(j0 + t + 1, k0c + t + 1)) { ok = false; break; }
-          } else {
-            tc_commit(bar(B_QEMPTY));  // every S MMA of the unit is issued: Q may be replaced
-          }
-          if (t == 0 && !mbar_wait(bar(B_OEMPTY), (uc & 1) ^ 1, wc)) { ok = false; break; }
-          if (!issue_PV(j0 + t, k0c + t, t == 0)) { ok = false; break; }
+        const int n0 = min(2, U.n_tiles);
+        for (int j = 0; j < n0 && ok; ++j) {
+          if (!wait_k(kc + j)) { ok = false; break; }
+          tc_fence_after();
+          if (mine) issue_S(J + j, kc + j);
+          commit(B_KEMPTY + (kc + j) % KV_STAGES, ((kc + j) / KV_STAGES) & 1);
         }
-        jt = j0 + U.n_tiles;
-        kc = k0c + U.n_tiles;
+        if (!ok) break;
+        if (U.n_tiles <= 2) commit(B_QEMPTY, uc & 1);
+        for (int t = 0; t < U.n_tiles; ++t) {
+          const uint32_t kct = kc + t;
+          const bool s_ahead = t + 2 < U.n_tiles;  // S of tile t+2 to issue after this PV
+          if (!mbar_wait(bar(B_VFULL + kct % KV_STAGES), (kct / KV_STAGES) & 1, wc)) { ok = false; break; }
+          if (mine) {
+            if (t == 0 && !mbar_wait(bar(B_OEMPTY + x), (ju & 1) ^ 1, wc)) { ok = false; break; }
+            if (!mbar_wait(bar(B_PFULL + 2 * x + (J & 1)), (J >> 1) & 1, wc)) { ok = false; break; }
+            tc_fence_after();
+            issue_PV(J, kct, t == 0);
+          }
+          if (s_ahead) {
+            // S(t+2) reuses the buffer of P(t): issued after the PV that reads it (in order)
+            if (!wait_k(kct + 2)) { ok = false; break; }
+            tc_fence_after();
+            if (mine) issue_S(J + 2, kct + 2);
+          }
+          if (mine) ++J;
+          commit(B_VEMPTY + kct % KV_STAGES, (kct / KV_STAGES) & 1);
+          if (s_ahead) {
+            commit(B_KEMPTY + (kct + 2) % KV_STAGES, ((kct + 2) / KV_STAGES) & 1);
+            if (t + 3 == U.n_tiles) commit(B_QEMPTY, uc & 1);  // every S of the unit is issued
+          }
+        }
+        if (!ok) break;
+        if (mine) ++ju;
+        kc += U.n_tiles;
       }
-      if (!ok && last_commit_bar != 0xffffffffu) mbar_wait_drain(bar(last_commit_bar), last_commit_par, 1000000);
+      if (!ok && any_commit) mbar_wait_drain(bar(last_bar), last_par, 1000000);
     }
   } else {
     // ---------------------------------------------------------------- softmax warps
-    const int q = warp & 3;
+    const int x = warp >> 2;  // 0 = head A, 1 = head B
+    const int q = warp & 3;   // TMEM lane quarter of this warp
     const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t jt = 0, uc = 0;
+    const uint32_t o_col = Cfg::o_col(x);
+    uint32_t J = 0;  // global tile counter of this head
     bool ok = true;
-    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
+    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
       const Unit U = make_unit(p, u);
+      const int h = x == 0 ? U.hA : U.hB;
+      if (h < 0) continue;  // single-head unit: nothing for head B
       const int i = U.q0 + r;  // query row (may be >= L on the last tile)
       float m_run = -INFINITY, l_run = 0.f;
-      for (int t = 0; t < U.n_tiles; ++t, ++jt) {
-        const int sb = jt & 1;
-        const bool got = mbar_wait(bar(B_SFULL0 + sb), (jt >> 1) & 1, wc);
+      for (int t = 0; t < U.n_tiles; ++t, ++J) {
+        const uint32_t s_col = Cfg::s_col(x, J);
+        const bool got = mbar_wait(bar(B_SFULL + 2 * x + (J & 1)), (J >> 1) & 1, wc);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
-        float s[BKV];
-        {
-          uint32_t rr[4][32];
+        uint32_t sr[BKV / 32][32];  // raw scores (fp32 bits)
 #pragma unroll
-          for (int c = 0; c < BKV / 32; ++c) tmem_ld32(lane_base + sb * BKV + c * 32, rr[c]);
-          tc_wait_ld();
-#pragma unroll
-          for (int c = 0; c < BKV / 32; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(rr[c][e]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_SEMPTY0 + sb));
+        for (int c = 0; c < BKV / 32; ++c) tmem_ld32(lane_base + s_col + c * 32, sr[c]);
+        tc_wait_ld();
         // mask (raw scores; the positive scale is applied inside the exp2 below)
         const int k0 = tile_kt(U, t) * BKV;
         const bool full_vis = (k0 + BKV - 1 <= U.q0) && (k0 + BKV <= p.L) &&
@@ -272,83 +331,81 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int e = 0; e < BKV; ++e) {
             const bool vis = (e <= hi) && (e >= lo || e < ml);
-            s[e] = vis ? s[e] : -INFINITY;
+            sr[e >> 5][e & 31] = vis ? sr[e >> 5][e & 31] : 0xff800000u;  // -inf
           }
         }
-        float mp[8];
+        auto sv = [&](int e) { return __uint_as_float(sr[e >> 5][e & 31]); };
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) mp[q8] = s[q8];
+        for (int e = 0; e < BKV; e += 8)
 #pragma unroll
-        for (int e = 8; e < BKV; ++e) mp[e & 7] = fmaxf(mp[e & 7], s[e]);
-        const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * p.scale_log2;
+          for (int j = 0; j < 4; ++j) m4[j] = max3f(m4[j], sv(e + 2 * j), sv(e + 2 * j + 1));
+        const float mt = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3])) * p.scale_log2;
         // running max (log2 units): set on the first tile; raised only when a tile exceeds it by > 2^8
-        bool need = (t == 0) ? true : (mt > m_run + kRescaleLog2);
+        const bool need = (t == 0) ? true : (mt > m_run + kRescaleLog2);
         if (t > 0 && __any_sync(0xffffffffu, need)) {
           const float m_new = fmaxf(m_run, mt);
           const float alpha = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - m_new);
-          // O holds PV of earlier tiles: wait for the last one, then scale O in TMEM
-          const uint32_t jp = jt - 1;
-          const bool g2 = mbar_wait(bar(B_PVDONE0 + (jp & 1)), (jp >> 1) & 1, wc);
+          // O must hold every earlier tile: wait for P V of tile J-1 (tile
+          // J-2 is complete, as S of this tile was issued after it)
+          const bool g2 = mbar_wait(bar(B_PVDONE + x), (J - 1) & 1, wc);
           if (!__all_sync(0xffffffffu, g2)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < DV / 32; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(lane_base + Cfg::O_COL + c * 32, rr);
+          for (int c = 0; c < DV / 16; ++c) {
+            uint32_t rr[16];
+            tmem_ld16(lane_base + o_col + c * 16, rr);
             tc_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-            tmem_st32(lane_base + Cfg::O_COL + c * 32, rr);
+            for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+            tmem_st16(lane_base + o_col + c * 16, rr);
           }
-          tc_wait_st();
           l_run *= alpha;
           m_run = m_new;
         } else if (t == 0) {
           m_run = mt;
         }
         const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-        // P buffer sb is free once PV of tile jt-2 completed
-        const bool g3 = mbar_wait(bar(B_PVDONE0 + sb), ((jt >> 1) & 1) ^ 1, wc);
-        if (!__all_sync(0xffffffffu, g3)) { ok = false; break; }
-        const uint32_t prow = sP + sb * Cfg::P_BYTES + r * 128;
-        float ls[8];
+        // P = 2^(s * scale - m) as fp16 pairs over the first 32 columns of the
+        // buffer; pairs of scores go through one f32x2 FMA and one f32x2 add
+        const uint64_t scale2 = pk2(p.scale_log2, p.scale_log2), negm2 = pk2(neg_m, neg_m);
+        uint64_t ls2[4] = {pk2(0.f, 0.f), pk2(0.f, 0.f), pk2(0.f, 0.f), pk2(0.f, 0.f)};
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) ls[q8] = 0.f;
+        for (int c = 0; c < BKV / 32; ++c) {  // 32 keys -> 16 packed columns
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < BKV / 8; ++c) {  // 16 chunks of 8 keys (16 bytes)
-          float pv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            pv[e] = ex2_approx(fmaf(s[c * 8 + e], p.scale_log2, neg_m));
-            ls[e] += pv[e];
+          for (int e2 = 0; e2 < 16; ++e2) {
+            const int e = c * 32 + 2 * e2;
+            const float2 y = up2(fma2(pk2(sv(e), sv(e + 1)), scale2, negm2));
+            const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+            ls2[e2 & 3] = add2(ls2[e2 & 3], pk2(p0, p1));
+            pk[e2] = pack_half2(p0, p1);
           }
-          const uint32_t w0 = pack_half2(pv[0], pv[1]), w1 = pack_half2(pv[2], pv[3]);
-          const uint32_t w2 = pack_half2(pv[4], pv[5]), w3 = pack_half2(pv[6], pv[7]);
-          const int sub = c >> 3, cc = c & 7;
-          const uint32_t addr = prow + sub * (BQ * 128) + ((cc ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
-                       : "memory");
+          tmem_st16(lane_base + s_col + c * 16, pk);
         }
-        const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-        l_run += lsum;
-        fence_proxy_async_smem();
+        {
+          const float2 a = up2(add2(add2(ls2[0], ls2[1]), add2(ls2[2], ls2[3])));
+          l_run += a.x + a.y;
+        }
+        tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PFULL0 + sb));
+        if (lane == 0) mbar_arrive(bar(B_PFULL + 2 * x + (J & 1)));
       }
       if (!ok) break;
-      // epilogue: O / l -> fp16
-      const uint32_t jl = jt - 1;
-      const bool g4 = mbar_wait(bar(B_PVDONE0 + (jl & 1)), (jl >> 1) & 1, wc);
+      // epilogue: O / l -> fp16, once the last two P V of this head completed
+      // (waited in order, so that each parity wait is unambiguous)
+      bool g4 = true;
+      if (U.n_tiles >= 2) g4 = mbar_wait(bar(B_PVDONE + x), (J - 2) & 1, wc);
+      g4 = g4 && mbar_wait(bar(B_PVDONE + x), (J - 1) & 1, wc);
       if (!__all_sync(0xffffffffu, g4)) { ok = false; break; }
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-      __half* orow = p.O + (static_cast<long long>(U.b) * p.L + i) * p.ldo + U.h * DV;
+      __half* orow = p.O + (static_cast<long long>(U.b) * p.L + i) * p.ldo + h * DV;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t rr[32];
-        tmem_ld32(lane_base + Cfg::O_COL + c * 32, rr);
+        tmem_ld32(lane_base + o_col + c * 32, rr);
         tc_wait_ld();
         if (i < p.L) {
 #pragma unroll
@@ -364,14 +421,14 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_OEMPTY));
+      if (lane == 0) mbar_arrive(bar(B_OEMPTY + x));
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  if (warp == W_MMA) tmem_dealloc(tmem, Cfg::TMEM_COLS);
 }
 
 template <int DV>
@@ -380,14 +437,14 @@ hymba_status launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMa
   auto kern = attn_tc_kernel<DV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<DV>::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
-  kern<<<grid, 192, AttnCfg<DV>::SMEM, st>>>(q, k, v, p);
+  kern<<<grid, NTHREADS, AttnCfg<DV>::SMEM, st>>>(q, k, v, p);
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 
-bool make_map3(CUtensorMap* m, const __half* base, int cols, int L, int B, long long ld) {
+bool make_map3(CUtensorMap* m, const __half* base, int cols, int L, int B, long long ld, int box_rows) {
   const uint64_t dims[3] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
   const uint64_t str[2] = {static_cast<uint64_t>(ld) * 2, static_cast<uint64_t>(ld) * 2 * L};
-  const uint32_t box[3] = {64, 128, 1};
+  const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), 1};
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -398,12 +455,12 @@ bool attn_tc_supported(int dh, int dv) { return dh == DH && (dv == 64 || dv == 1
 hymba_status attn_tc(int B, int L, int M, int Hq, int Hkv, int dh, int dv, int window, const __half* Q, long long ldq,
                      const __half* K, long long ldk, const __half* V, long long ldv, __half* O, long long ldo,
                      int32_t* status, uint64_t wait_ns, int num_sms, cudaStream_t st) {
-  if (!attn_tc_supported(dh, dv)) return HYMBA_ERR_UNSUPPORTED;
+  if (!attn_tc_supported(dh, dv) || Hq > MAX_HU || Hkv < 1 || Hkv > Hq) return HYMBA_ERR_UNSUPPORTED;
   auto al = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al(Q) || !al(K) || !al(V) || !al(O) || ldq % 8 || ldk % 8 || ldv % 8 || ldo % 8) return HYMBA_ERR_INVALID;
   CUtensorMap tq, tk, tv;
-  if (!make_map3(&tq, Q, Hq * dh, L, B, ldq) || !make_map3(&tk, K, Hkv * dh, L, B, ldk) ||
-      !make_map3(&tv, V, Hkv * dv, L, B, ldv))
+  if (!make_map3(&tq, Q, Hq * dh, L, B, ldq, BQ) || !make_map3(&tk, K, Hkv * dh, L, B, ldk, BKV) ||
+      !make_map3(&tv, V, Hkv * dv, L, B, ldv, BKV))
     return HYMBA_ERR_CUDA;
   AttnParams p{};
   p.B = B;
@@ -414,7 +471,18 @@ hymba_status attn_tc(int B, int L, int M, int Hq, int Hkv, int dh, int dv, int w
   p.dv = dv;
   p.window = window;
   p.n_qt = (L + BQ - 1) / BQ;
-  p.n_units = B * p.n_qt * Hq;
+  // head units: consecutive heads of one KV group in pairs, a group's odd head alone
+  int n_hu = 0;
+  for (int h = 0; h < Hq;) {
+    const int g = (h * Hkv) / Hq;
+    const bool pair = h + 1 < Hq && ((h + 1) * Hkv) / Hq == g;
+    p.hA[n_hu] = static_cast<int16_t>(h);
+    p.hB[n_hu] = static_cast<int16_t>(pair ? h + 1 : -1);
+    ++n_hu;
+    h += pair ? 2 : 1;
+  }
+  p.n_hu = n_hu;
+  p.n_units = B * p.n_qt * n_hu;
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(dh));
   p.O = O;
   p.ldo = ldo;

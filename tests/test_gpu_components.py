@@ -162,6 +162,19 @@ def test_attention_random_matches_oracle(use_tc, M, window, L, q_scale):
     np.testing.assert_allclose(got, exp, atol=4e-3 * max(1, np.abs(exp).max()), rtol=1e-2)
 
 
+@pytest.mark.parametrize("Hq,Hkv,dv,M,window,L", [(3, 3, 64, 16, 64, 301), (6, 1, 64, 128, 256, 700),
+                                                  (7, 7, 128, 0, 0, 130), (5, 1, 128, 128, 0, 400)])
+def test_attention_head_pairing_matches_oracle(Hq, Hkv, dv, M, window, L):
+    """The tensor-core kernel runs two query heads of one KV group per unit
+    and a group's odd head alone: groups of 1, 3, 5 and 6 heads, both V
+    widths."""
+    B, dh = 2, 64
+    Q, K, V = _attn_inputs(B, L, Hq, Hkv, dh, dv, 6, q_scale=2.0)
+    got = _run_attn(Q, K, V, M, window, 1)
+    exp = ref.attention(Q, K, V, M, window)
+    np.testing.assert_allclose(got, exp, atol=4e-3 * max(1, np.abs(exp).max()), rtol=1e-2)
+
+
 def test_bounded_wait_reports_timeout():
     """A wait on a barrier nothing arrives on gives up after its limit and the
     status word says so; the context stays usable."""
