@@ -319,76 +319,179 @@ __global__ void decode_attn_combine_kernel(int Hq, int dv, int nsplit, const flo
   }
 }
 
-// One decode step of the SSM branch with the dt projection fused: per
-// (sequence b, channel c) thread,
+// One decode step of the SSM branch with the dt projection fused:
 //   delta = softplus(dt[b] . W_dt[c] + bias[c]),  h = exp(delta A) h + delta u B[b],
 //   y = C[b] . h + D u,  g = y silu(z);  the state is updated in place.
-// A block owns 128 channels for DS_BB sequences; the W_dt rows of its
-// channels and the dt / B / C rows of its sequences sit in shared memory.
-constexpr int DS_THREADS = 128;
-constexpr int DS_BB = 8;
+// A block owns DS_CH channels x DS_SEQ sequences:
+//   0. every thread issues its loads of the state rows first (their HBM
+//      latency overlaps the rest), then dt (fp16) and W_dt (bf16 -> fp16,
+//      the same rounding as the prefill's weight conversion) are staged in
+//      shared memory with 8-byte vector loads, zero-padded to 16 columns;
+//   1. warps 0-3 compute delta for the block (16 sequences x 32 channels) on
+//      the tensor cores, m16n8k16 (one 8-channel n-tile per warp), then leave
+//      (delta, delta * u) in shared memory;
+//   2. four threads per (sequence, channel), one float4 of the 16 states
+//      each, so a warp reads and writes 8 consecutive channels' state rows
+//      (512 contiguous bytes); the four partial C.h are summed with shuffles.
+constexpr int DS_CH = 32;
+constexpr int DS_SEQ = 16;         // = the m16 MMA tile
+constexpr int DS_THREADS = 256;
+constexpr int DS_RMAX = 128;
+constexpr int DS_KSTR = DS_RMAX + 8;  // fp16 row stride of the staged tiles: conflict-free ldmatrix
+
+HY_DEV void ldsm_x4_dec(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+HY_DEV void ldsm_x2_dec(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
 
 template <int N>
-__global__ void __launch_bounds__(DS_THREADS)
+__global__ void __launch_bounds__(DS_THREADS, 3)
     decode_ssm_step_kernel(int B, int di, int R, const __half* __restrict__ u, long long ldu,
                            const __half* __restrict__ z, long long ldz, const __half* __restrict__ dtr,
                            long long ld_dtr, const float* __restrict__ BC, const __nv_bfloat16* __restrict__ W_dt,
                            const float* __restrict__ dt_bias, const float* __restrict__ A_log,
                            const float* __restrict__ D, float* __restrict__ state, __half* __restrict__ g,
-                           long long ldg) {
-  extern __shared__ float sm[];
-  float* sW = sm;                           // [DS_THREADS][R + 1]
-  float* sdt = sW + DS_THREADS * (R + 1);   // [DS_BB][R]
-  float* sbc = sdt + DS_BB * R;             // [DS_BB][2N]
-  const int c0 = blockIdx.x * DS_THREADS;
-  const int b0 = blockIdx.y * DS_BB;
+                           long long ldg, int32_t* __restrict__ pos) {
+  static_assert(N == 16, "four threads x float4 per state row");
+  __shared__ __align__(16) __half sW[DS_CH][DS_KSTR];     // W_dt rows of the block's channels (fp16)
+  __shared__ __align__(16) __half sdt[DS_SEQ][DS_KSTR];   // dt rows of the block's sequences
+  __shared__ __align__(16) float sbc[DS_SEQ][2 * N];      // [B | C] of each sequence
+  __shared__ __align__(16) float sA2[DS_CH][N];
+  __shared__ __align__(8) float2 sdu[DS_SEQ][DS_CH];      // (delta, delta * u)
+  const int c0 = blockIdx.x * DS_CH, b0 = blockIdx.y * DS_SEQ;
   const int tid = threadIdx.x;
-  for (int idx = tid; idx < DS_THREADS * R; idx += DS_THREADS) {
-    const int cc = idx / R, r = idx % R;
-    sW[cc * (R + 1) + r] = (c0 + cc < di) ? __bfloat162float(W_dt[static_cast<long long>(c0 + cc) * R + r]) : 0.f;
+  const int KP = (R + 15) / 16 * 16;  // padded dt rank
+  // ---- 0. state loads (phase-2 thread: quarter q of the rows j = tid/4 + 64 i)
+  constexpr int NJ = DS_SEQ * DS_CH / (DS_THREADS / 4);
+  const int q = tid & 3;
+  float4 hv[NJ];
+#pragma unroll
+  for (int i = 0; i < NJ; ++i) {
+    const int j = (tid >> 2) + i * (DS_THREADS / 4);
+    const int b = b0 + j / DS_CH, c = c0 + j % DS_CH;
+    hv[i] = (b < B && c < di)
+                ? reinterpret_cast<const float4*>(state + (static_cast<long long>(b) * di + c) * N)[q]
+                : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int idx = tid; idx < DS_BB * R; idx += DS_THREADS) {
-    const int bb = idx / R, r = idx % R;
-    sdt[idx] = (b0 + bb < B) ? __half2float(dtr[(b0 + bb) * ld_dtr + r]) : 0.f;
+  // W_dt rows: 8 threads per row, 4 values per 8-byte load
+  {
+    const int row = tid >> 3, l8 = tid & 7;  // 32 rows
+    const int c = c0 + row;
+    const bool vec = (reinterpret_cast<uintptr_t>(W_dt) & 7) == 0 && (R & 3) == 0;
+    for (int k4 = l8; k4 < KP / 4; k4 += 8) {
+      const int k = 4 * k4;
+      float f[4] = {0.f, 0.f, 0.f, 0.f};
+      if (c < di) {
+        const __nv_bfloat16* src = W_dt + static_cast<long long>(c) * R + k;
+        if (vec && k + 4 <= R) {
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+          f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (k + e < R) f[e] = __bfloat162float(src[e]);
+        }
+      }
+      *reinterpret_cast<uint2*>(&sW[row][k]) = make_uint2(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]));
+    }
   }
-  for (int idx = tid; idx < DS_BB * 2 * N; idx += DS_THREADS) {
-    const int bb = idx / (2 * N);
-    sbc[idx] = (b0 + bb < B) ? BC[(b0 + bb) * 2 * N + idx % (2 * N)] : 0.f;
+  // dt rows: 16 threads per row (the padding columns past R are zeroed, never read)
+  {
+    const int row = tid >> 4, l16 = tid & 15;
+    const int b = b0 + row;
+    for (int k4 = l16; k4 < KP / 4; k4 += 16) {
+      const int k = 4 * k4;
+      uint2 v = make_uint2(0u, 0u);
+      if (b < B) {
+        const __half* src = dtr + b * ld_dtr + k;
+        __half hh[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hh[e] = (k + e < R) ? src[e] : __float2half_rn(0.f);
+        v.x = *reinterpret_cast<const uint32_t*>(&hh[0]);
+        v.y = *reinterpret_cast<const uint32_t*>(&hh[2]);
+      }
+      *reinterpret_cast<uint2*>(&sdt[row][k]) = v;
+    }
+  }
+  for (int idx = tid; idx < DS_SEQ * 2 * N; idx += DS_THREADS) {
+    const int s = idx / (2 * N);
+    sbc[s][idx % (2 * N)] = (b0 + s < B) ? BC[(b0 + s) * 2 * N + idx % (2 * N)] : 0.f;
+  }
+  for (int idx = tid; idx < DS_CH * N; idx += DS_THREADS) {
+    const int cc = idx / N;
+    sA2[cc][idx % N] = (c0 + cc < di) ? -__expf(A_log[static_cast<long long>(c0) * N + idx]) * 1.4426950408889634f
+                                      : 0.f;
   }
   __syncthreads();
-  const int c = c0 + tid;
-  if (c >= di) return;
-  float A2[N];
-#pragma unroll
-  for (int n = 0; n < N; ++n) A2[n] = -__expf(A_log[c * N + n]) * 1.4426950408889634f;
-  const float bias = dt_bias[c], Dc = D[c];
-  const float* wr = sW + tid * (R + 1);
-  for (int bb = 0; bb < DS_BB; ++bb) {
-    const int b = b0 + bb;
-    if (b >= B) break;
-    float acc = bias;
-    for (int r = 0; r < R; ++r) acc = fmaf(sdt[bb * R + r], wr[r], acc);
-    const float dt = softplus_fast(acc);
-    const float uu = __half2float(u[b * ldu + c]);
-    const float du = dt * uu;
-    float4* hp = reinterpret_cast<float4*>(state + (static_cast<long long>(b) * di + c) * N);
-    float h[N];
-#pragma unroll
-    for (int q = 0; q < N / 4; ++q) {
-      const float4 v = hp[q];
-      h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
+  // every kernel of the step that reads pos ran before this one: advance it
+  if (pos != nullptr && blockIdx.x == 0 && tid < DS_SEQ && b0 + tid < B) pos[b0 + tid] += 1;
+  // ---- 1. delta = softplus(dt . W_dt^T + bias) on the tensor cores
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < DS_CH / 8) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint32_t a_base = smem_u32(&sdt[lane & 15][(lane >> 4) * 8]);
+    const uint32_t b_base = smem_u32(&sW[warp * 8 + (lane & 7)][((lane >> 3) & 1) * 8]);
+    for (int kk = 0; kk < KP / 16; ++kk) {
+      uint32_t af[4], b0f, b1f;
+      ldsm_x4_dec(a_base + kk * 32, af);
+      ldsm_x2_dec(b_base + kk * 32, b0f, b1f);
+      mma_16816_f16(acc, af, b0f, b1f);
     }
-    float y = 0.f;
+    // acc: rows (sequences) lane/4 and lane/4 + 8, columns (channels) 2(lane%4), +1
+    const int grp = lane >> 2, tig = lane & 3;
 #pragma unroll
-    for (int n = 0; n < N; ++n) {
-      h[n] = fmaf(ex2_approx(dt * A2[n]), h[n], du * sbc[bb * 2 * N + n]);
-      y = fmaf(sbc[bb * 2 * N + N + n], h[n], y);
+    for (int e = 0; e < 4; ++e) {
+      const int s = grp + (e >> 1) * 8, cl = warp * 8 + 2 * tig + (e & 1);
+      const int b = b0 + s, c = c0 + cl;
+      float dt = 0.f, uu = 0.f;
+      if (b < B && c < di) {
+        dt = softplus_fast(acc[e] + dt_bias[c]);
+        uu = __half2float(u[b * ldu + c]);
+      }
+      sdu[s][cl] = make_float2(dt, dt * uu);
     }
+  }
+  __syncthreads();
+  // ---- 2. state update, 4 threads per (sequence, channel): rows j = tid/4 + 64 i
+  //      are channel cl = (tid/4) % 32 of sequences s = (tid/4)/32 + 2 i
+  const int cl = (tid >> 2) % DS_CH, c = c0 + cl;
+  const int s_first = (tid >> 2) / DS_CH;
+  float4* hp = reinterpret_cast<float4*>(state + (static_cast<long long>(b0 + s_first) * di + c) * N) + q;
+  const long long hstep = static_cast<long long>(DS_THREADS / 4 / DS_CH) * di * N / 4;  // float4 per step of i
+  const float4 a = *reinterpret_cast<const float4*>(&sA2[cl][4 * q]);
+  const float Dc = c < di ? D[c] : 0.f;
 #pragma unroll
-    for (int q = 0; q < N / 4; ++q) hp[q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-    y = fmaf(Dc, uu, y);
-    const float zz = __half2float(z[b * ldz + c]);
-    g[b * ldg + c] = __float2half_rn(y * zz / (1.0f + __expf(-zz)));
+  for (int i = 0; i < NJ; ++i, hp += hstep) {
+    const int s = s_first + i * (DS_THREADS / 4 / DS_CH);
+    const int b = b0 + s;
+    const bool ok = b < B && c < di;
+    float4 h = hv[i];
+    const float2 du = sdu[s][cl];
+    const float4 bb = *reinterpret_cast<const float4*>(&sbc[s][4 * q]);
+    const float4 cc = *reinterpret_cast<const float4*>(&sbc[s][N + 4 * q]);
+    h.x = fmaf(ex2_approx(du.x * a.x), h.x, du.y * bb.x);
+    h.y = fmaf(ex2_approx(du.x * a.y), h.y, du.y * bb.y);
+    h.z = fmaf(ex2_approx(du.x * a.z), h.z, du.y * bb.z);
+    h.w = fmaf(ex2_approx(du.x * a.w), h.w, du.y * bb.w);
+    float y = fmaf(cc.x, h.x, fmaf(cc.y, h.y, fmaf(cc.z, h.z, cc.w * h.w)));
+    y += __shfl_xor_sync(0xffffffffu, y, 1);
+    y += __shfl_xor_sync(0xffffffffu, y, 2);
+    if (ok) {
+      *hp = h;
+      if (q == 0) {
+        const float uu = __half2float(u[b * ldu + c]);
+        const float zz = __half2float(z[b * ldz + c]);
+        y = fmaf(Dc, uu, y);
+        // y * silu(z) = y * z / (1 + 2^(-z log2 e))
+        g[b * ldg + c] = __float2half_rn(y * zz * rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * zz)));
+      }
+    }
   }
 }
 
@@ -510,21 +613,17 @@ hymba_status decode_attn_combine(int B, int Hq, int dv, int nsplit, const float*
   return last_err();
 }
 
-bool decode_ssm_step_supported(int N, int R) { return N == 16 && R <= 256; }
+bool decode_ssm_step_supported(int N, int R) { return N == 16 && R >= 1 && R <= DS_RMAX; }
 
 hymba_status decode_ssm_step(int B, int di, int N, int R, const __half* u, long long ldu, const __half* z,
                              long long ldz, const __half* dtr, long long ld_dtr, const float* BC,
                              const __nv_bfloat16* W_dt, const float* dt_bias, const float* A_log, const float* D,
-                             float* state, __half* g, long long ldg, cudaStream_t st) {
+                             float* state, __half* g, long long ldg, int32_t* pos, cudaStream_t st) {
   if (!decode_ssm_step_supported(N, R)) return HYMBA_ERR_UNSUPPORTED;
-  const size_t smem = (static_cast<size_t>(DS_THREADS) * (R + 1) + DS_BB * R + DS_BB * 2 * N) * sizeof(float);
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(decode_ssm_step_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return HYMBA_ERR_CUDA;
-  dim3 grid((di + DS_THREADS - 1) / DS_THREADS, (B + DS_BB - 1) / DS_BB);
-  decode_ssm_step_kernel<16><<<grid, DS_THREADS, smem, st>>>(B, di, R, u, ldu, z, ldz, dtr, ld_dtr, BC, W_dt,
-                                                               dt_bias, A_log, D, state, g, ldg);
+  if (B < 1 || di < 1) return HYMBA_OK;
+  dim3 grid((di + DS_CH - 1) / DS_CH, (B + DS_SEQ - 1) / DS_SEQ);
+  decode_ssm_step_kernel<16><<<grid, DS_THREADS, 0, st>>>(B, di, R, u, ldu, z, ldz, dtr, ld_dtr, BC, W_dt, dt_bias,
+                                                          A_log, D, state, g, ldg, pos);
   return last_err();
 }
 

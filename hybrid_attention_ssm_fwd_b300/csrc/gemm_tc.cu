@@ -8,7 +8,11 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator rows they own (TMEM
 //               lanes 32*(warp%4) ..), fused epilogue, direct global stores;
 //               then release the accumulator so the next tile's MMAs, which
-//               overlap this epilogue, can reuse it.
+//               overlap this epilogue, can reuse it.  With cvt_b (a bf16
+//               weight matrix against fp16 activations) these warps first
+//               convert each B stage of the tile to fp16 in place, in shared
+//               memory, and the MMA waits for that instead of the TMA: the
+//               weights are read from HBM once and never copied.
 //
 // Tiles are visited in row-major tile order (N fastest) by a static
 // round-robin over CTAs, so the CTAs resident at one time share a few A
@@ -99,8 +103,8 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + S * A_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE);
-  // bars: full[S], empty[S], tfull[2], tempty[2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  // bars: full[S], empty[S], tfull[2], tempty[2], cvt[S]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* rope_tab = reinterpret_cast<float*>(tmem_slot + 4);  // 32 floats
 
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(192, 1)
   auto empty = [&](int s) { return smem_u32(&bars[S + s]); };
   auto tfull = [&](int a) { return smem_u32(&bars[2 * S + a]); };
   auto tempty = [&](int a) { return smem_u32(&bars[2 * S + 2 + a]); };
+  auto cvt = [&](int s) { return smem_u32(&bars[2 * S + 4 + s]); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -120,6 +125,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(tfull(a), 1);
       mbar_init(tempty(a), 4);
     }
+    for (int s = 0; s < S; ++s) mbar_init(cvt(s), 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!mbar_wait(full(s), ph, wc)) { ok = false; break; }
+          if (!mbar_wait(p.cvt_b ? cvt(s) : full(s), ph, wc)) { ok = false; break; }
           tc_fence_after();
           const uint64_t da = sdesc_sw128(smem_u32(sA + s * A_BYTES), 16, 1024);
           const uint64_t db = sdesc_sw128(smem_u32(sB + s * Cfg::B_BYTES), 16, 1024);
@@ -200,11 +206,41 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
+    const int ct = threadIdx.x - 64;  // 0..127 over the four epilogue warps
     int local = 0;
+    uint32_t cit = 0;  // k-block counter of the conversion (follows the producer's)
+    bool cok = true;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++local) {
       const TileCoord c = tile_coord(p, t);
       const int a = local & 1;
       const uint32_t u = (local >> 1) & 1;
+      if (p.cvt_b) {
+        // bf16 -> fp16 of every B stage of this tile, in place (elementwise:
+        // the swizzled layout is unchanged)
+        for (int kb = c.kb0; kb < c.kb1 && cok; ++kb, ++cit) {
+          const int s = cit % S;
+          const bool gotb = mbar_wait(full(s), (cit / S) & 1, wc);
+          if (!__all_sync(0xffffffffu, gotb)) { cok = false; break; }
+          uint4* b16 = reinterpret_cast<uint4*>(sB + s * Cfg::B_BYTES);
+#pragma unroll
+          for (int i = ct; i < Cfg::B_BYTES / 16; i += 128) {
+            const uint4 v = b16[i];
+            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+            uint4 o;
+            uint32_t* o32 = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(b2[e]);
+              o32[e] = pack_half2(f.x, f.y);
+            }
+            b16[i] = o;
+          }
+          fence_proxy_async_smem();  // generic stores -> tensor-core reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(cvt(s));
+        }
+        if (!cok) break;
+      }
       const bool got = mbar_wait(tfull(a), u, wc);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
@@ -374,6 +410,7 @@ int gemm_pick_bn(int N, bool small_m) {
 hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, long long ldb, int epi,
                      GemmParams p, int bn, int splits, int num_sms, cudaStream_t st) {
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return HYMBA_OK;
+  if (p.cvt_b && ab_fmt != 0) return HYMBA_ERR_INVALID;  // converted B meets fp16 A
   if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) || (lda % 8) ||
       (ldb % 8) || lda < p.K || ldb < p.K)
     return HYMBA_ERR_INVALID;
@@ -390,7 +427,8 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
     const uint64_t str[1] = {static_cast<uint64_t>(ldb) * 2};
     const uint32_t box[2] = {BK, static_cast<uint32_t>(bn)};
-    if (!encode_tmap(&tb, dt, 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
+    const CUtensorMapDataType dtb = p.cvt_b ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : dt;
+    if (!encode_tmap(&tb, dtb, 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
   }
   p.tiles_m = (p.M + BM - 1) / BM;
   p.tiles_n = (p.N + bn - 1) / bn;

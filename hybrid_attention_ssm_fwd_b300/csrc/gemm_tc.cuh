@@ -33,6 +33,7 @@ struct GemmParams {
   int pos_base;
   int32_t* status;
   uint64_t wait_ns;
+  int cvt_b;  // B is bf16 in memory: converted to fp16 in shared memory before the MMA (A fp16)
 };
 
 // Launch C = A . B^T with the given epilogue.  ab_fmt: 0 fp16, 1 bf16.

@@ -128,8 +128,12 @@ Plan plan_ws(const Dims& x, bool decode) {
   p.g = take(r * x.di * e);
   p.s = take(r * x.di * e);
   if (x.dtype == HYMBA_BF16) {
-    p.wout = take(static_cast<size_t>(x.d) * x.di * 2);
-    p.wx = take(static_cast<size_t>(x.xo) * x.di * 2);
+    // fp16 weight copies: prefill converts W_out and W_x once per call; the
+    // decode GEMMs convert their bf16 tiles in shared memory instead
+    if (!decode) {
+      p.wout = take(static_cast<size_t>(x.d) * x.di * 2);
+      p.wx = take(static_cast<size_t>(x.xo) * x.di * 2);
+    }
     p.wdt = take(static_cast<size_t>(x.di) * x.Rp * 2);
     if (decode) {
       const size_t w1 = static_cast<size_t>(kDecodeSplitsX) * r * ((x.xo + 15) / 16 * 16);
@@ -454,8 +458,13 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   __half* g = at<__half>(ws, pl.g);
   __half* s = at<__half>(ws, pl.s);
   float* part = at<float>(ws, pl.part);
+  const bool ssm_fused = decode_ssm_step_supported(x.N, x.R);
   mk.mark();
-  TRY(convert_weights(x, pl, w, ws, st));
+  // W_x and W_out are converted to fp16 inside the GEMMs (cvt_b); only the
+  // unfused dt projection needs a converted W_dt
+  if (!ssm_fused)
+    TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_dt), x.R, at<__half>(ws, pl.wdt),
+                                      x.Rp, x.di, x.R, st));
   mk.mark();
   TRY(in_proj_bf16(x, Xn, w, proj, B, c->pos, x.M, 1, status, sms, st));
   mk.mark();
@@ -493,18 +502,19 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
     GemmParams p = gp(B, x.xo, x.di, status, x.wait_ns);
     p.C = part;
     p.ldc = ldp;
-    TRY(gemm_tc(0, u, x.di, at<__half>(ws, pl.wx), x.di, EPI_PARTIAL, p, 0, kDecodeSplitsX, sms, st));
+    p.cvt_b = 1;
+    TRY(gemm_tc(0, u, x.di, w->W_x, x.di, EPI_PARTIAL, p, 0, kDecodeSplitsX, sms, st));
     const int n_kb = (x.di + 63) / 64;
     const int kbs = (n_kb + std::min(kDecodeSplitsX, n_kb) - 1) / std::min(kDecodeSplitsX, n_kb);
     const int splits = (n_kb + kbs - 1) / kbs;
     TRY(splitk_reduce(splits, B, x.xo, part, ldp, RE_XPROJ, x.R, dtr, x.Rp, bc, 2 * x.N, nullptr, 0, false, st));
   }
   mk.mark();
-  if (decode_ssm_step_supported(x.N, x.R)) {
+  if (ssm_fused) {
     mk.mark();  // dt projection is fused into the step below
     TRY(decode_ssm_step(B, x.di, x.N, x.R, u, x.di, proj + x.z_col, x.P_in, dtr, x.Rp, bc,
                         static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, w->A_log, w->D, c->ssm_state, g, x.di,
-                        st));
+                        c->pos, st));  // also advances pos
   } else {
     GemmParams p = gp(B, x.di, x.R, status, x.wait_ns);
     p.C = delta;
@@ -522,7 +532,8 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
     GemmParams p = gp(B, x.d, x.di, status, x.wait_ns);
     p.C = part;
     p.ldc = x.d;
-    TRY(gemm_tc(0, s, x.di, at<__half>(ws, pl.wout), x.di, EPI_PARTIAL, p, 0, kDecodeSplitsOut, sms, st));
+    p.cvt_b = 1;
+    TRY(gemm_tc(0, s, x.di, w->W_out, x.di, EPI_PARTIAL, p, 0, kDecodeSplitsOut, sms, st));
     const int n_kb = (x.di + 63) / 64;
     const int sp = std::min(kDecodeSplitsOut, n_kb);
     const int kbs = (n_kb + sp - 1) / sp;
@@ -531,7 +542,7 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
                       x.residual == 1 ? static_cast<const __nv_bfloat16*>(Xn) : nullptr, x.d, x.residual == 2, st));
   }
   mk.mark();
-  TRY(pos_increment(B, c->pos, st));
+  if (!ssm_fused) TRY(pos_increment(B, c->pos, st));
   mk.mark();
   return HYMBA_OK;
 }
@@ -665,9 +676,10 @@ hymba_status hymba_layer_decode_events(const hymba_layer_desc* d, const hymba_la
 
 hymba_status hymba_test_gemm(int32_t M, int32_t N, int32_t K, int32_t ab_dtype, const void* A, int32_t lda,
                              const void* B, int32_t ldb, float* C, int32_t ldc, int32_t* dev_status, void* stream) {
-  if (M < 1 || N < 1 || K < 1 || !A || !B || !C || (ab_dtype != 1 && ab_dtype != 2) || ldc < N)
+  if (M < 1 || N < 1 || K < 1 || !A || !B || !C || ab_dtype < 1 || ab_dtype > 3 || ldc < N)
     return HYMBA_ERR_INVALID;
   GemmParams p{};
+  p.cvt_b = ab_dtype == 3 ? 1 : 0;
   p.M = M;
   p.N = N;
   p.K = K;

@@ -650,7 +650,9 @@ hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* 
   const bool vec_ok = std::is_same<T, __half>::value && di % 8 == 0 && (reinterpret_cast<uintptr_t>(beta1) & 15) == 0 &&
                       (reinterpret_cast<uintptr_t>(beta2) & 15) == 0 && (reinterpret_cast<uintptr_t>(att) & 15) == 0 &&
                       (reinterpret_cast<uintptr_t>(g) & 15) == 0 && (reinterpret_cast<uintptr_t>(s) & 15) == 0;
-  if (vec_ok && di <= 32 * 8 * FW_V) {
+  // one warp per row wants many rows (a decode step's 128 rows would fill
+  // 32 SMs): below that, one block per row
+  if (vec_ok && di <= 32 * 8 * FW_V && rows >= 4 * 148 * 4) {
     fuse_norm_warp_kernel<<<(rows + 3) / 4, 128, 0, st>>>(rows, di, reinterpret_cast<const __half*>(att),
                                                           reinterpret_cast<const __half*>(g), beta1, beta2, eps,
                                                           reinterpret_cast<__half*>(s));

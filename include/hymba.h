@@ -269,7 +269,10 @@ HYMBA_API int32_t hymba_abi_version(void);
 
 /* C[M, N] (fp32, row stride ldc) = A[M, K] . B[N, K]^T on the tcgen05 GEMM
  * (paper section 2.1: the shared input projection and W_out are these
- * GEMMs).  ab_dtype 1 = bf16 operands, 2 = fp16 operands.  K-major rows,
+ * GEMMs).  ab_dtype 1 = bf16 operands, 2 = fp16 operands, 3 = fp16 A with
+ * bf16 B converted to fp16 in shared memory (the decode step's weights, read
+ * once and never copied; a bf16 value outside fp16's normal range rounds as
+ * a float-to-half conversion does).  K-major rows,
  * 16-byte aligned, lda/ldb (elements) multiples of 8.                        */
 HYMBA_API hymba_status hymba_test_gemm(int32_t M, int32_t N, int32_t K, int32_t ab_dtype,
                              const void* A, int32_t lda, const void* B, int32_t ldb,

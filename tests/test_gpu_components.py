@@ -16,19 +16,22 @@ F = np.float64
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 200, 100), (1000, 1600, 3200), (37, 8960, 1600),
                                    (4500, 144, 96), (128, 64, 8)])
-@pytest.mark.parametrize("ab", [1, 2])
+@pytest.mark.parametrize("ab", [1, 2, 3])
 def test_gemm_tc_matches_fp64(M, N, K, ab):
+    """ab 1: bf16 x bf16; 2: fp16 x fp16; 3: fp16 A against a bf16 B that the
+    kernel converts to fp16 in shared memory (exact for these magnitudes)."""
     g = torch.Generator().manual_seed(M * 7 + N + K)
     dt = torch.bfloat16 if ab == 1 else torch.float16
+    dtb = torch.bfloat16 if ab in (1, 3) else torch.float16
     A = torch.randn(M, K, generator=g).to(dt)
-    B = (0.05 * torch.randn(N, K, generator=g)).to(dt)
+    B = (0.05 * torch.randn(N, K, generator=g)).to(dtb)
     C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     # rows must start on 16 bytes: pad the row stride to a multiple of 8 and
     # fill the padding with NaN, which the K tail must never read
     Kp = (K + 7) // 8 * 8
     Ad = torch.full((M, Kp), float("nan"), dtype=dt, device="cuda")
-    Bd = torch.full((N, Kp), float("nan"), dtype=dt, device="cuda")
+    Bd = torch.full((N, Kp), float("nan"), dtype=dtb, device="cuda")
     Ad[:, :K] = A.cuda()
     Bd[:, :K] = B.cuda()
     rc = hb.hymba_test_gemm(Ad[:, :K], Bd[:, :K], C, ab, status=st)
