@@ -18,11 +18,13 @@
 //              TMEM), so P stays <= 2^8.  At the end of a unit O / l is stored.
 //   warp 8     TMA: Q of both heads once per unit; K and V tiles through two
 //              6-stage rings (128-byte swizzle).
-//   warps 9,10 one thread each issues the MMAs of head A / head B (warp 9
-//              also owns TMEM).  S is double-buffered per head, so S of tile
-//              t+1 is computed while the softmax works on tile t, and S of tile
-//              t+2 is issued right after P V of tile t (it reuses that buffer):
-//                S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ...   for each head.
+//   warps 9-12 one thread each issues the MMAs of one kind for one head:
+//              S of head A, S of head B, P V of head A, P V of head B (warp
+//              9 also owns TMEM).  S is double-buffered per head, so S of
+//              tile t+1 is computed while the softmax works on tile t; S of
+//              tile t+2 reuses the buffer of tile t once P V of tile t has
+//              completed.  Four issuing threads keep the tensor core fed with
+//              these small MMAs (N = 64 / dv, K = 16).
 //              S = Q K^T reads Q and K from shared memory; O += P V reads P
 //              from TMEM and V from shared memory.
 // TMEM columns: S_A buffers [0,64) [64,128), S_B buffers [128,192) [192,256),
@@ -38,8 +40,8 @@ constexpr int DH = 64;         // Q/K head dim handled here
 constexpr int KV_STAGES = 6;   // K and V ring depth
 constexpr int MAX_HU = 128;    // head units (pairs or single heads)
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int NTHREADS = 352;  // 11 warps
-constexpr int W_TMA = 8, W_MMA = 9;  // MMA issuers: warps 9 (head A) and 10 (head B)
+constexpr int NTHREADS = 416;  // 13 warps
+constexpr int W_TMA = 8, W_MMA = 9;  // MMA issuers: warps 9-12
 
 struct AttnParams {
   int B, L, M, Hq, Hkv, dv, window, n_qt, n_hu, n_units;
@@ -109,7 +111,8 @@ enum {
   B_PFULL = B_SFULL + 4,              // [head][buffer], 4 arrivals (softmax warps)
   B_PVDONE = B_PFULL + 4,             // [head]
   B_OEMPTY = B_PVDONE + 2,            // [head], 4 arrivals
-  B_COUNT = B_OEMPTY + 2
+  B_PVFREE = B_OEMPTY + 2,            // [head][buffer]: P V of the buffer's tile completed
+  B_COUNT = B_PVFREE + 4
 };
 
 HY_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -208,13 +211,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_wait_drain(bar(B_QFULL), uc & 1, 1000000);
       }
     }
-  } else if (warp == W_MMA || warp == W_MMA + 1) {
+  } else if (warp >= W_MMA && warp < W_MMA + 4) {
     // ---------------------------------------------------------------- MMA issuers
-    // warp W_MMA + x issues every MMA of head x; both walk all units and the
-    // K/V/Q ring barriers take one arrival from each (a warp whose head is
-    // absent in a unit only waits and arrives)
+    // four issuing threads: warp W_MMA + x issues S = Q K^T of head x, warp
+    // W_MMA + 2 + x issues O += P V of head x.  Each walks all units; the
+    // ring barriers take one arrival from each thread of the pair that
+    // releases them (a thread whose head is absent in a unit only waits and
+    // arrives).  S of tile J reuses the buffer of tile J-2, so it waits until
+    // P V of tile J-2 has completed (PVFREE of that buffer).
     if (lane == 0) {
-      const int x = warp - W_MMA;
+      const int role = warp - W_MMA;  // 0, 1: S of head A, B;  2, 3: P V of head A, B
+      const int x = role & 1;
+      const bool is_s = role < 2;
       constexpr uint32_t idS = idesc_f16(128, BKV, 0, false, false);
       constexpr uint32_t idPV = idesc_f16(128, DV, 0, false, true);
       uint32_t J = 0;           // global tile counter of head x (S buffer = J & 1)
@@ -224,73 +232,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool any_commit = false;
       uint32_t last_bar = 0, last_par = 0;
       const uint64_t dq = sdesc_sw128(sQ + x * Cfg::Q_BYTES, 16, 1024);
-      auto wait_k = [&](uint32_t kcl) {
-        return mbar_wait(bar(B_KFULL + kcl % KV_STAGES), (kcl / KV_STAGES) & 1, wc);
-      };
       auto commit = [&](int b, uint32_t par) {
         tc_commit(bar(b));
         any_commit = true;
         last_bar = b;
         last_par = par;
       };
-      // S_x of head-x tile Jt (into buffer Jt & 1) from the K tile at ring position kcl
-      auto issue_S = [&](uint32_t Jt, uint32_t kcl) {
-        const uint64_t dk = sdesc_sw128(sK + (kcl % KV_STAGES) * Cfg::K_BYTES, 16, 1024);
-        const uint32_t d = tmem + Cfg::s_col(x, Jt);
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) tc_mma_f16(d, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
-        commit(B_SFULL + 2 * x + (Jt & 1), (Jt >> 1) & 1);
-      };
-      // O_x += P_x(Jt) V for the V tile at ring position kcl
-      auto issue_PV = [&](uint32_t Jt, uint32_t kcl, bool first) {
-        const uint32_t vbase = sV + (kcl % KV_STAGES) * Cfg::V_BYTES;
-        const uint32_t a = tmem + Cfg::s_col(x, Jt);
-#pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          const uint64_t db = sdesc_sw128(vbase + kk * 16 * 128, BKV * 128, 1024);
-          tc_mma_f16_ts(tmem + Cfg::o_col(x), a + kk * 8, db, idPV, (first && kk == 0) ? 0u : 1u);
-        }
-        commit(B_PVDONE + x, Jt & 1);
-      };
       for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
         const Unit U = make_unit(p, u);
         const bool mine = x == 0 || U.hB >= 0;
-        // the first (up to) two S tiles of the unit
-        if (!mbar_wait(bar(B_QFULL), uc & 1, wc)) { ok = false; break; }
-        const int n0 = min(2, U.n_tiles);
-        for (int j = 0; j < n0 && ok; ++j) {
-          if (!wait_k(kc + j)) { ok = false; break; }
-          tc_fence_after();
-          if (mine) issue_S(J + j, kc + j);
-          commit(B_KEMPTY + (kc + j) % KV_STAGES, ((kc + j) / KV_STAGES) & 1);
-        }
-        if (!ok) break;
-        if (U.n_tiles <= 2) commit(B_QEMPTY, uc & 1);
+        if (is_s && !mbar_wait(bar(B_QFULL), uc & 1, wc)) { ok = false; break; }
         for (int t = 0; t < U.n_tiles; ++t) {
           const uint32_t kct = kc + t;
-          const bool s_ahead = t + 2 < U.n_tiles;  // S of tile t+2 to issue after this PV
-          if (!mbar_wait(bar(B_VFULL + kct % KV_STAGES), (kct / KV_STAGES) & 1, wc)) { ok = false; break; }
-          if (mine) {
-            if (t == 0 && !mbar_wait(bar(B_OEMPTY + x), (ju & 1) ^ 1, wc)) { ok = false; break; }
-            if (!mbar_wait(bar(B_PFULL + 2 * x + (J & 1)), (J >> 1) & 1, wc)) { ok = false; break; }
-            tc_fence_after();
-            issue_PV(J, kct, t == 0);
-          }
-          if (s_ahead) {
-            // S(t+2) reuses the buffer of P(t): issued after the PV that reads it (in order)
-            if (!wait_k(kct + 2)) { ok = false; break; }
-            tc_fence_after();
-            if (mine) issue_S(J + 2, kct + 2);
-          }
-          if (mine) ++J;
-          commit(B_VEMPTY + kct % KV_STAGES, (kct / KV_STAGES) & 1);
-          if (s_ahead) {
-            commit(B_KEMPTY + (kct + 2) % KV_STAGES, ((kct + 2) / KV_STAGES) & 1);
-            if (t + 3 == U.n_tiles) commit(B_QEMPTY, uc & 1);  // every S of the unit is issued
+          const int slot = kct % KV_STAGES;
+          const uint32_t ph = (kct / KV_STAGES) & 1;
+          if (is_s) {
+            if (!mbar_wait(bar(B_KFULL + slot), ph, wc)) { ok = false; break; }
+            if (mine) {
+              if (J >= 2 && !mbar_wait(bar(B_PVFREE + 2 * x + (J & 1)), ((J >> 1) - 1) & 1, wc)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t dk = sdesc_sw128(sK + slot * Cfg::K_BYTES, 16, 1024);
+              const uint32_t d = tmem + Cfg::s_col(x, J);
+#pragma unroll
+              for (int kk = 0; kk < DH / 16; ++kk) tc_mma_f16(d, dq + 2 * kk, dk + 2 * kk, idS, kk > 0);
+              commit(B_SFULL + 2 * x + (J & 1), (J >> 1) & 1);
+              ++J;
+            }
+            commit(B_KEMPTY + slot, ph);
+            if (t + 1 == U.n_tiles) commit(B_QEMPTY, uc & 1);  // every S of the unit is issued
+          } else {
+            if (!mbar_wait(bar(B_VFULL + slot), ph, wc)) { ok = false; break; }
+            if (mine) {
+              if (t == 0 && !mbar_wait(bar(B_OEMPTY + x), (ju & 1) ^ 1, wc)) { ok = false; break; }
+              if (!mbar_wait(bar(B_PFULL + 2 * x + (J & 1)), (J >> 1) & 1, wc)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t vbase = sV + slot * Cfg::V_BYTES;
+              const uint32_t a = tmem + Cfg::s_col(x, J);
+#pragma unroll
+              for (int kk = 0; kk < BKV / 16; ++kk) {
+                const uint64_t db = sdesc_sw128(vbase + kk * 16 * 128, BKV * 128, 1024);
+                tc_mma_f16_ts(tmem + Cfg::o_col(x), a + kk * 8, db, idPV, (t == 0 && kk == 0) ? 0u : 1u);
+              }
+              commit(B_PVDONE + x, J & 1);
+              commit(B_PVFREE + 2 * x + (J & 1), (J >> 1) & 1);
+              ++J;
+            }
+            commit(B_VEMPTY + slot, ph);
           }
         }
         if (!ok) break;
-        if (mine) ++ju;
+        if (!is_s && mine) ++ju;
         kc += U.n_tiles;
       }
       if (!ok && any_commit) mbar_wait_drain(bar(last_bar), last_par, 1000000);
