@@ -351,8 +351,8 @@ HY_DEV void ldsm_x2_dec(uint32_t addr, uint32_t& r0, uint32_t& r1) {
 template <int N>
 __global__ void __launch_bounds__(DS_THREADS, 3)
     decode_ssm_step_kernel(int B, int di, int R, const __half* __restrict__ u, long long ldu,
-                           const __half* __restrict__ z, long long ldz, const __half* __restrict__ dtr,
-                           long long ld_dtr, const float* __restrict__ BC, const __nv_bfloat16* __restrict__ W_dt,
+                           const __half* __restrict__ z, long long ldz, const float* __restrict__ xp,
+                           long long ld_xp, const __nv_bfloat16* __restrict__ W_dt,
                            const float* __restrict__ dt_bias, const float* __restrict__ A_log,
                            const float* __restrict__ D, float* __restrict__ state, __half* __restrict__ g,
                            long long ldg, int32_t* __restrict__ pos) {
@@ -409,10 +409,10 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
       const int k = 4 * k4;
       uint2 v = make_uint2(0u, 0u);
       if (b < B) {
-        const __half* src = dtr + b * ld_dtr + k;
+        const float* src = xp + b * ld_xp + k;
         __half hh[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) hh[e] = (k + e < R) ? src[e] : __float2half_rn(0.f);
+        for (int e = 0; e < 4; ++e) hh[e] = __float2half_rn((k + e < R) ? src[e] : 0.f);  // dt rounds to fp16 as in prefill
         v.x = *reinterpret_cast<const uint32_t*>(&hh[0]);
         v.y = *reinterpret_cast<const uint32_t*>(&hh[2]);
       }
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
   }
   for (int idx = tid; idx < DS_SEQ * 2 * N; idx += DS_THREADS) {
     const int s = idx / (2 * N);
-    sbc[s][idx % (2 * N)] = (b0 + s < B) ? BC[(b0 + s) * 2 * N + idx % (2 * N)] : 0.f;
+    sbc[s][idx % (2 * N)] = (b0 + s < B) ? xp[(b0 + s) * ld_xp + R + idx % (2 * N)] : 0.f;
   }
   for (int idx = tid; idx < DS_CH * N; idx += DS_THREADS) {
     const int cc = idx / N;
@@ -616,13 +616,12 @@ hymba_status decode_attn_combine(int B, int Hq, int dv, int nsplit, const float*
 bool decode_ssm_step_supported(int N, int R) { return N == 16 && R >= 1 && R <= DS_RMAX; }
 
 hymba_status decode_ssm_step(int B, int di, int N, int R, const __half* u, long long ldu, const __half* z,
-                             long long ldz, const __half* dtr, long long ld_dtr, const float* BC,
-                             const __nv_bfloat16* W_dt, const float* dt_bias, const float* A_log, const float* D,
+                             long long ldz, const float* xp, long long ld_xp, const __nv_bfloat16* W_dt, const float* dt_bias, const float* A_log, const float* D,
                              float* state, __half* g, long long ldg, int32_t* pos, cudaStream_t st) {
   if (!decode_ssm_step_supported(N, R)) return HYMBA_ERR_UNSUPPORTED;
   if (B < 1 || di < 1) return HYMBA_OK;
   dim3 grid((di + DS_CH - 1) / DS_CH, (B + DS_SEQ - 1) / DS_SEQ);
-  decode_ssm_step_kernel<16><<<grid, DS_THREADS, 0, st>>>(B, di, R, u, ldu, z, ldz, dtr, ld_dtr, BC, W_dt, dt_bias,
+  decode_ssm_step_kernel<16><<<grid, DS_THREADS, 0, st>>>(B, di, R, u, ldu, z, ldz, xp, ld_xp, W_dt, dt_bias,
                                                           A_log, D, state, g, ldg, pos);
   return last_err();
 }

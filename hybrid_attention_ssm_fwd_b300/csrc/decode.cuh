@@ -67,9 +67,9 @@ hymba_status decode_attention_tc(int B, int M, int Hq, int Hkv, int dh, int dv, 
 // Decode step of the SSM branch with the dt projection fused (see decode.cu);
 // pos (may be null) is advanced by one for every sequence.
 bool decode_ssm_step_supported(int N, int R);
+// xp [B, ld_xp] fp32 = the x projection [dt (R) | B (N) | C (N)] of each sequence.
 hymba_status decode_ssm_step(int B, int di, int N, int R, const __half* u, long long ldu, const __half* z,
-                             long long ldz, const __half* dtr, long long ld_dtr, const float* BC,
-                             const __nv_bfloat16* W_dt, const float* dt_bias, const float* A_log, const float* D,
+                             long long ldz, const float* xp, long long ld_xp, const __nv_bfloat16* W_dt, const float* dt_bias, const float* A_log, const float* D,
                              float* state, __half* g, long long ldg, int32_t* pos, cudaStream_t st);
 
 hymba_status pos_increment(int B, int32_t* pos, cudaStream_t st);

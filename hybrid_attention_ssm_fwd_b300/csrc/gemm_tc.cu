@@ -341,6 +341,19 @@ __global__ void __launch_bounds__(192, 1)
                 if (j < valid) v[j] += rr[j];
             }
             store_f32x32(reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col, v, valid);
+          } else if (EPI == EPI_ATOMIC) {
+            float* dst = reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col;
+            if (valid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+              for (int g = 0; g < 32; g += 4)
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + g), "f"(v[g]),
+                             "f"(v[g + 1]), "f"(v[g + 2]), "f"(v[g + 3])
+                             : "memory");
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < valid) atomicAdd(dst + j, v[j]);
+            }
           } else {  // EPI_PARTIAL
             float* dst = reinterpret_cast<float*>(p.C) +
                          (static_cast<long long>(c.split) * p.M + row) * p.ldc + col;
@@ -437,7 +450,7 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
   p.kb_per_split = (p.n_kb + splits - 1) / splits;
   p.splits = (p.n_kb + p.kb_per_split - 1) / p.kb_per_split;
   p.total_tiles = p.tiles_m * p.tiles_n * p.splits;
-  if (p.splits > 1 && epi != EPI_PARTIAL) return HYMBA_ERR_INVALID;
+  if (p.splits > 1 && epi != EPI_PARTIAL && epi != EPI_ATOMIC) return HYMBA_ERR_INVALID;
   const int grid = std::min(p.total_tiles, std::max(1, num_sms));
   const uint32_t fmt = ab_fmt == 1 ? 1u : 0u;
   switch (epi) {
@@ -446,6 +459,7 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
     case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS>(bn, ta, tb, p, fmt, grid, st);
     case EPI_F32: return launch_epi<EPI_F32>(bn, ta, tb, p, fmt, grid, st);
     case EPI_PARTIAL: return launch_epi<EPI_PARTIAL>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_ATOMIC: return launch_epi<EPI_ATOMIC>(bn, ta, tb, p, fmt, grid, st);
     default: return HYMBA_ERR_INVALID;
   }
 }

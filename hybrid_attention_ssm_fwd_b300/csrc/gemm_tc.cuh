@@ -12,6 +12,7 @@ enum GemmEpi : int {
   EPI_SOFTPLUS = 2,  // C fp32 = softplus(acc + bias[col])
   EPI_F32 = 3,       // C fp32 = acc (+ bf16 residual)
   EPI_PARTIAL = 4,   // C fp32 + split*M*ldc = acc (split-K partial sums)
+  EPI_ATOMIC = 5,    // C fp32 += acc with vector atomics (split-K into a cleared or residual C)
 };
 
 struct GemmParams {

@@ -503,16 +503,24 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
     p.C = part;
     p.ldc = ldp;
     p.cvt_b = 1;
-    TRY(gemm_tc(0, u, x.di, w->W_x, x.di, EPI_PARTIAL, p, 0, kDecodeSplitsX, sms, st));
-    const int n_kb = (x.di + 63) / 64;
-    const int kbs = (n_kb + std::min(kDecodeSplitsX, n_kb) - 1) / std::min(kDecodeSplitsX, n_kb);
-    const int splits = (n_kb + kbs - 1) / kbs;
-    TRY(splitk_reduce(splits, B, x.xo, part, ldp, RE_XPROJ, x.R, dtr, x.Rp, bc, 2 * x.N, nullptr, 0, false, st));
+    if (ssm_fused) {
+      // split-K partials added straight into a cleared [B, ldp] fp32 buffer,
+      // which the SSM step reads as [dt | B | C]
+      if (cudaMemsetAsync(part, 0, static_cast<size_t>(B) * ldp * sizeof(float), st) != cudaSuccess)
+        return HYMBA_ERR_CUDA;
+      TRY(gemm_tc(0, u, x.di, w->W_x, x.di, EPI_ATOMIC, p, 0, kDecodeSplitsX, sms, st));
+    } else {
+      TRY(gemm_tc(0, u, x.di, w->W_x, x.di, EPI_PARTIAL, p, 0, kDecodeSplitsX, sms, st));
+      const int n_kb = (x.di + 63) / 64;
+      const int kbs = (n_kb + std::min(kDecodeSplitsX, n_kb) - 1) / std::min(kDecodeSplitsX, n_kb);
+      const int splits = (n_kb + kbs - 1) / kbs;
+      TRY(splitk_reduce(splits, B, x.xo, part, ldp, RE_XPROJ, x.R, dtr, x.Rp, bc, 2 * x.N, nullptr, 0, false, st));
+    }
   }
   mk.mark();
   if (ssm_fused) {
     mk.mark();  // dt projection is fused into the step below
-    TRY(decode_ssm_step(B, x.di, x.N, x.R, u, x.di, proj + x.z_col, x.P_in, dtr, x.Rp, bc,
+    TRY(decode_ssm_step(B, x.di, x.N, x.R, u, x.di, proj + x.z_col, x.P_in, part, (x.xo + 15) / 16 * 16,
                         static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, w->A_log, w->D, c->ssm_state, g, x.di,
                         c->pos, st));  // also advances pos
   } else {
@@ -530,16 +538,27 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   mk.mark();
   {
     GemmParams p = gp(B, x.d, x.di, status, x.wait_ns);
-    p.C = part;
-    p.ldc = x.d;
     p.cvt_b = 1;
-    TRY(gemm_tc(0, s, x.di, w->W_out, x.di, EPI_PARTIAL, p, 0, kDecodeSplitsOut, sms, st));
-    const int n_kb = (x.di + 63) / 64;
-    const int sp = std::min(kDecodeSplitsOut, n_kb);
-    const int kbs = (n_kb + sp - 1) / sp;
-    const int splits = (n_kb + kbs - 1) / kbs;
-    TRY(splitk_reduce(splits, B, x.d, part, x.d, RE_F32, 0, nullptr, 0, Y, x.d,
-                      x.residual == 1 ? static_cast<const __nv_bfloat16*>(Xn) : nullptr, x.d, x.residual == 2, st));
+    if (x.residual != 1) {
+      // split-K partials added straight into Y: cleared first, or holding the
+      // fp32 residual already (residual = 2)
+      if (x.residual == 0 &&
+          cudaMemsetAsync(Y, 0, static_cast<size_t>(B) * x.d * sizeof(float), st) != cudaSuccess)
+        return HYMBA_ERR_CUDA;
+      p.C = Y;
+      p.ldc = x.d;
+      TRY(gemm_tc(0, s, x.di, w->W_out, x.di, EPI_ATOMIC, p, 0, kDecodeSplitsOut, sms, st));
+    } else {
+      p.C = part;
+      p.ldc = x.d;
+      TRY(gemm_tc(0, s, x.di, w->W_out, x.di, EPI_PARTIAL, p, 0, kDecodeSplitsOut, sms, st));
+      const int n_kb = (x.di + 63) / 64;
+      const int sp = std::min(kDecodeSplitsOut, n_kb);
+      const int kbs = (n_kb + sp - 1) / sp;
+      const int splits = (n_kb + kbs - 1) / kbs;
+      TRY(splitk_reduce(splits, B, x.d, part, x.d, RE_F32, 0, nullptr, 0, Y, x.d,
+                        static_cast<const __nv_bfloat16*>(Xn), x.d, false, st));
+    }
   }
   mk.mark();
   if (!ssm_fused) TRY(pos_increment(B, c->pos, st));
