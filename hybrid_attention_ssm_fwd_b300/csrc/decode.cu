@@ -651,3 +651,62 @@ template hymba_status conv_step<__half>(int, int, int, const __half*, long long,
                                         float*, __half*, long long, cudaStream_t);
 
 }  // namespace hy
+
+namespace hy {
+namespace {
+
+// The decode step's K/V ring append and conv step in one launch (same
+// arithmetic as kv_append_kernel and conv_step_kernel): elements
+// [0, B*di) are conv channels, the rest ring entries of the new token.
+__global__ void decode_prep_kernel(int B, int di, int k, const __half* __restrict__ proj, long long ldp, int x_col,
+                                   int k_col, int v_col, int Hkv, int dh, int dv, int window, int cap,
+                                   const int32_t* __restrict__ pos, __nv_bfloat16* __restrict__ k_ring,
+                                   __nv_bfloat16* __restrict__ v_ring, const float* __restrict__ w,
+                                   const float* __restrict__ bias, float* __restrict__ conv_state,
+                                   __half* __restrict__ u, long long ldu, int append) {
+  const long long n_conv = static_cast<long long>(B) * di;
+  const int wk = Hkv * dh, wv = Hkv * dv;
+  const long long n = n_conv + (append ? static_cast<long long>(B) * (wk + wv) : 0);
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    if (idx < n_conv) {
+      const int b = static_cast<int>(idx / di), c = static_cast<int>(idx % di);
+      float* st = conv_state + idx * (k - 1);
+      const float xv = __half2float(proj[b * ldp + x_col + c]);
+      float acc = bias[c];
+      for (int j = 0; j < k - 1; ++j) acc = fmaf(w[c * k + j], st[j], acc);
+      acc = fmaf(w[c * k + k - 1], xv, acc);
+      for (int j = 0; j + 1 < k - 1; ++j) st[j] = st[j + 1];
+      if (k > 1) st[k - 2] = xv;
+      u[b * ldu + c] = __float2half_rn(acc / (1.0f + expf(-acc)));
+    } else {
+      const long long r = idx - n_conv;
+      const int b = static_cast<int>(r / (wk + wv)), c = static_cast<int>(r % (wk + wv));
+      const int p = pos[b];
+      const int slot = window > 0 ? p % cap : p;
+      if (slot < 0 || slot >= cap) continue;  // a full global cache: the token is not stored
+      if (c < wk)
+        k_ring[(static_cast<long long>(b) * cap + slot) * wk + c] =
+            __float2bfloat16_rn(__half2float(proj[b * ldp + k_col + c]));
+      else
+        v_ring[(static_cast<long long>(b) * cap + slot) * wv + (c - wk)] =
+            __float2bfloat16_rn(__half2float(proj[b * ldp + v_col + (c - wk)]));
+    }
+  }
+}
+
+}  // namespace
+
+hymba_status decode_prep(int B, int di, int k, const __half* proj, long long ldp, int x_col, int k_col, int v_col,
+                         int Hkv, int dh, int dv, int window, int cap, const int32_t* pos, __nv_bfloat16* k_ring,
+                         __nv_bfloat16* v_ring, const float* conv_w, const float* conv_b, float* conv_state,
+                         __half* u, long long ldu, bool append, cudaStream_t st) {
+  const long long n = static_cast<long long>(B) * di + (append ? static_cast<long long>(B) * Hkv * (dh + dv) : 0);
+  if (n <= 0) return HYMBA_OK;
+  decode_prep_kernel<<<static_cast<unsigned>(std::min<long long>((n + 255) / 256, 148 * 16)), 256, 0, st>>>(
+      B, di, k, proj, ldp, x_col, k_col, v_col, Hkv, dh, dv, window, cap, pos, k_ring, v_ring, conv_w, conv_b,
+      conv_state, u, ldu, append ? 1 : 0);
+  return last_err();
+}
+
+}  // namespace hy

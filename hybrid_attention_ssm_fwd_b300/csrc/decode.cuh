@@ -74,4 +74,11 @@ hymba_status decode_ssm_step(int B, int di, int N, int R, const __half* u, long 
 
 hymba_status pos_increment(int B, int32_t* pos, cudaStream_t st);
 
+// The ring append of the new token's K/V (when append) and the conv step in
+// one launch: u = silu(conv), conv_state shifted in place.
+hymba_status decode_prep(int B, int di, int k, const __half* proj, long long ldp, int x_col, int k_col, int v_col,
+                         int Hkv, int dh, int dv, int window, int cap, const int32_t* pos, __nv_bfloat16* k_ring,
+                         __nv_bfloat16* v_ring, const float* conv_w, const float* conv_b, float* conv_state,
+                         __half* u, long long ldu, bool append, cudaStream_t st);
+
 }  // namespace hy

@@ -468,10 +468,10 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   mk.mark();
   TRY(in_proj_bf16(x, Xn, w, proj, B, c->pos, x.M, 1, status, sms, st));
   mk.mark();
-  if (!x.kv_shared)
-    TRY(kv_append<__half, __nv_bfloat16>(B, x.Hkv, x.dh, x.dv, x.W, c->cap, proj, x.P_in, x.k_col, x.v_col, c->pos,
-                                         static_cast<__nv_bfloat16*>(c->k_ring),
-                                         static_cast<__nv_bfloat16*>(c->v_ring), st));
+  // the new token's K/V into the ring and the conv step, one launch
+  TRY(decode_prep(B, x.di, x.k, proj, x.P_in, x.x_col, x.k_col, x.v_col, x.Hkv, x.dh, x.dv, x.W, c->cap, c->pos,
+                  static_cast<__nv_bfloat16*>(c->k_ring), static_cast<__nv_bfloat16*>(c->v_ring), w->conv_w,
+                  w->conv_b, c->conv_state, u, x.di, !x.kv_shared, st));
   mk.mark();
   if (decode_attn_tc_supported(x.Hq, x.Hkv, x.dh, x.dv)) {
     TRY(decode_attention_tc(B, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, kvc->cap, pl.attn_splits, proj, x.P_in,
@@ -494,8 +494,7 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
         static_cast<const __nv_bfloat16*>(kvc->v_meta), static_cast<const __nv_bfloat16*>(kvc->k_ring),
         static_cast<const __nv_bfloat16*>(kvc->v_ring), c->pos, att, x.di, st));
   }
-  mk.mark();
-  TRY(conv_step<__half>(B, x.di, x.k, proj + x.x_col, x.P_in, w->conv_w, w->conv_b, c->conv_state, u, x.di, st));
+  mk.mark();  // (conv step ran with the ring append)
   mk.mark();
   {
     const int ldp = (x.xo + 15) / 16 * 16;
