@@ -50,6 +50,11 @@ class Cache(ctypes.Structure):
                 ("reserved", c_int32)]
 
 
+class Meta(ctypes.Structure):
+    _fields_ = [("k", c_void_p), ("v", c_void_p), ("ssm_state", c_void_p), ("conv_tail", c_void_p),
+                ("y", c_void_p)]
+
+
 WEIGHT_NAMES = [f[0] for f in LayerWeights._fields_]
 CACHE_NAMES = ["k_ring", "v_ring", "k_meta", "v_meta", "ssm_state", "conv_state", "pos"]
 
@@ -87,6 +92,16 @@ def lib() -> ctypes.CDLL:
     L.hymba_layer_decode_static.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, P(Cache),
                                             P(Cache), c_void_p, c_void_p]
     L.hymba_layer_decode_static.restype = c_int32
+    L.hymba_meta_prefill_workspace.argtypes = [P(LayerDesc)]
+    L.hymba_meta_prefill_workspace.restype = c_size_t
+    L.hymba_layer_fwd_meta_workspace.argtypes = [P(LayerDesc)]
+    L.hymba_layer_fwd_meta_workspace.restype = c_size_t
+    L.hymba_meta_prefill.argtypes = [P(LayerDesc), P(LayerWeights), c_void_p, P(Meta), P(KV), c_void_p, c_size_t,
+                                     c_void_p, c_void_p]
+    L.hymba_meta_prefill.restype = c_int32
+    L.hymba_layer_fwd_meta.argtypes = [P(LayerDesc), P(LayerWeights), P(Meta), c_void_p, c_void_p, P(Cache), P(KV),
+                                       P(KV), c_void_p, c_size_t, c_void_p, c_void_p]
+    L.hymba_layer_fwd_meta.restype = c_int32
     L.hymba_test_gemm.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
                                   c_void_p, c_int32, c_void_p, c_void_p]
     L.hymba_test_gemm.restype = c_int32
@@ -190,6 +205,39 @@ def hymba_layer_fwd_events(desc: LayerDesc, weights: LayerWeights, x, y, ws, eve
                                       _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), events, n_events,
                                       _stream(stream))
     return _check(rc, "hymba_layer_fwd_events") if check else rc
+
+
+def make_meta(m: Dict[str, "object"]) -> Meta:
+    return Meta(**{n: _ptr(m.get(n)) for n in ("k", "v", "ssm_state", "conv_tail", "y")})
+
+
+def meta_prefill_workspace(desc: LayerDesc) -> int:
+    return lib().hymba_meta_prefill_workspace(ctypes.byref(desc))
+
+
+def layer_fwd_meta_workspace(desc: LayerDesc) -> int:
+    return lib().hymba_layer_fwd_meta_workspace(ctypes.byref(desc))
+
+
+def hymba_meta_prefill(desc: LayerDesc, weights: LayerWeights, x_meta, meta: Meta, ws, kv_in: Optional[KV] = None,
+                       status=None, stream=None, check: bool = True) -> int:
+    """The layer over the meta rows alone, once for the batch (see include/hymba.h)."""
+    rc = lib().hymba_meta_prefill(ctypes.byref(desc), ctypes.byref(weights), _ptr(x_meta), ctypes.byref(meta),
+                                  ctypes.byref(kv_in) if kv_in is not None else None,
+                                  _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+    return _check(rc, "hymba_meta_prefill") if check else rc
+
+
+def hymba_layer_fwd_meta(desc: LayerDesc, weights: LayerWeights, meta: Meta, x, y, ws,
+                         cache_out: Optional[Cache] = None, kv_in: Optional[KV] = None, kv_out: Optional[KV] = None,
+                         status=None, stream=None, check: bool = True) -> int:
+    """Prefill of the real tokens from a meta-prefix state (see include/hymba.h)."""
+    rc = lib().hymba_layer_fwd_meta(ctypes.byref(desc), ctypes.byref(weights), ctypes.byref(meta), _ptr(x), _ptr(y),
+                                    ctypes.byref(cache_out) if cache_out is not None else None,
+                                    ctypes.byref(kv_in) if kv_in is not None else None,
+                                    ctypes.byref(kv_out) if kv_out is not None else None,
+                                    _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+    return _check(rc, "hymba_layer_fwd_meta") if check else rc
 
 
 def hymba_layer_decode(desc: LayerDesc, weights: LayerWeights, x_new, y, cache: Cache, ws,

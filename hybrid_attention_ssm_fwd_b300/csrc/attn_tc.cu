@@ -45,6 +45,11 @@ constexpr int W_TMA = 8, W_MMA = 9;  // MMA issuers: warps 9-12
 
 struct AttnParams {
   int B, L, M, Hq, Hkv, dv, window, n_qt, n_hu, n_units;
+  // L and M are logical (meta rows first).  Normally the Q/K/V/O tensors
+  // hold all L rows of a sequence (q_off = 0, Lq = L).  With meta_sep the
+  // meta keys come from their own [M, ...] tensors, shared by the batch, and
+  // Q/K/V/O hold only the Lq = L - M real rows (q_off = M).
+  int meta_sep, q_off, Lq;
   float scale_log2;  // log2(e) / sqrt(dh)
   __half* O;
   long long ldo;
@@ -67,7 +72,7 @@ HY_DEV Unit make_unit(const AttnParams& p, int u) {
   U.hA = p.hA[hu];
   U.hB = p.hB[hu];
   U.g = (U.hA * p.Hkv) / p.Hq;
-  U.q0 = qt * BQ;
+  U.q0 = p.q_off + qt * BQ;  // logical position of the tile's first row
   U.qv1 = min(U.q0 + BQ, p.L);
   const int diag = (U.qv1 - 1) / BKV;
   const int meta_last = p.M > 0 ? (p.M - 1) / BKV : -1;
@@ -142,7 +147,8 @@ HY_DEV void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint
 template <int DV>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ AttnParams p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKm,
+                   const __grid_constant__ CUtensorMap tmVm, const __grid_constant__ AttnParams p) {
   using Cfg = AttnCfg<DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -185,20 +191,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const Unit U = make_unit(p, u);
         if (!mbar_wait(bar(B_QEMPTY), (uc & 1) ^ 1, wc)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(B_QFULL), (U.hB >= 0 ? 2 : 1) * Cfg::Q_BYTES);
-        tma_load_3d(sQ, &tmQ, bar(B_QFULL), U.hA * DH, U.q0, U.b);
-        if (U.hB >= 0) tma_load_3d(sQ + Cfg::Q_BYTES, &tmQ, bar(B_QFULL), U.hB * DH, U.q0, U.b);
+        tma_load_3d(sQ, &tmQ, bar(B_QFULL), U.hA * DH, U.q0 - p.q_off, U.b);
+        if (U.hB >= 0) tma_load_3d(sQ + Cfg::Q_BYTES, &tmQ, bar(B_QFULL), U.hB * DH, U.q0 - p.q_off, U.b);
         for (int t = 0; t < U.n_tiles; ++t, ++kc) {
           const int s = kc % KV_STAGES;
           const uint32_t ph = (kc / KV_STAGES) & 1;
           const int k0 = tile_kt(U, t) * BKV;
+          // key source: the shared meta tensors, or this sequence's rows
+          const bool from_meta = p.meta_sep && k0 < p.M;
+          const CUtensorMap* mk = from_meta ? &tmKm : &tmK;
+          const CUtensorMap* mv = from_meta ? &tmVm : &tmV;
+          const int kr = from_meta ? k0 : k0 - p.q_off;
+          const int kb = from_meta ? 0 : U.b;
           if (!mbar_wait(bar(B_KEMPTY + s), ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(B_KFULL + s), Cfg::K_BYTES);
-          tma_load_3d(sK + s * Cfg::K_BYTES, &tmK, bar(B_KFULL + s), U.g * DH, k0, U.b);
+          tma_load_3d(sK + s * Cfg::K_BYTES, mk, bar(B_KFULL + s), U.g * DH, kr, kb);
           if (!mbar_wait(bar(B_VEMPTY + s), ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(bar(B_VFULL + s), Cfg::V_BYTES);
 #pragma unroll
           for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(sV + s * Cfg::V_BYTES + c * (BKV * 128), &tmV, bar(B_VFULL + s), U.g * DV + c * 64, k0, U.b);
+            tma_load_3d(sV + s * Cfg::V_BYTES + c * (BKV * 128), mv, bar(B_VFULL + s), U.g * DV + c * 64, kr, kb);
         }
       }
       // after a wait gave up, let the loads this thread issued land before
@@ -392,7 +404,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!__all_sync(0xffffffffu, g4)) { ok = false; break; }
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-      __half* orow = p.O + (static_cast<long long>(U.b) * p.L + i) * p.ldo + h * DV;
+      __half* orow = p.O + (static_cast<long long>(U.b) * p.Lq + (i - p.q_off)) * p.ldo + h * DV;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t rr[32];
@@ -423,12 +435,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 template <int DV>
-hymba_status launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const AttnParams& p,
-                    int grid, cudaStream_t st) {
+hymba_status launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& km,
+                    const CUtensorMap& vm, const AttnParams& p, int grid, cudaStream_t st) {
   auto kern = attn_tc_kernel<DV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<DV>::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
-  kern<<<grid, NTHREADS, AttnCfg<DV>::SMEM, st>>>(q, k, v, p);
+  kern<<<grid, NTHREADS, AttnCfg<DV>::SMEM, st>>>(q, k, v, km, vm, p);
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 
@@ -443,16 +455,31 @@ bool make_map3(CUtensorMap* m, const __half* base, int cols, int L, int B, long 
 
 bool attn_tc_supported(int dh, int dv) { return dh == DH && (dv == 64 || dv == 128); }
 
-hymba_status attn_tc(int B, int L, int M, int Hq, int Hkv, int dh, int dv, int window, const __half* Q, long long ldq,
-                     const __half* K, long long ldk, const __half* V, long long ldv, __half* O, long long ldo,
-                     int32_t* status, uint64_t wait_ns, int num_sms, cudaStream_t st) {
+namespace {
+
+hymba_status attn_tc_impl(int B, int L, int M, int Lq, const __half* Km, const __half* Vm, int Hq, int Hkv, int dh,
+                          int dv, int window, const __half* Q, long long ldq, const __half* K, long long ldk,
+                          const __half* V, long long ldv, __half* O, long long ldo, int32_t* status, uint64_t wait_ns,
+                          int num_sms, cudaStream_t st) {
   if (!attn_tc_supported(dh, dv) || Hq > MAX_HU || Hkv < 1 || Hkv > Hq) return HYMBA_ERR_UNSUPPORTED;
+  const bool sep = Km != nullptr;
+  if (sep && (M < 1 || M % BKV != 0 || !Vm)) return HYMBA_ERR_UNSUPPORTED;
   auto al = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; };
   if (!al(Q) || !al(K) || !al(V) || !al(O) || ldq % 8 || ldk % 8 || ldv % 8 || ldo % 8) return HYMBA_ERR_INVALID;
-  CUtensorMap tq, tk, tv;
-  if (!make_map3(&tq, Q, Hq * dh, L, B, ldq, BQ) || !make_map3(&tk, K, Hkv * dh, L, B, ldk, BKV) ||
-      !make_map3(&tv, V, Hkv * dv, L, B, ldv, BKV))
+  if (sep && (!al(Km) || !al(Vm))) return HYMBA_ERR_INVALID;
+  if (Lq < 1) return HYMBA_OK;
+  CUtensorMap tq, tk, tv, tkm, tvm;
+  if (!make_map3(&tq, Q, Hq * dh, Lq, B, ldq, BQ) || !make_map3(&tk, K, Hkv * dh, Lq, B, ldk, BKV) ||
+      !make_map3(&tv, V, Hkv * dv, Lq, B, ldv, BKV))
     return HYMBA_ERR_CUDA;
+  if (sep) {
+    if (!make_map3(&tkm, Km, Hkv * dh, M, 1, static_cast<long long>(Hkv) * dh, BKV) ||
+        !make_map3(&tvm, Vm, Hkv * dv, M, 1, static_cast<long long>(Hkv) * dv, BKV))
+      return HYMBA_ERR_CUDA;
+  } else {
+    tkm = tk;  // never read
+    tvm = tv;
+  }
   AttnParams p{};
   p.B = B;
   p.L = L;
@@ -461,7 +488,10 @@ hymba_status attn_tc(int B, int L, int M, int Hq, int Hkv, int dh, int dv, int w
   p.Hkv = Hkv;
   p.dv = dv;
   p.window = window;
-  p.n_qt = (L + BQ - 1) / BQ;
+  p.meta_sep = sep ? 1 : 0;
+  p.q_off = L - Lq;
+  p.Lq = Lq;
+  p.n_qt = (Lq + BQ - 1) / BQ;
   // head units: consecutive heads of one KV group in pairs, a group's odd head alone
   int n_hu = 0;
   for (int h = 0; h < Hq;) {
@@ -480,7 +510,24 @@ hymba_status attn_tc(int B, int L, int M, int Hq, int Hkv, int dh, int dv, int w
   p.status = status;
   p.wait_ns = wait_ns;
   const int grid = std::min(p.n_units, std::max(1, num_sms));
-  return dv == 128 ? launch<128>(tq, tk, tv, p, grid, st) : launch<64>(tq, tk, tv, p, grid, st);
+  return dv == 128 ? launch<128>(tq, tk, tv, tkm, tvm, p, grid, st) : launch<64>(tq, tk, tv, tkm, tvm, p, grid, st);
+}
+
+}  // namespace
+
+hymba_status attn_tc(int B, int L, int M, int Hq, int Hkv, int dh, int dv, int window, const __half* Q, long long ldq,
+                     const __half* K, long long ldk, const __half* V, long long ldv, __half* O, long long ldo,
+                     int32_t* status, uint64_t wait_ns, int num_sms, cudaStream_t st) {
+  return attn_tc_impl(B, L, M, L, nullptr, nullptr, Hq, Hkv, dh, dv, window, Q, ldq, K, ldk, V, ldv, O, ldo, status,
+                      wait_ns, num_sms, st);
+}
+
+hymba_status attn_tc_meta(int B, int T, int M, const __half* Km, const __half* Vm, int Hq, int Hkv, int dh, int dv,
+                          int window, const __half* Q, long long ldq, const __half* K, long long ldk, const __half* V,
+                          long long ldv, __half* O, long long ldo, int32_t* status, uint64_t wait_ns, int num_sms,
+                          cudaStream_t st) {
+  return attn_tc_impl(B, M + T, M, T, Km, Vm, Hq, Hkv, dh, dv, window, Q, ldq, K, ldk, V, ldv, O, ldo, status,
+                      wait_ns, num_sms, st);
 }
 
 }  // namespace hy

@@ -12,8 +12,10 @@
 // shared-memory stages with one 3-D TMA load (sequence, row, channel).  The
 // load of a tile that starts at row 0 begins at row -(K-1), which TMA fills
 // with zeros: that is the causal zero padding, and no row of the previous
-// sequence is ever read.  Each thread then computes 4 rows x 8 channels from
-// shared memory and writes 16-byte vectors of u.  Every wait is bounded.
+// sequence is ever read.  When a history `tail` is given (the meta rows
+// processed once for the whole batch), its K-1 rows replace that zero
+// padding in shared memory.  Each thread then computes 4 rows x 8 channels
+// from shared memory and writes 16-byte vectors of u.  Every wait is bounded.
 #include "simt.cuh"
 
 namespace hy {
@@ -36,8 +38,8 @@ struct ConvCfg {
 template <int K>
 __global__ void __launch_bounds__(CV_THREADS, 2)
     conv_tma_kernel(const __grid_constant__ CUtensorMap tmX, __half* __restrict__ u, long long ld_u, int B, int L,
-                    int di, const float* __restrict__ w, const float* __restrict__ bias, int32_t* status,
-                    uint64_t wait_ns) {
+                    int di, const float* __restrict__ w, const float* __restrict__ bias,
+                    const float* __restrict__ tail, int32_t* status, uint64_t wait_ns) {
   using Cfg = ConvCfg<K>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CV_S * Cfg::STAGE);
@@ -87,6 +89,16 @@ __global__ void __launch_bounds__(CV_THREADS, 2)
     bool ok = mbar_wait(smem_u32(&bars[s]), (it / CV_S) & 1, wc);
     if (!__syncthreads_and(ok)) break;
     const int tt = rt % n_tt, b = rt / n_tt;
+    if (tail != nullptr && tt == 0) {
+      // history rows of the first tile: the tail [di, K-1] (oldest first), not zeros
+      __half* hist = reinterpret_cast<__half*>(smem + s * Cfg::STAGE);
+      for (int i = tid; i < (K - 1) * CV_CW; i += CV_THREADS) {
+        const int j = i / CV_CW, cc = i % CV_CW, c = ct * CV_CW + cc;
+        hist[j * CV_CW + cc] = __float2half_rn(c < di ? tail[static_cast<long long>(c) * (K - 1) + j] : 0.f);
+      }
+      fence_proxy_async_smem();  // these stores come before the stage's next TMA write
+      __syncthreads();
+    }
     if (c0 < di) {
       const uint8_t* st = smem + s * Cfg::STAGE + cg * 16;
       const int r0 = rg * CV_RPT;  // first output row of this thread within the tile
@@ -149,7 +161,8 @@ __global__ void __launch_bounds__(CV_THREADS, 2)
 
 template <int K>
 hymba_status launch_conv(const CUtensorMap& m, __half* u, long long ld_u, int B, int L, int di, const float* w,
-                         const float* bias, int32_t* status, uint64_t wait_ns, int num_sms, cudaStream_t st) {
+                         const float* bias, const float* tail, int32_t* status, uint64_t wait_ns, int num_sms,
+                         cudaStream_t st) {
   using Cfg = ConvCfg<K>;
   auto kern = conv_tma_kernel<K>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
@@ -159,7 +172,7 @@ hymba_status launch_conv(const CUtensorMap& m, __half* u, long long ld_u, int B,
   const long long n_rt = static_cast<long long>(B) * ((L + CV_TT - 1) / CV_TT);
   const int per_ct = static_cast<int>(std::max(1LL, std::min(n_rt, (2LL * num_sms + n_ct - 1) / n_ct)));
   const int grid = n_ct * per_ct;
-  kern<<<grid, CV_THREADS, Cfg::SMEM, st>>>(m, u, ld_u, B, L, di, w, bias, status, wait_ns);
+  kern<<<grid, CV_THREADS, Cfg::SMEM, st>>>(m, u, ld_u, B, L, di, w, bias, tail, status, wait_ns);
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 
@@ -172,7 +185,7 @@ bool conv_tma_supported(int di, int k, long long ld_x, long long ld_u, const voi
 
 hymba_status conv_silu_tma(const __half* x, long long ld_x, __half* u, long long ld_u, int B, int L, int di, int k,
                            const float* w, const float* bias, int32_t* status, uint64_t wait_ns, int num_sms,
-                           cudaStream_t st) {
+                           cudaStream_t st, const float* tail) {
   if (!conv_tma_supported(di, k, ld_x, ld_u, x, u)) return HYMBA_ERR_UNSUPPORTED;
   if (B < 1 || L < 1) return HYMBA_OK;
   CUtensorMap m;
@@ -182,9 +195,9 @@ hymba_status conv_silu_tma(const __half* x, long long ld_x, __half* u, long long
   if (!encode_tmap(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, x, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE))
     return HYMBA_ERR_CUDA;
   switch (k) {
-    case 2: return launch_conv<2>(m, u, ld_u, B, L, di, w, bias, status, wait_ns, num_sms, st);
-    case 3: return launch_conv<3>(m, u, ld_u, B, L, di, w, bias, status, wait_ns, num_sms, st);
-    default: return launch_conv<4>(m, u, ld_u, B, L, di, w, bias, status, wait_ns, num_sms, st);
+    case 2: return launch_conv<2>(m, u, ld_u, B, L, di, w, bias, tail, status, wait_ns, num_sms, st);
+    case 3: return launch_conv<3>(m, u, ld_u, B, L, di, w, bias, tail, status, wait_ns, num_sms, st);
+    default: return launch_conv<4>(m, u, ld_u, B, L, di, w, bias, tail, status, wait_ns, num_sms, st);
   }
 }
 

@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(192, 1)
 
       if (EPI == EPI_F16 && p.rope_cols > 0 && col_tile < p.rope_cols) {
         // RoPE: 64-column heads, pair (i, i+32) rotated by pos * inv_freq[i]
-        const int posn = p.pos ? (p.pos_base + p.pos[min(row, p.M - 1)]) : (row % p.rows_per_seq);
+        const int posn = p.pos_base + (p.pos ? p.pos[min(row, p.M - 1)] : (row % p.rows_per_seq));
         for (int c0 = 0; c0 < BN; c0 += 64) {
           const int col = col_tile + c0;
           if (col >= p.N) break;

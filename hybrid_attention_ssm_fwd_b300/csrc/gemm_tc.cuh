@@ -29,7 +29,7 @@ struct GemmParams {
   int xproj_R;
   int rope_cols;          // 0 = no RoPE
   float rope_log2_step;   // log2(inv_freq[i]) = i * rope_log2_step
-  int rows_per_seq;       // position = row % rows_per_seq when pos == nullptr
+  int rows_per_seq;       // position = pos_base + row % rows_per_seq when pos == nullptr
   const int32_t* pos;     // decode: position = pos_base + pos[row]
   int pos_base;
   int32_t* status;

@@ -306,10 +306,19 @@ hymba_status in_proj_bf16(const Dims& x, const void* X, const hymba_layer_weight
   return HYMBA_OK;
 }
 
+// Meta-prefix precompute: `out` set = produce (x holds the M meta rows of one
+// sequence: B = 1, T = 0, L = M); `in` set = consume (x holds only the T real
+// rows of each sequence: L = T, while x.M keeps the logical meta count).
+struct MetaCtx {
+  const hymba_meta* in = nullptr;
+  const hymba_meta* out = nullptr;
+};
+
 hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const void* X, float* Y,
                       const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
-                      int32_t* status, Marks& mk, cudaStream_t st) {
+                      int32_t* status, Marks& mk, cudaStream_t st, const MetaCtx& mc = MetaCtx{}) {
   const int sms = num_sms();
+  const hymba_meta* mi = mc.in;
   const int rows = static_cast<int>(x.rows);
   __half* proj = at<__half>(ws, pl.proj);
   __half* u = at<__half>(ws, pl.u);
@@ -322,7 +331,8 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
   mk.mark();
   TRY(convert_weights(x, pl, w, ws, st));
   mk.mark();
-  TRY(in_proj_bf16(x, X, w, proj, rows, nullptr, 0, x.L, status, sms, st));
+  // positions: logical (meta rows first), so real rows start at M when the meta rows are cached
+  TRY(in_proj_bf16(x, X, w, proj, rows, nullptr, mi ? x.M : 0, x.L, status, sms, st));
   mk.mark();
 
   const __half* Kp = x.kv_shared ? static_cast<const __half*>(kv_in->k) : proj + x.k_col;
@@ -337,7 +347,10 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
   }
   mk.mark();
   // attention branch
-  if (attn_tc_supported(x.dh, x.dv)) {
+  if (mi) {
+    TRY(attn_tc_meta(x.B, x.T, x.M, static_cast<const __half*>(mi->k), static_cast<const __half*>(mi->v), x.Hq,
+                     x.Hkv, x.dh, x.dv, x.W, proj, x.P_in, Kp, ldk, Vp, ldv, att, x.di, status, x.wait_ns, sms, st));
+  } else if (attn_tc_supported(x.dh, x.dv)) {
     TRY(attn_tc(x.B, x.L, x.M, x.Hq, x.Hkv, x.dh, x.dv, x.W, proj, x.P_in, Kp, ldk, Vp, ldv, att, x.di, status,
                 x.wait_ns, sms, st));
   } else {
@@ -348,7 +361,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
   // SSM branch
   if (conv_tma_supported(x.di, x.k, x.P_in, x.di, proj + x.x_col, u))
     TRY(conv_silu_tma(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, status, x.wait_ns,
-                      sms, st));
+                      sms, st, mi ? mi->conv_tail : nullptr));
   else
     TRY(conv_silu<__half, __half>(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, st));
   mk.mark();
@@ -362,13 +375,13 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     TRY(gemm_tc(0, u, x.di, at<__half>(ws, pl.wx), x.di, EPI_XPROJ, p, 0, 1, sms, st));
   }
   mk.mark();
-  float* h_out = cache_out ? cache_out->ssm_state : nullptr;
+  float* h_out = cache_out ? cache_out->ssm_state : (mc.out ? mc.out->ssm_state : nullptr);
   if (scan_fused_supported(x.di, x.N, x.R)) {
     // dt projection + softplus run inside the scan (no delta in HBM)
     mk.mark();
     TRY(scan_fused_f16(x.B, x.L, x.di, x.N, x.R, u, x.di, proj + x.z_col, x.P_in, dtr, x.Rp,
-                       static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, bc, w->A_log, w->D, g, nullptr, h_out,
-                       status, x.wait_ns, 0, st));
+                       static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, bc, w->A_log, w->D, g,
+                       mi ? mi->ssm_state : nullptr, h_out, status, x.wait_ns, 0, st, mi != nullptr));
   } else {
     GemmParams p = gp(rows, x.di, x.R, status, x.wait_ns);
     p.C = delta;
@@ -393,12 +406,40 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     TRY(gemm_tc(0, s, x.di, at<__half>(ws, pl.wout), x.di, EPI_F32, p, 0, 1, sms, st));
   }
   mk.mark();
-  if (cache_out) {
+  if (cache_out && mi) {
+    // ring and conv tail from the real rows (the tail falls back on the meta
+    // rows' tail), the meta K/V from the cached meta state
+    TRY(emit_cache<__half, __nv_bfloat16>(
+        x.B, x.L, 0, x.T, cache_out->cap, x.Hkv, x.dh, x.dv, x.di, x.k, x.kv_shared ? nullptr : Kp, ldk, Vp, ldv,
+        proj + x.x_col, x.P_in, static_cast<__nv_bfloat16*>(cache_out->k_ring),
+        static_cast<__nv_bfloat16*>(cache_out->v_ring), nullptr, nullptr, cache_out->conv_state, cache_out->pos, st,
+        mi->conv_tail));
+    if (!x.kv_shared) {
+      TRY(copy2d<__half, __nv_bfloat16>(static_cast<const __half*>(mi->k), static_cast<long long>(x.Hkv) * x.dh,
+                                        static_cast<__nv_bfloat16*>(cache_out->k_meta),
+                                        static_cast<long long>(x.Hkv) * x.dh, x.M, x.Hkv * x.dh, st));
+      TRY(copy2d<__half, __nv_bfloat16>(static_cast<const __half*>(mi->v), static_cast<long long>(x.Hkv) * x.dv,
+                                        static_cast<__nv_bfloat16*>(cache_out->v_meta),
+                                        static_cast<long long>(x.Hkv) * x.dv, x.M, x.Hkv * x.dv, st));
+    }
+  } else if (cache_out) {
     TRY(emit_cache<__half, __nv_bfloat16>(
         x.B, x.L, x.M, x.T, cache_out->cap, x.Hkv, x.dh, x.dv, x.di, x.k, x.kv_shared ? nullptr : Kp, ldk, Vp, ldv,
         proj + x.x_col, x.P_in, static_cast<__nv_bfloat16*>(cache_out->k_ring),
         static_cast<__nv_bfloat16*>(cache_out->v_ring), static_cast<__nv_bfloat16*>(cache_out->k_meta),
         static_cast<__nv_bfloat16*>(cache_out->v_meta), cache_out->conv_state, cache_out->pos, st));
+  }
+  if (mc.out) {
+    // what the real tokens need from the meta rows: K/V (fp16) and the conv tail
+    if (!x.kv_shared) {
+      TRY(copy2d<__half, __half>(Kp, ldk, static_cast<__half*>(mc.out->k), static_cast<long long>(x.Hkv) * x.dh, x.M,
+                                 x.Hkv * x.dh, st));
+      TRY(copy2d<__half, __half>(Vp, ldv, static_cast<__half*>(mc.out->v), static_cast<long long>(x.Hkv) * x.dv, x.M,
+                                 x.Hkv * x.dv, st));
+    }
+    TRY(emit_cache<__half, __nv_bfloat16>(1, x.L, x.M, 0, 1, x.Hkv, x.dh, x.dv, x.di, x.k, nullptr, ldk, nullptr, ldv,
+                                          proj + x.x_col, x.P_in, nullptr, nullptr, nullptr, nullptr,
+                                          mc.out->conv_tail, nullptr, st));
   }
   mk.mark();
   return HYMBA_OK;
@@ -565,6 +606,31 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   return HYMBA_OK;
 }
 
+// Dims of a meta-prefix call: produce = the M meta rows of one sequence
+// (B = 1, T = 0, L = M); otherwise the T real rows of each sequence (L = T).
+hymba_status meta_dims(const hymba_layer_desc* d, bool produce, Dims* x) {
+  if (!d) return HYMBA_ERR_INVALID;
+  hymba_layer_desc dd = *d;
+  if (produce) {
+    dd.batch = 1;
+    dd.n_tokens = 1;  // validated as one token; the call processes none
+  }
+  TRY(check_desc(&dd, false, x));
+  if (x->dtype != HYMBA_BF16 || !attn_tc_supported(x->dh, x->dv) || x->M < 64 || x->M % 64 != 0 ||
+      !scan_fused_supported(x->di, x->N, x->R) || (x->theta > 0 && x->dh != 64))
+    return HYMBA_ERR_UNSUPPORTED;
+  if (produce) {
+    x->B = 1;
+    x->T = 0;
+    x->L = x->M;
+    x->rows = x->M;
+  } else {
+    x->L = x->T;
+    x->rows = static_cast<long long>(x->B) * x->T;
+  }
+  return HYMBA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -644,6 +710,77 @@ hymba_status hymba_layer_fwd_events(const hymba_layer_desc* d, const hymba_layer
                                     const hymba_kv* kv_out, void* ws, size_t ws_bytes, int32_t* dev_status,
                                     void* const* events, int32_t n_events, void* stream) {
   return layer_fwd_impl(d, w, x_in, y, cache_out, kv_in, kv_out, ws, ws_bytes, dev_status, events, n_events, stream);
+}
+
+size_t hymba_meta_prefill_workspace(const hymba_layer_desc* d) {
+  Dims x;
+  if (meta_dims(d, true, &x) != HYMBA_OK) return 0;
+  return plan_ws(x, false).total;
+}
+
+hymba_status hymba_meta_prefill(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_meta,
+                                const hymba_meta* meta, const hymba_kv* kv_in, void* ws, size_t ws_bytes,
+                                int32_t* dev_status, void* stream) {
+  Dims x;
+  TRY(meta_dims(d, true, &x));
+  TRY(check_weights(w, x));
+  if (!x_meta || !meta || !meta->ssm_state || !meta->conv_tail || !meta->y || !ws) return HYMBA_ERR_INVALID;
+  if (!x.kv_shared && (!meta->k || !meta->v)) return HYMBA_ERR_INVALID;
+  if ((x.kv_shared != 0) != (kv_in != nullptr)) return HYMBA_ERR_INVALID;
+  if (kv_in && (!kv_in->k || !kv_in->v || !aligned(kv_in->k, 16) || !aligned(kv_in->v, 16))) return HYMBA_ERR_INVALID;
+  if (!aligned(x_meta, 16) || !aligned(meta->y, 16) || !aligned(ws, 256) || !aligned(meta->ssm_state, 4) ||
+      !aligned(meta->conv_tail, 4) || (meta->k && !aligned(meta->k, 16)) || (meta->v && !aligned(meta->v, 16)))
+    return HYMBA_ERR_INVALID;
+  const Plan pl = plan_ws(x, false);
+  if (ws_bytes < pl.total) return HYMBA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  Marks mk;
+  mk.st = st;
+  MetaCtx mc;
+  mc.out = meta;
+  return fwd_bf16(x, pl, w, x_meta, meta->y, nullptr, kv_in, nullptr, ws, dev_status, mk, st, mc);
+}
+
+size_t hymba_layer_fwd_meta_workspace(const hymba_layer_desc* d) {
+  Dims x;
+  if (meta_dims(d, false, &x) != HYMBA_OK) return 0;
+  return plan_ws(x, false).total;
+}
+
+hymba_status hymba_layer_fwd_meta(const hymba_layer_desc* d, const hymba_layer_weights* w, const hymba_meta* meta,
+                                  const void* x_in, float* y, const hymba_cache* cache_out, const hymba_kv* kv_in,
+                                  const hymba_kv* kv_out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                  void* stream) {
+  Dims x;
+  TRY(meta_dims(d, false, &x));
+  TRY(check_weights(w, x));
+  if (!meta || !meta->k || !meta->v || !meta->ssm_state || !meta->conv_tail || !x_in || !y || !ws)
+    return HYMBA_ERR_INVALID;
+  if (!aligned(meta->k, 16) || !aligned(meta->v, 16) || !aligned(meta->ssm_state, 4) || !aligned(meta->conv_tail, 4))
+    return HYMBA_ERR_INVALID;
+  if ((x.kv_shared != 0) != (kv_in != nullptr)) return HYMBA_ERR_INVALID;
+  if (kv_in && (!kv_in->k || !kv_in->v || !aligned(kv_in->k, 16) || !aligned(kv_in->v, 16))) return HYMBA_ERR_INVALID;
+  if (kv_out && (!kv_out->k || !kv_out->v)) return HYMBA_ERR_INVALID;
+  if (!aligned(x_in, 16) || !aligned(y, 16) || !aligned(ws, 256)) return HYMBA_ERR_INVALID;
+  if (cache_out) {
+    if (!cache_out->ssm_state || !cache_out->conv_state || cache_out->reserved != 0) return HYMBA_ERR_INVALID;
+    if (!x.kv_shared) {
+      if (!cache_out->k_ring || !cache_out->v_ring || !cache_out->k_meta || !cache_out->v_meta)
+        return HYMBA_ERR_INVALID;
+      if (cache_out->cap < 1) return HYMBA_ERR_INVALID;
+      if (x.W > 0 ? cache_out->cap < x.W : cache_out->cap < x.T) return HYMBA_ERR_INVALID;
+    }
+  }
+  const Plan pl = plan_ws(x, false);
+  if (ws_bytes < pl.total) return HYMBA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  Marks mk;
+  mk.st = st;
+  MetaCtx mc;
+  mc.in = meta;
+  return fwd_bf16(x, pl, w, x_in, y, cache_out, kv_in, kv_out, ws, dev_status, mk, st, mc);
 }
 
 static hymba_status layer_decode_impl(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_new,

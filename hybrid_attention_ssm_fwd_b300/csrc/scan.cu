@@ -87,6 +87,7 @@ struct ScanArgs {
   const float* D;
   __half* g;
   const float* h0;
+  long long h0_bs;  // elements between the initial states of two sequences (0: one shared state)
   float* h_out;
   int32_t* status;
   uint64_t wait_ns;
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH>::NT, 3)
     for (int p = 0; p < NS / 2; ++p) {
       const int s0 = c * N + sub * NS + 2 * p;
       A2[p] = pk2(-__expf(a.A_log[s0]) * kLog2e, -__expf(a.A_log[s0 + 1]) * kLog2e);
-      const long long hb = (static_cast<long long>(b) * di + c) * N + sub * NS + 2 * p;
+      const long long hb = static_cast<long long>(b) * a.h0_bs + static_cast<long long>(c) * N + sub * NS + 2 * p;
       h2[p] = a.h0 ? pk2(a.h0[hb], a.h0[hb + 1]) : pk2(0.f, 0.f);
     }
     bool ok = true;
@@ -497,7 +498,7 @@ hymba_status scan_f16(int B, int L, int di, int N, const __half* u, long long ld
     if (!map2(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, di, static_cast<long long>(B) * L, di,
               block_channels(tpc), SC_T))
       return HYMBA_ERR_CUDA;
-    ScanArgs args{L, di, 0, nullptr, nullptr, A_log, D, g, h0, h_out, status, wait_ns};
+    ScanArgs args{L, di, 0, nullptr, nullptr, A_log, D, g, h0, static_cast<long long>(di) * N, h_out, status, wait_ns};
     return launch_tpc<0>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
   }
   return scan_simt<__half>(B, L, di, N, u, ld_u, z, ld_z, delta, di, BC, BC + N, 2 * N, A_log, D, g, di, h0, h_out,
@@ -508,7 +509,7 @@ hymba_status scan_fused_f16(int B, int L, int di, int N, int R, const __half* u,
                             long long ld_z, const __half* dtr, long long ld_dtr, const __nv_bfloat16* W_dt,
                             const float* dt_bias, const float* BC, const float* A_log, const float* D, __half* g,
                             const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, int tpc,
-                            cudaStream_t st) {
+                            cudaStream_t st, bool h0_shared) {
   if (!scan_fused_supported(di, N, R)) return HYMBA_ERR_UNSUPPORTED;
   if (ld_u % 8 || ld_z % 8 || ld_dtr % 8 || !aligned16(u) || !aligned16(z) || !aligned16(dtr) || !aligned16(BC) ||
       !aligned16(g))
@@ -519,7 +520,8 @@ hymba_status scan_fused_f16(int B, int L, int di, int N, int R, const __half* u,
   CUtensorMap mX;
   if (!map2(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, dtr, R, static_cast<long long>(B) * L, ld_dtr, KS * 16, SC_T))
     return HYMBA_ERR_CUDA;
-  ScanArgs args{L, di, R, W_dt, dt_bias, A_log, D, g, h0, h_out, status, wait_ns};
+  ScanArgs args{L, di, R, W_dt, dt_bias, A_log, D, g, h0, h0_shared ? 0LL : static_cast<long long>(di) * N, h_out,
+                status, wait_ns};
   return launch_fused(KS, tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
 }
 

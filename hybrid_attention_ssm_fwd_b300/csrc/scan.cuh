@@ -24,7 +24,7 @@ hymba_status scan_fused_f16(int B, int L, int di, int N, int R, const __half* u,
                             long long ld_z, const __half* dtr, long long ld_dtr, const __nv_bfloat16* W_dt,
                             const float* dt_bias, const float* BC, const float* A_log, const float* D, __half* g,
                             const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, int tpc,
-                            cudaStream_t st);
+                            cudaStream_t st, bool h0_shared = false);  // h0_shared: h0 is [di, N], one for all
 
 // One block waits on an mbarrier nothing arrives on, bounded by limit_us,
 // and records HYMBA_ERR_TIMEOUT in *status.

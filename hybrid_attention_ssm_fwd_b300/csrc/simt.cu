@@ -566,7 +566,7 @@ __global__ void emit_ring_kernel(int B, int L, int M, int T, int cap, int n_keep
 
 template <typename TS>
 __global__ void emit_conv_tail_kernel(int B, int L, int di, int k, const TS* __restrict__ x, long long ldx,
-                                      float* __restrict__ conv_state) {
+                                      float* __restrict__ conv_state, const float* __restrict__ prev) {
   const long long n = static_cast<long long>(B) * di * (k - 1);
   for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -574,7 +574,9 @@ __global__ void emit_conv_tail_kernel(int B, int L, int di, int k, const TS* __r
     const int c = static_cast<int>((idx / (k - 1)) % di);
     const int b = static_cast<int>(idx / (static_cast<long long>(k - 1) * di));
     const int row = L - (k - 1) + j;
-    conv_state[idx] = row >= 0 ? to_f(x[(static_cast<long long>(b) * L + row) * ldx + c]) : 0.f;
+    // rows before the first come from `prev` ([di, k-1], oldest first), else zero
+    conv_state[idx] = row >= 0 ? to_f(x[(static_cast<long long>(b) * L + row) * ldx + c])
+                               : (prev ? prev[static_cast<long long>(c) * (k - 1) + (k - 1) + row] : 0.f);
   }
 }
 
@@ -701,7 +703,7 @@ template <typename TS, typename TC>
 hymba_status emit_cache(int B, int L, int M, int T, int cap, int Hkv, int dh, int dv, int di, int k,
                         const TS* Kp, long long ldk, const TS* Vp, long long ldv, const TS* xp, long long ldx,
                         TC* k_ring, TC* v_ring, TC* k_meta, TC* v_meta, float* conv_state, int32_t* pos,
-                        cudaStream_t st) {
+                        cudaStream_t st, const float* prev_tail) {
   if (pos) fill_i32_kernel<<<(B + 255) / 256, 256, 0, st>>>(B, pos, T);
   const int n_keep = std::min(T, cap);
   if (Kp && k_ring && n_keep > 0) {
@@ -721,7 +723,7 @@ hymba_status emit_cache(int B, int L, int M, int T, int cap, int Hkv, int dh, in
   if (conv_state && k > 1) {
     const long long n = static_cast<long long>(B) * di * (k - 1);
     emit_conv_tail_kernel<TS><<<std::min<long long>(grid1d(n, 256), 148 * 32), 256, 0, st>>>(B, L, di, k, xp,
-                                                                                          ldx, conv_state);
+                                                                                          ldx, conv_state, prev_tail);
   }
   return last_err();
 }
@@ -766,11 +768,11 @@ template hymba_status copy2d<__half, __nv_bfloat16>(const __half*, long long, __
                                                     long long, int, cudaStream_t);
 template hymba_status emit_cache<float, float>(int, int, int, int, int, int, int, int, int, int, const float*,
                                                long long, const float*, long long, const float*, long long,
-                                               float*, float*, float*, float*, float*, int32_t*, cudaStream_t);
+                                               float*, float*, float*, float*, float*, int32_t*, cudaStream_t, const float*);
 template hymba_status emit_cache<__half, __nv_bfloat16>(int, int, int, int, int, int, int, int, int, int,
                                                         const __half*, long long, const __half*, long long,
                                                         const __half*, long long, __nv_bfloat16*,
                                                         __nv_bfloat16*, __nv_bfloat16*, __nv_bfloat16*, float*,
-                                                        int32_t*, cudaStream_t);
+                                                        int32_t*, cudaStream_t, const float*);
 
 }  // namespace hy

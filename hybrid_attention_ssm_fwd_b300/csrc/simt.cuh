@@ -33,9 +33,11 @@ hymba_status conv_silu(const TI* x, long long ld_x, TO* u, long long ld_u, int B
 // fp16 conv + SiLU fed by TMA (conv.cu): the same result as conv_silu for
 // k in 2..4, di % 8 == 0, 16-byte aligned x and u, row strides % 8 == 0.
 bool conv_tma_supported(int di, int k, long long ld_x, long long ld_u, const void* x, const void* u);
+// tail (may be null): [di, k-1] fp32 history rows (oldest first) used in
+// place of the zero padding before row 0 of every sequence.
 hymba_status conv_silu_tma(const __half* x, long long ld_x, __half* u, long long ld_u, int B, int L, int di, int k,
                            const float* w, const float* bias, int32_t* status, uint64_t wait_ns, int num_sms,
-                           cudaStream_t st);
+                           cudaStream_t st, const float* tail = nullptr);
 
 // Generic selective scan + gate, one thread per (b, channel), N <= 64.
 // delta fp32 [B,L,di]; BC: B at Bm[row*ld_bc + n], C at Cm[row*ld_bc + n].
@@ -66,12 +68,14 @@ hymba_status copy2d(const TS* src, long long lds, TD* dst, long long ldd, long l
                     cudaStream_t st);
 
 // Prefill cache emission: ring K/V (last min(T, cap) tokens at slot t % cap),
-// meta K/V (from sequence 0), the conv tail (last k-1 x rows, fp32) and
+// meta K/V (from sequence 0), the conv tail (last k-1 x rows, fp32; rows
+// before the first from prev_tail [di, k-1] when given, else zero) and
 // pos[b] = T.
 template <typename TS, typename TC>
 hymba_status emit_cache(int B, int L, int M, int T, int cap, int Hkv, int dh, int dv, int di, int k,
                         const TS* Kp, long long ldk, const TS* Vp, long long ldv, const TS* xp,
                         long long ldx, TC* k_ring, TC* v_ring, TC* k_meta, TC* v_meta,
-                        float* conv_state, int32_t* pos, cudaStream_t st);
+                        float* conv_state, int32_t* pos, cudaStream_t st,
+                        const float* prev_tail = nullptr);
 
 }  // namespace hy

@@ -97,6 +97,54 @@ class HymbaLayer:
                            status=self.status)
         return y
 
+    def _scratch(self, nbytes: int) -> torch.Tensor:
+        if nbytes == 0:
+            raise hb.HymbaError(hb.HYMBA_ERR_UNSUPPORTED, "workspace query")
+        if self.ws.numel() < nbytes:
+            self.ws = torch.empty(nbytes, dtype=torch.uint8, device=self.ws.device)
+        return self.ws
+
+    def meta_prefill(self, x_meta: torch.Tensor, y: Optional[torch.Tensor] = None,
+                     kv_in=None) -> Dict[str, torch.Tensor]:
+        """The layer over the M meta rows alone ([M, d]), once for a whole
+        batch.  Returns the state forward_meta starts the real tokens from:
+        meta K/V (fp16; the producer's when kv_in is given), the SSM state
+        [di, N], the conv tail [di, k-1] and Y of the meta rows [M, d] (``y``,
+        when given, is that buffer: residual mode 2 adds into it)."""
+        s = self.shape
+        dev = x_meta.device
+        kd = kv_dtype(s)
+        meta = {
+            "ssm_state": torch.empty(s.di, s.N, device=dev, dtype=torch.float32),
+            "conv_tail": torch.empty(s.di, max(s.k - 1, 1), device=dev, dtype=torch.float32),
+            "y": y if y is not None else torch.empty(s.M, s.d, device=dev, dtype=torch.float32),
+        }
+        if kv_in is None:
+            meta["k"] = torch.empty(s.M, s.Hkv, s.dh, device=dev, dtype=kd)
+            meta["v"] = torch.empty(s.M, s.Hkv, s.dv, device=dev, dtype=kd)
+        else:
+            meta["k"], meta["v"] = kv_in
+        ws = self._scratch(hb.meta_prefill_workspace(self.desc))
+        hb.hymba_meta_prefill(self.desc, self.weights, x_meta, hb.make_meta(meta), ws,
+                              kv_in=hb.KV(kv_in[0].data_ptr(), kv_in[1].data_ptr()) if kv_in is not None else None,
+                              status=self.status)
+        return meta
+
+    def forward_meta(self, meta: Dict[str, torch.Tensor], x: torch.Tensor, y: Optional[torch.Tensor] = None,
+                     cache_out=None, cap: int = 0, kv_in=None, kv_out=None) -> torch.Tensor:
+        """Prefill of the real tokens x [B, T, d] from a meta_prefill state;
+        returns Y of the real rows [B, T, d].  kv_in / kv_out hold T rows."""
+        s = self.shape
+        if y is None:
+            y = torch.empty(s.B, s.T, s.d, dtype=torch.float32, device=x.device)
+        ws = self._scratch(hb.layer_fwd_meta_workspace(self.desc))
+        hb.hymba_layer_fwd_meta(self.desc, self.weights, hb.make_meta(meta), x, y, ws,
+                                cache_out=hb.make_cache(cache_out, cap) if cache_out is not None else None,
+                                kv_in=hb.KV(kv_in[0].data_ptr(), kv_in[1].data_ptr()) if kv_in is not None else None,
+                                kv_out=hb.KV(kv_out[0].data_ptr(), kv_out[1].data_ptr()) if kv_out is not None
+                                else None, status=self.status)
+        return y
+
     def decode(self, x_new: torch.Tensor, cache: Dict[str, torch.Tensor], cap: int,
                y: Optional[torch.Tensor] = None, shared_cache=None, shared_cap: int = 0) -> torch.Tensor:
         s = self.shape

@@ -191,6 +191,60 @@ HYMBA_API hymba_status hymba_layer_fwd_events(const hymba_layer_desc* d, const h
                                               size_t ws_bytes, int32_t* dev_status, void* const* events,
                                               int32_t n_events, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Meta-prefix precompute.  The M meta tokens are learned vectors prepended
+ * to every input (paper section 2.3), so their rows of a layer are the same
+ * for every sequence: hymba_meta_prefill runs the layer once over those M
+ * rows and keeps what the real tokens need from them; hymba_layer_fwd_meta
+ * then runs the layer over the real tokens of a whole batch from that
+ * state.  The result equals hymba_layer_fwd on [meta rows | tokens] (rows M..
+ * of Y) without recomputing the prefix B times.
+ * Supported on HYMBA_BF16 with head_dim 64, v_head_dim 64 or 128 and n_meta a
+ * positive multiple of 64 (HYMBA_ERR_UNSUPPORTED otherwise).
+ * ------------------------------------------------------------------------- */
+typedef struct hymba_meta {
+  void* k;              /* [M, Hkv, dh] fp16, post-RoPE (a KV-sharing layer
+                           points at its producer's meta K/V)                */
+  void* v;              /* [M, Hkv, dv] fp16                                 */
+  float* ssm_state;     /* [di, N] fp32: the SSM state after the meta rows   */
+  float* conv_tail;     /* [di, k-1] fp32: the last k-1 x rows, oldest first */
+  float* y;             /* [M, d] fp32: Y of the meta rows                   */
+} hymba_meta;
+
+/* Bytes of scratch memory hymba_meta_prefill needs (desc.batch and
+ * desc.n_tokens are ignored: one copy of the meta rows is processed).        */
+HYMBA_API size_t hymba_meta_prefill_workspace(const hymba_layer_desc* d);
+
+/* Runs the layer over the M meta rows alone and fills `meta` (every buffer
+ * device memory owned by the caller).
+ *   x_meta   [M, d] device, bf16: the meta rows of X~.
+ *   kv_in    non-NULL exactly when desc.kv_shared: the producer layer's meta
+ *            K/V ([M, Hkv, dh] / [M, Hkv, dv] fp16); meta->k / meta->v are
+ *            then not written.
+ * Errors as hymba_layer_fwd.                                                */
+HYMBA_API hymba_status hymba_meta_prefill(const hymba_layer_desc* d, const hymba_layer_weights* w,
+                                          const void* x_meta, const hymba_meta* meta, const hymba_kv* kv_in,
+                                          void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Bytes of scratch memory hymba_layer_fwd_meta needs for `d`.              */
+HYMBA_API size_t hymba_layer_fwd_meta_workspace(const hymba_layer_desc* d);
+
+/* Prefill of the real tokens from a hymba_meta_prefill state.
+ *   x        [B, T, d] device bf16: the real tokens only (no meta rows).
+ *   y        [B, T, d] device fp32: Y of the real tokens (position M + t);
+ *            residual 1 adds x, residual 2 updates y in place.
+ *   meta     the state written by hymba_meta_prefill with the same weights.
+ *   cache_out, kv_in, kv_out as hymba_layer_fwd, with the K/V of kv_in and
+ *            kv_out holding the T real rows ([B, T, Hkv, .]); the meta K/V of
+ *            cache_out are copied from meta->k / meta->v.  With cache_out,
+ *            T >= k-1 is not required: the conv tail falls back on
+ *            meta->conv_tail.                                               */
+HYMBA_API hymba_status hymba_layer_fwd_meta(const hymba_layer_desc* d, const hymba_layer_weights* w,
+                                            const hymba_meta* meta, const void* x, float* y,
+                                            const hymba_cache* cache_out, const hymba_kv* kv_in,
+                                            const hymba_kv* kv_out, void* ws, size_t ws_bytes,
+                                            int32_t* dev_status, void* stream);
+
 /* Bytes of scratch memory hymba_layer_decode needs for `d` (0 on invalid). */
 HYMBA_API size_t hymba_layer_decode_workspace(const hymba_layer_desc* d);
 

@@ -132,3 +132,47 @@ def test_decode_argument_checks():
 def test_unaligned_bf16_shapes_unsupported():
     d = _desc(d_model=1604)
     assert hb.layer_fwd_workspace(d) == 0
+
+
+def test_meta_prefix_workspace_and_support():
+    # the meta-prefix calls: bf16, dh 64, M a positive multiple of 64
+    d = _desc()
+    assert hb.meta_prefill_workspace(d) > 0
+    assert hb.layer_fwd_meta_workspace(_desc(n_tokens=256)) > hb.meta_prefill_workspace(d)  # B*T vs M rows
+    assert hb.meta_prefill_workspace(_desc(n_meta=96)) == 0
+    assert hb.layer_fwd_meta_workspace(_desc(n_meta=0)) == 0
+    assert hb.layer_fwd_meta_workspace(_desc(dtype=hb.HYMBA_F32)) == 0
+
+
+def test_meta_prefix_rejects_bad_arguments_before_launch():
+    d = _desc()
+    w = _fake_weights()
+    ws = ctypes.c_void_p(0x100000)
+    full = hb.Meta(k=0x400000, v=0x500000, ssm_state=0x600000, conv_tail=0x700000, y=0x800000)
+    L = hb.lib()
+    # no meta state
+    rc = L.hymba_layer_fwd_meta(ctypes.byref(d), ctypes.byref(w), None, 0x200000, 0x300000, None, None, None, ws,
+                                1 << 40, None, None)
+    assert rc == hb.HYMBA_ERR_INVALID
+    # missing meta K/V on a layer that owns its K/V
+    part = hb.Meta(k=0, v=0, ssm_state=0x600000, conv_tail=0x700000, y=0x800000)
+    rc = L.hymba_layer_fwd_meta(ctypes.byref(d), ctypes.byref(w), ctypes.byref(part), 0x200000, 0x300000, None, None,
+                                None, ws, 1 << 40, None, None)
+    assert rc == hb.HYMBA_ERR_INVALID
+    rc = L.hymba_meta_prefill(ctypes.byref(d), ctypes.byref(w), 0x200000, ctypes.byref(part), None, ws, 1 << 40,
+                              None, None)
+    assert rc == hb.HYMBA_ERR_INVALID
+    # kv_in given on a layer that owns its K/V
+    kv = hb.KV(k=0x900000, v=0xa00000)
+    rc = L.hymba_meta_prefill(ctypes.byref(d), ctypes.byref(w), 0x200000, ctypes.byref(full), ctypes.byref(kv), ws,
+                              1 << 40, None, None)
+    assert rc == hb.HYMBA_ERR_INVALID
+    # workspace too small
+    rc = L.hymba_meta_prefill(ctypes.byref(d), ctypes.byref(w), 0x200000, ctypes.byref(full), None, ws, 16, None,
+                              None)
+    assert rc == hb.HYMBA_ERR_WORKSPACE
+    # unsupported meta count
+    d96 = _desc(n_meta=96)
+    rc = L.hymba_layer_fwd_meta(ctypes.byref(d96), ctypes.byref(w), ctypes.byref(full), 0x200000, 0x300000, None,
+                                None, None, ws, 1 << 40, None, None)
+    assert rc == hb.HYMBA_ERR_UNSUPPORTED
