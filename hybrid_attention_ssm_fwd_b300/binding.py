@@ -109,10 +109,11 @@ def lib() -> ctypes.CDLL:
                                                   c_void_p]
     L.hymba_test_conv.restype = c_int32
     L.hymba_test_scan.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
-                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32,
+                                  c_void_p]
     L.hymba_test_scan.restype = c_int32
     L.hymba_test_scan_fused.argtypes = [c_int32] * 5 + [c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_int32] + \
-        [c_void_p] * 7 + [c_int32, c_void_p]
+        [c_void_p] * 7 + [c_int32, c_int32, c_void_p]
     L.hymba_test_scan_fused.restype = c_int32
     L.hymba_test_attention.argtypes = [c_int32] * 9 + [c_void_p] * 6
     L.hymba_test_attention.restype = c_int32
@@ -293,22 +294,24 @@ def hymba_test_conv(x, u, conv_w, conv_b, status=None, stream=None) -> int:
                                  _ptr(status), _stream(stream))
 
 
-def hymba_test_scan(u, z, delta, BC, A_log, D, g, h_out=None, threads_per_channel=0, stream=None) -> int:
+def hymba_test_scan(u, z, delta, BC, A_log, D, g, h_out=None, threads_per_channel=0, channels_per_thread=0,
+                    stream=None) -> int:
     B, L, di = delta.shape
     N = A_log.shape[1]
     return lib().hymba_test_scan(B, L, di, N, _ptr(u), u.stride(1), _ptr(z), z.stride(1), _ptr(delta),
                                  _ptr(BC), _ptr(A_log), _ptr(D), _ptr(g), _ptr(h_out), threads_per_channel,
-                                 _stream(stream))
+                                 channels_per_thread, _stream(stream))
 
 
 def hymba_test_scan_fused(u, z, dtr, W_dt, dt_bias, BC, A_log, D, g, h_out=None, threads_per_channel=0,
-                          stream=None) -> int:
+                          channels_per_thread=0, stream=None) -> int:
     B, L, di = u.shape
     N = A_log.shape[1]
     R = W_dt.shape[1]
     return lib().hymba_test_scan_fused(B, L, di, N, R, _ptr(u), u.stride(1), _ptr(z), z.stride(1), _ptr(dtr),
                                        dtr.stride(1), _ptr(W_dt), _ptr(dt_bias), _ptr(BC), _ptr(A_log), _ptr(D),
-                                       _ptr(g), _ptr(h_out), threads_per_channel, _stream(stream))
+                                       _ptr(g), _ptr(h_out), threads_per_channel, channels_per_thread,
+                                       _stream(stream))
 
 
 def hymba_test_attention(Q, K, V, O, M: int, window: int, use_tc: bool, status=None, stream=None) -> int:

@@ -381,7 +381,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     mk.mark();
     TRY(scan_fused_f16(x.B, x.L, x.di, x.N, x.R, u, x.di, proj + x.z_col, x.P_in, dtr, x.Rp,
                        static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, bc, w->A_log, w->D, g,
-                       mi ? mi->ssm_state : nullptr, h_out, status, x.wait_ns, 0, st, mi != nullptr));
+                       mi ? mi->ssm_state : nullptr, h_out, status, x.wait_ns, 0, 0, st, mi != nullptr));
   } else {
     GemmParams p = gp(rows, x.di, x.R, status, x.wait_ns);
     p.C = delta;
@@ -390,7 +390,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     TRY(gemm_tc(0, dtr, x.Rp, at<__half>(ws, pl.wdt), x.Rp, EPI_SOFTPLUS, p, 0, 1, sms, st));
     mk.mark();
     TRY(scan_f16(x.B, x.L, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, bc, w->A_log, w->D, g, nullptr, h_out,
-                 status, x.wait_ns, 0, st));
+                 status, x.wait_ns, 0, 0, st));
   }
   mk.mark();
   // fuse + out_proj
@@ -857,31 +857,38 @@ hymba_status hymba_test_conv(int32_t B, int32_t L, int32_t di, int32_t k, const 
                        dev_status, 2000000000ull, num_sms(), static_cast<cudaStream_t>(stream));
 }
 
+static bool scan_layout_ok(int32_t tpc, int32_t cpt) {
+  if (tpc == 0) return cpt == 0;
+  if (tpc != 1 && tpc != 2 && tpc != 4) return false;
+  return cpt == 0 || cpt == 1 || (cpt == 2 && tpc != 1);
+}
+
 hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t N, const void* u, int32_t ld_u, const void* z,
                              int32_t ld_z, const float* delta, const float* BC, const float* A_log, const float* D,
-                             void* g, float* h_out, int32_t threads_per_channel, void* stream) {
+                             void* g, float* h_out, int32_t threads_per_channel, int32_t channels_per_thread,
+                             void* stream) {
   if (B < 1 || L < 1 || di < 1 || N < 1 || N > 64 || !u || !z || !delta || !BC || !A_log || !D || !g ||
-      (threads_per_channel != 0 && threads_per_channel != 1 && threads_per_channel != 2 && threads_per_channel != 4))
+      !scan_layout_ok(threads_per_channel, channels_per_thread))
     return HYMBA_ERR_INVALID;
   cudaGetLastError();
   return scan_f16(B, L, di, N, static_cast<const __half*>(u), ld_u, static_cast<const __half*>(z), ld_z, delta, BC,
                   A_log, D, static_cast<__half*>(g), nullptr, h_out, nullptr, 2000000000ull, threads_per_channel,
-                  static_cast<cudaStream_t>(stream));
+                  channels_per_thread, static_cast<cudaStream_t>(stream));
 }
 
 hymba_status hymba_test_scan_fused(int32_t B, int32_t L, int32_t di, int32_t N, int32_t R, const void* u,
                                    int32_t ld_u, const void* z, int32_t ld_z, const void* dtr, int32_t ld_dtr,
                                    const void* W_dt, const float* dt_bias, const float* BC, const float* A_log,
                                    const float* D, void* g, float* h_out, int32_t threads_per_channel,
-                                   void* stream) {
+                                   int32_t channels_per_thread, void* stream) {
   if (B < 1 || L < 1 || di < 1 || N < 1 || R < 1 || !u || !z || !dtr || !W_dt || !dt_bias || !BC || !A_log || !D ||
-      !g || (threads_per_channel != 0 && threads_per_channel != 1 && threads_per_channel != 2 && threads_per_channel != 4))
+      !g || !scan_layout_ok(threads_per_channel, channels_per_thread))
     return HYMBA_ERR_INVALID;
   cudaGetLastError();
   return scan_fused_f16(B, L, di, N, R, static_cast<const __half*>(u), ld_u, static_cast<const __half*>(z), ld_z,
                         static_cast<const __half*>(dtr), ld_dtr, static_cast<const __nv_bfloat16*>(W_dt), dt_bias, BC,
                         A_log, D, static_cast<__half*>(g), nullptr, h_out, nullptr, 2000000000ull, threads_per_channel,
-                        static_cast<cudaStream_t>(stream));
+                        channels_per_thread, static_cast<cudaStream_t>(stream));
 }
 
 hymba_status hymba_test_attention(int32_t B, int32_t L, int32_t M, int32_t Hq, int32_t Hkv, int32_t dh, int32_t dv,

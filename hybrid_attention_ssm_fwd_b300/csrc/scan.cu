@@ -13,7 +13,8 @@
 // overlap the work of the others:
 //   delta warps (ND)  per chunk: delta for the block's channels x SC_T rows
 //                     (fused mode: mma.sync of the dt tile against W_dt
-//                     fragments kept in shared memory, then softplus;
+//                     fragments held in registers or shared memory, then
+//                     softplus;
 //                     otherwise the delta tile itself) and delta*u, as
 //                     (d, d*u) pairs; rows past the end of the sequence get
 //                     d = 0, which leaves the state unchanged;
@@ -40,21 +41,24 @@ namespace {
 
 constexpr int SC_N = 16;  // states per channel on this path
 constexpr int SC_T = 16;  // time rows per chunk
+constexpr int SC_H = 8;   // rows per partial-sum reduction of C.h
 constexpr int SC_S = 3;   // TMA pipeline stages
 constexpr float kLog2e = 1.4426950408889634f;
 
-// KS = 16-wide k steps of the fused dt projection (0: delta is an input).
-template <int KS, int TPC, int CH>
+// KS = 16-wide k steps of the fused dt projection (0: delta is an input);
+// TPC threads share a channel's states; each scan thread runs CPT adjacent
+// channels over the same states, so one read of B_t / C_t serves CPT channels.
+template <int KS, int TPC, int CH, int CPT>
 struct ScanCfg {
-  static constexpr int NWS = CH * TPC / 32;           // scan warps
+  static constexpr int NWS = CH * TPC / (32 * CPT);   // scan warps
   static constexpr int ND = CH >= 64 ? CH / 32 : 1;   // delta warps
   static constexpr int NW = NWS + ND + 1;             // + gate warp
   static constexpr int NT = NW * 32;
   static constexpr int W_DELTA = NWS;                 // first delta warp
   static constexpr int W_GATE = NWS + ND;
-  static constexpr int CHW = 32 / TPC;                // channels per scan warp
+  static constexpr int CHW = 32 * CPT / TPC;          // channels per scan warp
   static constexpr int NS = SC_N / TPC;               // states per scan thread
-  static constexpr int RPL = SC_T / TPC;              // rows of y each scan thread stores
+  static constexpr int RPL = SC_H / TPC;              // rows of y a scan thread stores per SC_H rows
   static constexpr int CHD = CH / ND;                 // channels per delta warp
   static constexpr int NTD = CHD / 8;                 // mma n-tiles per delta warp
   static constexpr int KP = KS * 16;                  // padded dt rank
@@ -69,14 +73,19 @@ struct ScanCfg {
   static constexpr int DU_STR = CH + 4;               // float2 per row of a (d, d*u) tile
   static constexpr int DU_BYTES = SC_T * DU_STR * 8;
   static constexpr int Y_BYTES = SC_T * CH * 4;       // C.h [SC_T][CH] fp32
-  static constexpr int W_BYTES = KS > 0 ? (CH / 8) * KS * 32 * 8 : 0;  // W_dt mma fragments
+  // W_dt mma fragments: in registers when three blocks of NT threads leave
+  // 128 registers a thread, otherwise in shared memory
+  static constexpr bool W_REG = NT <= 160;
+  static constexpr int W_BYTES = KS > 0 && !W_REG ? (CH / 8) * KS * 32 * 8 : 0;
   static constexpr int OFF_DU = SC_S * STAGE;
   static constexpr int OFF_Y = OFF_DU + 2 * DU_BYTES;
   static constexpr int OFF_W = OFF_Y + 2 * Y_BYTES;
   static constexpr int OFF_BAR = OFF_W + W_BYTES;
   static constexpr int N_BAR = SC_S + 8;
   static constexpr int SMEM = 128 + OFF_BAR + N_BAR * 8;
-  static_assert(NWS >= 1 && CHD % 8 == 0 && CH % 8 == 0 && SC_T % TPC == 0, "scan block shape");
+  static_assert(NWS >= 1 && CHD % 8 == 0 && CH % 8 == 0 && SC_H % TPC == 0 && SC_T % SC_H == 0 && (CPT == 1 || CPT == 2) &&
+                    CH % CHW == 0,
+                "scan block shape");
 };
 
 struct ScanArgs {
@@ -99,28 +108,33 @@ HY_DEV void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 
-// softplus(v) = ln(1 + e^v).  For e = e^v < 1/8 the alternating series of
-// ln(1 + e) to the e^6 term (truncation < e^7/7 < 7e-8 relative to the
-// result); above that ln2 * log2(1 + e), where 1 + e >= 1.125 keeps lg2's
-// relative error near 1e-6.  The second branch is taken by the whole warp or
-// skipped, so the common case costs one SFU operation.
+// softplus(v) = max(v, 0) + log1p(e) with e = e^-|v| in (0, 1], and
+// log1p(e) = e q(e), q a degree-7 polynomial fitted to log1p(e)/e on [0, 1]
+// (least squares on Chebyshev nodes, reweighted toward equal relative error):
+// relative error of e q(e) below 4e-7 in float32 arithmetic.  One SFU
+// operation and no branch.
 HY_DEV float softplus_scan(float v) {
-  if (v > 15.0f) return v;
-  const float e = ex2_approx(v * kLog2e);
-  float r = e * fmaf(e, fmaf(e, fmaf(e, fmaf(e, fmaf(e, -1.0f / 6, 0.2f), -0.25f), 1.0f / 3), -0.5f), 1.0f);
-  if (e >= 0.125f) r = lg2_approx(1.0f + e) * 0.6931471805599453f;
-  return r;
+  const float e = ex2_approx(-fabsf(v) * kLog2e);
+  float q = -0.008539227768778801f;
+  q = fmaf(q, e, 0.044089701026678085f);
+  q = fmaf(q, e, -0.10768181085586548f);
+  q = fmaf(q, e, 0.1774524748325348f);
+  q = fmaf(q, e, -0.2449546456336975f);
+  q = fmaf(q, e, 0.33275479078292847f);
+  q = fmaf(q, e, -0.4999740421772003f);
+  q = fmaf(q, e, 0.9999998211860657f);
+  return fmaxf(v, 0.f) + e * q;
 }
 
 // y * silu(z) = y * z / (1 + 2^(-z log2 e))
 HY_DEV float gate1(float y, float z) { return y * z * rcp_approx(1.0f + ex2_approx(-kLog2e * z)); }
 
-template <int KS, int TPC, int CH>
-__global__ void __launch_bounds__(ScanCfg<KS, TPC, CH>::NT, 3)
+template <int KS, int TPC, int CH, int CPT>
+__global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
     scan_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmU,
                 const __grid_constant__ CUtensorMap tmZ, const __grid_constant__ CUtensorMap tmBC,
                 const ScanArgs a) {
-  using Cfg = ScanCfg<KS, TPC, CH>;
+  using Cfg = ScanCfg<KS, TPC, CH, CPT>;
   constexpr int N = SC_N;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -164,16 +178,18 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH>::NT, 3)
     // ------------------------------------------------------------ scan warps
     constexpr int NS = Cfg::NS;
     const int sub = lane % TPC;
-    const int chl = warp * Cfg::CHW + lane / TPC;
+    const int chl = warp * Cfg::CHW + (lane / TPC) * CPT;  // first of this thread's CPT channels
     const int c = c0 + chl;
-    uint64_t A2[NS / 2], h2[NS / 2];
+    uint64_t A2[CPT][NS / 2], h2[CPT][NS / 2];
 #pragma unroll
-    for (int p = 0; p < NS / 2; ++p) {
-      const int s0 = c * N + sub * NS + 2 * p;
-      A2[p] = pk2(-__expf(a.A_log[s0]) * kLog2e, -__expf(a.A_log[s0 + 1]) * kLog2e);
-      const long long hb = static_cast<long long>(b) * a.h0_bs + static_cast<long long>(c) * N + sub * NS + 2 * p;
-      h2[p] = a.h0 ? pk2(a.h0[hb], a.h0[hb + 1]) : pk2(0.f, 0.f);
-    }
+    for (int j = 0; j < CPT; ++j)
+#pragma unroll
+      for (int p = 0; p < NS / 2; ++p) {
+        const int s0 = (c + j) * N + sub * NS + 2 * p;
+        A2[j][p] = pk2(-__expf(a.A_log[s0]) * kLog2e, -__expf(a.A_log[s0 + 1]) * kLog2e);
+        const long long hb = static_cast<long long>(b) * a.h0_bs + static_cast<long long>(c + j) * N + sub * NS + 2 * p;
+        h2[j][p] = a.h0 ? pk2(a.h0[hb], a.h0[hb + 1]) : pk2(0.f, 0.f);
+      }
     bool ok = true;
     for (int k = 0; k < n_chunks; ++k) {
       const int i = k & 1;
@@ -182,60 +198,95 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH>::NT, 3)
       const float2* du_p = du_tile(k) + chl;
       const float* sBC = reinterpret_cast<const float*>(stage(k) + Cfg::OFF_BC);
       float* y_p = y_tile(k) + chl;
-      // C.h stays in registers until the chunk is done: no store inside the
-      // loop, so the loads of later rows can be issued early
-      float yr[SC_T];
+      // C.h of SC_H rows stays in registers, then a transposing butterfly sums
+      // the TPC partials: no store inside the row loop, so the loads of later
+      // rows can be issued early
 #pragma unroll
-      for (int t = 0; t < SC_T; ++t) {
-        const float2 q = du_p[t * Cfg::DU_STR];
-        const uint64_t dt2 = pk2(q.x, q.x), du2 = pk2(q.y, q.y);
-        const float4* Bp = reinterpret_cast<const float4*>(sBC + t * 2 * N + sub * NS);
-        const float4* Cp = reinterpret_cast<const float4*>(sBC + t * 2 * N + N + sub * NS);
-        uint64_t y0 = pk2(0.f, 0.f), y1 = pk2(0.f, 0.f);
+      for (int hh = 0; hh < SC_T / SC_H; ++hh) {
+        float yr[CPT][SC_H];
 #pragma unroll
-        for (int qq = 0; qq < NS / 4; ++qq) {
-          const float4 bb = Bp[qq], cc = Cp[qq];
+        for (int tr = 0; tr < SC_H; ++tr) {
+          const int t = hh * SC_H + tr;
+          // (delta, delta*u) of the thread's channels: one 8- or 16-byte load
+          float dl[CPT], dul[CPT];
+          if constexpr (CPT == 2) {
+            const float4 q = *reinterpret_cast<const float4*>(du_p + t * Cfg::DU_STR);
+            dl[0] = q.x;
+            dul[0] = q.y;
+            dl[1] = q.z;
+            dul[1] = q.w;
+          } else {
+            const float2 q = du_p[t * Cfg::DU_STR];
+            dl[0] = q.x;
+            dul[0] = q.y;
+          }
+          const float4* Bp = reinterpret_cast<const float4*>(sBC + t * 2 * N + sub * NS);
+          const float4* Cp = reinterpret_cast<const float4*>(sBC + t * 2 * N + N + sub * NS);
+          uint64_t y0[CPT], y1[CPT];
 #pragma unroll
-          for (int p2 = 0; p2 < 2; ++p2) {
-            const int p = qq * 2 + p2;
-            const float2 ea = up2(mul2(dt2, A2[p]));
-            const uint64_t av = pk2(ex2_approx(ea.x), ex2_approx(ea.y));
-            const uint64_t bu = mul2(du2, p2 == 0 ? pk2(bb.x, bb.y) : pk2(bb.z, bb.w));
-            h2[p] = fma2(av, h2[p], bu);
-            if (p2 == 0)
-              y0 = fma2(pk2(cc.x, cc.y), h2[p], y0);
-            else
-              y1 = fma2(pk2(cc.z, cc.w), h2[p], y1);
+          for (int j = 0; j < CPT; ++j) y0[j] = y1[j] = pk2(0.f, 0.f);
+#pragma unroll
+          for (int qq = 0; qq < NS / 4; ++qq) {
+            const float4 bb = Bp[qq], cc = Cp[qq];
+#pragma unroll
+            for (int p2 = 0; p2 < 2; ++p2) {
+              const int p = qq * 2 + p2;
+              const uint64_t bp = p2 == 0 ? pk2(bb.x, bb.y) : pk2(bb.z, bb.w);
+              const uint64_t cp = p2 == 0 ? pk2(cc.x, cc.y) : pk2(cc.z, cc.w);
+#pragma unroll
+              for (int j = 0; j < CPT; ++j) {
+                const float2 ea = up2(mul2(pk2(dl[j], dl[j]), A2[j][p]));
+                const uint64_t av = pk2(ex2_approx(ea.x), ex2_approx(ea.y));
+                h2[j][p] = fma2(av, h2[j][p], mul2(pk2(dul[j], dul[j]), bp));
+                if (p2 == 0)
+                  y0[j] = fma2(cp, h2[j][p], y0[j]);
+                else
+                  y1[j] = fma2(cp, h2[j][p], y1[j]);
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < CPT; ++j) {
+            const float2 ys = up2(add2(y0[j], y1[j]));
+            yr[j][tr] = ys.x + ys.y;
           }
         }
-        const float2 ys = up2(add2(y0, y1));
-        yr[t] = ys.x + ys.y;
-      }
-      // sum the TPC partials of each row: a transposing butterfly leaves
-      // lane `sub` with the totals of rows sub*RPL .. sub*RPL + RPL - 1
+        // lane `sub` ends with the totals of rows sub*RPL .. sub*RPL + RPL - 1
+        // of these SC_H rows
 #pragma unroll
-      for (int o = TPC / 2, m = SC_T; o >= 1; o >>= 1, m >>= 1) {
-        const bool upper = (sub & o) != 0;
+        for (int o = TPC / 2, m = SC_H; o >= 1; o >>= 1, m >>= 1) {
+          const bool upper = (sub & o) != 0;
 #pragma unroll
-        for (int j = 0; j < m / 2; ++j) {
-          const float keep = upper ? yr[m / 2 + j] : yr[j];
-          const float send = upper ? yr[j] : yr[m / 2 + j];
-          yr[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          for (int j = 0; j < CPT; ++j)
+#pragma unroll
+            for (int r = 0; r < m / 2; ++r) {
+              const float keep = upper ? yr[j][m / 2 + r] : yr[j][r];
+              const float send = upper ? yr[j][r] : yr[j][m / 2 + r];
+              yr[j][r] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < Cfg::RPL; ++r) {
+          const int row = hh * SC_H + sub * Cfg::RPL + r;
+          if constexpr (CPT == 2)
+            *reinterpret_cast<float2*>(y_p + row * CH) = make_float2(yr[0][r], yr[1][r]);
+          else
+            y_p[row * CH] = yr[0][r];
         }
       }
-#pragma unroll
-      for (int j = 0; j < Cfg::RPL; ++j) y_p[(sub * Cfg::RPL + j) * CH] = yr[j];
       mbar_arrive(du_empty(i));
       mbar_arrive(y_full(i));
     }
     if (ok && a.h_out) {
 #pragma unroll
-      for (int p = 0; p < NS / 2; ++p) {
-        const float2 hv = up2(h2[p]);
-        const long long hb = (static_cast<long long>(b) * di + c) * N + sub * NS + 2 * p;
-        a.h_out[hb] = hv.x;
-        a.h_out[hb + 1] = hv.y;
-      }
+      for (int j = 0; j < CPT; ++j)
+#pragma unroll
+        for (int p = 0; p < NS / 2; ++p) {
+          const float2 hv = up2(h2[j][p]);
+          const long long hb = (static_cast<long long>(b) * di + c + j) * N + sub * NS + 2 * p;
+          a.h_out[hb] = hv.x;
+          a.h_out[hb + 1] = hv.y;
+        }
     }
   } else if (warp < Cfg::W_GATE) {
     // ------------------------------------------------------------ delta warps
@@ -243,14 +294,17 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH>::NT, 3)
     const int grp = lane >> 2, tig = lane & 3;
     const int dc0 = dw * Cfg::CHD;  // first channel of this warp within the block
     constexpr int NTD = Cfg::NTD;
-    // W_dt as mma B fragments, [n-tile][k-step][lane] x 2 registers, in shared memory
-    uint2* sW = reinterpret_cast<uint2*>(smem + Cfg::OFF_W);
+    // W_dt as mma B fragments for the whole sequence: wreg[n-tile][k-step],
+    // or [n-tile][k-step][lane] in shared memory
+    constexpr bool WR = Cfg::W_REG;
+    uint2 wreg[WR ? NTD : 1][WR && KS > 0 ? KS : 1];
+    uint2* sW = reinterpret_cast<uint2*>(smem + Cfg::OFF_W) + dw * NTD * KS * 32 + lane;
     float bias_c[NTD][2];
     if constexpr (KS > 0) {
 #pragma unroll
       for (int nt = 0; nt < NTD; ++nt) {
-        const int ntg = dw * NTD + nt;
-        const int ch = c0 + ntg * 8 + grp;
+        const int ch = c0 + dc0 + nt * 8 + grp;
+#pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           uint32_t f[2];
 #pragma unroll
@@ -261,7 +315,10 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH>::NT, 3)
                 r0 + 1 < a.R ? __bfloat162float(a.W_dt[static_cast<long long>(ch) * a.R + r0 + 1]) : 0.f;
             f[hh] = pack_half2(v0, v1);
           }
-          sW[(ntg * KS + kk) * 32 + lane] = make_uint2(f[0], f[1]);
+          if constexpr (WR)
+            wreg[nt][kk] = make_uint2(f[0], f[1]);
+          else
+            sW[(nt * KS + kk) * 32] = make_uint2(f[0], f[1]);
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) bias_c[nt][e] = a.dt_bias[c0 + dc0 + nt * 8 + tig * 2 + e];
@@ -283,14 +340,13 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH>::NT, 3)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
         const uint32_t abase = smem_u32(st) + ((lane & 15) * Cfg::KP + (lane >> 4) * 8) * 2;
-        const uint2* wf = sW + dw * NTD * KS * 32 + lane;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           uint32_t af[4];
           ldsm_x4(abase + kk * 32, af);
 #pragma unroll
           for (int nt = 0; nt < NTD; ++nt) {
-            const uint2 bw = wf[(nt * KS + kk) * 32];
+            const uint2 bw = WR ? wreg[WR ? nt : 0][WR ? kk : 0] : sW[(nt * KS + kk) * 32];
             mma_16816_f16(acc[nt], af, bw.x, bw.y);
           }
         }
@@ -407,17 +463,17 @@ bool map2(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, l
   return encode_tmap(m, dt, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int KS, int TPC, int CH>
+template <int KS, int TPC, int CH, int CPT>
 hymba_status launch_scan(int B, int L, int di, const CUtensorMap& mX, const __half* u, long long ld_u,
                          const __half* z, long long ld_z, const float* BC, const ScanArgs& args, cudaStream_t st) {
-  using Cfg = ScanCfg<KS, TPC, CH>;
+  using Cfg = ScanCfg<KS, TPC, CH, CPT>;
   const long long rows = static_cast<long long>(B) * L;
   CUtensorMap mU, mZ, mBC;
   if (!map2(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, u, di, rows, ld_u, CH, SC_T) ||
       !map2(&mZ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, z, di, rows, ld_z, CH, SC_T) ||
       !map2(&mBC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BC, 2 * SC_N, rows, 2 * SC_N, 2 * SC_N, SC_T))
     return HYMBA_ERR_CUDA;
-  auto kern = scan_kernel<KS, TPC, CH>;
+  auto kern = scan_kernel<KS, TPC, CH, CPT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
   dim3 grid(di / CH, B);
@@ -425,60 +481,73 @@ hymba_status launch_scan(int B, int L, int di, const CUtensorMap& mX, const __ha
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 
-// Threads per channel, from the channels each SM gets: the recurrence of one
-// thread is a long chain of dependent steps, so with few channels per SM the
-// states are split over more threads (measured on B300: 16 states per thread
-// from ~300 channels per SM, 8 from ~80, 4 below).
-int pick_tpc(int B, int di, int num_sms) {
+// Threads per channel and channels per thread, from the channels each SM
+// gets.  Each thread walks its chains (states x channels) through the whole
+// sequence; fewer chains per thread mean more warps to hide the latency of
+// each step, while two channels per thread halve the shared-memory reads of
+// B_t / C_t.  Measured on B300 at d_inner 3200, L 8320 (scan alone):
+//   ~43 channels/SM:  (4,1) 0.57 ms, (4,2) 0.69, (2,1) 0.70, (2,2) 0.91
+//   ~86 channels/SM:  (4,2) 1.03 ms, (2,1) 1.12, (4,1) 1.13, (2,2) 1.31
+//   ~173 channels/SM: (2,2) 1.45 ms, (4,2) 1.49, (1,1) 1.51, (2,1) 1.64
+struct ScanLayout {
+  int tpc, cpt;
+};
+
+ScanLayout pick_layout(int B, int di, int num_sms) {
   const long long per_sm = static_cast<long long>(B) * di / num_sms;
-  if (per_sm >= 300) return 1;
-  if (per_sm >= 80) return 2;
-  return 4;
+  if (per_sm >= 128) return {2, 2};
+  if (per_sm >= 64) return {4, 2};
+  return {4, 1};
 }
 
 // Channels per block: 64 (one wave of 2-3 blocks per SM at the 1.5B
 // shapes), 16 at four threads per channel so that a small batch still
 // spreads over the SMs.
-int block_channels(int tpc) { return tpc == 4 ? 16 : 64; }
+int block_channels(ScanLayout lo) { return lo.tpc == 4 && lo.cpt == 1 ? 16 : 64; }
 
 template <int KS>
-hymba_status launch_tpc(int tpc, int B, int L, int di, const CUtensorMap& mX, const __half* u, long long ld_u,
-                        const __half* z, long long ld_z, const float* BC, const ScanArgs& args, cudaStream_t st) {
-  switch (tpc) {
-    case 1: return launch_scan<KS, 1, 64>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 2: return launch_scan<KS, 2, 64>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 4: return launch_scan<KS, 4, 16>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    default: return HYMBA_ERR_UNSUPPORTED;
-  }
+hymba_status launch_layout(ScanLayout lo, int B, int L, int di, const CUtensorMap& mX, const __half* u,
+                           long long ld_u, const __half* z, long long ld_z, const float* BC, const ScanArgs& args,
+                           cudaStream_t st) {
+  if (lo.tpc == 1 && lo.cpt == 1) return launch_scan<KS, 1, 64, 1>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+  if (lo.tpc == 2 && lo.cpt == 1) return launch_scan<KS, 2, 64, 1>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+  if (lo.tpc == 2 && lo.cpt == 2) return launch_scan<KS, 2, 64, 2>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+  if (lo.tpc == 4 && lo.cpt == 1) return launch_scan<KS, 4, 16, 1>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+  if (lo.tpc == 4 && lo.cpt == 2) return launch_scan<KS, 4, 64, 2>(B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+  return HYMBA_ERR_UNSUPPORTED;
 }
 
-hymba_status launch_fused(int KS, int tpc, int B, int L, int di, const CUtensorMap& mX, const __half* u,
+hymba_status launch_fused(int KS, ScanLayout lo, int B, int L, int di, const CUtensorMap& mX, const __half* u,
                           long long ld_u, const __half* z, long long ld_z, const float* BC, const ScanArgs& args,
                           cudaStream_t st) {
   switch (KS) {
-    case 1: return launch_tpc<1>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 2: return launch_tpc<2>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 3: return launch_tpc<3>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 4: return launch_tpc<4>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 5: return launch_tpc<5>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 6: return launch_tpc<6>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 7: return launch_tpc<7>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
-    case 8: return launch_tpc<8>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 1: return launch_layout<1>(lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 2: return launch_layout<2>(lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 3: return launch_layout<3>(lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 4: return launch_layout<4>(lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 5: return launch_layout<5>(lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 6: return launch_layout<6>(lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 7: return launch_layout<7>(lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    case 8: return launch_layout<8>(lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
     default: return HYMBA_ERR_UNSUPPORTED;
   }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-int resolve_tpc(int tpc, int B, int di) {
+// tpc == 0: both chosen here; otherwise cpt 0 means one channel per thread.
+// {-1, -1} for a combination that has no kernel.
+ScanLayout resolve_layout(int tpc, int cpt, int B, int di) {
+  ScanLayout lo{tpc, cpt == 0 ? 1 : cpt};
   if (tpc == 0) {
     int dev = 0, n = kNumSMsHint;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    tpc = pick_tpc(B, di, n > 0 ? n : kNumSMsHint);
+    lo = pick_layout(B, di, n > 0 ? n : kNumSMsHint);
   }
-  if (tpc != 1 && tpc != 2 && tpc != 4) return -1;
-  if (di % block_channels(tpc) != 0) tpc = 4;  // 16-channel blocks fit any di % 16 == 0
-  return tpc;
+  const bool known = lo.tpc == 1 ? lo.cpt == 1 : (lo.tpc == 2 || lo.tpc == 4) && (lo.cpt == 1 || lo.cpt == 2);
+  if (!known) return {-1, -1};
+  if (di % block_channels(lo) != 0) lo = {4, 1};  // 16-channel blocks fit any di % 16 == 0
+  return lo;
 }
 
 }  // namespace
@@ -488,18 +557,18 @@ bool scan_fused_supported(int di, int N, int R) { return di % 16 == 0 && N == SC
 hymba_status scan_f16(int B, int L, int di, int N, const __half* u, long long ld_u, const __half* z,
                       long long ld_z, const float* delta, const float* BC, const float* A_log, const float* D,
                       __half* g, const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, int tpc,
-                      cudaStream_t st) {
+                      int cpt, cudaStream_t st) {
   const bool tma_ok = di % 16 == 0 && ld_u % 8 == 0 && ld_z % 8 == 0 && aligned16(u) && aligned16(z) &&
                       aligned16(delta) && aligned16(BC) && aligned16(g);
   if (tma_ok && N == SC_N) {
-    tpc = resolve_tpc(tpc, B, di);
-    if (tpc < 0) return HYMBA_ERR_INVALID;
+    const ScanLayout lo = resolve_layout(tpc, cpt, B, di);
+    if (lo.tpc < 0) return HYMBA_ERR_INVALID;
     CUtensorMap mX;
     if (!map2(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, di, static_cast<long long>(B) * L, di,
-              block_channels(tpc), SC_T))
+              block_channels(lo), SC_T))
       return HYMBA_ERR_CUDA;
     ScanArgs args{L, di, 0, nullptr, nullptr, A_log, D, g, h0, static_cast<long long>(di) * N, h_out, status, wait_ns};
-    return launch_tpc<0>(tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+    return launch_layout<0>(lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
   }
   return scan_simt<__half>(B, L, di, N, u, ld_u, z, ld_z, delta, di, BC, BC + N, 2 * N, A_log, D, g, di, h0, h_out,
                            st);
@@ -509,20 +578,20 @@ hymba_status scan_fused_f16(int B, int L, int di, int N, int R, const __half* u,
                             long long ld_z, const __half* dtr, long long ld_dtr, const __nv_bfloat16* W_dt,
                             const float* dt_bias, const float* BC, const float* A_log, const float* D, __half* g,
                             const float* h0, float* h_out, int32_t* status, uint64_t wait_ns, int tpc,
-                            cudaStream_t st, bool h0_shared) {
+                            int cpt, cudaStream_t st, bool h0_shared) {
   if (!scan_fused_supported(di, N, R)) return HYMBA_ERR_UNSUPPORTED;
   if (ld_u % 8 || ld_z % 8 || ld_dtr % 8 || !aligned16(u) || !aligned16(z) || !aligned16(dtr) || !aligned16(BC) ||
       !aligned16(g))
     return HYMBA_ERR_INVALID;
-  tpc = resolve_tpc(tpc, B, di);
-  if (tpc < 0) return HYMBA_ERR_INVALID;
+  const ScanLayout lo = resolve_layout(tpc, cpt, B, di);
+  if (lo.tpc < 0) return HYMBA_ERR_INVALID;
   const int KS = (R + 15) / 16;
   CUtensorMap mX;
   if (!map2(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, dtr, R, static_cast<long long>(B) * L, ld_dtr, KS * 16, SC_T))
     return HYMBA_ERR_CUDA;
   ScanArgs args{L, di, R, W_dt, dt_bias, A_log, D, g, h0, h0_shared ? 0LL : static_cast<long long>(di) * N, h_out,
                 status, wait_ns};
-  return launch_fused(KS, tpc, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
+  return launch_fused(KS, lo, B, L, di, mX, u, ld_u, z, ld_z, BC, args, st);
 }
 
 hymba_status wait_timeout_probe(uint32_t limit_us, int32_t* status, cudaStream_t st) {

@@ -348,12 +348,16 @@ HYMBA_API hymba_status hymba_test_conv(int32_t B, int32_t L, int32_t di, int32_t
  * delta: fp32 [B, L, di]; BC: fp32 [B, L, 2N] ([B | C]); A_log [di, N], D [di]
  * fp32.  g: fp16 [B, L, di] = (C.h + D u) silu(z); h_out [B, di, N] fp32
  * final state (may be NULL).  threads_per_channel: how many threads share
- * one channel's states (1, 2 or 4; 0 = the choice hymba_layer_fwd makes).   */
+ * one channel's states (1, 2 or 4); channels_per_thread: how many adjacent
+ * channels one thread runs over those states (0 or 1, or 2 with two or four
+ * threads per channel); both 0 = the choice hymba_layer_fwd makes.  Other
+ * combinations: HYMBA_ERR_INVALID.                                         */
 HYMBA_API hymba_status hymba_test_scan(int32_t B, int32_t L, int32_t di, int32_t N,
                              const void* u, int32_t ld_u, const void* z, int32_t ld_z,
                              const float* delta, const float* BC, const float* A_log,
                              const float* D, void* g, float* h_out,
-                             int32_t threads_per_channel, void* stream);
+                             int32_t threads_per_channel, int32_t channels_per_thread,
+                             void* stream);
 
 /* The same scan with the dt projection fused in, as hymba_layer_fwd runs it:
  * delta = softplus(dtr . W_dt^T + dt_bias) is computed inside the kernel.
@@ -365,7 +369,8 @@ HYMBA_API hymba_status hymba_test_scan_fused(int32_t B, int32_t L, int32_t di, i
                                              const void* dtr, int32_t ld_dtr, const void* W_dt,
                                              const float* dt_bias, const float* BC, const float* A_log,
                                              const float* D, void* g, float* h_out,
-                                             int32_t threads_per_channel, void* stream);
+                                             int32_t threads_per_channel, int32_t channels_per_thread,
+                                             void* stream);
 
 /* The bf16-path attention kernel alone (section 2.2 window + section 2.3 meta
  * prefix): Q [B, L, Hq, dh], K [B, L, Hkv, dh], V [B, L, Hkv, dv] fp16 ->

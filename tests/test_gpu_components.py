@@ -60,7 +60,7 @@ def _scan_inputs(B, L, di, N, seed, u0=None, d0=None, b0=None, c0=None):
         A_log.astype(np.float32).astype(F), D.astype(np.float32).astype(F)
 
 
-def _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc=0):
+def _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc=0, cpt=0):
     B, L, di = u.shape
     N = Bm.shape[-1]
     dev = "cuda"
@@ -72,21 +72,22 @@ def _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc=0):
     tD = torch.from_numpy(D).to(dev, torch.float32)
     g = torch.empty(B, L, di, device=dev, dtype=torch.float16)
     h = torch.empty(B, di, N, device=dev, dtype=torch.float32)
-    assert hb.hymba_test_scan(tu, tz, td, bc, ta, tD, g, h, threads_per_channel=tpc) == 0
+    assert hb.hymba_test_scan(tu, tz, td, bc, ta, tD, g, h, threads_per_channel=tpc, channels_per_thread=cpt) == 0
     torch.cuda.synchronize()
     return g.float().cpu().numpy().astype(F), h.cpu().numpy().astype(F)
 
 
-@pytest.mark.parametrize("tpc", [1, 2, 4])
-def test_scan_closed_form_on_gpu(tpc):
+@pytest.mark.parametrize("tpc,cpt", [(1, 1), (2, 1), (2, 2), (4, 1), (4, 2)])
+def test_scan_closed_form_on_gpu(tpc, cpt):
     """Constant u, Delta, B, C with D = 0: the state follows the geometric
     series exactly, so C.h dominates the output (the case the end-to-end
     tolerance cannot see).  Every split of the 16 states over 1, 2 or 4
-    threads per channel."""
+    threads per channel, and two channels per thread at two or four threads
+    per channel."""
     B, L, di, N = 2, 700, 64, 16
     u, z, dl, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 1, u0=0.75, d0=0.05, b0=1.25, c0=-0.5)
     D[:] = 0
-    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc)
+    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc, cpt)
     A = -np.exp(A_log)
     a = np.exp(0.05 * A)                                              # [di, N]
     t = np.arange(L)[:, None, None]
@@ -105,11 +106,12 @@ def test_scan_special_cases_on_gpu():
     assert np.all(h == 0)
 
 
-@pytest.mark.parametrize("tpc,L", [(1, 517), (2, 517), (4, 517), (2, 3), (4, 18)])
-def test_scan_random_matches_oracle(tpc, L):
+@pytest.mark.parametrize("tpc,cpt,L", [(1, 1, 517), (2, 1, 517), (2, 2, 517), (4, 1, 517), (4, 2, 517), (2, 1, 3),
+                                       (2, 2, 3), (4, 1, 18), (4, 2, 18)])
+def test_scan_random_matches_oracle(tpc, cpt, L):
     B, di, N = 3, 192, 16
     u, z, dl, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 3)
-    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc)
+    g, h = _run_scan(u, z, dl, Bm, Cm, A_log, D, tpc, cpt)
     y, hr = ref.selective_scan(u, dl, -np.exp(A_log), Bm, Cm, D)
     gr = y * ref.silu(z)
     np.testing.assert_allclose(h, hr, rtol=1e-4, atol=1e-5 * np.abs(hr).max())
@@ -189,7 +191,7 @@ def test_bounded_wait_reports_timeout():
     assert float((x * 2).sum().item()) == 8.0
 
 
-def _run_scan_fused(u, z, dtr, W_dt, dt_bias, Bm, Cm, A_log, D, tpc=0):
+def _run_scan_fused(u, z, dtr, W_dt, dt_bias, Bm, Cm, A_log, D, tpc=0, cpt=0):
     B, L, di = u.shape
     N = Bm.shape[-1]
     R = W_dt.shape[1]
@@ -206,7 +208,8 @@ def _run_scan_fused(u, z, dtr, W_dt, dt_bias, Bm, Cm, A_log, D, tpc=0):
     tD = torch.from_numpy(D).to(dev, torch.float32)
     g = torch.empty(B, L, di, device=dev, dtype=torch.float16)
     h = torch.empty(B, di, N, device=dev, dtype=torch.float32)
-    assert hb.hymba_test_scan_fused(tu, tz, tdt, tw, tb, bc, ta, tD, g, h, threads_per_channel=tpc) == 0
+    assert hb.hymba_test_scan_fused(tu, tz, tdt, tw, tb, bc, ta, tD, g, h, threads_per_channel=tpc,
+                                    channels_per_thread=cpt) == 0
     torch.cuda.synchronize()
     return g.float().cpu().numpy().astype(F), h.cpu().numpy().astype(F)
 
@@ -233,10 +236,12 @@ def test_fused_scan_closed_form_on_gpu():
     np.testing.assert_allclose(g, expect_g, rtol=3e-3, atol=1e-3 * np.abs(expect_g).max())
 
 
-@pytest.mark.parametrize("R,di,L,tpc", [(100, 192, 517, 0), (100, 192, 517, 1), (100, 192, 517, 2),
-                                        (100, 192, 517, 4), (64, 128, 130, 2), (8, 64, 33, 1), (128, 48, 70, 4),
-                                        (17, 64, 1, 2)])
-def test_fused_scan_random_matches_oracle(R, di, L, tpc):
+@pytest.mark.parametrize("R,di,L,tpc,cpt", [(100, 192, 517, 0, 0), (100, 192, 517, 1, 1), (100, 192, 517, 2, 1),
+                                            (100, 192, 517, 2, 2), (100, 192, 517, 4, 1), (64, 128, 130, 2, 1),
+                                            (64, 128, 130, 2, 2), (8, 64, 33, 1, 1), (128, 48, 70, 4, 1),
+                                            (17, 64, 1, 2, 1), (17, 64, 1, 2, 2), (100, 192, 517, 4, 2),
+                                            (64, 128, 130, 4, 2)])
+def test_fused_scan_random_matches_oracle(R, di, L, tpc, cpt):
     B, N = 2, 16
     u, z, _, Bm, Cm, A_log, D = _scan_inputs(B, L, di, N, 8)
     rng = np.random.default_rng(9)
@@ -244,7 +249,7 @@ def test_fused_scan_random_matches_oracle(R, di, L, tpc):
     W_dt = synth_bf16(rng.standard_normal((di, R)) * 0.1)
     dt0 = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), di))
     bias = (dt0 + np.log(-np.expm1(-dt0))).astype(np.float32).astype(F)
-    g, h = _run_scan_fused(u, z, dtr, W_dt, bias, Bm, Cm, A_log, D, tpc)
+    g, h = _run_scan_fused(u, z, dtr, W_dt, bias, Bm, Cm, A_log, D, tpc, cpt)
     dl = ref.softplus(dtr @ W_dt.T + bias)
     y, hr = ref.selective_scan(u, dl, -np.exp(A_log), Bm, Cm, D)
     gr = y * ref.silu(z)
