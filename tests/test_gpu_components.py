@@ -15,7 +15,10 @@ F = np.float64
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 200, 100), (1000, 1600, 3200), (37, 8960, 1600),
-                                   (4500, 144, 96), (128, 64, 8)])
+                                   (4500, 144, 96), (128, 64, 8),
+                                   # 8+ row blocks run as 2-CTA cluster pairs; 9 and 17 blocks leave a
+                                   # padding tile in the last pair
+                                   (1115, 520, 200), (2100, 300, 64), (1921, 176, 72)])
 @pytest.mark.parametrize("ab", [1, 2, 3])
 def test_gemm_tc_matches_fp64(M, N, K, ab):
     """ab 1: bf16 x bf16; 2: fp16 x fp16; 3: fp16 A against a bf16 B that the

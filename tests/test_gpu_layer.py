@@ -64,6 +64,8 @@ BF16_CASES = [
     dict(B=1, T=300, M=128, d=1600, Hq=25, Hkv=5, di=3200, window=256),   # 1.5B widths
     dict(B=3, T=1, M=0, window=1),
     dict(residual=True),
+    dict(B=3, T=333),                     # 1047 rows: the projections run as cluster pairs, 9 row blocks
+    dict(B=5, T=240, residual=True),      # 1280 rows, 10 row blocks
 ]
 
 
