@@ -191,6 +191,26 @@ def draw_layer_params(rng: np.random.Generator, s: LayerShape) -> Dict[str, np.n
     return p
 
 
+def draw_block_params(rng: np.random.Generator, s: LayerShape, F: int) -> Dict[str, np.ndarray]:
+    """One residual block: the hybrid-head layer's parameters, then norm1,
+    norm2 [d] (1 + N(0, 0.1^2)), W_gate, W_up [F, d] ~ N(0, 1/d) and W_down
+    [d, F] ~ N(0, 1/F), matrices rounded to the storage dtype."""
+    p = draw_layer_params(rng, s)
+    p["norm1"] = (1.0 + _normal(rng, (s.d,), 0.1)).astype(np.float32)
+    p["norm2"] = (1.0 + _normal(rng, (s.d,), 0.1)).astype(np.float32)
+    p["W_gate"] = store_round(_normal(rng, (F, s.d), 1.0 / math.sqrt(s.d)), s.dtype)
+    p["W_up"] = store_round(_normal(rng, (F, s.d), 1.0 / math.sqrt(s.d)), s.dtype)
+    p["W_down"] = store_round(_normal(rng, (s.d, F), 1.0 / math.sqrt(F)), s.dtype)
+    return p
+
+
+def make_block_inputs(s: LayerShape, F: int, seed: int, n_blocks: int = 1):
+    """The stream X~ [B, L, d] and n_blocks blocks' parameters."""
+    rng = np.random.default_rng(seed)
+    tok = draw_tokens(rng, s)
+    return tok, [draw_block_params(rng, s, F) for _ in range(n_blocks)]
+
+
 def draw_tokens(rng: np.random.Generator, s: LayerShape) -> Dict[str, np.ndarray]:
     """X [B,T,d] and meta [M,d] (storage-rounded), plus X~ = [meta; X] [B,L,d]."""
     X = store_round(_normal(rng, (s.B, s.T, s.d)), s.dtype)
