@@ -278,6 +278,7 @@ def run_ours(args, rank, world, local_rank):
         return out
     out["e2e"] = run_e2e(args, torch, hb, hl, dev, stream)
     out["meta_prefix"] = run_meta_prefix(args, torch, hb, hl, dev, stream)
+    out["block"] = run_block(args, torch, hb, hl, dev, stream)
     out["decode"] = run_decode(args, torch, hb, hl, dev, stream, peaks, peak_src)
     out["global_prefill"] = run_prefill_extra(args, torch, hb, hl, dev, stream, synth.hymba15b_global(rope_theta=10000.0),
                                               "Hymba-1.5B-shaped global-attention layer, batch 2 x (8192 + 128)")
@@ -402,6 +403,40 @@ def run_meta_prefix(args, torch, hb, hl, dev, stream):
            "value": round(s.B * s.T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
            "status": layer.check_status()}
     del layer, X, Y, xm, meta, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_block(args, torch, hb, hl, dev, stream):
+    """The full residual block around the main workload's layer (RMSNorm ->
+    layer -> add, RMSNorm -> GeLU-gated MLP with F = 3 d -> add), applied in
+    place to the fp32 stream each step."""
+    s = synth.hymba15b_swa(rope_theta=10000.0, B=args.batch)
+    d_ff = 3 * s.d
+    tok, blocks = synth.make_block_inputs(s, d_ff, 4)
+    blk = hl.HymbaBlock(s, hl.block_params_to_device(blocks[0], s, dev), d_ff)
+    x = torch.from_numpy(tok["Xt"]).to(dev)
+    del tok, blocks
+    for _ in range(args.warmup):
+        blk.forward(x)
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 10))
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(n):
+        blk.forward(x)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    fl = layer_flops(s)
+    rows = s.B * s.L
+    tot = fl["in_proj"] + fl["attention"] + fl["x_proj"] + fl["dt_proj"] + fl["out_proj"] + 6.0 * rows * s.d * d_ff
+    out = {"workload": f"residual block around the main workload's layer, gated MLP F = {d_ff}, batch {s.B} x "
+                       f"({s.T} + {s.M})",
+           "value": round(s.B * s.T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+           "tflops": round(tot / (ms / 1e3) / 1e12, 1), "status": blk.check_status()}
+    del blk, x
     torch.cuda.empty_cache()
     return out
 

@@ -50,6 +50,11 @@ class Cache(ctypes.Structure):
                 ("reserved", c_int32)]
 
 
+class BlockWeights(ctypes.Structure):
+    _fields_ = [("mix", LayerWeights), ("norm1", c_void_p), ("norm2", c_void_p), ("W_gu", c_void_p),
+                ("W_down", c_void_p)]
+
+
 class Meta(ctypes.Structure):
     _fields_ = [("k", c_void_p), ("v", c_void_p), ("ssm_state", c_void_p), ("conv_tail", c_void_p),
                 ("y", c_void_p)]
@@ -102,6 +107,11 @@ def lib() -> ctypes.CDLL:
     L.hymba_layer_fwd_meta.argtypes = [P(LayerDesc), P(LayerWeights), P(Meta), c_void_p, c_void_p, P(Cache), P(KV),
                                        P(KV), c_void_p, c_size_t, c_void_p, c_void_p]
     L.hymba_layer_fwd_meta.restype = c_int32
+    L.hymba_block_fwd_workspace.argtypes = [P(LayerDesc), c_int32]
+    L.hymba_block_fwd_workspace.restype = c_size_t
+    L.hymba_block_fwd.argtypes = [P(LayerDesc), P(BlockWeights), c_int32, c_void_p, c_void_p, c_size_t, c_void_p,
+                                  c_void_p]
+    L.hymba_block_fwd.restype = c_int32
     L.hymba_test_gemm.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
                                   c_void_p, c_int32, c_void_p, c_void_p]
     L.hymba_test_gemm.restype = c_int32
@@ -206,6 +216,23 @@ def hymba_layer_fwd_events(desc: LayerDesc, weights: LayerWeights, x, y, ws, eve
                                       _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), events, n_events,
                                       _stream(stream))
     return _check(rc, "hymba_layer_fwd_events") if check else rc
+
+
+def make_block_weights(w: Dict[str, "object"]) -> BlockWeights:
+    return BlockWeights(mix=make_weights(w), norm1=_ptr(w["norm1"]), norm2=_ptr(w["norm2"]), W_gu=_ptr(w["W_gu"]),
+                        W_down=_ptr(w["W_down"]))
+
+
+def block_fwd_workspace(desc: LayerDesc, d_ff: int) -> int:
+    return lib().hymba_block_fwd_workspace(ctypes.byref(desc), d_ff)
+
+
+def hymba_block_fwd(desc: LayerDesc, weights: BlockWeights, d_ff: int, x, ws, status=None, stream=None,
+                    check: bool = True) -> int:
+    """One residual block on the fp32 stream x, in place (see include/hymba.h)."""
+    rc = lib().hymba_block_fwd(ctypes.byref(desc), ctypes.byref(weights), d_ff, _ptr(x), _ptr(ws),
+                               ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+    return _check(rc, "hymba_block_fwd") if check else rc
 
 
 def make_meta(m: Dict[str, "object"]) -> Meta:

@@ -375,6 +375,27 @@ __global__ void __launch_bounds__(192, 1)
                 if (j < valid) v[j] += rr[j];
             }
             store_f32x32(reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col, v, valid);
+          } else if (EPI == EPI_GEGLU) {
+            // exact GeLU, x Phi(x) with Phi from erff; 16 outputs per 32 columns
+            float o[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float gt = v[2 * e], up = v[2 * e + 1];
+              o[e] = 0.5f * gt * (1.0f + erff(gt * 0.7071067811865476f)) * up;
+              over |= !(fabsf(o[e]) <= kHalfMax);
+            }
+            __half* dst = reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col / 2;
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {
+              if (gg * 8 < valid / 2) {
+                uint4 q;
+                q.x = pack_half2(o[gg * 8 + 0], o[gg * 8 + 1]);
+                q.y = pack_half2(o[gg * 8 + 2], o[gg * 8 + 3]);
+                q.z = pack_half2(o[gg * 8 + 4], o[gg * 8 + 5]);
+                q.w = pack_half2(o[gg * 8 + 6], o[gg * 8 + 7]);
+                *reinterpret_cast<uint4*>(dst + gg * 8) = q;
+              }
+            }
           } else if (EPI == EPI_ATOMIC) {
             float* dst = reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col;
             if (valid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
@@ -516,6 +537,7 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
   p.total_tiles = p.tiles_m * p.tiles_n * p.splits;
   p.total_pairs = (p.tiles_m + 1) / 2 * p.tiles_n;
   if (p.splits > 1 && epi != EPI_PARTIAL && epi != EPI_ATOMIC) return HYMBA_ERR_INVALID;
+  if (epi == EPI_GEGLU && (p.N % 16 || p.ldc % 8 || (reinterpret_cast<uintptr_t>(p.C) & 15))) return HYMBA_ERR_INVALID;
   const int grid = std::min(p.total_tiles, std::max(1, num_sms));
   const uint32_t fmt = ab_fmt == 1 ? 1u : 0u;
   if (pair) {
@@ -524,6 +546,7 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
       case EPI_XPROJ: return launch_epi<EPI_XPROJ, true>(bn, ta, tb, p, fmt, num_sms, st);
       case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS, true>(bn, ta, tb, p, fmt, num_sms, st);
       case EPI_F32: return launch_epi<EPI_F32, true>(bn, ta, tb, p, fmt, num_sms, st);
+      case EPI_GEGLU: return launch_epi<EPI_GEGLU, true>(bn, ta, tb, p, fmt, num_sms, st);
       default: return HYMBA_ERR_INVALID;
     }
   }
@@ -534,6 +557,7 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
     case EPI_F32: return launch_epi<EPI_F32, false>(bn, ta, tb, p, fmt, grid, st);
     case EPI_PARTIAL: return launch_epi<EPI_PARTIAL, false>(bn, ta, tb, p, fmt, grid, st);
     case EPI_ATOMIC: return launch_epi<EPI_ATOMIC, false>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_GEGLU: return launch_epi<EPI_GEGLU, false>(bn, ta, tb, p, fmt, grid, st);
     default: return HYMBA_ERR_INVALID;
   }
 }

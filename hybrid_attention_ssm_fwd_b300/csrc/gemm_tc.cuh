@@ -13,6 +13,7 @@ enum GemmEpi : int {
   EPI_F32 = 3,       // C fp32 = acc (+ bf16 residual)
   EPI_PARTIAL = 4,   // C fp32 + split*M*ldc = acc (split-K partial sums)
   EPI_ATOMIC = 5,    // C fp32 += acc with vector atomics (split-K into a cleared or residual C)
+  EPI_GEGLU = 6,     // columns (2j, 2j+1) = (gate j, up j): C fp16 [., N/2] = GeLU(gate) * up (N % 16 == 0)
 };
 
 struct GemmParams {

@@ -783,6 +783,91 @@ hymba_status hymba_layer_fwd_meta(const hymba_layer_desc* d, const hymba_layer_w
   return fwd_bf16(x, pl, w, x_in, y, cache_out, kv_in, kv_out, ws, dev_status, mk, st, mc);
 }
 
+// ---- full residual block ---------------------------------------------------
+
+namespace {
+
+struct BlockPlan {
+  Plan layer;
+  size_t xn, h, wdown, total;
+};
+
+hymba_status block_dims(const hymba_layer_desc* d, int32_t d_ff, Dims* x) {
+  if (!d) return HYMBA_ERR_INVALID;
+  TRY(check_desc(d, false, x));
+  if (x->dtype != HYMBA_BF16 || x->residual != 0) return d->residual != 0 ? HYMBA_ERR_INVALID : HYMBA_ERR_UNSUPPORTED;
+  if (d_ff < 8 || d_ff % 8 || x->d % 8) return HYMBA_ERR_UNSUPPORTED;
+  x->residual = 2;  // the layer adds its output into the stream
+  return HYMBA_OK;
+}
+
+BlockPlan plan_block(const Dims& x, int d_ff) {
+  BlockPlan b{};
+  b.layer = plan_ws(x, false);
+  size_t off = align_up(b.layer.total, 256);
+  const size_t r = static_cast<size_t>(x.rows);
+  b.xn = off;
+  off = align_up(off + r * x.d * 2, 256);
+  b.h = off;
+  off = align_up(off + r * static_cast<size_t>(d_ff) * 2, 256);
+  b.wdown = off;
+  off = align_up(off + static_cast<size_t>(x.d) * d_ff * 2, 256);
+  b.total = off;
+  return b;
+}
+
+}  // namespace
+
+size_t hymba_block_fwd_workspace(const hymba_layer_desc* d, int32_t d_ff) {
+  Dims x;
+  if (block_dims(d, d_ff, &x) != HYMBA_OK) return 0;
+  return plan_block(x, d_ff).total;
+}
+
+hymba_status hymba_block_fwd(const hymba_layer_desc* d, const hymba_block_weights* w, int32_t d_ff, float* xs,
+                             void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  Dims x;
+  TRY(block_dims(d, d_ff, &x));
+  if (!w || !xs || !ws) return HYMBA_ERR_INVALID;
+  TRY(check_weights(&w->mix, x));
+  if (!w->norm1 || !w->norm2 || !w->W_gu || !w->W_down) return HYMBA_ERR_INVALID;
+  if (!aligned(xs, 16) || !aligned(ws, 256) || !aligned(w->norm1, 16) || !aligned(w->norm2, 16) ||
+      !aligned(w->W_gu, 16) || !aligned(w->W_down, 16))
+    return HYMBA_ERR_INVALID;
+  const BlockPlan bp = plan_block(x, d_ff);
+  if (ws_bytes < bp.total) return HYMBA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  const int sms = num_sms();
+  const int rows = static_cast<int>(x.rows);
+  __nv_bfloat16* xn = at<__nv_bfloat16>(ws, bp.xn);
+  __half* h = at<__half>(ws, bp.h);
+  __half* wdown = at<__half>(ws, bp.wdown);
+  // x += Layer(RMSNorm(x; norm1))
+  TRY(rmsnorm_bf16(rows, x.d, xs, x.d, w->norm1, x.eps, xn, x.d, st));
+  Marks mk;
+  mk.st = st;
+  TRY(fwd_bf16(x, bp.layer, &w->mix, xn, xs, nullptr, nullptr, nullptr, ws, dev_status, mk, st));
+  // x += W_down (GeLU(W_gate h) * (W_up h)),  h = RMSNorm(x; norm2)
+  TRY(rmsnorm_bf16(rows, x.d, xs, x.d, w->norm2, x.eps, xn, x.d, st));
+  TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_down), d_ff, wdown, d_ff, x.d, d_ff, st));
+  {
+    GemmParams p = gp(rows, 2 * d_ff, x.d, dev_status, x.wait_ns);
+    p.C = h;
+    p.ldc = d_ff;
+    TRY(gemm_tc(1, xn, x.d, w->W_gu, x.d, EPI_GEGLU, p, 0, 1, sms, st));
+  }
+  {
+    GemmParams p = gp(rows, x.d, d_ff, dev_status, x.wait_ns);
+    p.C = xs;
+    p.ldc = x.d;
+    p.resid_f32 = xs;
+    p.ld_resid = x.d;
+    TRY(gemm_tc(0, h, d_ff, wdown, d_ff, EPI_F32, p, 0, 1, sms, st));
+  }
+  return HYMBA_OK;
+}
+
 static hymba_status layer_decode_impl(const hymba_layer_desc* d, const hymba_layer_weights* w, const void* x_new,
                                       float* y, const hymba_cache* cache, const hymba_cache* shared_cache, void* ws,
                                       size_t ws_bytes, int32_t* dev_status, void* const* events, int32_t n_events,

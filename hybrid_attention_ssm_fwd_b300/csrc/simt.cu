@@ -532,6 +532,34 @@ __global__ void copy2d_kernel(const TS* __restrict__ src, long long lds, TD* __r
   for (long long r = blockIdx.y; r < rows; r += gridDim.y) dst[r * ldd + c] = from_f<TD>(to_f(src[r * lds + c]));
 }
 
+// RMSNorm of fp32 rows with a learned weight, stored as bf16: one warp per
+// row, two passes over the row (the second hits L1/L2).
+__global__ void __launch_bounds__(256) rmsnorm_bf16_kernel(int rows, int d, const float* __restrict__ x,
+                                                           long long ldx, const float* __restrict__ w, float eps,
+                                                           __nv_bfloat16* __restrict__ y, long long ldy) {
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + row * ldx);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  const int n4 = d / 4;
+  float ss = 0.f;
+  for (int i = lane; i < n4; i += 32) {
+    const float4 v = xr[i];
+    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float r = rsqrtf(ss / d + eps);
+  uint2* yr = reinterpret_cast<uint2*>(y + row * ldy);
+  for (int i = lane; i < n4; i += 32) {
+    const float4 v = xr[i], g = __ldg(w4 + i);
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x * r * g.x, v.y * r * g.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z * r * g.z, v.w * r * g.w);
+    yr[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  }
+}
+
 __global__ void bf16_to_f16_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n8) {
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -667,6 +695,16 @@ hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* 
     return last_err();
   }
   fuse_norm_kernel<T><<<rows, 256, 0, st>>>(di, att, g, beta1, beta2, eps, s);
+  return last_err();
+}
+
+hymba_status rmsnorm_bf16(int rows, int d, const float* x, long long ldx, const float* w, float eps,
+                          __nv_bfloat16* y, long long ldy, cudaStream_t st) {
+  if (rows <= 0) return HYMBA_OK;
+  if (d % 4 || ldx % 4 || ldy % 4 || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(w) & 15) ||
+      (reinterpret_cast<uintptr_t>(y) & 7))
+    return HYMBA_ERR_INVALID;
+  rmsnorm_bf16_kernel<<<(rows + 7) / 8, 256, 0, st>>>(rows, d, x, ldx, w, eps, y, ldy);
   return last_err();
 }
 

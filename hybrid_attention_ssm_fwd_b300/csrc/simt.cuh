@@ -49,6 +49,11 @@ hymba_status scan_simt(int B, int L, int di, int N, const T* u, long long ld_u, 
                        long long ld_g, const float* h0, float* h_out, cudaStream_t st);
 
 // s = beta1 * att / rms(att) + beta2 * g / rms(g), rms over di; one block/row.
+// y = bf16(x / sqrt(mean(x^2) + eps) * w) per row of d fp32 values (d % 4 == 0,
+// 16-byte aligned x and w, 8-byte aligned y).
+hymba_status rmsnorm_bf16(int rows, int d, const float* x, long long ldx, const float* w, float eps,
+                          __nv_bfloat16* y, long long ldy, cudaStream_t st);
+
 template <typename T>
 hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* beta1,
                        const float* beta2, float eps, T* s, cudaStream_t st);

@@ -157,3 +157,45 @@ class HymbaLayer:
 
     def check_status(self) -> int:
         return int(self.status.item())
+
+
+def block_params_to_device(pb: Dict[str, np.ndarray], shape, device="cuda") -> Dict[str, torch.Tensor]:
+    """A residual block's parameters: the layer's, the two RMSNorm weights
+    (fp32), W_gate / W_up interleaved row by row into W_gu [2F, d] and W_down
+    [d, F] (storage dtype)."""
+    out = params_to_device(pb, shape, device)
+    dt = storage_dtype(shape)
+    for n in ("norm1", "norm2"):
+        out[n] = torch.from_numpy(np.ascontiguousarray(pb[n], dtype=np.float32)).to(device)
+    Fh, d = pb["W_gate"].shape
+    gu = np.empty((2 * Fh, d), np.float32)
+    gu[0::2] = pb["W_gate"]
+    gu[1::2] = pb["W_up"]
+    out["W_gu"] = torch.from_numpy(gu).to(device=device, dtype=dt)
+    out["W_down"] = torch.from_numpy(np.ascontiguousarray(pb["W_down"], dtype=np.float32)).to(device=device, dtype=dt)
+    return out
+
+
+class HymbaBlock:
+    """One residual block (RMSNorm -> hybrid-head layer -> add; RMSNorm ->
+    gated MLP -> add) on one device, applied in place to an fp32 stream."""
+
+    def __init__(self, shape, params: Dict[str, torch.Tensor], d_ff: int, wait_limit_us: int = 0):
+        self.shape = shape
+        self.params = params
+        self.d_ff = d_ff
+        self.desc = hb.make_desc(shape, wait_limit_us, residual_mode=0)
+        self.weights = hb.make_block_weights(params)
+        nbytes = hb.block_fwd_workspace(self.desc, d_ff)
+        if nbytes == 0:
+            raise hb.HymbaError(hb.HYMBA_ERR_UNSUPPORTED, "block workspace query")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=params["W_in"].device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=params["W_in"].device)
+
+    def forward(self, x: torch.Tensor) -> torch.Tensor:
+        """x: [B, L, d] fp32 stream, updated in place and returned."""
+        hb.hymba_block_fwd(self.desc, self.weights, self.d_ff, x, self.ws, status=self.status)
+        return x
+
+    def check_status(self) -> int:
+        return int(self.status.item())

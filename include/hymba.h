@@ -245,6 +245,44 @@ HYMBA_API hymba_status hymba_layer_fwd_meta(const hymba_layer_desc* d, const hym
                                             const hymba_kv* kv_out, void* ws, size_t ws_bytes,
                                             int32_t* dev_status, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Full residual block around the hybrid-head layer.  The Hymba pages give no
+ * block structure of their own; this follows the residual pattern and gated
+ * MLP of "Griffin: Mixing Gated Linear Recurrences with Local Attention for
+ * Efficient Language Models" (section 2.1 residual block, section 2.2 MLP
+ * block):
+ *     x = x + Layer(RMSNorm(x; norm1))
+ *     x = x + W_down (GeLU(W_gate h) * (W_up h)),  h = RMSNorm(x; norm2)
+ * RMSNorm(x; w) = x / sqrt(mean(x^2) + eps) * w over the d channels of a row;
+ * GeLU(v) = v Phi(v) (exact, erf).  The sub-block inputs are stored in bf16
+ * (the layer's input type); the stream x stays fp32.
+ * Supported on HYMBA_BF16 (the layer's own constraints), d % 8 == 0 and
+ * d_ff % 8 == 0.
+ * ------------------------------------------------------------------------- */
+typedef struct hymba_block_weights {
+  hymba_layer_weights mix;  /* the hybrid-head layer                          */
+  const float* norm1;       /* [d] fp32: RMSNorm weight before the layer      */
+  const float* norm2;       /* [d] fp32: RMSNorm weight before the MLP        */
+  const void* W_gu;         /* [2*d_ff, d] bf16: gate and up rows interleaved,
+                               row 2j = W_gate row j, row 2j+1 = W_up row j    */
+  const void* W_down;       /* [d, d_ff] bf16                                 */
+} hymba_block_weights;
+
+/* Bytes of scratch memory hymba_block_fwd needs (0 on invalid). */
+HYMBA_API size_t hymba_block_fwd_workspace(const hymba_layer_desc* d, int32_t d_ff);
+
+/* One residual block over the whole stream (meta rows included).
+ *   d        the layer's descriptor; desc.residual must be 0 (the block adds
+ *            the stream itself).
+ *   x        [B, L, d] device fp32, the residual stream: read, then
+ *            overwritten with the block's output.
+ *   d_ff     the MLP width F.
+ * Errors as hymba_layer_fwd; HYMBA_ERR_RANGE in *dev_status if an fp16
+ * intermediate (layer activations, the MLP's gated hidden layer) overflows. */
+HYMBA_API hymba_status hymba_block_fwd(const hymba_layer_desc* d, const hymba_block_weights* w, int32_t d_ff,
+                                       float* x, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                       void* stream);
+
 /* Bytes of scratch memory hymba_layer_decode needs for `d` (0 on invalid). */
 HYMBA_API size_t hymba_layer_decode_workspace(const hymba_layer_desc* d);
 

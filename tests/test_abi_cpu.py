@@ -176,3 +176,20 @@ def test_meta_prefix_rejects_bad_arguments_before_launch():
     rc = L.hymba_layer_fwd_meta(ctypes.byref(d96), ctypes.byref(w), ctypes.byref(full), 0x200000, 0x300000, None,
                                 None, None, ws, 1 << 40, None, None)
     assert rc == hb.HYMBA_ERR_UNSUPPORTED
+
+
+def test_block_workspace_and_argument_checks():
+    d = _desc(residual=0)
+    n = hb.block_fwd_workspace(d, 4800)
+    assert n > hb.layer_fwd_workspace(d)
+    assert hb.block_fwd_workspace(d, 4801) == 0                      # d_ff % 8 != 0
+    assert hb.block_fwd_workspace(_desc(residual=1), 4800) == 0      # the block adds the stream itself
+    assert hb.block_fwd_workspace(_desc(residual=0, dtype=hb.HYMBA_F32), 4800) == 0
+    w = hb.BlockWeights(mix=_fake_weights(), norm1=0x400000, norm2=0x500000, W_gu=0x600000, W_down=0)
+    rc = hb.lib().hymba_block_fwd(ctypes.byref(d), ctypes.byref(w), 4800, 0x200000, ctypes.c_void_p(0x100000),
+                                  1 << 40, None, None)
+    assert rc == hb.HYMBA_ERR_INVALID                                 # W_down missing
+    w.W_down = 0x700000
+    rc = hb.lib().hymba_block_fwd(ctypes.byref(d), ctypes.byref(w), 4800, 0x200000, ctypes.c_void_p(0x100000),
+                                  16, None, None)
+    assert rc == hb.HYMBA_ERR_WORKSPACE
