@@ -224,6 +224,15 @@ HY_DEV void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch.  pdl_wait: wait until the stream's preceding
+// kernel has completed and its memory is visible (returns at once when this
+// grid was launched without a programmatic dependency); nothing a preceding
+// kernel writes may be touched before it.  pdl_trigger: let the next kernel of
+// the stream be scheduled now (it still waits for this grid in its own
+// pdl_wait); issued after pdl_wait, so at most two kernels are in flight.
+HY_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+HY_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 HY_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 HY_DEV void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -365,5 +374,24 @@ bool encode_tmap(CUtensorMap* out, CUtensorMapDataType dt, int rank, const void*
                  CUtensorMapSwizzle swz);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Launch `kern` so that it may start while the stream's preceding kernel
+// finishes (programmatic stream serialization); the kernel must call pdl_wait()
+// before touching anything a preceding kernel writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 }  // namespace hy

@@ -299,6 +299,8 @@ __global__ void __launch_bounds__(DA_THREADS)
 // Merges the splits of each (b, head): o = sum_s 2^(m_s - m) o_s / sum_s 2^(m_s - m) l_s.
 __global__ void decode_attn_combine_kernel(int Hq, int dv, int nsplit, const float* __restrict__ part,
                                            __half* __restrict__ out, long long ldo) {
+  pdl_wait();
+  pdl_trigger();
   const int h = blockIdx.x, b = blockIdx.y;
   const float* pp = part + (static_cast<long long>(b) * Hq + h) * nsplit * (dv + 2);
   float m = -INFINITY;
@@ -362,21 +364,11 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
   __shared__ __align__(16) float sbc[DS_SEQ][2 * N];      // [B | C] of each sequence
   __shared__ __align__(16) float sA2[DS_CH][N];
   __shared__ __align__(8) float2 sdu[DS_SEQ][DS_CH];      // (delta, delta * u)
+  __shared__ __align__(16) __half su[DS_SEQ][DS_CH];      // u and z of the block's (sequence, channel) tile
+  __shared__ __align__(16) __half sz[DS_SEQ][DS_CH];
   const int c0 = blockIdx.x * DS_CH, b0 = blockIdx.y * DS_SEQ;
   const int tid = threadIdx.x;
   const int KP = (R + 15) / 16 * 16;  // padded dt rank
-  // ---- 0. state loads (phase-2 thread: quarter q of the rows j = tid/4 + 64 i)
-  constexpr int NJ = DS_SEQ * DS_CH / (DS_THREADS / 4);
-  const int q = tid & 3;
-  float4 hv[NJ];
-#pragma unroll
-  for (int i = 0; i < NJ; ++i) {
-    const int j = (tid >> 2) + i * (DS_THREADS / 4);
-    const int b = b0 + j / DS_CH, c = c0 + j % DS_CH;
-    hv[i] = (b < B && c < di)
-                ? reinterpret_cast<const float4*>(state + (static_cast<long long>(b) * di + c) * N)[q]
-                : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   // W_dt rows: 8 threads per row, 4 values per 8-byte load
   {
     const int row = tid >> 3, l8 = tid & 7;  // 32 rows
@@ -401,6 +393,26 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
       *reinterpret_cast<uint2*>(&sW[row][k]) = make_uint2(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]));
     }
   }
+  for (int idx = tid; idx < DS_CH * N; idx += DS_THREADS) {
+    const int cc = idx / N;
+    sA2[cc][idx % N] = (c0 + cc < di) ? -__expf(A_log[static_cast<long long>(c0) * N + idx]) * 1.4426950408889634f
+                                      : 0.f;
+  }
+  // everything above reads weights only; the rest reads what earlier kernels wrote
+  pdl_wait();
+  pdl_trigger();
+  // ---- 0. state loads (phase-2 thread: quarter q of the rows j = tid/4 + 64 i)
+  constexpr int NJ = DS_SEQ * DS_CH / (DS_THREADS / 4);
+  const int q = tid & 3;
+  float4 hv[NJ];
+#pragma unroll
+  for (int i = 0; i < NJ; ++i) {
+    const int j = (tid >> 2) + i * (DS_THREADS / 4);
+    const int b = b0 + j / DS_CH, c = c0 + j % DS_CH;
+    hv[i] = (b < B && c < di)
+                ? reinterpret_cast<const float4*>(state + (static_cast<long long>(b) * di + c) * N)[q]
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   // dt rows: 16 threads per row (the padding columns past R are zeroed, never read)
   {
     const int row = tid >> 4, l16 = tid & 15;
@@ -423,10 +435,21 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
     const int s = idx / (2 * N);
     sbc[s][idx % (2 * N)] = (b0 + s < B) ? xp[(b0 + s) * ld_xp + R + idx % (2 * N)] : 0.f;
   }
-  for (int idx = tid; idx < DS_CH * N; idx += DS_THREADS) {
-    const int cc = idx / N;
-    sA2[cc][idx % N] = (c0 + cc < di) ? -__expf(A_log[static_cast<long long>(c0) * N + idx]) * 1.4426950408889634f
-                                      : 0.f;
+  // u and z tiles: threads 0..63 load u, 64..127 z, 8 channels (16 bytes) each
+  if (tid < 2 * DS_SEQ * (DS_CH / 8)) {
+    const bool is_z = tid >= DS_SEQ * (DS_CH / 8);
+    const int t = is_z ? tid - DS_SEQ * (DS_CH / 8) : tid;
+    const int s = t / (DS_CH / 8), c8 = (t % (DS_CH / 8)) * 8;
+    const int b = b0 + s, c = c0 + c8;
+    const __half* src = is_z ? z + b * ldz + c : u + b * ldu + c;
+    const long long ld = is_z ? ldz : ldu;
+    __half* dst = is_z ? &sz[s][c8] : &su[s][c8];
+    if (b < B && c + 8 <= di && ((reinterpret_cast<uintptr_t>(src) | static_cast<uintptr_t>(ld * 2)) & 15) == 0) {
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dst[e] = (b < B && c + e < di) ? src[e] : __float2half_rn(0.f);
+    }
   }
   __syncthreads();
   // every kernel of the step that reads pos ran before this one: advance it
@@ -452,7 +475,7 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
       float dt = 0.f, uu = 0.f;
       if (b < B && c < di) {
         dt = softplus_fast(acc[e] + dt_bias[c]);
-        uu = __half2float(u[b * ldu + c]);
+        uu = __half2float(su[s][cl]);
       }
       sdu[s][cl] = make_float2(dt, dt * uu);
     }
@@ -485,8 +508,8 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
     if (ok) {
       *hp = h;
       if (q == 0) {
-        const float uu = __half2float(u[b * ldu + c]);
-        const float zz = __half2float(z[b * ldz + c]);
+        const float uu = __half2float(su[s][cl]);
+        const float zz = __half2float(sz[s][cl]);
         y = fmaf(Dc, uu, y);
         // y * silu(z) = y * z / (1 + 2^(-z log2 e))
         g[b * ldg + c] = __float2half_rn(y * zz * rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * zz)));
@@ -609,7 +632,9 @@ hymba_status decode_attention_split(int B, int M, int Hq, int Hkv, int dh, int d
 
 hymba_status decode_attn_combine(int B, int Hq, int dv, int nsplit, const float* part, __half* out, long long ldo,
                                  cudaStream_t st) {
-  decode_attn_combine_kernel<<<dim3(Hq, B), 128, 0, st>>>(Hq, dv, nsplit, part, out, ldo);
+  if (launch_pdl(decode_attn_combine_kernel, dim3(Hq, B), dim3(128), 0, st, Hq, dv, nsplit, part, out, ldo) !=
+      cudaSuccess)
+    return HYMBA_ERR_CUDA;
   return last_err();
 }
 
@@ -621,8 +646,9 @@ hymba_status decode_ssm_step(int B, int di, int N, int R, const __half* u, long 
   if (!decode_ssm_step_supported(N, R)) return HYMBA_ERR_UNSUPPORTED;
   if (B < 1 || di < 1) return HYMBA_OK;
   dim3 grid((di + DS_CH - 1) / DS_CH, (B + DS_SEQ - 1) / DS_SEQ);
-  decode_ssm_step_kernel<16><<<grid, DS_THREADS, 0, st>>>(B, di, R, u, ldu, z, ldz, xp, ld_xp, W_dt, dt_bias,
-                                                          A_log, D, state, g, ldg, pos);
+  if (launch_pdl(decode_ssm_step_kernel<16>, grid, dim3(DS_THREADS), 0, st, B, di, R, u, ldu, z, ldz, xp, ld_xp, W_dt,
+                 dt_bias, A_log, D, state, g, ldg, pos) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
   return last_err();
 }
 
@@ -664,6 +690,8 @@ __global__ void decode_prep_kernel(int B, int di, int k, const __half* __restric
                                    __nv_bfloat16* __restrict__ v_ring, const float* __restrict__ w,
                                    const float* __restrict__ bias, float* __restrict__ conv_state,
                                    __half* __restrict__ u, long long ldu, int append) {
+  pdl_wait();
+  pdl_trigger();
   const long long n_conv = static_cast<long long>(B) * di;
   const int wk = Hkv * dh, wv = Hkv * dv;
   const long long n = n_conv + (append ? static_cast<long long>(B) * (wk + wv) : 0);
@@ -703,9 +731,10 @@ hymba_status decode_prep(int B, int di, int k, const __half* proj, long long ldp
                          __half* u, long long ldu, bool append, cudaStream_t st) {
   const long long n = static_cast<long long>(B) * di + (append ? static_cast<long long>(B) * Hkv * (dh + dv) : 0);
   if (n <= 0) return HYMBA_OK;
-  decode_prep_kernel<<<static_cast<unsigned>(std::min<long long>((n + 255) / 256, 148 * 16)), 256, 0, st>>>(
-      B, di, k, proj, ldp, x_col, k_col, v_col, Hkv, dh, dv, window, cap, pos, k_ring, v_ring, conv_w, conv_b,
-      conv_state, u, ldu, append ? 1 : 0);
+  if (launch_pdl(decode_prep_kernel, dim3(static_cast<unsigned>(std::min<long long>((n + 255) / 256, 148 * 16))),
+                 dim3(256), 0, st, B, di, k, proj, ldp, x_col, k_col, v_col, Hkv, dh, dv, window, cap, pos, k_ring,
+                 v_ring, conv_w, conv_b, conv_state, u, ldu, append ? 1 : 0) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
   return last_err();
 }
 

@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(DA_WARPS * 32, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
   const WaitCtl wc{&abort_flag, a.status, a.wait_ns};
   uint8_t* ring = smem + warp * WARP_BYTES;
   const int G = a.Hq / a.Hkv;
@@ -369,12 +371,16 @@ hymba_status decode_attention_tc(int B, int M, int Hq, int Hkv, int dh, int dv, 
     if (cudaFuncSetAttribute(decode_attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return HYMBA_ERR_CUDA;
-    decode_attn_tc_kernel<128><<<grid, DA_WARPS * 32, smem, st>>>(mKr, mVr, mKm, mVm, a);
+    if (launch_pdl(decode_attn_tc_kernel<128>, dim3(grid), dim3(DA_WARPS * 32), smem, st, mKr, mVr, mKm, mVm, a) !=
+        cudaSuccess)
+      return HYMBA_ERR_CUDA;
   } else {
     if (cudaFuncSetAttribute(decode_attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return HYMBA_ERR_CUDA;
-    decode_attn_tc_kernel<64><<<grid, DA_WARPS * 32, smem, st>>>(mKr, mVr, mKm, mVm, a);
+    if (launch_pdl(decode_attn_tc_kernel<64>, dim3(grid), dim3(DA_WARPS * 32), smem, st, mKr, mVr, mKm, mVm, a) !=
+        cudaSuccess)
+      return HYMBA_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return HYMBA_ERR_CUDA;
   return decode_attn_combine(B, Hq, dv, nsplit, part, out, ldo, st);

@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (PAIR) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
+  pdl_wait();  // only the setup above may overlap the preceding kernel
+  pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   const WaitCtl wc{abort_flag, p.status, p.wait_ns};
 
@@ -442,19 +444,21 @@ hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmP
     attr_done = true;
   }
   if constexpr (!PAIR) {
-    kern<<<grid, 192, Cfg::SMEM, st>>>(ta, tb, p, idesc);
+    if (launch_pdl(kern, dim3(grid), dim3(192), Cfg::SMEM, st, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
   } else {
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(192, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
     // persistent: no more clusters than can be resident at once (a GPC with an
     // odd SM count leaves one SM out), so no tile waits for a second wave
     static int max_clusters = 0;
@@ -466,6 +470,7 @@ hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmP
     }
     const int clusters = std::max(1, std::min(std::min(grid / 2, max_clusters), p.total_pairs));
     cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;

@@ -500,6 +500,14 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   __half* s = at<__half>(ws, pl.s);
   float* part = at<float>(ws, pl.part);
   const bool ssm_fused = decode_ssm_step_supported(x.N, x.R);
+  const int ldp_x = (x.xo + 15) / 16 * 16;
+  // the buffers the split-K GEMMs add into are cleared first, so that the
+  // step's kernels follow one another with nothing in between (each may
+  // start while the one before it finishes)
+  if (ssm_fused && cudaMemsetAsync(part, 0, static_cast<size_t>(B) * ldp_x * sizeof(float), st) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
+  if (x.residual == 0 && cudaMemsetAsync(Y, 0, static_cast<size_t>(B) * x.d * sizeof(float), st) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
   mk.mark();
   // W_x and W_out are converted to fp16 inside the GEMMs (cvt_b); only the
   // unfused dt projection needs a converted W_dt
@@ -544,10 +552,8 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
     p.ldc = ldp;
     p.cvt_b = 1;
     if (ssm_fused) {
-      // split-K partials added straight into a cleared [B, ldp] fp32 buffer,
-      // which the SSM step reads as [dt | B | C]
-      if (cudaMemsetAsync(part, 0, static_cast<size_t>(B) * ldp * sizeof(float), st) != cudaSuccess)
-        return HYMBA_ERR_CUDA;
+      // split-K partials added straight into the [B, ldp] fp32 buffer cleared
+      // at the start, which the SSM step reads as [dt | B | C]
       TRY(gemm_tc(0, u, x.di, w->W_x, x.di, EPI_ATOMIC, p, 0, kDecodeSplitsX, sms, st));
     } else {
       TRY(gemm_tc(0, u, x.di, w->W_x, x.di, EPI_PARTIAL, p, 0, kDecodeSplitsX, sms, st));
@@ -580,11 +586,8 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
     GemmParams p = gp(B, x.d, x.di, status, x.wait_ns);
     p.cvt_b = 1;
     if (x.residual != 1) {
-      // split-K partials added straight into Y: cleared first, or holding the
-      // fp32 residual already (residual = 2)
-      if (x.residual == 0 &&
-          cudaMemsetAsync(Y, 0, static_cast<size_t>(B) * x.d * sizeof(float), st) != cudaSuccess)
-        return HYMBA_ERR_CUDA;
+      // split-K partials added straight into Y, which holds the fp32 residual
+      // already (residual = 2) or was cleared at the start of the step
       p.C = Y;
       p.ldc = x.d;
       TRY(gemm_tc(0, s, x.di, w->W_out, x.di, EPI_ATOMIC, p, 0, kDecodeSplitsOut, sms, st));

@@ -261,6 +261,8 @@ __global__ void __launch_bounds__(256) fuse_norm_kernel(int di, const T* __restr
                                                         const float* __restrict__ beta1,
                                                         const float* __restrict__ beta2, float eps,
                                                         T* __restrict__ s) {
+  pdl_wait();
+  pdl_trigger();
   const long long row = blockIdx.x;
   const T* a = att + row * di;
   const T* gg = g + row * di;
@@ -309,6 +311,8 @@ __global__ void __launch_bounds__(256) fuse_norm_vec_kernel(int di, const __half
                                                             const float* __restrict__ beta1,
                                                             const float* __restrict__ beta2, float eps,
                                                             __half* __restrict__ s) {
+  pdl_wait();
+  pdl_trigger();
   const long long row = blockIdx.x;
   const int nch = di / 8;
   const uint4* a4 = reinterpret_cast<const uint4*>(att + row * di);
@@ -384,6 +388,8 @@ __global__ void __launch_bounds__(128) fuse_norm_warp_kernel(int rows, int di, c
                                                              const float* __restrict__ beta1,
                                                              const float* __restrict__ beta2, float eps,
                                                              __half* __restrict__ s) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -683,18 +689,21 @@ hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* 
   // one warp per row wants many rows (a decode step's 128 rows would fill
   // 32 SMs): below that, one block per row
   if (vec_ok && di <= 32 * 8 * FW_V && rows >= 4 * 148 * 4) {
-    fuse_norm_warp_kernel<<<(rows + 3) / 4, 128, 0, st>>>(rows, di, reinterpret_cast<const __half*>(att),
-                                                          reinterpret_cast<const __half*>(g), beta1, beta2, eps,
-                                                          reinterpret_cast<__half*>(s));
+    if (launch_pdl(fuse_norm_warp_kernel, dim3((rows + 3) / 4), dim3(128), 0, st, rows, di,
+                   reinterpret_cast<const __half*>(att), reinterpret_cast<const __half*>(g), beta1, beta2, eps,
+                   reinterpret_cast<__half*>(s)) != cudaSuccess)
+      return HYMBA_ERR_CUDA;
     return last_err();
   }
   if (vec_ok && di <= 8 * 256 * FN_MAXC) {
-    fuse_norm_vec_kernel<<<rows, 256, 0, st>>>(di, reinterpret_cast<const __half*>(att),
-                                               reinterpret_cast<const __half*>(g), beta1, beta2, eps,
-                                               reinterpret_cast<__half*>(s));
+    if (launch_pdl(fuse_norm_vec_kernel, dim3(rows), dim3(256), 0, st, di, reinterpret_cast<const __half*>(att),
+                   reinterpret_cast<const __half*>(g), beta1, beta2, eps, reinterpret_cast<__half*>(s)) !=
+        cudaSuccess)
+      return HYMBA_ERR_CUDA;
     return last_err();
   }
-  fuse_norm_kernel<T><<<rows, 256, 0, st>>>(di, att, g, beta1, beta2, eps, s);
+  if (launch_pdl(fuse_norm_kernel<T>, dim3(rows), dim3(256), 0, st, di, att, g, beta1, beta2, eps, s) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
   return last_err();
 }
 
