@@ -61,6 +61,7 @@ class LayerShape:
     rope_theta: float = 0.0   # 0 disables RoPE
     eps: float = 1e-6
     dtype: str = "bf16"       # "bf16" or "f32"
+    fusion: str = "sum"       # "sum" (eq. 3) or "concat" (the ablation: W_out is [d, 2 di])
 
     @property
     def L(self) -> int:
@@ -176,7 +177,7 @@ def draw_layer_params(rng: np.random.Generator, s: LayerShape) -> Dict[str, np.n
     """
     p: Dict[str, np.ndarray] = {}
     p["W_in"] = store_round(_normal(rng, (s.P_in, s.d), 0.02), s.dtype)
-    p["W_out"] = store_round(_normal(rng, (s.d, s.di), 0.02), s.dtype)
+    p["W_out"] = store_round(_normal(rng, (s.d, s.di * (2 if s.fusion == "concat" else 1)), 0.02), s.dtype)
     p["W_x"] = store_round(_normal(rng, (s.xproj_out, s.di), 0.02), s.dtype)
     p["W_dt"] = store_round(_normal(rng, (s.di, s.R), 0.02), s.dtype)
     p["conv_w"] = _normal(rng, (s.di, s.k), 0.02)

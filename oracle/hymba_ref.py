@@ -236,9 +236,16 @@ def ssm_branch(x: np.ndarray, z: np.ndarray, p: Dict[str, np.ndarray], s,
 
 
 def fuse_and_project(att: np.ndarray, g: np.ndarray, p, s, X: Optional[np.ndarray]) -> np.ndarray:
-    """Eq. (3): Y = W_out(beta1 * norm(att) + beta2 * norm(g)) (+ X if residual)."""
-    sm = (np.asarray(p["beta1"], F) * rms_norm(att, s.eps)
-          + np.asarray(p["beta2"], F) * rms_norm(g, s.eps))
+    """Eq. (3): Y = W_out(beta1 * norm(att) + beta2 * norm(g)) (+ X if residual).
+
+    With ``s.fusion == "concat"`` the ablation of the Hymba page's appendix B
+    (Table 10, concatenation instead of the averaging fusion): the two
+    normalised, beta-scaled branches are concatenated and W_out is [d, 2 di]:
+    Y = W_out [beta1 * norm(att) ; beta2 * norm(g)].
+    """
+    a = np.asarray(p["beta1"], F) * rms_norm(att, s.eps)
+    b = np.asarray(p["beta2"], F) * rms_norm(g, s.eps)
+    sm = np.concatenate([a, b], axis=-1) if getattr(s, "fusion", "sum") == "concat" else a + b
     Y = sm @ np.asarray(p["W_out"], F).T
     if s.residual:
         Y = Y + np.asarray(X, F)

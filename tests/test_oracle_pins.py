@@ -539,3 +539,41 @@ def test_stack_kv_sharing_layer_uses_producer_kv():
         np.testing.assert_array_equal(o["Y"], out["Y"][i])
         X, prev = o["Y"], o
     assert shapes[2].kv_shared and not shapes[1].kv_shared
+
+
+# ---------------------------------------------------------------------------
+# concatenation fusion (the ablation of the Hymba page's appendix B, Table 10)
+# ---------------------------------------------------------------------------
+
+
+def test_concat_fusion_with_repeated_w_out_equals_sum_fusion():
+    """W_out [W | W] applied to [a ; b] is W (a + b): the concatenation
+    variant must then reproduce eq. (3) exactly; [W | 0] keeps only the
+    attention branch (the beta2 = 0 case of eq. 3)."""
+    s = tiny()
+    sc = synth.with_(s, fusion="concat")
+    p = inputs(s, 7)
+    y_sum = ref.layer_fwd(p, p["Xt"], s)["Y"]
+    q = dict(p)
+    q["W_out"] = np.concatenate([p["W_out"], p["W_out"]], axis=1)
+    np.testing.assert_allclose(ref.layer_fwd(q, p["Xt"], sc)["Y"], y_sum, rtol=1e-12, atol=1e-13)
+    q["W_out"] = np.concatenate([p["W_out"], np.zeros_like(p["W_out"])], axis=1)
+    p0 = dict(p)
+    p0["beta2"] = np.zeros_like(p["beta2"])
+    np.testing.assert_allclose(ref.layer_fwd(q, p["Xt"], sc)["Y"], ref.layer_fwd(p0, p["Xt"], s)["Y"],
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_concat_fusion_decode_matches_prefill():
+    T0, n = 30, 6
+    s = synth.tiny_f32(T=T0 + n, rope_theta=10000.0, fusion="concat")
+    p = inputs(s, 8)
+    assert p["W_out"].shape == (s.d, 2 * s.di)
+    full = ref.layer_fwd(p, p["Xt"], s)["Y"]
+    s0 = synth.with_(s, T=T0)
+    cache = ref.layer_fwd(p, p["Xt"][:, : s0.L], s0, cache_cap=s.window)["cache"]
+    sd = synth.with_(s, T=1)
+    for i in range(n):
+        r = ref.layer_decode(p, p["Xt"][:, s0.L + i], cache, sd)
+        np.testing.assert_allclose(r["y"], full[:, s0.L + i], rtol=1e-10, atol=1e-12)
+        cache = r["cache"]
