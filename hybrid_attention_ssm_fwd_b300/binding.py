@@ -31,7 +31,8 @@ class LayerDesc(ctypes.Structure):
         ("n_q_heads", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32), ("v_head_dim", c_int32),
         ("d_inner", c_int32), ("d_state", c_int32), ("d_conv", c_int32), ("dt_rank", c_int32),
         ("window", c_int32), ("kv_shared", c_int32), ("residual", c_int32), ("dtype", c_int32),
-        ("rope_theta", c_float), ("eps", c_float), ("wait_limit_us", c_uint32), ("reserved", c_int32 * 3),
+        ("rope_theta", c_float), ("eps", c_float), ("wait_limit_us", c_uint32), ("fusion", c_int32),
+        ("reserved", c_int32 * 2),
     ]
 
 
@@ -171,7 +172,8 @@ def make_desc(shape, wait_limit_us: int = 0, residual_mode: Optional[int] = None
                      kv_shared=int(shape.kv_shared),
                      residual=int(shape.residual) if residual_mode is None else residual_mode,
                      dtype=HYMBA_BF16 if shape.dtype == "bf16" else HYMBA_F32, rope_theta=shape.rope_theta,
-                     eps=shape.eps, wait_limit_us=wait_limit_us)
+                     eps=shape.eps, wait_limit_us=wait_limit_us,
+                     fusion=1 if getattr(shape, "fusion", "sum") == "concat" else 0)
 
 
 def make_weights(w: Dict[str, "object"]) -> LayerWeights:

@@ -27,6 +27,7 @@ namespace {
 
 struct Dims {
   int B, T, M, L, d, Hq, Hkv, dh, dv, di, N, k, R, W, kv_shared, residual, dtype;
+  int fusion, sw;  // sw = width of the fused rows s (and K of out_proj): di, or 2 di concatenated
   float theta, eps;
   uint64_t wait_ns;
   long long rows;
@@ -42,7 +43,8 @@ hymba_status check_desc(const hymba_layer_desc* d, bool decode, Dims* o) {
   if (d->batch < 1 || d->n_tokens < 1 || d->n_meta < 0 || d->d_model < 1 || d->n_q_heads < 1 ||
       d->n_kv_heads < 1 || d->head_dim < 2 || (d->head_dim & 1) || d->v_head_dim < 1 || d->d_inner < 1 ||
       d->d_state < 1 || d->d_state > 64 || d->d_conv < 1 || d->d_conv > 8 || d->dt_rank < 1 || d->window < 0 ||
-      !is_flag(d->kv_shared) || d->residual < 0 || d->residual > 2 || !(d->eps >= 0.f) || !(d->rope_theta >= 0.f))
+      !is_flag(d->kv_shared) || d->residual < 0 || d->residual > 2 || !(d->eps >= 0.f) || !(d->rope_theta >= 0.f) ||
+      !is_flag(d->fusion))
     return HYMBA_ERR_INVALID;
   if (d->dtype != HYMBA_F32 && d->dtype != HYMBA_BF16) return HYMBA_ERR_INVALID;
   if (d->n_q_heads % d->n_kv_heads != 0) return HYMBA_ERR_INVALID;
@@ -66,6 +68,8 @@ hymba_status check_desc(const hymba_layer_desc* d, bool decode, Dims* o) {
   x.W = d->window;
   x.kv_shared = d->kv_shared;
   x.residual = d->residual;
+  x.fusion = d->fusion;
+  x.sw = d->fusion ? 2 * d->d_inner : d->d_inner;
   x.dtype = d->dtype;
   x.theta = d->rope_theta;
   x.eps = d->eps;
@@ -126,12 +130,12 @@ Plan plan_ws(const Dims& x, bool decode) {
   p.delta = fused ? 0 : take(r * x.di * 4);
   p.att = take(r * x.di * e);
   p.g = take(r * x.di * e);
-  p.s = take(r * x.di * e);
+  p.s = take(r * x.sw * e);
   if (x.dtype == HYMBA_BF16) {
     // fp16 weight copies: prefill converts W_out and W_x once per call; the
     // decode GEMMs convert their bf16 tiles in shared memory instead
     if (!decode) {
-      p.wout = take(static_cast<size_t>(x.d) * x.di * 2);
+      p.wout = take(static_cast<size_t>(x.d) * x.sw * 2);
       p.wx = take(static_cast<size_t>(x.xo) * x.di * 2);
     }
     p.wdt = take(static_cast<size_t>(x.di) * x.Rp * 2);
@@ -242,9 +246,9 @@ hymba_status fwd_f32(const Dims& x, const Plan& pl, const hymba_layer_weights* w
   TRY(scan_simt<float>(x.B, x.L, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, x.di, bc, bc + x.N, 2 * x.N,
                        w->A_log, w->D, g, x.di, nullptr, h_out, st));
   mk.mark();
-  TRY(fuse_norm<float>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  TRY(fuse_norm<float>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st, x.fusion != 0));
   mk.mark();
-  TRY(gemm_simt<float>(rows, x.d, x.di, s, x.di, static_cast<const float*>(w->W_out), x.di, SE_RESID, Y, x.d,
+  TRY(gemm_simt<float>(rows, x.d, x.sw, s, x.sw, static_cast<const float*>(w->W_out), x.sw, SE_RESID, Y, x.d,
                        nullptr, 0, 0, nullptr, x.residual == 1 ? X : x.residual == 2 ? Y : nullptr, x.d, st));
   mk.mark();
   if (cache_out) {
@@ -274,8 +278,8 @@ GemmParams gp(int M, int N, int K, int32_t* status, uint64_t wait_ns) {
 
 hymba_status convert_weights(const Dims& x, const Plan& pl, const hymba_layer_weights* w, void* ws,
                              cudaStream_t st) {
-  TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_out), x.di, at<__half>(ws, pl.wout),
-                                    x.di, x.d, x.di, st));
+  TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_out), x.sw, at<__half>(ws, pl.wout),
+                                    x.sw, x.d, x.sw, st));
   TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_x), x.di, at<__half>(ws, pl.wx), x.di,
                                     x.xo, x.di, st));
   TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_dt), x.R, at<__half>(ws, pl.wdt), x.Rp,
@@ -394,16 +398,16 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
   }
   mk.mark();
   // fuse + out_proj
-  TRY(fuse_norm<__half>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  TRY(fuse_norm<__half>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st, x.fusion != 0));
   mk.mark();
   {
-    GemmParams p = gp(rows, x.d, x.di, status, x.wait_ns);
+    GemmParams p = gp(rows, x.d, x.sw, status, x.wait_ns);
     p.C = Y;
     p.ldc = x.d;
     p.resid = x.residual == 1 ? static_cast<const __nv_bfloat16*>(X) : nullptr;
     p.resid_f32 = x.residual == 2 ? Y : nullptr;
     p.ld_resid = x.d;
-    TRY(gemm_tc(0, s, x.di, at<__half>(ws, pl.wout), x.di, EPI_F32, p, 0, 1, sms, st));
+    TRY(gemm_tc(0, s, x.sw, at<__half>(ws, pl.wout), x.sw, EPI_F32, p, 0, 1, sms, st));
   }
   mk.mark();
   if (cache_out && mi) {
@@ -479,8 +483,8 @@ hymba_status decode_f32(const Dims& x, const Plan& pl, const hymba_layer_weights
                        nullptr, 0, 0, w->dt_bias, nullptr, 0, st));
   TRY(scan_simt<float>(B, 1, x.di, x.N, u, x.di, proj + x.z_col, x.P_in, delta, x.di, bc, bc + x.N, 2 * x.N,
                        w->A_log, w->D, g, x.di, c->ssm_state, c->ssm_state, st));
-  TRY(fuse_norm<float>(B, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
-  TRY(gemm_simt<float>(B, x.d, x.di, s, x.di, static_cast<const float*>(w->W_out), x.di, SE_RESID, Y, x.d, nullptr,
+  TRY(fuse_norm<float>(B, x.di, att, g, w->beta1, w->beta2, x.eps, s, st, x.fusion != 0));
+  TRY(gemm_simt<float>(B, x.d, x.sw, s, x.sw, static_cast<const float*>(w->W_out), x.sw, SE_RESID, Y, x.d, nullptr,
                        0, 0, nullptr, x.residual == 1 ? Xn : x.residual == 2 ? Y : nullptr, x.d, st));
   return pos_increment(B, c->pos, st);
 }
@@ -580,22 +584,22 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
                           w->A_log, w->D, g, x.di, c->ssm_state, c->ssm_state, st));
   }
   mk.mark();
-  TRY(fuse_norm<__half>(B, x.di, att, g, w->beta1, w->beta2, x.eps, s, st));
+  TRY(fuse_norm<__half>(B, x.di, att, g, w->beta1, w->beta2, x.eps, s, st, x.fusion != 0));
   mk.mark();
   {
-    GemmParams p = gp(B, x.d, x.di, status, x.wait_ns);
+    GemmParams p = gp(B, x.d, x.sw, status, x.wait_ns);
     p.cvt_b = 1;
     if (x.residual != 1) {
       // split-K partials added straight into Y, which holds the fp32 residual
       // already (residual = 2) or was cleared at the start of the step
       p.C = Y;
       p.ldc = x.d;
-      TRY(gemm_tc(0, s, x.di, w->W_out, x.di, EPI_ATOMIC, p, 0, kDecodeSplitsOut, sms, st));
+      TRY(gemm_tc(0, s, x.sw, w->W_out, x.sw, EPI_ATOMIC, p, 0, kDecodeSplitsOut, sms, st));
     } else {
       p.C = part;
       p.ldc = x.d;
-      TRY(gemm_tc(0, s, x.di, w->W_out, x.di, EPI_PARTIAL, p, 0, kDecodeSplitsOut, sms, st));
-      const int n_kb = (x.di + 63) / 64;
+      TRY(gemm_tc(0, s, x.sw, w->W_out, x.sw, EPI_PARTIAL, p, 0, kDecodeSplitsOut, sms, st));
+      const int n_kb = (x.sw + 63) / 64;
       const int sp = std::min(kDecodeSplitsOut, n_kb);
       const int kbs = (n_kb + sp - 1) / sp;
       const int splits = (n_kb + kbs - 1) / kbs;

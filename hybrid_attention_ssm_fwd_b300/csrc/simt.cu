@@ -255,12 +255,29 @@ __global__ void scan_simt_kernel(int B, int L, int di, int N, const T* __restric
 // ---------------------------------------------------------------------------
 // fused RMSNorm x2, beta scaling and sum (one block per row)
 // ---------------------------------------------------------------------------
+// concatenation fusion: 8 channels of beta1 * att * ra to `da` and of
+// beta2 * g * rg to `dg` (the two halves of a 2 di wide row)
+__device__ __forceinline__ void fuse_norm_concat8(const uint4& av, const uint4& gv, const float* b1, const float* b2,
+                                                  float ra, float rg, uint4* da, uint4* dg) {
+  const __half2* ah = reinterpret_cast<const __half2*>(&av);
+  const __half2* gh = reinterpret_cast<const __half2*>(&gv);
+  uint32_t oa[4], og[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 fa = __half22float2(ah[e]), fg = __half22float2(gh[e]);
+    oa[e] = pack_half2(__ldg(b1 + 2 * e) * fa.x * ra, __ldg(b1 + 2 * e + 1) * fa.y * ra);
+    og[e] = pack_half2(__ldg(b2 + 2 * e) * fg.x * rg, __ldg(b2 + 2 * e + 1) * fg.y * rg);
+  }
+  *da = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+  *dg = make_uint4(og[0], og[1], og[2], og[3]);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) fuse_norm_kernel(int di, const T* __restrict__ att,
                                                         const T* __restrict__ g,
                                                         const float* __restrict__ beta1,
                                                         const float* __restrict__ beta2, float eps,
-                                                        T* __restrict__ s) {
+                                                        T* __restrict__ s, int concat) {
   pdl_wait();
   pdl_trigger();
   const long long row = blockIdx.x;
@@ -298,14 +315,22 @@ __global__ void __launch_bounds__(256) fuse_norm_kernel(int di, const T* __restr
   }
   __syncthreads();
   const float ra = red[0][0], rg = red[1][0];
-  for (int c = threadIdx.x; c < di; c += blockDim.x)
-    s[row * di + c] = from_f<T>(beta1[c] * to_f(a[c]) * ra + beta2[c] * to_f(gg[c]) * rg);
+  if (concat) {
+    for (int c = threadIdx.x; c < di; c += blockDim.x) {
+      s[row * 2 * di + c] = from_f<T>(beta1[c] * to_f(a[c]) * ra);
+      s[row * 2 * di + di + c] = from_f<T>(beta2[c] * to_f(gg[c]) * rg);
+    }
+  } else {
+    for (int c = threadIdx.x; c < di; c += blockDim.x)
+      s[row * di + c] = from_f<T>(beta1[c] * to_f(a[c]) * ra + beta2[c] * to_f(gg[c]) * rg);
+  }
 }
 
 // fp16 fused norm: 16-byte vectors kept in registers (one HBM read of att
 // and g), up to FN_MAXC vectors of each per thread.
 constexpr int FN_MAXC = 4;
 
+template <bool CONCAT>
 __global__ void __launch_bounds__(256) fuse_norm_vec_kernel(int di, const __half* __restrict__ att,
                                                             const __half* __restrict__ g,
                                                             const float* __restrict__ beta1,
@@ -353,11 +378,13 @@ __global__ void __launch_bounds__(256) fuse_norm_vec_kernel(int di, const __half
     tg += red[1][i];
   }
   const float ra = rsqrtf(ta / di + eps), rg = rsqrtf(tg / di + eps);
-  uint4* s4 = reinterpret_cast<uint4*>(s + row * di);
+  uint4* s4 = reinterpret_cast<uint4*>(s + row * di * (CONCAT ? 2 : 1));
 #pragma unroll
   for (int q = 0; q < FN_MAXC; ++q) {
     const int ch = threadIdx.x + q * 256;
-    if (ch < nch) {
+    if (CONCAT && ch < nch) {
+      fuse_norm_concat8(av[q], gv[q], beta1 + ch * 8, beta2 + ch * 8, ra, rg, s4 + ch, s4 + nch + ch);
+    } else if (!CONCAT && ch < nch) {
       const __half2* ah = reinterpret_cast<const __half2*>(&av[q]);
       const __half2* gh = reinterpret_cast<const __half2*>(&gv[q]);
       const float4 b1a = *reinterpret_cast<const float4*>(beta1 + ch * 8);
@@ -383,6 +410,7 @@ __global__ void __launch_bounds__(256) fuse_norm_vec_kernel(int di, const __half
 // in flight), and the two sums of squares are reduced with shuffles only.
 constexpr int FW_V = 16;  // di <= 32 * 8 * FW_V = 4096
 
+template <bool CONCAT>
 __global__ void __launch_bounds__(128) fuse_norm_warp_kernel(int rows, int di, const __half* __restrict__ att,
                                                              const __half* __restrict__ g,
                                                              const float* __restrict__ beta1,
@@ -425,11 +453,13 @@ __global__ void __launch_bounds__(128) fuse_norm_warp_kernel(int rows, int di, c
     sg += __shfl_xor_sync(0xffffffffu, sg, o);
   }
   const float ra = rsqrtf(sa / di + eps), rg = rsqrtf(sg / di + eps);
-  uint4* s4 = reinterpret_cast<uint4*>(s + row * di);
+  uint4* s4 = reinterpret_cast<uint4*>(s + row * di * (CONCAT ? 2 : 1));
 #pragma unroll
   for (int q = 0; q < FW_V; ++q) {
     const int ch = lane + q * 32;
-    if (ch < nch) {
+    if (CONCAT && ch < nch) {
+      fuse_norm_concat8(av[q], gv[q], beta1 + ch * 8, beta2 + ch * 8, ra, rg, s4 + ch, s4 + nch + ch);
+    } else if (!CONCAT && ch < nch) {
       const __half2* ah = reinterpret_cast<const __half2*>(&av[q]);
       const __half2* gh = reinterpret_cast<const __half2*>(&gv[q]);
       const float4 b1a = __ldg(reinterpret_cast<const float4*>(beta1 + ch * 8));
@@ -681,7 +711,8 @@ hymba_status scan_simt(int B, int L, int di, int N, const T* u, long long ld_u, 
 
 template <typename T>
 hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* beta1, const float* beta2,
-                       float eps, T* s, cudaStream_t st) {
+                       float eps, T* s, cudaStream_t st, bool concat) {
+  const int cc = concat ? 1 : 0;
   if (rows <= 0) return HYMBA_OK;
   const bool vec_ok = std::is_same<T, __half>::value && di % 8 == 0 && (reinterpret_cast<uintptr_t>(beta1) & 15) == 0 &&
                       (reinterpret_cast<uintptr_t>(beta2) & 15) == 0 && (reinterpret_cast<uintptr_t>(att) & 15) == 0 &&
@@ -689,20 +720,22 @@ hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* 
   // one warp per row wants many rows (a decode step's 128 rows would fill
   // 32 SMs): below that, one block per row
   if (vec_ok && di <= 32 * 8 * FW_V && rows >= 4 * 148 * 4) {
-    if (launch_pdl(fuse_norm_warp_kernel, dim3((rows + 3) / 4), dim3(128), 0, st, rows, di,
-                   reinterpret_cast<const __half*>(att), reinterpret_cast<const __half*>(g), beta1, beta2, eps,
-                   reinterpret_cast<__half*>(s)) != cudaSuccess)
-      return HYMBA_ERR_CUDA;
-    return last_err();
-  }
-  if (vec_ok && di <= 8 * 256 * FN_MAXC) {
-    if (launch_pdl(fuse_norm_vec_kernel, dim3(rows), dim3(256), 0, st, di, reinterpret_cast<const __half*>(att),
+    if (launch_pdl(cc ? fuse_norm_warp_kernel<true> : fuse_norm_warp_kernel<false>, dim3((rows + 3) / 4),
+                   dim3(128), 0, st, rows, di, reinterpret_cast<const __half*>(att),
                    reinterpret_cast<const __half*>(g), beta1, beta2, eps, reinterpret_cast<__half*>(s)) !=
         cudaSuccess)
       return HYMBA_ERR_CUDA;
     return last_err();
   }
-  if (launch_pdl(fuse_norm_kernel<T>, dim3(rows), dim3(256), 0, st, di, att, g, beta1, beta2, eps, s) != cudaSuccess)
+  if (vec_ok && di <= 8 * 256 * FN_MAXC) {
+    if (launch_pdl(cc ? fuse_norm_vec_kernel<true> : fuse_norm_vec_kernel<false>, dim3(rows), dim3(256), 0, st, di,
+                   reinterpret_cast<const __half*>(att), reinterpret_cast<const __half*>(g), beta1, beta2, eps,
+                   reinterpret_cast<__half*>(s)) != cudaSuccess)
+      return HYMBA_ERR_CUDA;
+    return last_err();
+  }
+  if (launch_pdl(fuse_norm_kernel<T>, dim3(rows), dim3(256), 0, st, di, att, g, beta1, beta2, eps, s, cc) !=
+      cudaSuccess)
     return HYMBA_ERR_CUDA;
   return last_err();
 }
@@ -796,9 +829,9 @@ template hymba_status scan_simt<__half>(int, int, int, int, const __half*, long 
                                         const float*, const float*, __half*, long long, const float*, float*,
                                         cudaStream_t);
 template hymba_status fuse_norm<float>(int, int, const float*, const float*, const float*, const float*, float,
-                                       float*, cudaStream_t);
+                                       float*, cudaStream_t, bool);
 template hymba_status fuse_norm<__half>(int, int, const __half*, const __half*, const float*, const float*,
-                                        float, __half*, cudaStream_t);
+                                        float, __half*, cudaStream_t, bool);
 template hymba_status attention_simt<float>(int, int, int, int, int, int, int, int, const float*, long long,
                                             const float*, long long, const float*, long long, float*,
                                             long long, cudaStream_t);

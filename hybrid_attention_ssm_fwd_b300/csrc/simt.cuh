@@ -48,15 +48,16 @@ hymba_status scan_simt(int B, int L, int di, int N, const T* u, long long ld_u, 
                        const float* Cm, long long ld_bc, const float* A_log, const float* D, T* g,
                        long long ld_g, const float* h0, float* h_out, cudaStream_t st);
 
-// s = beta1 * att / rms(att) + beta2 * g / rms(g), rms over di; one block/row.
 // y = bf16(x / sqrt(mean(x^2) + eps) * w) per row of d fp32 values (d % 4 == 0,
 // 16-byte aligned x and w, 8-byte aligned y).
 hymba_status rmsnorm_bf16(int rows, int d, const float* x, long long ldx, const float* w, float eps,
                           __nv_bfloat16* y, long long ldy, cudaStream_t st);
 
+// s = beta1 * att / rms(att) + beta2 * g / rms(g), rms over di (rows di wide);
+// concat: s = [beta1 * att / rms(att) | beta2 * g / rms(g)] (rows 2 di wide).
 template <typename T>
 hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* beta1,
-                       const float* beta2, float eps, T* s, cudaStream_t st);
+                       const float* beta2, float eps, T* s, cudaStream_t st, bool concat = false);
 
 // SIMT attention: Q rows [B, L] with row stride ldq (head h at h*dh), K/V
 // with strides ldk/ldv (KV head g at g*dh / g*dv), O [B, L, ldo] (head h at

@@ -103,7 +103,11 @@ typedef struct hymba_layer_desc {
                            counting the meta rows); 0 disables RoPE          */
   float eps;            /* RMSNorm epsilon (1e-6 in the reference workloads) */
   uint32_t wait_limit_us; /* bound on any single in-kernel wait; 0 = 2 s     */
-  int32_t reserved[3];  /* must be 0                                         */
+  int32_t fusion;       /* 0: beta-weighted sum of the branches (eq. 3),
+                           W_out [d, di]; 1: concatenation of the normalised,
+                           beta-scaled branches (the appendix B ablation),
+                           W_out [d, 2*di]                                    */
+  int32_t reserved[2];  /* must be 0                                         */
 } hymba_layer_desc;
 
 /* Layer parameters (device pointers).  Matrices are in desc.dtype, vectors

@@ -193,3 +193,13 @@ def test_block_workspace_and_argument_checks():
     rc = hb.lib().hymba_block_fwd(ctypes.byref(d), ctypes.byref(w), 4800, 0x200000, ctypes.c_void_p(0x100000),
                                   16, None, None)
     assert rc == hb.HYMBA_ERR_WORKSPACE
+
+
+def test_fusion_flag_values():
+    assert hb.layer_fwd_workspace(_desc(fusion=1)) > hb.layer_fwd_workspace(_desc(fusion=0))   # s rows 2 di wide
+    assert hb.layer_fwd_workspace(_desc(fusion=2)) == 0
+    d = _desc(fusion=2)
+    w = _fake_weights()
+    rc = hb.lib().hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, None, None, None,
+                                  ctypes.c_void_p(0x100000), 1 << 40, None, None)
+    assert rc == hb.HYMBA_ERR_INVALID

@@ -19,7 +19,8 @@ F = np.float64
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(window=0), dict(rope_theta=10000.0), dict(T=37, window=8),
-                                dict(B=3, T=5, M=0, window=1), dict(residual=True, rope_theta=500.0)])
+                                dict(B=3, T=5, M=0, window=1), dict(residual=True, rope_theta=500.0),
+                                dict(fusion="concat")])
 def test_fp32_tiny_prefill(kw):
     s = synth.tiny_f32(**kw)
     p = synth.make_layer_inputs(s, 0)
@@ -66,6 +67,8 @@ BF16_CASES = [
     dict(residual=True),
     dict(B=3, T=333),                     # 1047 rows: the projections run as cluster pairs, 9 row blocks
     dict(B=5, T=240, residual=True),      # 1280 rows, 10 row blocks
+    dict(fusion="concat"),                # concatenated branches, W_out [d, 2 di]
+    dict(B=3, T=333, fusion="concat", residual=True),
 ]
 
 
@@ -177,3 +180,34 @@ def test_bf16_decode_per_sequence_positions(kw, cap, pos):
     c = cache_np(cache)
     assert np.all(c["pos"] == np.asarray(pos) + 1)
     assert_bf16_close(c["k_ring"], r["cache"]["k_ring"], "decode k_ring")
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(residual=True)])
+def test_bf16_decode_concat_fusion(kw):
+    """The concatenation variant through the decode step (norm writes both
+    halves, out_proj reduces over 2 di)."""
+    s = small_bf16(B=6, T=1, window=64, fusion="concat", **kw)
+    inp = synth.make_decode_inputs(s, 9, cap=64, pos=300)
+    assert inp["W_out"].shape == (s.d, 2 * s.di)
+    cache = hl.cache_to_device(inp, s)
+    layer = hl.HymbaLayer(s, hl.params_to_device(inp, s), decode=True)
+    y = layer.decode(hl.tokens_to_device(inp["x_new"], s), cache, 64).cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.check_status() == 0
+    keys = ("k_ring", "v_ring", "k_meta", "v_meta", "ssm_state", "conv_state", "pos")
+    r = ref.layer_decode(inp, inp["x_new"], {k: inp[k] for k in keys}, s)
+    assert_bf16_close(y, r["y"], f"decode concat {kw}")
+
+
+def test_fp32_decode_concat_fusion_chain():
+    T0, n = 30, 8
+    s = synth.tiny_f32(T=T0 + n, rope_theta=10000.0, fusion="concat")
+    p = synth.make_layer_inputs(s, 10)
+    s0 = synth.with_(s, T=T0)
+    _, cache, _ = run_prefill(s0, p, cap=s.window, Xt=p["Xt"][:, : s0.L])
+    sd = synth.with_(s, T=1)
+    layer = hl.HymbaLayer(sd, hl.params_to_device(p, sd), decode=True)
+    ys = [layer.decode(hl.tokens_to_device(p["Xt"][:, s0.L + i], sd), cache, s.window).cpu().numpy()
+          for i in range(n)]
+    yr = ref.layer_fwd(p, p["Xt"], s)["Y"][:, s0.L:]
+    assert_f32_close(np.stack(ys, 1), yr, "fp32 concat decode chain")

@@ -35,6 +35,7 @@ META_CASES = [
     dict(B=3, T=2),                                                      # fewer real rows than one tile
     dict(B=2, T=300, M=128, d=1600, Hq=25, Hkv=5, di=3200, window=256),  # 1.5B widths (dv = 128)
     dict(B=4, T=300),                                                    # 1200 real rows: cluster-pair GEMMs
+    dict(fusion="concat"),
 ]
 
 
