@@ -492,15 +492,21 @@ hymba_status launch_epi(int bn, const CUtensorMap& ta, const CUtensorMap& tb, co
 
 }  // namespace
 
+// Tile width: least padded N, each width weighted by its measured cost per
+// column relative to 256-wide tiles (narrower tiles issue more MMAs and
+// epilogues per FLOP: in_proj at 256 reached 0.80 of peak, out_proj at 160
+// 0.70), so a wide tile wins unless it pads N by more than a few percent.
 int gemm_pick_bn(int N, bool small_m) {
   if (small_m) return 64;
   static const int cand[] = {256, 160, 144, 128, 64};
+  static const int cost[] = {100, 108, 110, 112, 125};
   int best = 256;
-  long long best_pad = 1LL << 60;
-  for (int bn : cand) {
-    const long long pad = static_cast<long long>((N + bn - 1) / bn) * bn;
-    if (pad < best_pad) {
-      best_pad = pad;
+  long long best_cost = 1LL << 60;
+  for (int i = 0; i < 5; ++i) {
+    const int bn = cand[i];
+    const long long c = static_cast<long long>((N + bn - 1) / bn) * bn * cost[i];
+    if (c < best_cost) {
+      best_cost = c;
       best = bn;
     }
   }
