@@ -364,39 +364,54 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
   __shared__ __align__(16) float sbc[DS_SEQ][2 * N];      // [B | C] of each sequence
   __shared__ __align__(16) float sA2[DS_CH][N];
   __shared__ __align__(8) float2 sdu[DS_SEQ][DS_CH];      // (delta, delta * u)
+  __shared__ float sbias[DS_CH], sD[DS_CH];                // dt_bias and D of the block's channels
   __shared__ __align__(16) __half su[DS_SEQ][DS_CH];      // u and z of the block's (sequence, channel) tile
   __shared__ __align__(16) __half sz[DS_SEQ][DS_CH];
   const int c0 = blockIdx.x * DS_CH, b0 = blockIdx.y * DS_SEQ;
   const int tid = threadIdx.x;
   const int KP = (R + 15) / 16 * 16;  // padded dt rank
-  // W_dt rows: 8 threads per row, 4 values per 8-byte load
+  // W_dt rows: 8 threads per row, 4 values per 8-byte load; every load of a
+  // thread is issued before the first is used (one round trip, not four)
   {
+    constexpr int NK = DS_RMAX / 4 / 8;
     const int row = tid >> 3, l8 = tid & 7;  // 32 rows
     const int c = c0 + row;
     const bool vec = (reinterpret_cast<uintptr_t>(W_dt) & 7) == 0 && (R & 3) == 0;
-    for (int k4 = l8; k4 < KP / 4; k4 += 8) {
-      const int k = 4 * k4;
-      float f[4] = {0.f, 0.f, 0.f, 0.f};
-      if (c < di) {
+    uint2 raw[NK];
+#pragma unroll
+    for (int i = 0; i < NK; ++i) {
+      const int k = 4 * (l8 + 8 * i);
+      raw[i] = make_uint2(0u, 0u);
+      if (c < di && k < KP) {
         const __nv_bfloat16* src = W_dt + static_cast<long long>(c) * R + k;
         if (vec && k + 4 <= R) {
-          const uint2 v = *reinterpret_cast<const uint2*>(src);
-          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-          f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+          raw[i] = *reinterpret_cast<const uint2*>(src);
         } else {
+          __nv_bfloat16 e4[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (k + e < R) f[e] = __bfloat162float(src[e]);
+          for (int e = 0; e < 4; ++e) e4[e] = k + e < R ? src[e] : __float2bfloat16_rn(0.f);
+          raw[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&e4[0]), *reinterpret_cast<const uint32_t*>(&e4[2]));
         }
       }
-      *reinterpret_cast<uint2*>(&sW[row][k]) = make_uint2(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]));
+    }
+#pragma unroll
+    for (int i = 0; i < NK; ++i) {
+      const int k = 4 * (l8 + 8 * i);
+      if (k < KP) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[i].y));
+        *reinterpret_cast<uint2*>(&sW[row][k]) = make_uint2(pack_half2(a.x, a.y), pack_half2(b.x, b.y));
+      }
     }
   }
   for (int idx = tid; idx < DS_CH * N; idx += DS_THREADS) {
     const int cc = idx / N;
     sA2[cc][idx % N] = (c0 + cc < di) ? -__expf(A_log[static_cast<long long>(c0) * N + idx]) * 1.4426950408889634f
                                       : 0.f;
+  }
+  if (tid < DS_CH) {
+    sbias[tid] = c0 + tid < di ? dt_bias[c0 + tid] : 0.f;
+    sD[tid] = c0 + tid < di ? D[c0 + tid] : 0.f;
   }
   // everything above reads weights only; the rest reads what earlier kernels wrote
   pdl_wait();
@@ -413,22 +428,36 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
                 ? reinterpret_cast<const float4*>(state + (static_cast<long long>(b) * di + c) * N)[q]
                 : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  // dt rows: 16 threads per row (the padding columns past R are zeroed, never read)
+  // dt rows: 16 threads per row, all loads issued first (the padding columns
+  // past R are zeroed, never read); dt rounds to fp16 as in prefill
   {
+    constexpr int NK = DS_RMAX / 4 / 16;
     const int row = tid >> 4, l16 = tid & 15;
     const int b = b0 + row;
-    for (int k4 = l16; k4 < KP / 4; k4 += 16) {
-      const int k = 4 * k4;
-      uint2 v = make_uint2(0u, 0u);
-      if (b < B) {
-        const float* src = xp + b * ld_xp + k;
-        __half hh[4];
+    const bool vec = ((reinterpret_cast<uintptr_t>(xp) | static_cast<uintptr_t>(ld_xp * 4)) & 15) == 0;
+    float4 raw[NK];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) hh[e] = __float2half_rn((k + e < R) ? src[e] : 0.f);  // dt rounds to fp16 as in prefill
-        v.x = *reinterpret_cast<const uint32_t*>(&hh[0]);
-        v.y = *reinterpret_cast<const uint32_t*>(&hh[2]);
+    for (int i = 0; i < NK; ++i) {
+      const int k = 4 * (l16 + 16 * i);
+      raw[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (b < B && k < KP) {
+        const float* src = xp + b * ld_xp + k;
+        if (vec && k + 4 <= R) {
+          raw[i] = *reinterpret_cast<const float4*>(src);
+        } else {
+          raw[i].x = k < R ? src[0] : 0.f;
+          raw[i].y = k + 1 < R ? src[1] : 0.f;
+          raw[i].z = k + 2 < R ? src[2] : 0.f;
+          raw[i].w = k + 3 < R ? src[3] : 0.f;
+        }
       }
-      *reinterpret_cast<uint2*>(&sdt[row][k]) = v;
+    }
+#pragma unroll
+    for (int i = 0; i < NK; ++i) {
+      const int k = 4 * (l16 + 16 * i);
+      if (k < KP)
+        *reinterpret_cast<uint2*>(&sdt[row][k]) =
+            make_uint2(pack_half2(raw[i].x, raw[i].y), pack_half2(raw[i].z, raw[i].w));
     }
   }
   for (int idx = tid; idx < DS_SEQ * 2 * N; idx += DS_THREADS) {
@@ -474,7 +503,7 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
       const int b = b0 + s, c = c0 + cl;
       float dt = 0.f, uu = 0.f;
       if (b < B && c < di) {
-        dt = softplus_fast(acc[e] + dt_bias[c]);
+        dt = softplus_fast(acc[e] + sbias[cl]);
         uu = __half2float(su[s][cl]);
       }
       sdu[s][cl] = make_float2(dt, dt * uu);
@@ -488,7 +517,7 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
   float4* hp = reinterpret_cast<float4*>(state + (static_cast<long long>(b0 + s_first) * di + c) * N) + q;
   const long long hstep = static_cast<long long>(DS_THREADS / 4 / DS_CH) * di * N / 4;  // float4 per step of i
   const float4 a = *reinterpret_cast<const float4*>(&sA2[cl][4 * q]);
-  const float Dc = c < di ? D[c] : 0.f;
+  const float Dc = sD[cl];
 #pragma unroll
   for (int i = 0; i < NJ; ++i, hp += hstep) {
     const int s = s_first + i * (DS_THREADS / 4 / DS_CH);
