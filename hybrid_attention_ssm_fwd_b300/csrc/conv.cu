@@ -14,8 +14,10 @@
 // with zeros: that is the causal zero padding, and no row of the previous
 // sequence is ever read.  When a history `tail` is given (the meta rows
 // processed once for the whole batch), its K-1 rows replace that zero
-// padding in shared memory.  Each thread then computes 4 rows x 8 channels
-// from shared memory and writes 16-byte vectors of u.  Every wait is bounded.
+// padding in shared memory.  Each thread then computes 8 rows x 4 channels
+// from shared memory and writes 8-byte vectors of u (a warp covers 256
+// contiguous bytes of a row); at 64 registers a thread, four blocks fit on an
+// SM.  Every wait is bounded.
 #include "simt.cuh"
 
 namespace hy {
@@ -24,8 +26,9 @@ namespace {
 constexpr int CV_TT = 64;       // rows per tile
 constexpr int CV_CW = 128;      // channels per tile (256-byte rows)
 constexpr int CV_S = 3;         // ring stages
-constexpr int CV_THREADS = 256; // 16 channel groups x 16 row groups
-constexpr int CV_RPT = CV_TT / (CV_THREADS / (CV_CW / 8));  // rows per thread = 4
+constexpr int CV_VEC = 4;       // channels per thread (one 8-byte vector)
+constexpr int CV_THREADS = 256; // 32 channel groups x 8 row groups
+constexpr int CV_RPT = CV_TT / (CV_THREADS / (CV_CW / CV_VEC));  // rows per thread = 8
 constexpr float kCvLog2e = 1.4426950408889634f;
 
 template <int K>
@@ -36,7 +39,7 @@ struct ConvCfg {
 };
 
 template <int K>
-__global__ void __launch_bounds__(CV_THREADS, 2)
+__global__ void __launch_bounds__(CV_THREADS, 4)
     conv_tma_kernel(const __grid_constant__ CUtensorMap tmX, __half* __restrict__ u, long long ld_u, int B, int L,
                     int di, const float* __restrict__ w, const float* __restrict__ bias,
                     const float* __restrict__ tail, int32_t* status, uint64_t wait_ns) {
@@ -45,7 +48,7 @@ __global__ void __launch_bounds__(CV_THREADS, 2)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CV_S * Cfg::STAGE);
   __shared__ int abort_flag;
   const int tid = threadIdx.x;
-  const int cg = tid % (CV_CW / 8), rg = tid / (CV_CW / 8);
+  const int cg = tid % (CV_CW / CV_VEC), rg = tid / (CV_CW / CV_VEC);
   // block -> (channel tile ct, slot j); slot j walks row tiles j, j + per_ct, ...
   const int n_ct = (di + CV_CW - 1) / CV_CW, n_tt = (L + CV_TT - 1) / CV_TT;
   const int per_ct = gridDim.x / n_ct;
@@ -75,10 +78,10 @@ __global__ void __launch_bounds__(CV_THREADS, 2)
       }
     }
   }
-  const int c0 = ct * CV_CW + cg * 8;
-  float wt[8][K], bs[8];
+  const int c0 = ct * CV_CW + cg * CV_VEC;
+  float wt[CV_VEC][K], bs[CV_VEC];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
+  for (int e = 0; e < CV_VEC; ++e) {
     bs[e] = c0 < di ? __ldg(bias + c0 + e) : 0.f;
 #pragma unroll
     for (int j = 0; j < K; ++j) wt[e][j] = c0 < di ? __ldg(w + (c0 + e) * K + j) : 0.f;
@@ -100,15 +103,15 @@ __global__ void __launch_bounds__(CV_THREADS, 2)
       __syncthreads();
     }
     if (c0 < di) {
-      const uint8_t* st = smem + s * Cfg::STAGE + cg * 16;
+      const uint8_t* st = smem + s * Cfg::STAGE + cg * (CV_VEC * 2);
       const int r0 = rg * CV_RPT;  // first output row of this thread within the tile
-      float win[K][8];             // win[j] = x row (output row - K + 1 + j)
+      float win[K][CV_VEC];        // win[j] = x row (output row - K + 1 + j)
 #pragma unroll
       for (int j = 0; j < K - 1; ++j) {
-        const uint4 q = *reinterpret_cast<const uint4*>(st + (r0 + j) * (CV_CW * 2));
+        const uint2 q = *reinterpret_cast<const uint2*>(st + (r0 + j) * (CV_CW * 2));
         const __half2* hq = reinterpret_cast<const __half2*>(&q);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < CV_VEC / 2; ++e) {
           const float2 f = __half22float2(hq[e]);
           win[j][2 * e] = f.x;
           win[j][2 * e + 1] = f.y;
@@ -117,17 +120,17 @@ __global__ void __launch_bounds__(CV_THREADS, 2)
       const long long row_base = static_cast<long long>(b) * L + tt * CV_TT;
 #pragma unroll
       for (int r = 0; r < CV_RPT; ++r) {
-        const uint4 q = *reinterpret_cast<const uint4*>(st + (r0 + r + K - 1) * (CV_CW * 2));
+        const uint2 q = *reinterpret_cast<const uint2*>(st + (r0 + r + K - 1) * (CV_CW * 2));
         const __half2* hq = reinterpret_cast<const __half2*>(&q);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < CV_VEC / 2; ++e) {
           const float2 f = __half22float2(hq[e]);
           win[K - 1][2 * e] = f.x;
           win[K - 1][2 * e + 1] = f.y;
         }
-        float o[8];
+        float o[CV_VEC];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < CV_VEC; ++e) {
           float acc = bs[e];
 #pragma unroll
           for (int j = 0; j < K; ++j) acc = fmaf(wt[e][j], win[j][e], acc);
@@ -136,12 +139,11 @@ __global__ void __launch_bounds__(CV_THREADS, 2)
 #pragma unroll
         for (int j = 0; j + 1 < K; ++j)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) win[j][e] = win[j + 1][e];
+          for (int e = 0; e < CV_VEC; ++e) win[j][e] = win[j + 1][e];
         const int t = tt * CV_TT + r0 + r;
         if (t < L)
-          *reinterpret_cast<uint4*>(u + (row_base + r0 + r) * ld_u + c0) =
-              make_uint4(pack_half2(o[0], o[1]), pack_half2(o[2], o[3]), pack_half2(o[4], o[5]),
-                         pack_half2(o[6], o[7]));
+          *reinterpret_cast<uint2*>(u + (row_base + r0 + r) * ld_u + c0) =
+              make_uint2(pack_half2(o[0], o[1]), pack_half2(o[2], o[3]));
       }
     }
     __syncthreads();  // every thread is done with stage s
@@ -167,10 +169,10 @@ hymba_status launch_conv(const CUtensorMap& m, __half* u, long long ld_u, int B,
   auto kern = conv_tma_kernel<K>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
-  // every channel tile gets the same number of blocks (about two per SM in all)
+  // every channel tile gets the same number of blocks (about four per SM in all)
   const int n_ct = (di + CV_CW - 1) / CV_CW;
   const long long n_rt = static_cast<long long>(B) * ((L + CV_TT - 1) / CV_TT);
-  const int per_ct = static_cast<int>(std::max(1LL, std::min(n_rt, (2LL * num_sms + n_ct - 1) / n_ct)));
+  const int per_ct = static_cast<int>(std::max(1LL, std::min(n_rt, (4LL * num_sms + n_ct - 1) / n_ct)));
   const int grid = n_ct * per_ct;
   kern<<<grid, CV_THREADS, Cfg::SMEM, st>>>(m, u, ld_u, B, L, di, w, bias, tail, status, wait_ns);
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
