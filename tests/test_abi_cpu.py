@@ -203,3 +203,20 @@ def test_fusion_flag_values():
     rc = hb.lib().hymba_layer_fwd(ctypes.byref(d), ctypes.byref(w), 0x200000, 0x300000, None, None, None,
                                   ctypes.c_void_p(0x100000), 1 << 40, None, None)
     assert rc == hb.HYMBA_ERR_INVALID
+
+
+def test_block_weight_interleave_layout():
+    """W_gu rows 2j / 2j+1 hold W_gate row j / W_up row j, as the header
+    documents for hymba_block_weights (checked on the host, no GPU)."""
+    import numpy as np
+    import torch
+    from hybrid_attention_ssm_fwd_b300 import layer as hl
+    s = synth.tiny_f32(B=1, T=8, M=0)
+    _, blocks = synth.make_block_inputs(s, 24, 0)
+    pb = blocks[0]
+    dev = hl.block_params_to_device(pb, s, device="cpu")
+    gu = dev["W_gu"].numpy()
+    assert gu.shape == (48, s.d)
+    np.testing.assert_array_equal(gu[0::2], pb["W_gate"])
+    np.testing.assert_array_equal(gu[1::2], pb["W_up"])
+    assert dev["W_down"].shape == (s.d, 24) and dev["norm1"].dtype == torch.float32
