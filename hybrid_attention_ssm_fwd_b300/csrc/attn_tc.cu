@@ -150,6 +150,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKm,
                    const __grid_constant__ CUtensorMap tmVm, const __grid_constant__ AttnParams p) {
   using Cfg = AttnCfg<DV>;
+  pdl_wait();  // nothing before: the preceding kernel may still hold this SM's tensor memory
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
@@ -440,7 +442,8 @@ hymba_status launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMa
   auto kern = attn_tc_kernel<DV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<DV>::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
-  kern<<<grid, NTHREADS, AttnCfg<DV>::SMEM, st>>>(q, k, v, km, vm, p);
+  if (launch_pdl(kern, dim3(grid), dim3(NTHREADS), AttnCfg<DV>::SMEM, st, q, k, v, km, vm, p) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 

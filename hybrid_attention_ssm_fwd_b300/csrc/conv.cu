@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(CV_THREADS, 4)
                     int di, const float* __restrict__ w, const float* __restrict__ bias,
                     const float* __restrict__ tail, int32_t* status, uint64_t wait_ns) {
   using Cfg = ConvCfg<K>;
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + CV_S * Cfg::STAGE);
   __shared__ int abort_flag;
@@ -174,7 +176,9 @@ hymba_status launch_conv(const CUtensorMap& m, __half* u, long long ld_u, int B,
   const long long n_rt = static_cast<long long>(B) * ((L + CV_TT - 1) / CV_TT);
   const int per_ct = static_cast<int>(std::max(1LL, std::min(n_rt, (4LL * num_sms + n_ct - 1) / n_ct)));
   const int grid = n_ct * per_ct;
-  kern<<<grid, CV_THREADS, Cfg::SMEM, st>>>(m, u, ld_u, B, L, di, w, bias, tail, status, wait_ns);
+  if (launch_pdl(kern, dim3(grid), dim3(CV_THREADS), Cfg::SMEM, st, m, u, ld_u, B, L, di, w, bias, tail, status,
+                 wait_ns) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 

@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
                 const ScanArgs a) {
   using Cfg = ScanCfg<KS, TPC, CH, CPT>;
   constexpr int N = SC_N;
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
@@ -477,7 +479,8 @@ hymba_status launch_scan(int B, int L, int di, const CUtensorMap& mX, const __ha
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
   dim3 grid(di / CH, B);
-  kern<<<grid, Cfg::NT, Cfg::SMEM, st>>>(mX, mU, mZ, mBC, args);
+  if (launch_pdl(kern, grid, dim3(Cfg::NT), Cfg::SMEM, st, mX, mU, mZ, mBC, args) != cudaSuccess)
+    return HYMBA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 
