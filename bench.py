@@ -188,7 +188,7 @@ def run_ours(args, rank, world, local_rank):
     if args.only_decode:
         return {"decode": run_decode(args, torch, hb, hl, dev, torch.cuda.current_stream(dev), peaks, peak_src)}
     s = synth.hymba15b_swa(rope_theta=10000.0, B=args.batch)
-    p = synth.make_layer_inputs(s, 1 + rank)
+    p = synth.make_layer_inputs(s, rank_seed(rank))
     params = hl.params_to_device(p, s, dev)
     layer = hl.HymbaLayer(s, params)
     X = hl.tokens_to_device(p["Xt"], s, dev)
@@ -231,13 +231,7 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {layer.check_status()} in the timed region")
     stage_ms = {name: statistics.mean(ev[k].elapsed_time(ev[k + 1]) for ev in ev_sets)
                 for k, name in enumerate(STAGES)}
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    tokens = s.B * s.T
-    value = tokens * world / (ms_max / 1e3)
+    ms_max, value = job_throughput(ms, s.B * s.T, world, dev)
 
     fl = layer_flops(s)
     total_flops = fl["in_proj"] + fl["attention"] + fl["x_proj"] + fl["dt_proj"] + fl["out_proj"]
@@ -288,6 +282,25 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
     return out
+
+
+def job_throughput(ms_local: float, tokens_per_rank: int, world: int, device):
+    """Whole-job throughput of a data-parallel step: every rank processes its
+    own tokens_per_rank (weak scaling) and the slowest rank sets the pace, so
+    the job's step time is the max over ranks.  Returns (ms_max, tokens/s)."""
+    ms_max = float(ms_local)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_max], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    return ms_max, tokens_per_rank * world / (ms_max / 1e3)
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own batch of the workload (seeded by its rank)."""
+    return 1 + rank
 
 
 def ctypes_array(events):
