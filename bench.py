@@ -16,8 +16,8 @@ Multi-GPU (torchrun, one process per GPU): every rank runs its own batch
 (weak scaling, no collective on the data path); the slowest rank's time is
 used and `value` counts the tokens of all ranks.
 
---impl reference times the float64 CPU oracle (the reference arm of this
-build) on the host on bounded samples of the same workload.
+--impl reference times the float64 CPU oracle (there is no other reference
+implementation) on the host on bounded samples of the same workload.
 """
 from __future__ import annotations
 

@@ -5,7 +5,7 @@ CPU-baseline leg of ``bench.py`` may import this module.  The product (the CUDA
 library and its binding) never calls it, and it shares no code with it.
 
 Source: "Hymba: A Hybrid-head Architecture for Small Language Models" (Dong et
-al., 2024), as summarised on the pages this build follows:
+al., 2024), as summarised on the web pages about it:
 
 * section 2.1, eq. (3): one shared input projection yields the attention Q/K/V,
   the SSM input and the output gate; each branch is normalised and scaled by a
