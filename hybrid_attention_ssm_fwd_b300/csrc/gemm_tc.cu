@@ -26,6 +26,8 @@
 // (each commits to both CTAs' "empty" barrier).  Every wait is bounded.
 #include "gemm_tc.cuh"
 
+#include <atomic>
+
 namespace hy {
 namespace {
 
@@ -432,16 +434,25 @@ __global__ void __launch_bounds__(192, 1)
   if (PAIR) cluster_sync();  // no CTA leaves while its peer may still write into its shared memory
 }
 
+// Kernel attributes and occupancy figures belong to one device: the
+// launchers cache them per device ordinal (devices past the table's end are
+// set up on every call).
+constexpr int kMaxDevices = 64;
+
 template <int BN, int EPI, bool PAIR>
 hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, uint32_t idesc, int grid,
                        cudaStream_t st) {
   using Cfg = GemmCfg<BN>;
   auto kern = gemm_tc_kernel<BN, EPI, PAIR>;
-  static bool attr_done = false;  // benign race: idempotent attribute set
-  if (!attr_done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return HYMBA_ERR_CUDA;
+  const bool cached = dev < kMaxDevices;
+  // setting the attribute twice is harmless, so two threads may race here
+  static std::atomic<bool> attr_done[kMaxDevices];
+  if (!cached || !attr_done[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
       return HYMBA_ERR_CUDA;
-    attr_done = true;
+    if (cached) attr_done[dev].store(true, std::memory_order_release);
   }
   if constexpr (!PAIR) {
     if (launch_pdl(kern, dim3(grid), dim3(192), Cfg::SMEM, st, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
@@ -461,12 +472,14 @@ hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmP
     cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
     // persistent: no more clusters than can be resident at once (a GPC with an
     // odd SM count leaves one SM out), so no tile waits for a second wave
-    static int max_clusters = 0;
+    static std::atomic<int> max_clusters_dev[kMaxDevices];
+    int max_clusters = cached ? max_clusters_dev[dev].load(std::memory_order_relaxed) : 0;
     if (max_clusters == 0) {
       cfg.gridDim = dim3(2 * std::max(1, grid / 2), 1, 1);
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return HYMBA_ERR_CUDA;
       max_clusters = n;
+      if (cached) max_clusters_dev[dev].store(n, std::memory_order_relaxed);
     }
     const int clusters = std::max(1, std::min(std::min(grid / 2, max_clusters), p.total_pairs));
     cfg.gridDim = dim3(2 * clusters, 1, 1);

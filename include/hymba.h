@@ -26,9 +26,9 @@
  *    device; the library never dereferences them on the host.
  *  - The caller owns every buffer.  The library allocates no memory, keeps no
  *    pointer after a call returns and keeps no state between calls apart
- *    from one-time kernel attributes and occupancy figures it caches (and the
- *    static scratch of hymba_layer_decode_static); calls on different
- *    streams are independent.
+ *    from kernel attributes and occupancy figures it caches per device (and
+ *    the per-device static scratch of hymba_layer_decode_static); calls on
+ *    different streams and different devices are independent.
  *  - Calls are stream-ordered and asynchronous: inputs must stay valid and
  *    outputs must not be read until `stream` reaches the call.  `stream` is a
  *    cudaStream_t passed as void* (NULL = the legacy default stream).
