@@ -287,6 +287,38 @@ def layer_fwd(p: Dict[str, np.ndarray], Xt: np.ndarray, s,
     return out
 
 
+def layer_fwd_rows(p: Dict[str, np.ndarray], Xt: np.ndarray, s, rows,
+                   kv_in: Optional[Tuple[np.ndarray, np.ndarray]] = None) -> np.ndarray:
+    """Y at the query rows ``rows`` only (indices into X~'s L rows), for
+    sequences too long for the whole-layer oracle.
+
+    The same steps as layer_fwd, eq. (3) of the Hymba page, cut to what these
+    rows depend on: the layer is causal, so only the prefix up to the last
+    requested row is projected and scanned, and attention runs for the
+    requested query rows alone.  Returns [B, len(rows), d].
+    """
+    Xt = np.asarray(Xt, F)
+    rows = np.asarray(rows)
+    n = int(rows.max()) + 1
+    Xp = Xt[:, :n]
+    proj = Xp @ np.asarray(p["W_in"], F).T
+    parts = split_projection(proj, s)
+    positions = np.arange(n)
+    Q = parts["Q"]
+    if s.rope_theta > 0:
+        Q = rope(Q, positions, s.rope_theta)
+    if s.kv_shared:
+        assert kv_in is not None
+        K, V = (np.asarray(a, F)[:, :n] for a in kv_in)
+    else:
+        K, V = parts["K"], parts["V"]
+        if s.rope_theta > 0:
+            K = rope(K, positions, s.rope_theta)
+    att = attention(Q, K, V, s.M, s.window, rows=rows)
+    g, _ = ssm_branch(parts["x"], parts["z"], p, s)
+    return fuse_and_project(att, g[:, rows], p, s, Xt[:, rows])
+
+
 def emit_cache(K, V, x, h, s, cap: int) -> Dict[str, np.ndarray]:
     """Decode state after a prefill of T real tokens (reading 8)."""
     B = K.shape[0]

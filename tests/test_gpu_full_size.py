@@ -1,0 +1,111 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times (same shapes, seeds and calls), on outputs the float64 oracle
+can compute at these sizes.
+
+The layer is causal and its sequences are independent, so a sampled row of a
+sampled sequence needs only that sequence's prefix: ``layer_fwd_rows`` projects
+and scans the prefix and attends for the sampled query rows alone.  The rows
+sampled are the meta rows' edge, the first real row, both sides of the
+sliding-window edge (meta always visible; "Hymba: A Hybrid-head Architecture
+for Small Language Models", sections 2.2 and 2.3), a middle row and the last
+rows.  Sequence 0 is checked on its early rows, the batch's last sequence on
+all of them, so both ends of the batch and of the sequence are covered.
+
+* Hymba-1.5B-shaped SWA layer: batch 8 x (8192 + 128 meta), window 1024.
+* The same shapes as a global-attention layer: batch 2 x (8192 + 128).
+* Decode step, batch 128, 8192 tokens of history in a 1024-slot ring plus
+  the meta K/V: y, the SSM state and the ring slot written for three
+  sequences (first, middle, last); pos of all.
+* 300M-ablation-shaped 4-layer stack (global, then three SWA layers; layers
+  1 -> 2 share K/V), batch 32 x (2048 + 128): every row of the last sequence
+  after every layer, each layer fed the oracle's stream for that sequence
+  (the tolerance is per output; chained, the residual stream would carry
+  the sum of the layers' errors, which stays within the relative bound but
+  not the absolute one by layer 2).
+"""
+import numpy as np
+import pytest
+import torch
+
+from hybrid_attention_ssm_fwd_b300 import layer as hl
+from hybrid_attention_ssm_fwd_b300 import synth
+from oracle import hymba_ref as ref
+from tests.gpu_util import assert_bf16_close, cache_np, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(s):
+    M, W, L = s.M, s.window if s.window > 0 else 1024, s.L
+    return np.array(sorted({0, M - 1, M, M + 1, M + W - 1, M + W, M + W + 1, L // 2 + 3, L - 2, L - 1}))
+
+
+@pytest.mark.parametrize("make,seed,what", [
+    (lambda: synth.hymba15b_swa(rope_theta=10000.0), 1, "SWA layer, batch 8 x 8K"),
+    (lambda: synth.hymba15b_global(rope_theta=10000.0), 2, "global layer, batch 2 x 8K"),
+])
+def test_full_size_prefill_sampled_rows(make, seed, what):
+    s = make()
+    p = synth.make_layer_inputs(s, seed)
+    y, _, _ = run_prefill(s, p)
+    assert np.all(np.isfinite(y)), f"{what}: non-finite output"
+    rows = _rows(s)
+    early = rows[rows <= s.M + 1025]
+    last = s.B - 1
+    assert_bf16_close(y[0, early], ref.layer_fwd_rows(p, p["Xt"][:1], s, early)[0], f"{what}, sequence 0")
+    assert_bf16_close(y[last, rows], ref.layer_fwd_rows(p, p["Xt"][last:], s, rows)[0], f"{what}, sequence {last}")
+
+
+def test_full_size_decode_batch128_sampled_sequences():
+    s = synth.hymba15b_decode(rope_theta=10000.0)
+    cap = s.window
+    inp = synth.make_decode_inputs(s, 4, cap=cap, pos=8192)
+    cache = hl.cache_to_device(inp, s)
+    layer = hl.HymbaLayer(s, hl.params_to_device(inp, s), decode=True)
+    y = layer.decode(hl.tokens_to_device(inp["x_new"], s), cache, cap).cpu().numpy()
+    torch.cuda.synchronize()
+    assert layer.check_status() == 0
+    assert np.all(np.isfinite(y))
+    idx = [0, s.B // 2 - 1, s.B - 1]
+    per_seq = ("k_ring", "v_ring", "ssm_state", "conv_state", "pos")
+    sub = {k: inp[k][idx] for k in per_seq}
+    sub.update(k_meta=inp["k_meta"], v_meta=inp["v_meta"])
+    r = ref.layer_decode(inp, inp["x_new"][idx], sub, synth.with_(s, B=len(idx)))
+    assert_bf16_close(y[idx], r["y"], "decode batch 128, y")
+    c = cache_np(cache)
+    assert_bf16_close(c["ssm_state"][idx], r["cache"]["ssm_state"], "decode batch 128, ssm_state")
+    slot = 8192 % cap
+    assert_bf16_close(c["k_ring"][idx, slot], r["cache"]["k_ring"][:, slot], "decode batch 128, k slot")
+    assert_bf16_close(c["v_ring"][idx, slot], r["cache"]["v_ring"][:, slot], "decode batch 128, v slot")
+    assert np.all(c["pos"] == 8193)
+
+
+def test_full_size_stack_each_layer_last_sequence():
+    """Each layer of the stack on its own: before layer i the last sequence's
+    stream is set to the oracle's stream entering layer i (the other 31 keep
+    the GPU's), so the comparison after layer i measures that layer's error,
+    not the sum the residual stream carries from the layers before it.  The
+    K/V that layer 2 reuses come from the GPU's layer 1 on that same input."""
+    shapes = [synth.with_(s, rope_theta=10000.0) for s in synth.ablation300m_stack()]
+    tok, layers = synth.make_stack_inputs(shapes, seed=3)
+    b = shapes[0].B - 1
+    out = ref.stack_fwd(layers, tok["Xt"][b:b + 1], [synth.with_(s, B=1) for s in shapes])
+    y = torch.from_numpy(tok["Xt"].astype(np.float32)).cuda()
+    kv = None
+    for i, (p, s) in enumerate(zip(layers, shapes)):
+        if i > 0:
+            y[b] = torch.from_numpy(out["Y"][i - 1][0].astype(np.float32)).cuda()
+        X = y.to(torch.bfloat16)
+        layer = hl.HymbaLayer(s, hl.params_to_device(p, s), residual_mode=2)
+        kv_out = None
+        if i == 1:
+            kd = hl.kv_dtype(s)
+            kv_out = (torch.empty(s.B, s.L, s.Hkv, s.dh, device="cuda", dtype=kd),
+                      torch.empty(s.B, s.L, s.Hkv, s.dv, device="cuda", dtype=kd))
+        layer.forward(X, y=y, kv_in=kv if s.kv_shared else None, kv_out=kv_out)
+        torch.cuda.synchronize()
+        assert layer.check_status() == 0
+        assert_bf16_close(y[b].cpu().numpy(), out["Y"][i][0], f"stack batch 32 x 2K, layer {i}, sequence {b}")
+        if kv_out is not None:
+            kv = kv_out
+        del layer, X

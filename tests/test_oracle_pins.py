@@ -348,6 +348,46 @@ def test_layer_full_tiny_config_matches_loop_oracle():
     np.testing.assert_allclose(y, yb, rtol=1e-12, atol=1e-12 * np.abs(yb).max())
 
 
+@pytest.mark.parametrize("kw", [dict(), dict(window=0), dict(window=5, rope_theta=10000.0), dict(residual=True),
+                                dict(fusion="concat"), dict(B=2, T=20)])
+def test_layer_rows_matches_loop_oracle(kw):
+    """The row-sampled oracle (used at sizes the whole-layer oracle cannot
+    take) against the loop-only oracle's whole layer (the vectorised one for
+    the concatenation fusion): meta rows, the first
+    real row, rows on both sides of the window edge, the last row."""
+    s = tiny(**kw)
+    if s.T > 24:
+        s = synth.with_(s, T=24)
+    p = inputs(s, seed=5)
+    if s.fusion == "concat":  # the loop-only oracle has the sum fusion alone
+        yb = ref.layer_fwd(p, p["Xt"], s)["Y"]
+    else:
+        yb = np.array(brute.layer_fwd(p, p["Xt"], s)["Y"])
+    rows = np.array(sorted({0, s.M - 1, s.M, s.M + 4, s.M + 5, s.M + 6, s.L - 2, s.L - 1}))
+    y = ref.layer_fwd_rows(p, p["Xt"], s, rows)
+    np.testing.assert_allclose(y, yb[:, rows], rtol=1e-12, atol=1e-12 * np.abs(yb).max())
+    # a prefix cut: rows that stop short of the end need only their prefix
+    early = rows[rows < s.M + 5]
+    y2 = ref.layer_fwd_rows(p, p["Xt"], s, early)
+    np.testing.assert_allclose(y2, yb[:, early], rtol=1e-12, atol=1e-12 * np.abs(yb).max())
+
+
+def test_layer_rows_kv_shared_matches_whole_layer():
+    s = synth.with_(tiny(rope_theta=10000.0, T=20), kv_shared=True)
+    p = inputs(synth.with_(s, kv_shared=False), seed=6)
+    qn = s.Hq * s.dh
+    kvn = s.Hkv * (s.dh + s.dv)
+    W = p["W_in"].astype(F)
+    cons = dict(p)
+    cons["W_in"] = np.concatenate([W[:qn], W[qn + kvn:]], 0)
+    rng = np.random.default_rng(6)
+    kv = (rng.standard_normal((s.B, s.L, s.Hkv, s.dh)), rng.standard_normal((s.B, s.L, s.Hkv, s.dv)))
+    y = ref.layer_fwd(cons, p["Xt"], s, kv_in=kv)["Y"]
+    rows = np.array([1, s.M, s.L - 1])
+    np.testing.assert_allclose(ref.layer_fwd_rows(cons, p["Xt"], s, rows, kv_in=kv), y[:, rows], rtol=1e-12,
+                               atol=1e-12 * np.abs(y).max())
+
+
 def test_window_at_least_L_equals_global():
     s = tiny()
     p = inputs(s)
