@@ -58,6 +58,11 @@ def load_peaks():
 EX2_PER_CLK_PER_SM = 32
 SM_COUNT = 148
 SM_MAX_GHZ = 2.032
+# fp32 lanes of one SM (FMA / FMUL per clock): the scan's other ALU bound.
+# Per state and row it needs 4 fp32 operations: delta*A (the ex2 argument),
+# decay*h + (delta*u)*B (a multiply and an FMA) and the C.h accumulation (FMA).
+FP32_PER_CLK_PER_SM = 128
+SCAN_FP32_OPS_PER_STATE = 4
 
 
 def stage_work(s) -> dict:
@@ -75,6 +80,7 @@ def stage_work(s) -> dict:
         "conv": ("hbm", rows * s.di * (2 + 2), "B"),                       # x in, u out (fp16)
         "fuse_norm": ("hbm", rows * s.di * (2 + 2 + 2), "B"),              # att, g in; s out
         "scan": ("alu", rows * s.di * s.N, "ex2"),                         # exp(delta A) per state
+        "scan_fma": ("fma", rows * s.di * s.N * SCAN_FP32_OPS_PER_STATE, "fp32 op"),
         "scan_hbm": ("hbm", rows * (s.di * (2 + 2 + 2) + Rp * 2 + 2 * s.N * 4), "B"),  # u, z, g; dt, B|C
     }
 
@@ -86,10 +92,26 @@ def stage_roofline(name, work, ms, peaks):
         achieved, peak, u = amount / t / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     elif bound == "hbm":
         achieved, peak, u = amount / t / 1e9, peaks["hbm_gbs"], "GB/s"
+    elif bound == "fma":
+        achieved, peak, u = amount / t / 1e12, FP32_PER_CLK_PER_SM * SM_COUNT * SM_MAX_GHZ / 1e3, "Tfp32op/s"
     else:
         achieved, peak, u = amount / t / 1e12, EX2_PER_CLK_PER_SM * SM_COUNT * SM_MAX_GHZ / 1e3, "Tex2/s"
     return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": u,
             "frac": round(achieved / peak, 4), "ms": round(ms, 4)}
+
+
+def stage_rooflines(s, stage_ms: dict, peaks: dict):
+    """Every stage against its own bound, plus the scan against its HBM and
+    fp32-pipe bounds (timed as the one scan stage).  Returns the per-kernel
+    rooflines and the dominant kernel: the longest stage."""
+    work = stage_work(s)
+
+    def stage(k):
+        return "scan" if k.startswith("scan") else k
+
+    kernels = {k: stage_roofline(k, w, stage_ms[stage(k)], peaks) for k, w in work.items()}
+    dom = max((k for k in work if stage(k) == k), key=lambda k: stage_ms[k])
+    return kernels, dom
 
 
 def layer_flops(s) -> dict:
@@ -236,10 +258,7 @@ def run_ours(args, rank, world, local_rank):
     fl = layer_flops(s)
     total_flops = fl["in_proj"] + fl["attention"] + fl["x_proj"] + fl["dt_proj"] + fl["out_proj"]
     peak = peaks["bf16_tflops"]
-    # every stage against its own bound; the dominant kernel is the longest stage
-    work = stage_work(s)
-    kernels = {k: stage_roofline(k, w, stage_ms["scan" if k == "scan_hbm" else k], peaks) for k, w in work.items()}
-    dom = max((k for k in work if k != "scan_hbm"), key=lambda k: stage_ms[k])
+    kernels, dom = stage_rooflines(s, stage_ms, peaks)
     traffic = load_traffic(dom)
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -258,7 +277,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline": dict({"kernel": dom}, **{k: v for k, v in kernels[dom].items() if k != "ms"},
                          traffic=traffic,
                          peak_source={"tensor": f"{peak_src} bf16 (burst)", "hbm": f"{peak_src} HBM copy",
-                                      "alu": "SFU ex2: 32 per clock per SM x 148 SMs x 2.032 GHz"}[
+                                      "alu": "SFU ex2: 32 per clock per SM x 148 SMs x 2.032 GHz",
+                                      "fma": "fp32 lanes: 128 per clock per SM x 148 SMs x 2.032 GHz"}[
                                           kernels[dom]["bound"]]),
         "kernels": kernels,
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
