@@ -156,6 +156,30 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr()
 
 
+def _arg(t, what: str, dtype=None, numel: int = 0) -> int:
+    """Device address of a tensor argument, after the checks the C side cannot
+    make on a bare pointer: present, of the expected dtype, contiguous, with
+    at least ``numel`` elements, on a CUDA device."""
+    if t is None:
+        raise ValueError(f"{what}: a tensor is required")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{what}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{what}: {t.numel()} elements, needs at least {numel}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{what}: must be on a CUDA device, not {t.device}")
+    return t.data_ptr()
+
+
+def _io_dtypes(desc):
+    """(activation input dtype, output dtype) of a layer call: x in the
+    descriptor's dtype (bf16 or fp32), y always fp32."""
+    import torch
+    return (torch.bfloat16 if desc.dtype == HYMBA_BF16 else torch.float32), torch.float32
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         import torch
@@ -198,11 +222,14 @@ def hymba_layer_fwd(desc: LayerDesc, weights: LayerWeights, x, y, ws, cache_out:
                     kv_in: Optional[KV] = None, kv_out: Optional[KV] = None, status=None, stream=None,
                     check: bool = True) -> int:
     """Prefill forward through the C ABI (see include/hymba.h)."""
-    rc = lib().hymba_layer_fwd(ctypes.byref(desc), ctypes.byref(weights), _ptr(x), _ptr(y),
+    xd, yd = _io_dtypes(desc)
+    n = desc.batch * (desc.n_tokens + desc.n_meta) * desc.d_model
+    px, py = _arg(x, "hymba_layer_fwd x", xd, n), _arg(y, "hymba_layer_fwd y", yd, n)
+    rc = lib().hymba_layer_fwd(ctypes.byref(desc), ctypes.byref(weights), px, py,
                                ctypes.byref(cache_out) if cache_out is not None else None,
                                ctypes.byref(kv_in) if kv_in is not None else None,
                                ctypes.byref(kv_out) if kv_out is not None else None,
-                               _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+                               _arg(ws, "ws"), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
     return _check(rc, "hymba_layer_fwd") if check else rc
 
 
@@ -211,11 +238,14 @@ def hymba_layer_fwd_events(desc: LayerDesc, weights: LayerWeights, x, y, ws, eve
                            kv_out: Optional[KV] = None, status=None, stream=None, check: bool = True) -> int:
     """hymba_layer_fwd that records per-stage CUDA events (``events`` is a
     ctypes array of cudaEvent_t handles)."""
-    rc = lib().hymba_layer_fwd_events(ctypes.byref(desc), ctypes.byref(weights), _ptr(x), _ptr(y),
+    xd, yd = _io_dtypes(desc)
+    n = desc.batch * (desc.n_tokens + desc.n_meta) * desc.d_model
+    px, py = _arg(x, "hymba_layer_fwd_events x", xd, n), _arg(y, "hymba_layer_fwd_events y", yd, n)
+    rc = lib().hymba_layer_fwd_events(ctypes.byref(desc), ctypes.byref(weights), px, py,
                                       ctypes.byref(cache_out) if cache_out is not None else None,
                                       ctypes.byref(kv_in) if kv_in is not None else None,
                                       ctypes.byref(kv_out) if kv_out is not None else None,
-                                      _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), events, n_events,
+                                      _arg(ws, "ws"), ws.numel() * ws.element_size(), _ptr(status), events, n_events,
                                       _stream(stream))
     return _check(rc, "hymba_layer_fwd_events") if check else rc
 
@@ -232,7 +262,8 @@ def block_fwd_workspace(desc: LayerDesc, d_ff: int) -> int:
 def hymba_block_fwd(desc: LayerDesc, weights: BlockWeights, d_ff: int, x, ws, status=None, stream=None,
                     check: bool = True) -> int:
     """One residual block on the fp32 stream x, in place (see include/hymba.h)."""
-    rc = lib().hymba_block_fwd(ctypes.byref(desc), ctypes.byref(weights), d_ff, _ptr(x), _ptr(ws),
+    px = _arg(x, "hymba_block_fwd x", _io_dtypes(desc)[1], desc.batch * (desc.n_tokens + desc.n_meta) * desc.d_model)
+    rc = lib().hymba_block_fwd(ctypes.byref(desc), ctypes.byref(weights), d_ff, px, _arg(ws, "hymba_block_fwd ws"),
                                ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
     return _check(rc, "hymba_block_fwd") if check else rc
 
@@ -252,9 +283,10 @@ def layer_fwd_meta_workspace(desc: LayerDesc) -> int:
 def hymba_meta_prefill(desc: LayerDesc, weights: LayerWeights, x_meta, meta: Meta, ws, kv_in: Optional[KV] = None,
                        status=None, stream=None, check: bool = True) -> int:
     """The layer over the meta rows alone, once for the batch (see include/hymba.h)."""
-    rc = lib().hymba_meta_prefill(ctypes.byref(desc), ctypes.byref(weights), _ptr(x_meta), ctypes.byref(meta),
+    px = _arg(x_meta, "hymba_meta_prefill x_meta", _io_dtypes(desc)[0], desc.n_meta * desc.d_model)
+    rc = lib().hymba_meta_prefill(ctypes.byref(desc), ctypes.byref(weights), px, ctypes.byref(meta),
                                   ctypes.byref(kv_in) if kv_in is not None else None,
-                                  _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+                                  _arg(ws, "ws"), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
     return _check(rc, "hymba_meta_prefill") if check else rc
 
 
@@ -262,21 +294,27 @@ def hymba_layer_fwd_meta(desc: LayerDesc, weights: LayerWeights, meta: Meta, x, 
                          cache_out: Optional[Cache] = None, kv_in: Optional[KV] = None, kv_out: Optional[KV] = None,
                          status=None, stream=None, check: bool = True) -> int:
     """Prefill of the real tokens from a meta-prefix state (see include/hymba.h)."""
-    rc = lib().hymba_layer_fwd_meta(ctypes.byref(desc), ctypes.byref(weights), ctypes.byref(meta), _ptr(x), _ptr(y),
+    xd, yd = _io_dtypes(desc)
+    n = desc.batch * desc.n_tokens * desc.d_model
+    px, py = _arg(x, "hymba_layer_fwd_meta x", xd, n), _arg(y, "hymba_layer_fwd_meta y", yd, n)
+    rc = lib().hymba_layer_fwd_meta(ctypes.byref(desc), ctypes.byref(weights), ctypes.byref(meta), px, py,
                                     ctypes.byref(cache_out) if cache_out is not None else None,
                                     ctypes.byref(kv_in) if kv_in is not None else None,
                                     ctypes.byref(kv_out) if kv_out is not None else None,
-                                    _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+                                    _arg(ws, "ws"), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
     return _check(rc, "hymba_layer_fwd_meta") if check else rc
 
 
 def hymba_layer_decode(desc: LayerDesc, weights: LayerWeights, x_new, y, cache: Cache, ws,
                        shared_cache: Optional[Cache] = None, status=None, stream=None, check: bool = True) -> int:
     """One decode step through the C ABI (see include/hymba.h)."""
-    rc = lib().hymba_layer_decode(ctypes.byref(desc), ctypes.byref(weights), _ptr(x_new), _ptr(y),
+    xd, yd = _io_dtypes(desc)
+    n = desc.batch * desc.d_model
+    px, py = _arg(x_new, "hymba_layer_decode x_new", xd, n), _arg(y, "hymba_layer_decode y", yd, n)
+    rc = lib().hymba_layer_decode(ctypes.byref(desc), ctypes.byref(weights), px, py,
                                   ctypes.byref(cache),
                                   ctypes.byref(shared_cache) if shared_cache is not None else None,
-                                  _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+                                  _arg(ws, "ws"), ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
     return _check(rc, "hymba_layer_decode") if check else rc
 
 
@@ -284,10 +322,13 @@ def hymba_layer_decode_events(desc: LayerDesc, weights: LayerWeights, x_new, y, 
                               n_events: int, shared_cache: Optional[Cache] = None, status=None, stream=None,
                               check: bool = True) -> int:
     """hymba_layer_decode that records per-stage CUDA events."""
-    rc = lib().hymba_layer_decode_events(ctypes.byref(desc), ctypes.byref(weights), _ptr(x_new), _ptr(y),
+    xd, yd = _io_dtypes(desc)
+    n = desc.batch * desc.d_model
+    px, py = _arg(x_new, "hymba_layer_decode_events x_new", xd, n), _arg(y, "hymba_layer_decode_events y", yd, n)
+    rc = lib().hymba_layer_decode_events(ctypes.byref(desc), ctypes.byref(weights), px, py,
                                          ctypes.byref(cache),
                                          ctypes.byref(shared_cache) if shared_cache is not None else None,
-                                         _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), events, n_events,
+                                         _arg(ws, "ws"), ws.numel() * ws.element_size(), _ptr(status), events, n_events,
                                          _stream(stream))
     return _check(rc, "hymba_layer_decode_events") if check else rc
 
@@ -301,7 +342,10 @@ def hymba_layer_decode_static(desc: LayerDesc, weights: LayerWeights, x_new, y, 
     """hymba_layer_decode with the library's built-in scratch buffer instead of
     a workspace, for callers that cannot allocate device memory (see
     include/hymba.h).  Calls must not overlap on the GPU."""
-    rc = lib().hymba_layer_decode_static(ctypes.byref(desc), ctypes.byref(weights), _ptr(x_new), _ptr(y),
+    xd, yd = _io_dtypes(desc)
+    n = desc.batch * desc.d_model
+    px, py = _arg(x_new, "hymba_layer_decode_static x_new", xd, n), _arg(y, "hymba_layer_decode_static y", yd, n)
+    rc = lib().hymba_layer_decode_static(ctypes.byref(desc), ctypes.byref(weights), px, py,
                                          ctypes.byref(cache),
                                          ctypes.byref(shared_cache) if shared_cache is not None else None,
                                          _ptr(status), _stream(stream))

@@ -220,3 +220,38 @@ def test_block_weight_interleave_layout():
     np.testing.assert_array_equal(gu[0::2], pb["W_gate"])
     np.testing.assert_array_equal(gu[1::2], pb["W_up"])
     assert dev["W_down"].shape == (s.d, 24) and dev["norm1"].dtype == torch.float32
+
+
+def test_binding_checks_tensor_arguments_before_the_call():
+    """The ctypes wrappers check what a bare pointer cannot carry (dtype,
+    contiguity, size, device) and raise before anything reaches the
+    library."""
+    import torch
+    s = synth.hymba15b_swa(B=2, T=64)
+    desc = hb.make_desc(s)
+    w = hb.LayerWeights(*[0x10000 * (i + 1) for i in range(11)])
+    n = s.B * s.L * s.d
+    x = torch.zeros(s.B, s.L, s.d, dtype=torch.bfloat16)
+    y = torch.zeros(s.B, s.L, s.d, dtype=torch.float32)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    cases = [
+        (x.float(), y, "dtype"),                       # fp32 input to a bf16 layer
+        (x.transpose(0, 1), y, "contiguous"),
+        (x.reshape(-1)[: n - 1], y, "elements"),       # one element short
+        (x, y, "CUDA"),                                # right in every way but on the host
+    ]
+    for xx, yy, word in cases:
+        with pytest.raises(ValueError, match=word):
+            hb.hymba_layer_fwd(desc, w, xx, yy, ws)
+    # y is checked the same way (each tensor's own checks run before the next's)
+    with pytest.raises(ValueError, match="dtype"):
+        hb._arg(y.to(torch.bfloat16), "y", hb._io_dtypes(desc)[1], n)
+    with pytest.raises(ValueError, match="required"):
+        hb._arg(None, "y")
+    sd = synth.with_(s, T=1)
+    dd = hb.make_desc(sd)
+    with pytest.raises(ValueError, match="elements"):
+        hb.hymba_layer_decode(dd, w, torch.zeros(sd.B, sd.d - 8, dtype=torch.bfloat16),
+                              torch.zeros(sd.B, sd.d), hb.Cache(), ws)
+    with pytest.raises(ValueError, match="dtype"):
+        hb.hymba_block_fwd(desc, hb.BlockWeights(), 4800, x, ws)
