@@ -59,3 +59,31 @@ def test_row_sampled_oracle_equals_whole_layer(case, data):
     rows = np.array(sorted(data.draw(st.sets(st.integers(0, s.L - 1), min_size=1, max_size=s.L))))
     np.testing.assert_allclose(ref.layer_fwd_rows(p, p["Xt"], s, rows), y[:, rows], rtol=1e-12,
                                atol=1e-12 * max(1.0, np.abs(y).max()))
+
+
+@settings(max_examples=40, deadline=None, suppress_health_check=[HealthCheck.too_slow])
+@given(tiny_layers(), st.integers(1, 5), st.integers(0, 2))
+def test_prefill_then_decode_equals_longer_prefill(case, n, extra_cap):
+    """T0 prefilled tokens with their cache, then n decode steps, reproduce the
+    last n rows of one prefill over T0 + n tokens, and leave the same SSM
+    state and conv tail (ring capacity = window, or a little more; a global
+    layer's cache holds every token)."""
+    s, seed = case
+    T0 = s.T
+    sl = synth.with_(s, T=T0 + n)
+    p = synth.make_layer_inputs(sl, seed)
+    cap = s.window + extra_cap if s.window > 0 else T0 + n
+    s0 = synth.with_(sl, T=T0)
+    cache = ref.layer_fwd(p, p["Xt"][:, : s0.L], s0, cache_cap=cap)["cache"]
+    sd = synth.with_(sl, T=1)
+    ys = []
+    for i in range(n):
+        r = ref.layer_decode(p, p["Xt"][:, s0.L + i], cache, sd)
+        ys.append(r["y"])
+        cache = r["cache"]
+    full = ref.layer_fwd(p, p["Xt"], sl, cache_cap=cap)
+    scale = max(1.0, np.abs(full["Y"]).max())
+    np.testing.assert_allclose(np.stack(ys, 1), full["Y"][:, s.M + T0:], rtol=1e-11, atol=1e-11 * scale)
+    np.testing.assert_allclose(cache["ssm_state"], full["cache"]["ssm_state"], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(cache["conv_state"], full["cache"]["conv_state"], rtol=1e-13, atol=1e-15)
+    assert np.all(cache["pos"] == T0 + n)
