@@ -1,5 +1,8 @@
 // Decode-step kernels: ring-buffer K/V append, attention over meta + ring,
 // conv step from the carried tail, split-K reduction, position advance.
+// One new token per sequence through the layer of eq. 3 ("Hymba: A Hybrid-head Architecture for Small Language Models",
+// section 2.1), with the sliding-window cache and the meta K/V that every
+// later token sees (sections 2.2 and 2.3).
 #include <algorithm>
 
 #include "decode.cuh"

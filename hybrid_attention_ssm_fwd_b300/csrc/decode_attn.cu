@@ -1,6 +1,7 @@
 // Decode-step attention over the meta prefix and the sliding-window ring
-// (section 2.2 window + section 2.3 meta tokens of the Hymba paper) for bf16
-// caches: one new query row per sequence, GQA heads grouped per KV head.
+// ("Hymba: A Hybrid-head Architecture for Small Language Models", section 2.2
+// window and section 2.3 meta tokens) for bf16 caches: one new query row per
+// sequence, GQA heads grouped per KV head.
 //
 // The step is bound by reading the cache (K and V of every visible key once),
 // so the kernel is built to keep HBM busy:

@@ -1,4 +1,7 @@
-// Persistent warp-specialised tcgen05 GEMM for sm_103a.
+// Persistent warp-specialised tcgen05 GEMM for sm_103a: the layer's dense
+// projections -- the shared input projection and W_out of eq. 3
+// ("Hymba: A Hybrid-head Architecture for Small Language Models",
+// section 2.1) and the SSM branch's x_proj -- plus the residual block's MLP.
 //
 //   warp 0      TMA producer: 128x64 A tile + BNx64 B tile per stage (128-byte
 //               swizzle), completion counted on the stage's "full" mbarrier.

@@ -1,5 +1,8 @@
 // Selective scan + gate of the SSM branch on the bf16 path, and the
-// bounded-wait probe.
+// bounded-wait probe.  The SSM heads are M_ssm of the hybrid-head layer
+// ("Hymba: A Hybrid-head Architecture for Small Language Models",
+// section 2.1, eq. 3), running in parallel with the attention heads on the
+// same input projection.
 //
 // Recurrence (per batch b, channel c, state n), run literally in time:
 //     h_t = exp(delta_t * A) * h_{t-1} + (delta_t * u_t) * B_t

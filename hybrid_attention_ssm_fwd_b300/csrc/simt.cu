@@ -1,4 +1,7 @@
-// SIMT kernels of the hybrid-head layer (fp32 path and generic pieces).
+// SIMT kernels of the hybrid-head layer (fp32 path and generic pieces): every
+// stage of eq. 3 ("Hymba: A Hybrid-head Architecture for Small Language Models",
+// section 2.1) in fp32, and on the bf16 path the fused norm / beta / sum
+// that feeds W_out, the cache emission and the block's RMSNorm.
 #include <algorithm>
 #include <type_traits>
 

@@ -157,8 +157,9 @@ typedef struct hymba_cache {
 /* Bytes of scratch memory hymba_layer_fwd needs for `d` (0 on invalid d).  */
 HYMBA_API size_t hymba_layer_fwd_workspace(const hymba_layer_desc* d);
 
-/* Prefill forward of one layer over X~ (paper section 2.1 eq. 3; meta
- * tokens section 2.3; window / KV sharing section 2.2).
+/* Prefill forward of one layer over X~ (Hymba page, section 2.1 eq. 3;
+ * meta tokens section 2.3; window / KV sharing section 2.2).  "Hymba page"
+ * is "Hymba: A Hybrid-head Architecture for Small Language Models" throughout.
  *   x        [B, L, d] device, desc.dtype: X~ with the M meta rows first.
  *            Meta rows must be identical across the batch when cache_out is
  *            given (the cache keeps one copy of the meta K/V).
@@ -199,7 +200,7 @@ HYMBA_API hymba_status hymba_layer_fwd_events(const hymba_layer_desc* d, const h
 
 /* ---------------------------------------------------------------------------
  * Meta-prefix precompute.  The M meta tokens are learned vectors prepended
- * to every input (paper section 2.3), so their rows of a layer are the same
+ * to every input (Hymba page, section 2.3), so their rows of a layer are the same
  * for every sequence: hymba_meta_prefill runs the layer once over those M
  * rows and keeps what the real tokens need from them; hymba_layer_fwd_meta
  * then runs the layer over the real tokens of a whole batch from that
@@ -366,7 +367,7 @@ HYMBA_API int32_t hymba_abi_version(void);
  * ------------------------------------------------------------------------- */
 
 /* C[M, N] (fp32, row stride ldc) = A[M, K] . B[N, K]^T on the tcgen05 GEMM
- * (paper section 2.1: the shared input projection and W_out are these
+ * (Hymba page, section 2.1: the shared input projection and W_out are these
  * GEMMs).  ab_dtype 1 = bf16 operands, 2 = fp16 operands, 3 = fp16 A with
  * bf16 B converted to fp16 in shared memory (the decode step's weights, read
  * once and never copied; a bf16 value outside fp16's normal range rounds as
