@@ -617,6 +617,19 @@ def oracle_sample(T_sample: int, seed: int):
     return s.T, time.perf_counter() - t0
 
 
+def oracle_decode_sample(n_seq: int, seed: int):
+    """One bounded decode sample: the float64 oracle's decode step for n_seq
+    sequences at the 1.5B shapes over an 8192-token history (full 1024-slot
+    ring + 128 meta K/V).  Returns (tokens, seconds)."""
+    from oracle import hymba_ref as ref
+    s = synth.hymba15b_decode(B=n_seq, rope_theta=10000.0)
+    inp = synth.make_decode_inputs(s, seed, cap=s.window, pos=8192)
+    cache = {k: inp[k] for k in ("k_ring", "v_ring", "k_meta", "v_meta", "ssm_state", "conv_state", "pos")}
+    t0 = time.perf_counter()
+    ref.layer_decode(inp, inp["x_new"], cache, s)
+    return n_seq, time.perf_counter() - t0
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -627,9 +640,13 @@ def cpu_cores() -> int:
 def cpu_baseline(args):
     T = args.cpu_sample_tokens
     toks, sec = oracle_sample(T, 11)
+    n_dec, sec_dec = oracle_decode_sample(16, 12)
     return {"value": round(toks / sec, 2), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
             "sample": f"float64 NumPy oracle, 1 sequence x ({T} + 128 meta) tokens at the 1.5B SWA shapes, "
-                      f"{sec:.1f} s"}
+                      f"{sec:.1f} s",
+            "decode": {"value": round(n_dec / sec_dec, 2), "unit": "tokens/s",
+                       "sample": f"one decode step of {n_dec} sequences over an 8192-token history "
+                                 f"(1024-slot ring + 128 meta), {sec_dec:.1f} s"}}
 
 
 def run_reference(args, rank, world):

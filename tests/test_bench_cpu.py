@@ -77,3 +77,13 @@ def test_stage_rooflines_dominant_kernel_and_scan_bounds():
     # the longest stage wins even when it is not the scan
     stage_ms["in_proj"] = 2.0
     assert bench.stage_rooflines(s, stage_ms, peaks)[1] == "in_proj"
+
+
+def test_cpu_baseline_line():
+    """The oracle's timed CPU baseline (prefill sample and decode sample)
+    carries the keys of the bench line."""
+    from types import SimpleNamespace
+    cb = bench.cpu_baseline(SimpleNamespace(cpu_sample_tokens=64))
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["value"] > 0 and cb["cores"] >= 1
+    assert "64 + 128 meta" in cb["sample"]
+    assert cb["decode"]["unit"] == "tokens/s" and cb["decode"]["value"] > 0
