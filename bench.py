@@ -597,7 +597,7 @@ def run_decode(args, torch, hb, hl, dev, stream, peaks, peak_src):
             "us_per_step_graph": round(g_us, 2) if isinstance(g_us, float) else g_us, "stage_us": stage_us,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes,
-                         "peak_source": f"{peak_src} HBM copy"},
+                         "traffic": load_traffic("decode_step"), "peak_source": f"{peak_src} HBM copy"},
             "status": layer.check_status()}
 
 
