@@ -253,6 +253,7 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {layer.check_status()} in the timed region")
     stage_ms = {name: statistics.mean(ev[k].elapsed_time(ev[k + 1]) for ev in ev_sets)
                 for k, name in enumerate(STAGES)}
+    step_each = [ev[0].elapsed_time(ev[len(STAGES)]) for ev in ev_sets]
     ms_max, value = job_throughput(ms, s.B * s.T, world, dev)
 
     fl = layer_flops(s)
@@ -282,6 +283,9 @@ def run_ours(args, rank, world, local_rank):
                                           kernels[dom]["bound"]]),
         "kernels": kernels,
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        # each timed call alone (its first to its last stage event), beside the mean over the K steps above
+        "step_ms": {"median": round(statistics.median(step_each), 4), "min": round(min(step_each), 4),
+                    "max": round(max(step_each), 4)},
         "clocks": clk,
         # per layer call: W_out, W_x (bf16 -> fp16 copies) and W_dt conversions, then in_proj,
         # attention, conv, x_proj, scan, fuse_norm, out_proj (the ncu launch list shows the same)
