@@ -548,7 +548,7 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
   p.tiles_m = (p.M + BM - 1) / BM;
   // cluster pairs share each B block: worth it once there are many row blocks
   // (the projections of a prefill), not for split-K or converted-B launches
-  const bool pair = splits <= 1 && !p.cvt_b && p.tiles_m >= 8 && num_sms >= 2;
+  const bool pair = !p.no_pair && splits <= 1 && !p.cvt_b && p.tiles_m >= 8 && num_sms >= 2;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
     const uint64_t str[1] = {static_cast<uint64_t>(ldb) * 2};

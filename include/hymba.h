@@ -109,7 +109,12 @@ typedef struct hymba_layer_desc {
                            W_out [d, di]; 1: concatenation of the normalised,
                            beta-scaled branches (the appendix B ablation),
                            W_out [d, 2*di]                                    */
-  int32_t reserved[2];  /* must be 0                                         */
+  int32_t no_multicast; /* 1: never pair CTAs into 2-CTA clusters whose TMA
+                           loads multicast a shared operand tile (the
+                           projection GEMMs then run one CTA per tile); for
+                           processes that each drive one GPU of a multi-GPU
+                           job.  0: allowed (default)                         */
+  int32_t reserved;     /* must be 0                                         */
 } hymba_layer_desc;
 
 /* Layer parameters (device pointers).  Matrices are in desc.dtype, vectors
