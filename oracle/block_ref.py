@@ -83,6 +83,21 @@ def block_fwd(pb: Dict[str, np.ndarray], X: np.ndarray, s) -> Dict[str, np.ndarr
     return {"Y1": Y1, "Y": Y}
 
 
+def block_fwd_rows(pb: Dict[str, np.ndarray], X: np.ndarray, s, rows) -> np.ndarray:
+    """The block's output Y at the rows ``rows`` only, for sequences too long
+    for block_fwd.  The MLP sub-block and both norms act row by row, so row r
+    needs only the mixer's output at r, which in turn needs only the causal
+    prefix up to r (hymba_ref.layer_fwd_rows).  Returns [B, len(rows), d]."""
+    assert not s.residual
+    X = np.asarray(X, F)
+    rows = np.asarray(rows)
+    n = int(rows.max()) + 1
+    xn = round_bf16(rmsnorm(X[:, :n], pb["norm1"], s.eps))
+    Y1 = X[:, rows] + hr.layer_fwd_rows(pb, xn, s, rows)
+    hn = round_bf16(rmsnorm(Y1, pb["norm2"], s.eps))
+    return Y1 + gated_mlp(hn, pb["W_gate"], pb["W_up"], pb["W_down"])
+
+
 def blocks_fwd(blocks: List[Dict[str, np.ndarray]], X: np.ndarray, shapes) -> np.ndarray:
     """A stack of residual blocks; each block's input is the previous output."""
     Y = np.asarray(X, F)

@@ -95,6 +95,19 @@ def test_block_composition():
     np.testing.assert_allclose(out["Y"], out["Y1"] + mlp, rtol=1e-13, atol=1e-13)
 
 
+def test_block_rows_matches_whole_block():
+    """The row-sampled block oracle (for sequences too long for block_fwd)
+    reproduces the whole block's rows: meta rows, the first real row, both
+    sides of the window edge, the last row, and a prefix that stops early."""
+    s, tok, pb = _block_case(6)
+    X = tok["Xt"].astype(F)
+    Y = br.block_fwd(pb, X, s)["Y"]
+    for rows in ([0, s.M - 1, s.M, s.M + 15, s.M + 16, s.L - 1], [1, 2, 3], [s.L - 1]):
+        rows = np.array(rows)
+        np.testing.assert_allclose(br.block_fwd_rows(pb, X, s, rows), Y[:, rows], rtol=1e-12,
+                                   atol=1e-12 * np.abs(Y).max())
+
+
 def test_block_with_zeroed_sub_blocks():
     s, tok, pb = _block_case(4)
     X = tok["Xt"].astype(F)
