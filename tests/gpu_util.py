@@ -3,7 +3,6 @@ import numpy as np
 import torch
 
 from hybrid_attention_ssm_fwd_b300 import layer as hl
-from hybrid_attention_ssm_fwd_b300 import synth
 
 # Tolerances of the workload statement: bf16 path max-abs <= 2e-2 and relative
 # Frobenius <= 1e-2; fp32 path relative <= 1e-4.

@@ -7,7 +7,6 @@ GeLU on one branch, expansion 3)."""
 import math
 
 import numpy as np
-import pytest
 import scipy.integrate
 import torch
 
