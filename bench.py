@@ -215,7 +215,7 @@ def run_ours(args, rank, world, local_rank):
     s = synth.hymba15b_swa(rope_theta=10000.0, B=args.batch)
     p = synth.make_layer_inputs(s, rank_seed(rank))
     params = hl.params_to_device(p, s, dev)
-    layer = hl.HymbaLayer(s, params, no_multicast=args.no_multicast)
+    layer = hl.HymbaLayer(s, params)
     X = hl.tokens_to_device(p["Xt"], s, dev)
     Y = torch.empty(s.B, s.L, s.d, dtype=torch.float32, device=dev)
     del p
@@ -274,9 +274,7 @@ def run_ours(args, rank, world, local_rank):
                    "heads": f"{s.Hq}q/{s.Hkv}kv x 64", "d_inner": s.di, "d_state": s.N, "rope_theta": s.rope_theta,
                    "activations": "fp16 (fp32 accumulate; delta/B/C/state/Y fp32)",
                    "l2": "inputs larger than L2 (X~ 213 MB, projection 1.19 GB per step)",
-                   "parallelism": f"dp{world} (independent batches, no collective)",
-                   "gemm_clusters": "one-CTA tiles (multicast off: several ranks)" if args.no_multicast
-                   else "2-CTA clusters multicasting B for the projections"},
+                   "parallelism": f"dp{world} (independent batches, no collective)"},
         "layer_tflops": round(total_flops / (ms_max / 1e3) / 1e12, 1),
         "roofline_layer": {"bound": "tensor", "achieved_tflops": round(total_flops / (ms_max / 1e3) / 1e12, 1),
                            "peak": peak, "frac": round(total_flops / (ms_max / 1e3) / 1e12 / peak, 4),
@@ -361,7 +359,7 @@ def run_e2e(args, torch, hb, hl, dev, stream):
     layer, Y -> pinned host, every step."""
     s = synth.hymba15b_swa(rope_theta=10000.0)
     p = synth.make_layer_inputs(s, 7)
-    layer = hl.HymbaLayer(s, hl.params_to_device(p, s, dev), no_multicast=args.no_multicast)
+    layer = hl.HymbaLayer(s, hl.params_to_device(p, s, dev))
     Xh = torch.from_numpy(p["Xt"]).to(torch.bfloat16).pin_memory()
     Yh = torch.empty(s.B, s.L, s.d, dtype=torch.float32).pin_memory()
     Xd = torch.empty_like(Xh, device=dev)
@@ -391,7 +389,7 @@ def run_e2e(args, torch, hb, hl, dev, stream):
 
 def run_prefill_extra(args, torch, hb, hl, dev, stream, s, name):
     p = synth.make_layer_inputs(s, 2)
-    layer = hl.HymbaLayer(s, hl.params_to_device(p, s, dev), no_multicast=args.no_multicast)
+    layer = hl.HymbaLayer(s, hl.params_to_device(p, s, dev))
     X = hl.tokens_to_device(p["Xt"], s, dev)
     Y = torch.empty(s.B, s.L, s.d, dtype=torch.float32, device=dev)
     del p
@@ -422,7 +420,7 @@ def run_meta_prefix(args, torch, hb, hl, dev, stream):
     (hymba_layer_fwd_meta), both inside each timed step."""
     s = synth.hymba15b_swa(rope_theta=10000.0, B=args.batch)
     p = synth.make_layer_inputs(s, 3)
-    layer = hl.HymbaLayer(s, hl.params_to_device(p, s, dev), no_multicast=args.no_multicast)
+    layer = hl.HymbaLayer(s, hl.params_to_device(p, s, dev))
     xm = hl.tokens_to_device(p["meta"], s, dev)
     X = hl.tokens_to_device(p["X"], s, dev)
     del p
@@ -462,7 +460,7 @@ def run_block(args, torch, hb, hl, dev, stream):
     s = synth.hymba15b_swa(rope_theta=10000.0, B=args.batch)
     d_ff = 3 * s.d
     tok, blocks = synth.make_block_inputs(s, d_ff, 4)
-    blk = hl.HymbaBlock(s, hl.block_params_to_device(blocks[0], s, dev), d_ff, no_multicast=args.no_multicast)
+    blk = hl.HymbaBlock(s, hl.block_params_to_device(blocks[0], s, dev), d_ff)
     x = torch.from_numpy(tok["Xt"]).to(dev)
     del tok, blocks
     for _ in range(args.warmup):
@@ -492,7 +490,7 @@ def run_block(args, torch, hb, hl, dev, stream):
 def run_stack(args, torch, hb, hl, dev, stream):
     shapes = [synth.with_(s, rope_theta=10000.0) for s in synth.ablation300m_stack()]
     tok, layers = synth.make_stack_inputs(shapes, seed=3)
-    L = [hl.HymbaLayer(s, hl.params_to_device(p, s, dev), residual_mode=2, no_multicast=args.no_multicast)
+    L = [hl.HymbaLayer(s, hl.params_to_device(p, s, dev), residual_mode=2)
          for p, s in zip(layers, shapes)]
     s0 = shapes[0]
     X0 = torch.from_numpy(tok["Xt"]).to(dev)
@@ -550,7 +548,7 @@ def run_decode(args, torch, hb, hl, dev, stream, peaks, peak_src):
     cap = s.window
     inp = synth.make_decode_inputs(s, 4, cap=cap, pos=8192)
     cache = hl.cache_to_device(inp, s, dev)
-    layer = hl.HymbaLayer(s, hl.params_to_device(inp, s, dev), decode=True, no_multicast=args.no_multicast)
+    layer = hl.HymbaLayer(s, hl.params_to_device(inp, s, dev), decode=True)
     xn = hl.tokens_to_device(inp["x_new"], s, dev)
     y = torch.empty(s.B, s.d, dtype=torch.float32, device=dev)
     cc = hb.make_cache(cache, cap)
@@ -711,9 +709,6 @@ def main():
         if out is not None:
             print(json.dumps(out), flush=True)
         return
-    # one process per GPU of a multi-GPU job: the 2-CTA multicast clusters of
-    # the projection GEMMs stay off (plain one-CTA tiles)
-    args.no_multicast = world > 1
     if world > 1:
         import torch
         import torch.distributed as dist

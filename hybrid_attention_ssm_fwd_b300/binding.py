@@ -32,7 +32,7 @@ class LayerDesc(ctypes.Structure):
         ("d_inner", c_int32), ("d_state", c_int32), ("d_conv", c_int32), ("dt_rank", c_int32),
         ("window", c_int32), ("kv_shared", c_int32), ("residual", c_int32), ("dtype", c_int32),
         ("rope_theta", c_float), ("eps", c_float), ("wait_limit_us", c_uint32), ("fusion", c_int32),
-        ("no_multicast", c_int32), ("reserved", c_int32),
+        ("reserved0", c_int32), ("reserved", c_int32),
     ]
 
 
@@ -187,12 +187,9 @@ def _stream(stream) -> Optional[int]:
     return stream if isinstance(stream, int) else stream.cuda_stream
 
 
-def make_desc(shape, wait_limit_us: int = 0, residual_mode: Optional[int] = None,
-              no_multicast: bool = False) -> LayerDesc:
+def make_desc(shape, wait_limit_us: int = 0, residual_mode: Optional[int] = None) -> LayerDesc:
     """LayerDesc from a synth.LayerShape-like object.  residual_mode overrides
-    the shape's flag: 1 adds the layer input, 2 accumulates into y in place.
-    no_multicast keeps the projection GEMMs off 2-CTA multicast clusters (for
-    a process that drives one GPU of a multi-GPU job)."""
+    the shape's flag: 1 adds the layer input, 2 accumulates into y in place."""
     return LayerDesc(batch=shape.B, n_tokens=shape.T, n_meta=shape.M, d_model=shape.d, n_q_heads=shape.Hq,
                      n_kv_heads=shape.Hkv, head_dim=shape.dh, v_head_dim=shape.dv, d_inner=shape.di,
                      d_state=shape.N, d_conv=shape.k, dt_rank=shape.R, window=shape.window,
@@ -200,8 +197,7 @@ def make_desc(shape, wait_limit_us: int = 0, residual_mode: Optional[int] = None
                      residual=int(shape.residual) if residual_mode is None else residual_mode,
                      dtype=HYMBA_BF16 if shape.dtype == "bf16" else HYMBA_F32, rope_theta=shape.rope_theta,
                      eps=shape.eps, wait_limit_us=wait_limit_us,
-                     fusion=1 if getattr(shape, "fusion", "sum") == "concat" else 0,
-                     no_multicast=int(bool(no_multicast)))
+                     fusion=1 if getattr(shape, "fusion", "sum") == "concat" else 0)
 
 
 def make_weights(w: Dict[str, "object"]) -> LayerWeights:

@@ -194,36 +194,6 @@ HY_DEV void tc_commit(uint32_t bar) {
       : "memory");
 }
 
-// Completion of this thread's prior MMAs arrives on the mbarrier at the same
-// offset in every CTA of ctaMask (a cluster-wide stage release).
-HY_DEV void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
-// 2-D tiled TMA load delivered to the same shared-memory offset in every CTA
-// of ctaMask, each CTA's mbarrier at `bar`'s offset counting the bytes.
-HY_DEV void tma_load_2d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x, int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar), "h"(mask)
-      : "memory");
-}
-
-HY_DEV uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA in the cluster (release / acquire).
-HY_DEV void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Programmatic dependent launch.  pdl_wait: wait until the stream's preceding
 // kernel has completed and its memory is visible (returns at once when this
 // grid was launched without a programmatic dependency); nothing a preceding

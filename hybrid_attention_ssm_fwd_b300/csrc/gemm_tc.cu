@@ -19,14 +19,7 @@
 //
 // Tiles are visited in row-major tile order (N fastest) by a static
 // round-robin over CTAs, so the CTAs resident at one time share a few A
-// row-blocks and the weight matrix stays in L2.
-//
-// Cluster pairs (PAIR, large M): the two CTAs of a 2-CTA cluster compute
-// vertically adjacent tiles (m = 2i, 2i+1; the same n) in lockstep.  Each
-// loads its own A block and one half of the shared B block, multicast into
-// both CTAs' stage, so a CTA pulls 128 + BN/2 instead of 128 + BN operand rows
-// per k-step from L2.  A stage is refilled once both CTAs' MMAs released it
-// (each commits to both CTAs' "empty" barrier).  Every wait is bounded.
+// row-blocks and the weight matrix stays in L2.  Every wait is bounded.
 #include "gemm_tc.cuh"
 
 #include <atomic>
@@ -53,18 +46,6 @@ struct GemmCfg {
 struct TileCoord {
   int m, n, kb0, kb1, split;
 };
-
-// tile pair t of a cluster-pair launch, for the CTA of cluster rank r
-HY_DEV TileCoord pair_coord(const GemmParams& p, int t, int r) {
-  TileCoord c;
-  const int mp = t / p.tiles_n;
-  c.n = t - mp * p.tiles_n;
-  c.m = 2 * mp + r;  // may be tiles_m (odd tiles_m): rows past M load as zeros and are not stored
-  c.split = 0;
-  c.kb0 = 0;
-  c.kb1 = p.n_kb;
-  return c;
-}
 
 HY_DEV TileCoord tile_coord(const GemmParams& p, int t) {
   TileCoord c;
@@ -116,7 +97,7 @@ HY_DEV bool any_over_half(const float (&v)[32]) {
   return o;
 }
 
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p, const uint32_t idesc) {
@@ -140,17 +121,16 @@ __global__ void __launch_bounds__(192, 1)
   auto tempty = [&](int a) { return smem_u32(&bars[2 * S + 2 + a]); };
   auto cvt = [&](int s) { return smem_u32(&bars[2 * S + 4 + s]); };
 
-  // tile walk: this CTA's tiles, or its cluster's tile pairs
-  const int rank = PAIR ? static_cast<int>(cluster_rank()) : 0;
-  const int t_first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int t_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  const int t_count = PAIR ? p.total_pairs : p.total_tiles;
-  auto coord = [&](int t) { return PAIR ? pair_coord(p, t, rank) : tile_coord(p, t); };
+  // tile walk: a static round-robin over the CTAs
+  const int t_first = static_cast<int>(blockIdx.x);
+  const int t_step = static_cast<int>(gridDim.x);
+  const int t_count = p.total_tiles;
+  auto coord = [&](int t) { return tile_coord(p, t); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), PAIR ? 2 : 1);  // PAIR: both CTAs' MMAs release the stage
+      mbar_init(empty(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull(a), 1);
@@ -164,7 +144,6 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   pdl_wait();  // only the setup above may overlap the preceding kernel
   pdl_trigger();
@@ -187,11 +166,7 @@ __global__ void __launch_bounds__(192, 1)
           if (!mbar_wait(empty(s), ph ^ 1, wc)) { ok = false; break; }
           mbar_arrive_expect_tx(full(s), Cfg::STAGE);
           tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full(s), kb * BK, c.m * BM);
-          if constexpr (PAIR)  // this CTA's half of B, into both CTAs (tmB's box is BN/2 rows)
-            tma_load_2d_mc(smem_u32(sB + s * Cfg::B_BYTES + rank * (Cfg::B_BYTES / 2)), &tmB, full(s), kb * BK,
-                           c.n * BN + rank * (BN / 2), 0x3);
-          else
-            tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full(s), kb * BK, c.n * BN);
+          tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full(s), kb * BK, c.n * BN);
           issued |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
         }
@@ -217,17 +192,14 @@ __global__ void __launch_bounds__(192, 1)
         for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!mbar_wait(!PAIR && p.cvt_b ? cvt(s) : full(s), ph, wc)) { ok = false; break; }
+          if (!mbar_wait(p.cvt_b ? cvt(s) : full(s), ph, wc)) { ok = false; break; }
           tc_fence_after();
           const uint64_t da = sdesc_sw128(smem_u32(sA + s * A_BYTES), 16, 1024);
           const uint64_t db = sdesc_sw128(smem_u32(sB + s * Cfg::B_BYTES), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
-          if constexpr (PAIR)
-            tc_commit_mc(empty(s), 0x3);  // the stage is free in both CTAs once both have used it
-          else
-            tc_commit(empty(s));
+          tc_commit(empty(s));
           committed |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
         }
@@ -255,7 +227,7 @@ __global__ void __launch_bounds__(192, 1)
       const TileCoord c = coord(t);
       const int a = local & 1;
       const uint32_t u = (local >> 1) & 1;
-      if (!PAIR && p.cvt_b) {
+      if (p.cvt_b) {
         // bf16 -> fp16 of every B stage of this tile, in place (elementwise:
         // the swizzled layout is unchanged)
         for (int kb = c.kb0; kb < c.kb1 && cok; ++kb, ++cit) {
@@ -434,7 +406,6 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
-  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still write into its shared memory
 }
 
 // Kernel attributes and occupancy figures belong to one device: the
@@ -442,11 +413,11 @@ __global__ void __launch_bounds__(192, 1)
 // set up on every call).
 constexpr int kMaxDevices = 64;
 
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI>
 hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, uint32_t idesc, int grid,
                        cudaStream_t st) {
   using Cfg = GemmCfg<BN>;
-  auto kern = gemm_tc_kernel<BN, EPI, PAIR>;
+  auto kern = gemm_tc_kernel<BN, EPI>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return HYMBA_ERR_CUDA;
   const bool cached = dev < kMaxDevices;
@@ -457,51 +428,20 @@ hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmP
       return HYMBA_ERR_CUDA;
     if (cached) attr_done[dev].store(true, std::memory_order_release);
   }
-  if constexpr (!PAIR) {
-    if (launch_pdl(kern, dim3(grid), dim3(192), Cfg::SMEM, st, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.blockDim = dim3(192, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::SMEM;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
-    // persistent: no more clusters than can be resident at once (a GPC with an
-    // odd SM count leaves one SM out), so no tile waits for a second wave
-    static std::atomic<int> max_clusters_dev[kMaxDevices];
-    int max_clusters = cached ? max_clusters_dev[dev].load(std::memory_order_relaxed) : 0;
-    if (max_clusters == 0) {
-      cfg.gridDim = dim3(2 * std::max(1, grid / 2), 1, 1);
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return HYMBA_ERR_CUDA;
-      max_clusters = n;
-      if (cached) max_clusters_dev[dev].store(n, std::memory_order_relaxed);
-    }
-    const int clusters = std::max(1, std::min(std::min(grid / 2, max_clusters), p.total_pairs));
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
-  }
+  if (launch_pdl(kern, dim3(grid), dim3(192), Cfg::SMEM, st, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 
-template <int EPI, bool PAIR>
+template <int EPI>
 hymba_status launch_epi(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                         uint32_t ab_fmt, int grid, cudaStream_t st) {
   const uint32_t id = idesc_f16(BM, bn, ab_fmt, false, false);
   switch (bn) {
-    case 64: return launch_bn<64, EPI, PAIR>(ta, tb, p, id, grid, st);
-    case 128: return launch_bn<128, EPI, PAIR>(ta, tb, p, id, grid, st);
-    case 144: return launch_bn<144, EPI, PAIR>(ta, tb, p, id, grid, st);
-    case 160: return launch_bn<160, EPI, PAIR>(ta, tb, p, id, grid, st);
-    case 256: return launch_bn<256, EPI, PAIR>(ta, tb, p, id, grid, st);
+    case 64: return launch_bn<64, EPI>(ta, tb, p, id, grid, st);
+    case 128: return launch_bn<128, EPI>(ta, tb, p, id, grid, st);
+    case 144: return launch_bn<144, EPI>(ta, tb, p, id, grid, st);
+    case 160: return launch_bn<160, EPI>(ta, tb, p, id, grid, st);
+    case 256: return launch_bn<256, EPI>(ta, tb, p, id, grid, st);
     default: return HYMBA_ERR_UNSUPPORTED;
   }
 }
@@ -546,13 +486,10 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
     if (!encode_tmap(&ta, dt, 2, A, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
   }
   p.tiles_m = (p.M + BM - 1) / BM;
-  // cluster pairs share each B block: worth it once there are many row blocks
-  // (the projections of a prefill), not for split-K or converted-B launches
-  const bool pair = !p.no_pair && splits <= 1 && !p.cvt_b && p.tiles_m >= 8 && num_sms >= 2;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
     const uint64_t str[1] = {static_cast<uint64_t>(ldb) * 2};
-    const uint32_t box[2] = {BK, static_cast<uint32_t>(pair ? bn / 2 : bn)};
+    const uint32_t box[2] = {BK, static_cast<uint32_t>(bn)};
     const CUtensorMapDataType dtb = p.cvt_b ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : dt;
     if (!encode_tmap(&tb, dtb, 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
   }
@@ -562,29 +499,18 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
   p.kb_per_split = (p.n_kb + splits - 1) / splits;
   p.splits = (p.n_kb + p.kb_per_split - 1) / p.kb_per_split;
   p.total_tiles = p.tiles_m * p.tiles_n * p.splits;
-  p.total_pairs = (p.tiles_m + 1) / 2 * p.tiles_n;
   if (p.splits > 1 && epi != EPI_PARTIAL && epi != EPI_ATOMIC) return HYMBA_ERR_INVALID;
   if (epi == EPI_GEGLU && (p.N % 16 || p.ldc % 8 || (reinterpret_cast<uintptr_t>(p.C) & 15))) return HYMBA_ERR_INVALID;
   const int grid = std::min(p.total_tiles, std::max(1, num_sms));
   const uint32_t fmt = ab_fmt == 1 ? 1u : 0u;
-  if (pair) {
-    switch (epi) {
-      case EPI_F16: return launch_epi<EPI_F16, true>(bn, ta, tb, p, fmt, num_sms, st);
-      case EPI_XPROJ: return launch_epi<EPI_XPROJ, true>(bn, ta, tb, p, fmt, num_sms, st);
-      case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS, true>(bn, ta, tb, p, fmt, num_sms, st);
-      case EPI_F32: return launch_epi<EPI_F32, true>(bn, ta, tb, p, fmt, num_sms, st);
-      case EPI_GEGLU: return launch_epi<EPI_GEGLU, true>(bn, ta, tb, p, fmt, num_sms, st);
-      default: return HYMBA_ERR_INVALID;
-    }
-  }
   switch (epi) {
-    case EPI_F16: return launch_epi<EPI_F16, false>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_XPROJ: return launch_epi<EPI_XPROJ, false>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS, false>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_F32: return launch_epi<EPI_F32, false>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_PARTIAL: return launch_epi<EPI_PARTIAL, false>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_ATOMIC: return launch_epi<EPI_ATOMIC, false>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_GEGLU: return launch_epi<EPI_GEGLU, false>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_F16: return launch_epi<EPI_F16>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_XPROJ: return launch_epi<EPI_XPROJ>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_F32: return launch_epi<EPI_F32>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_PARTIAL: return launch_epi<EPI_PARTIAL>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_ATOMIC: return launch_epi<EPI_ATOMIC>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_GEGLU: return launch_epi<EPI_GEGLU>(bn, ta, tb, p, fmt, grid, st);
     default: return HYMBA_ERR_INVALID;
   }
 }

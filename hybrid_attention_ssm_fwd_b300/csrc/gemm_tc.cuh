@@ -36,8 +36,6 @@ struct GemmParams {
   int32_t* status;
   uint64_t wait_ns;
   int cvt_b;  // B is bf16 in memory: converted to fp16 in shared memory before the MMA (A fp16)
-  int total_pairs;  // cluster-pair launch: (vertically adjacent tile pairs) = ceil(tiles_m / 2) * tiles_n
-  int no_pair;      // 1: never launch as cluster pairs (no multicast TMA loads)
 };
 
 // Launch C = A . B^T with the given epilogue.  ab_fmt: 0 fp16, 1 bf16.

@@ -28,7 +28,6 @@ namespace {
 struct Dims {
   int B, T, M, L, d, Hq, Hkv, dh, dv, di, N, k, R, W, kv_shared, residual, dtype;
   int fusion, sw;  // sw = width of the fused rows s (and K of out_proj): di, or 2 di concatenated
-  int no_multicast;  // 1: no cluster-pair (multicast) GEMMs
   float theta, eps;
   uint64_t wait_ns;
   long long rows;
@@ -44,7 +43,7 @@ hymba_status check_desc(const hymba_layer_desc* d, bool decode, Dims* o) {
       d->n_kv_heads < 1 || d->head_dim < 2 || (d->head_dim & 1) || d->v_head_dim < 1 || d->d_inner < 1 ||
       d->d_state < 1 || d->d_state > 64 || d->d_conv < 1 || d->d_conv > 8 || d->dt_rank < 1 || d->window < 0 ||
       !is_flag(d->kv_shared) || d->residual < 0 || d->residual > 2 || !(d->eps >= 0.f) || !(d->rope_theta >= 0.f) ||
-      !is_flag(d->fusion) || !is_flag(d->no_multicast))
+      !is_flag(d->fusion) || d->reserved0 != 0)
     return HYMBA_ERR_INVALID;
   if (d->dtype != HYMBA_F32 && d->dtype != HYMBA_BF16) return HYMBA_ERR_INVALID;
   if (d->n_q_heads % d->n_kv_heads != 0) return HYMBA_ERR_INVALID;
@@ -69,7 +68,6 @@ hymba_status check_desc(const hymba_layer_desc* d, bool decode, Dims* o) {
   x.kv_shared = d->kv_shared;
   x.residual = d->residual;
   x.fusion = d->fusion;
-  x.no_multicast = d->no_multicast;
   x.sw = d->fusion ? 2 * d->d_inner : d->d_inner;
   x.dtype = d->dtype;
   x.theta = d->rope_theta;
@@ -266,9 +264,8 @@ hymba_status fwd_f32(const Dims& x, const Plan& pl, const hymba_layer_weights* w
 // ---------------------------------------------------------------------------
 // bf16 path (tensor cores)
 // ---------------------------------------------------------------------------
-GemmParams gp(int M, int N, int K, int32_t* status, uint64_t wait_ns, int no_multicast) {
+GemmParams gp(int M, int N, int K, int32_t* status, uint64_t wait_ns) {
   GemmParams p{};
-  p.no_pair = no_multicast;
   p.M = M;
   p.N = N;
   p.K = K;
@@ -292,7 +289,7 @@ hymba_status convert_weights(const Dims& x, const Plan& pl, const hymba_layer_we
 hymba_status in_proj_bf16(const Dims& x, const void* X, const hymba_layer_weights* w, __half* proj, int rows,
                           const int32_t* pos, int pos_base, int rows_per_seq, int32_t* status, int sms,
                           cudaStream_t st) {
-  GemmParams p = gp(rows, x.P_in, x.d, status, x.wait_ns, x.no_multicast);
+  GemmParams p = gp(rows, x.P_in, x.d, status, x.wait_ns);
   p.C = proj;
   p.ldc = x.P_in;
   const bool fused_rope = x.theta > 0 && x.dh == 64;
@@ -372,7 +369,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     TRY(conv_silu<__half, __half>(proj + x.x_col, x.P_in, u, x.di, x.B, x.L, x.di, x.k, w->conv_w, w->conv_b, st));
   mk.mark();
   {
-    GemmParams p = gp(rows, x.xo, x.di, status, x.wait_ns, x.no_multicast);
+    GemmParams p = gp(rows, x.xo, x.di, status, x.wait_ns);
     p.C = bc;
     p.ldc = 2 * x.N;
     p.C2 = dtr;
@@ -389,7 +386,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
                        static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, bc, w->A_log, w->D, g,
                        mi ? mi->ssm_state : nullptr, h_out, status, x.wait_ns, 0, 0, st, mi != nullptr));
   } else {
-    GemmParams p = gp(rows, x.di, x.R, status, x.wait_ns, x.no_multicast);
+    GemmParams p = gp(rows, x.di, x.R, status, x.wait_ns);
     p.C = delta;
     p.ldc = x.di;
     p.bias = w->dt_bias;
@@ -403,7 +400,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
   TRY(fuse_norm<__half>(rows, x.di, att, g, w->beta1, w->beta2, x.eps, s, st, x.fusion != 0));
   mk.mark();
   {
-    GemmParams p = gp(rows, x.d, x.sw, status, x.wait_ns, x.no_multicast);
+    GemmParams p = gp(rows, x.d, x.sw, status, x.wait_ns);
     p.C = Y;
     p.ldc = x.d;
     p.resid = x.residual == 1 ? static_cast<const __nv_bfloat16*>(X) : nullptr;
@@ -553,7 +550,7 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   mk.mark();
   {
     const int ldp = (x.xo + 15) / 16 * 16;
-    GemmParams p = gp(B, x.xo, x.di, status, x.wait_ns, x.no_multicast);
+    GemmParams p = gp(B, x.xo, x.di, status, x.wait_ns);
     p.C = part;
     p.ldc = ldp;
     p.cvt_b = 1;
@@ -576,7 +573,7 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
                         static_cast<const __nv_bfloat16*>(w->W_dt), w->dt_bias, w->A_log, w->D, c->ssm_state, g, x.di,
                         c->pos, st));  // also advances pos
   } else {
-    GemmParams p = gp(B, x.di, x.R, status, x.wait_ns, x.no_multicast);
+    GemmParams p = gp(B, x.di, x.R, status, x.wait_ns);
     p.C = delta;
     p.ldc = x.di;
     p.bias = w->dt_bias;
@@ -589,7 +586,7 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   TRY(fuse_norm<__half>(B, x.di, att, g, w->beta1, w->beta2, x.eps, s, st, x.fusion != 0));
   mk.mark();
   {
-    GemmParams p = gp(B, x.d, x.sw, status, x.wait_ns, x.no_multicast);
+    GemmParams p = gp(B, x.d, x.sw, status, x.wait_ns);
     p.cvt_b = 1;
     if (x.residual != 1) {
       // split-K partials added straight into Y, which holds the fp32 residual
@@ -861,13 +858,13 @@ hymba_status hymba_block_fwd(const hymba_layer_desc* d, const hymba_block_weight
   TRY(rmsnorm_bf16(rows, x.d, xs, x.d, w->norm2, x.eps, xn, x.d, st));
   TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_down), d_ff, wdown, d_ff, x.d, d_ff, st));
   {
-    GemmParams p = gp(rows, 2 * d_ff, x.d, dev_status, x.wait_ns, x.no_multicast);
+    GemmParams p = gp(rows, 2 * d_ff, x.d, dev_status, x.wait_ns);
     p.C = h;
     p.ldc = d_ff;
     TRY(gemm_tc(1, xn, x.d, w->W_gu, x.d, EPI_GEGLU, p, 0, 1, sms, st));
   }
   {
-    GemmParams p = gp(rows, x.d, d_ff, dev_status, x.wait_ns, x.no_multicast);
+    GemmParams p = gp(rows, x.d, d_ff, dev_status, x.wait_ns);
     p.C = xs;
     p.ldc = x.d;
     p.resid_f32 = xs;

@@ -73,10 +73,10 @@ class HymbaLayer:
     """One hybrid-head layer on one device."""
 
     def __init__(self, shape, params: Dict[str, torch.Tensor], wait_limit_us: int = 0, decode: bool = False,
-                 residual_mode: Optional[int] = None, no_multicast: bool = False):
+                 residual_mode: Optional[int] = None):
         self.shape = shape
         self.params = params
-        self.desc = hb.make_desc(shape, wait_limit_us, residual_mode, no_multicast)
+        self.desc = hb.make_desc(shape, wait_limit_us, residual_mode)
         self.weights = hb.make_weights(params)
         dev = params["W_in"].device
         nbytes = hb.layer_decode_workspace(self.desc) if decode else hb.layer_fwd_workspace(self.desc)
@@ -180,12 +180,11 @@ class HymbaBlock:
     """One residual block (RMSNorm -> hybrid-head layer -> add; RMSNorm ->
     gated MLP -> add) on one device, applied in place to an fp32 stream."""
 
-    def __init__(self, shape, params: Dict[str, torch.Tensor], d_ff: int, wait_limit_us: int = 0,
-                 no_multicast: bool = False):
+    def __init__(self, shape, params: Dict[str, torch.Tensor], d_ff: int, wait_limit_us: int = 0):
         self.shape = shape
         self.params = params
         self.d_ff = d_ff
-        self.desc = hb.make_desc(shape, wait_limit_us, residual_mode=0, no_multicast=no_multicast)
+        self.desc = hb.make_desc(shape, wait_limit_us, residual_mode=0)
         self.weights = hb.make_block_weights(params)
         nbytes = hb.block_fwd_workspace(self.desc, d_ff)
         if nbytes == 0:

@@ -109,11 +109,7 @@ typedef struct hymba_layer_desc {
                            W_out [d, di]; 1: concatenation of the normalised,
                            beta-scaled branches (the appendix B ablation),
                            W_out [d, 2*di]                                    */
-  int32_t no_multicast; /* 1: never pair CTAs into 2-CTA clusters whose TMA
-                           loads multicast a shared operand tile (the
-                           projection GEMMs then run one CTA per tile); for
-                           processes that each drive one GPU of a multi-GPU
-                           job.  0: allowed (default)                         */
+  int32_t reserved0;    /* must be 0                                         */
   int32_t reserved;     /* must be 0                                         */
 } hymba_layer_desc;
 
@@ -331,8 +327,8 @@ HYMBA_API hymba_status hymba_layer_decode(const hymba_layer_desc* d, const hymba
  * library, held until the process exits).  It allocates nothing.
  *   - Shapes whose decode workspace (hymba_layer_decode_workspace) exceeds
  *     HYMBA_STATIC_SCRATCH_BYTES are rejected with HYMBA_ERR_WORKSPACE before
- *     anything is launched.  The 1.5B-shaped decode at batch 128 needs about
- *     23 MiB.
+ *     anything is launched; hymba_layer_decode_workspace gives a shape's
+ *     need (the 1.5B-shaped decode at batch 128 fits).
  *   - The first call on a device looks up that device's address of the
  *     buffer (cudaGetSymbolAddress, with that device current); make that first
  *     call before any stream capture.

@@ -76,17 +76,12 @@ def test_reserved_fields_must_be_zero():
     assert hb.layer_fwd_workspace(d) == 0
 
 
-def test_no_multicast_flag():
-    """desc.no_multicast is a flag: 0 and 1 accepted (same workspace, the
-    choice only changes how the GEMMs are launched), anything else rejected."""
+def test_reserved0_must_be_zero():
+    """desc.reserved0 is a reserved word: any nonzero value is rejected."""
     d = _desc()
-    n0 = hb.layer_fwd_workspace(d)
-    d.no_multicast = 1
-    assert hb.layer_fwd_workspace(d) == n0 > 0
-    assert hb.layer_decode_workspace(hb.make_desc(synth.hymba15b_decode(), no_multicast=True)) > 0
-    d.no_multicast = 2
+    assert hb.layer_fwd_workspace(d) > 0
+    d.reserved0 = 1
     assert hb.layer_fwd_workspace(d) == 0
-    assert hb.make_desc(synth.hymba15b_swa(), no_multicast=True).no_multicast == 1
 
 
 def test_null_and_misaligned_pointers_rejected():
