@@ -38,13 +38,7 @@ from oracle import hymba_ref as hr
 F = np.float64
 
 
-def round_bf16(a: np.ndarray) -> np.ndarray:
-    """Round to the nearest bfloat16 (ties to even), returned as float64:
-    float32 bits + 0x7FFF + (bit 16), truncated to the top 16 bits."""
-    f = np.ascontiguousarray(np.asarray(a, np.float64).astype(np.float32))
-    u = f.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32).astype(F)
+round_bf16 = hr.round_bf16
 
 
 def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:

@@ -235,7 +235,8 @@ def ssm_branch(x: np.ndarray, z: np.ndarray, p: Dict[str, np.ndarray], s,
     return y * silu(z), h
 
 
-def fuse_and_project(att: np.ndarray, g: np.ndarray, p, s, X: Optional[np.ndarray]) -> np.ndarray:
+def fuse_and_project(att: np.ndarray, g: np.ndarray, p, s, X: Optional[np.ndarray],
+                     residual: Optional[bool] = None) -> np.ndarray:
     """Eq. (3): Y = W_out(beta1 * norm(att) + beta2 * norm(g)) (+ X if residual).
 
     With ``s.fusion == "concat"`` the ablation of the Hymba page's appendix B
@@ -247,18 +248,20 @@ def fuse_and_project(att: np.ndarray, g: np.ndarray, p, s, X: Optional[np.ndarra
     b = np.asarray(p["beta2"], F) * rms_norm(g, s.eps)
     sm = np.concatenate([a, b], axis=-1) if getattr(s, "fusion", "sum") == "concat" else a + b
     Y = sm @ np.asarray(p["W_out"], F).T
-    if s.residual:
+    if s.residual if residual is None else residual:
         Y = Y + np.asarray(X, F)
     return Y
 
 
 def layer_fwd(p: Dict[str, np.ndarray], Xt: np.ndarray, s,
               kv_in: Optional[Tuple[np.ndarray, np.ndarray]] = None,
-              cache_cap: Optional[int] = None, want_branches: bool = False) -> Dict[str, np.ndarray]:
+              cache_cap: Optional[int] = None, want_branches: bool = False,
+              residual: Optional[bool] = None) -> Dict[str, np.ndarray]:
     """Prefill forward of one hybrid-head layer on X~ [B, L, d] (meta rows first).
 
     Returns a dict with Y [B,L,d]; K/V (post-RoPE, [B,L,Hkv,dh|dv]) for a
     sharing consumer; and, when ``cache_cap`` is given, the decode cache.
+    ``residual`` overrides the shape's residual flag when given.
     """
     Xt = np.asarray(Xt, F)
     B, L, d = Xt.shape
@@ -278,7 +281,7 @@ def layer_fwd(p: Dict[str, np.ndarray], Xt: np.ndarray, s,
             K = rope(K, positions, s.rope_theta)
     att = attention(Q, K, V, s.M, s.window)
     g, h = ssm_branch(parts["x"], parts["z"], p, s)
-    Y = fuse_and_project(att, g, p, s, Xt)
+    Y = fuse_and_project(att, g, p, s, Xt, residual)
     out = {"Y": Y, "K": K, "V": V}
     if want_branches:
         out.update(att=att, g=g, x=parts["x"], z=parts["z"])
@@ -405,15 +408,34 @@ def layer_decode(p: Dict[str, np.ndarray], x_new: np.ndarray, cache: Dict[str, n
     return {"y": Y, "cache": new, "att": att, "g": g[:, 0, :]}
 
 
-def stack_fwd(layers, Xt: np.ndarray, shapes) -> Dict[str, list]:
-    """Residual stack X_{l+1} = X_l + Y_l (each layer has residual=True); a
-    kv_shared layer consumes the previous layer's K/V."""
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 (ties to even), returned as float64:
+    float32 bits + 0x7FFF + (bit 16), truncated to the top 16 bits."""
+    f = np.ascontiguousarray(np.asarray(a, np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(F)
+
+
+def stack_fwd(layers, Xt: np.ndarray, shapes, round_inputs: bool = True) -> Dict[str, list]:
+    """Residual stack X_{l+1} = X_l + Y_l(X~_l) of hybrid-head layers (the
+    Hymba pages describe no pre-norm or FFN for it); a kv_shared layer
+    consumes the previous layer's post-RoPE K/V (section 2.2).
+
+    Reading: the stream X_l is kept at full precision (fp32 on the device,
+    float64 here) and each layer's input X~_l is the stream rounded to
+    bfloat16, the input type of a bf16 layer; the residual adds the unrounded
+    stream.  round_inputs=False feeds the stream unrounded (the fp32 path).
+    Every layer's own residual flag is ignored: the stack adds the stream.
+    Returns the stream after each layer.
+    """
     X = np.asarray(Xt, F)
     outs, prev = [], None
     for p, s in zip(layers, shapes):
         kv = (prev["K"], prev["V"]) if s.kv_shared else None
-        o = layer_fwd(p, X, s, kv_in=kv)
-        outs.append(o["Y"])
-        X = o["Y"]
+        Xin = round_bf16(X) if round_inputs else X
+        o = layer_fwd(p, Xin, s, kv_in=kv, residual=False)
+        X = X + o["Y"]
+        outs.append(X)
         prev = o
     return {"Y": outs}

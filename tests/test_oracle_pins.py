@@ -566,19 +566,162 @@ def test_decode_visible_slots_count():
     assert len(ref.decode_visible_slots(2, 0, 10)) == 3
 
 
-def test_stack_kv_sharing_layer_uses_producer_kv():
-    shapes = synth.ablation300m_stack(B=1, T=12, M=4, d=32, Hq=2, Hkv=1, dh=8, di=32, N=4)
+def _tiny_stack(seed=3):
+    shapes = synth.ablation300m_stack(B=2, T=12, M=4, d=32, Hq=2, Hkv=1, dh=8, di=32, N=4)
     shapes = [synth.with_(s, window=(0 if i == 0 else 6), rope_theta=10000.0) for i, s in enumerate(shapes)]
-    tok, layers = synth.make_stack_inputs(shapes, seed=3)
-    out = ref.stack_fwd(layers, tok["Xt"], shapes)
-    # recompute layer 2 by hand from layer 1's K/V
+    tok, layers = synth.make_stack_inputs(shapes, seed=seed)
+    return shapes, tok, layers
+
+
+def _silence(p):
+    """beta1 = beta2 = 0: the layer's output is exactly zero (eq. 3)."""
+    q = dict(p)
+    q["beta1"] = np.zeros_like(p["beta1"])
+    q["beta2"] = np.zeros_like(p["beta2"])
+    return q
+
+
+def test_stack_of_silent_layers_is_the_identity():
+    """With beta1 = beta2 = 0 in every layer each Y_l is zero, so the residual
+    stack X_{l+1} = X_l + Y_l returns its input after every layer, bit for
+    bit (a dropped residual would return zeros)."""
+    shapes, tok, layers = _tiny_stack()
+    out = ref.stack_fwd([_silence(p) for p in layers], tok["Xt"], shapes)
+    for Y in out["Y"]:
+        np.testing.assert_array_equal(Y, tok["Xt"].astype(F))
+
+
+def test_stack_single_active_layer_adds_its_output():
+    """Only layer j active: the stack's output is X + Y_j(X), the stream plus
+    one layer's output on it; earlier layers leave the stream unchanged."""
+    shapes, tok, layers = _tiny_stack()
     X = tok["Xt"].astype(F)
-    prev = None
-    for i, (p, s) in enumerate(zip(layers, shapes)):
-        o = ref.layer_fwd(p, X, s, kv_in=(prev["K"], prev["V"]) if s.kv_shared else None)
-        np.testing.assert_array_equal(o["Y"], out["Y"][i])
-        X, prev = o["Y"], o
-    assert shapes[2].kv_shared and not shapes[1].kv_shared
+    for j in (0, 1, 3):
+        q = [p if i == j else _silence(p) for i, p in enumerate(layers)]
+        out = ref.stack_fwd(q, X, shapes)
+        Yj = ref.layer_fwd(q[j], X, shapes[j], residual=False)["Y"]
+        assert np.abs(Yj).max() > 1e-3
+        np.testing.assert_allclose(out["Y"][-1], X + Yj, rtol=1e-13, atol=1e-13)
+        for i in range(j):
+            np.testing.assert_array_equal(out["Y"][i], X)
+
+
+def test_stack_consumer_reads_the_previous_layers_kv():
+    """Layer 1 silent (Y_1 = 0), so layer 2 sees the same input as layer 1.
+    Then layer 2 sharing layer 1's K/V must equal layer 2 recomputing K/V with
+    layer 1's W_K/W_V (the tied-weights form of section 2.2).  Taking layer
+    0's K/V instead, or layer 2's own, breaks the equality."""
+    shapes, tok, layers = _tiny_stack(seed=5)
+    q = list(layers)
+    q[1] = _silence(layers[1])
+    q[3] = _silence(layers[3])
+    out = ref.stack_fwd(q, tok["Xt"], shapes)
+    X1 = out["Y"][0]                                   # stream entering layers 1 and 2
+    s1, s2 = shapes[1], shapes[2]
+    qn = s1.Hq * s1.dh
+    kvn = s1.Hkv * (s1.dh + s1.dv)
+    W1 = layers[1]["W_in"].astype(F)
+    W2 = layers[2]["W_in"].astype(F)                    # the consumer has no K/V rows
+    tied = dict(layers[2])
+    tied["W_in"] = np.concatenate([W2[:qn], W1[qn:qn + kvn], W2[qn:]], 0)
+    s_tied = synth.with_(s2, kv_shared=False, window=s1.window)
+    Y2 = ref.layer_fwd(tied, ref.round_bf16(X1), s_tied, residual=False)["Y"]
+    np.testing.assert_allclose(out["Y"][2], X1 + Y2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(out["Y"][3], out["Y"][2])
+
+
+def test_stack_rounds_each_layer_input_to_bf16():
+    """Two active layers: layer 1 reads the stream X_1 = X_0 + Y_0 rounded to
+    bfloat16 (torch's conversion here, not the oracle's), while the residual
+    adds the unrounded X_1."""
+    import torch
+    shapes, tok, layers = _tiny_stack(seed=7)
+    q = [layers[0], layers[1], _silence(layers[2]), _silence(layers[3])]
+    X0 = tok["Xt"].astype(F)
+    out = ref.stack_fwd(q, X0, shapes)
+    X1 = X0 + ref.layer_fwd(q[0], X0, shapes[0], residual=False)["Y"]
+    X1b = torch.from_numpy(X1.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.abs(X1b - X1).max() > 0
+    X2 = X1 + ref.layer_fwd(q[1], X1b, shapes[1], residual=False)["Y"]
+    np.testing.assert_allclose(out["Y"][1], X2, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(out["Y"][3], X2, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# KV sharing in decode (section 2.2: consecutive layers share K and V)
+# ---------------------------------------------------------------------------
+
+
+def _producer_consumer(seed_p=21, seed_c=22, T=30, window=8, rope=10000.0):
+    s = tiny(T=T, window=window, rope_theta=rope)
+    pp = inputs(s, seed_p)
+    pc = inputs(s, seed_c)
+    qn = s.Hq * s.dh
+    kvn = s.Hkv * (s.dh + s.dv)
+    Wc = pc["W_in"].astype(F)
+    cons = dict(pc)
+    cons["W_in"] = np.concatenate([Wc[:qn], Wc[qn + kvn:]], 0)   # no K/V rows
+    tied = dict(pc)
+    tied["W_in"] = np.concatenate([Wc[:qn], pp["W_in"].astype(F)[qn:qn + kvn], Wc[qn + kvn:]], 0)
+    return s, pp, cons, tied
+
+
+def test_decode_kv_shared_equals_tied_recomputation():
+    """On the same token and the same history, the consumer decoding from the
+    producer's cache (already holding this token's K/V) equals the consumer
+    with its own cache and the producer's W_K/W_V: output, SSM state, conv
+    tail and position."""
+    T0 = 20
+    s, pp, cons, tied = _producer_consumer()
+    s0 = synth.with_(s, T=T0)
+    sd = synth.with_(s, T=1)
+    X = pp["Xt"]
+    prod_c = ref.layer_fwd(pp, X[:, : s0.L], s0, cache_cap=s.window)["cache"]
+    tied_c = ref.layer_fwd(tied, X[:, : s0.L], s0, cache_cap=s.window)["cache"]
+    x_new = X[:, s0.L]
+    prod = ref.layer_decode(pp, x_new, prod_c, sd)
+    own = {k: tied_c[k] for k in ("ssm_state", "conv_state", "pos")}
+    shared = ref.layer_decode(cons, x_new, own, synth.with_(sd, kv_shared=True), shared_cache=prod["cache"])
+    ref_t = ref.layer_decode(tied, x_new, tied_c, sd)
+    np.testing.assert_allclose(shared["y"], ref_t["y"], rtol=1e-12, atol=1e-13)
+    for k in ("ssm_state", "conv_state"):
+        np.testing.assert_allclose(shared["cache"][k], ref_t["cache"][k], rtol=1e-12, atol=1e-14)
+    assert np.all(shared["cache"]["pos"] == T0 + 1)
+    # the producer's cache is what makes the difference: its pre-step cache
+    # (without this token) gives another answer
+    stale = ref.layer_decode(cons, x_new, own, synth.with_(sd, kv_shared=True), shared_cache=prod_c)
+    assert np.abs(stale["y"] - shared["y"]).max() > 1e-6
+
+
+@pytest.mark.parametrize("T0,n,window", [(12, 10, 8), (5, 6, 0)])
+def test_decode_chain_of_shared_consumer_equals_longer_prefill(T0, n, window):
+    """Producer and consumer prefill T0 tokens (the consumer from the
+    producer's K/V), then n decode steps, producer first; the consumer's
+    outputs equal its rows of the longer prefill from the producer's longer
+    K/V, and so do its SSM state and conv tail."""
+    s, pp, cons, _ = _producer_consumer(T=T0 + n, window=window)
+    cap = window if window > 0 else T0 + n
+    sc = synth.with_(s, kv_shared=True)
+    X = pp["Xt"]
+    s0 = synth.with_(s, T=T0)
+    sc0 = synth.with_(sc, T=T0)
+    po = ref.layer_fwd(pp, X[:, : s0.L], s0, cache_cap=cap)
+    co = ref.layer_fwd(cons, X[:, : s0.L], sc0, kv_in=(po["K"], po["V"]), cache_cap=cap)
+    pc, cc = po["cache"], {k: co["cache"][k] for k in ("ssm_state", "conv_state", "pos")}
+    sd, scd = synth.with_(s, T=1), synth.with_(sc, T=1)
+    ys = []
+    for i in range(n):
+        x = X[:, s0.L + i]
+        rp = ref.layer_decode(pp, x, pc, sd)
+        pc = rp["cache"]
+        rc = ref.layer_decode(cons, x, cc, scd, shared_cache=pc)
+        cc = rc["cache"]
+        ys.append(rc["y"])
+    pf = ref.layer_fwd(pp, X, s)
+    cf = ref.layer_fwd(cons, X, sc, kv_in=(pf["K"], pf["V"]), cache_cap=cap)
+    np.testing.assert_allclose(np.stack(ys, 1), cf["Y"][:, s.M + T0:], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(cc["ssm_state"], cf["cache"]["ssm_state"], rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(cc["conv_state"], cf["cache"]["conv_state"], rtol=1e-12, atol=1e-14)
 
 
 # ---------------------------------------------------------------------------
