@@ -38,6 +38,7 @@ from hybrid_attention_ssm_fwd_b300 import synth  # noqa: E402
 
 METRIC = "hybrid-head layer prefill tokens/s @8K bf16; decode tok/s; % of roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+E2E_CHUNK = 2
 STAGES = ["convert", "in_proj", "kv_export", "attention", "conv", "x_proj", "dt_proj", "scan", "fuse_norm",
           "out_proj", "cache"]
 
@@ -74,7 +75,9 @@ def stage_work(s) -> dict:
     return {
         "in_proj": ("tensor", fl["in_proj"], "FLOP"),
         "attention": ("tensor", fl["attention"], "FLOP"),
-        "x_proj": ("tensor", fl["x_proj"], "FLOP"),
+        # x_proj has N = R + 2N_state = 132 columns against K = d_inner: about
+        # 130 FLOP per byte, so it is HBM-bound: u in, W_x, dt (fp16) and B|C (fp32) out
+        "x_proj": ("hbm", rows * (s.di * 2 + Rp * 2 + 2 * s.N * 4) + s.xproj_out * s.di * 2, "B"),
         "out_proj": ("tensor", fl["out_proj"], "FLOP"),
         "conv": ("hbm", rows * s.di * (2 + 2), "B"),                       # x in, u out (fp16)
         "fuse_norm": ("hbm", rows * s.di * (2 + 2 + 2), "B"),              # att, g in; s out
@@ -224,12 +227,12 @@ def run_ours(args, rank, world, local_rank):
     ev_sets = [make_events(torch, nev) for _ in range(args.steps)]
     evp = [(ctypes_array(e)) for e in ev_sets]
 
-    def step(i=None):
-        if i is None:
-            hb.hymba_layer_fwd(layer.desc, layer.weights, X, Y, layer.ws, status=layer.status, stream=stream)
-        else:
-            hb.hymba_layer_fwd_events(layer.desc, layer.weights, X, Y, layer.ws, evp[i], nev, status=layer.status,
-                                      stream=stream)
+    def step():
+        hb.hymba_layer_fwd(layer.desc, layer.weights, X, Y, layer.ws, status=layer.status, stream=stream)
+
+    def step_events(i):
+        hb.hymba_layer_fwd_events(layer.desc, layer.weights, X, Y, layer.ws, evp[i], nev, status=layer.status,
+                                  stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -243,9 +246,11 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # the headline: K plain calls (every kernel launched with programmatic
+    # dependent launch, so each may start while the one before it finishes)
     t0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    for _ in range(args.steps):
+        step()
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -254,6 +259,12 @@ def run_ours(args, rank, world, local_rank):
     ms = t0.elapsed_time(t1) / args.steps
     if layer.check_status() != 0:
         raise RuntimeError(f"device status {layer.check_status()} in the timed region")
+    # per-kernel times: a second, instrumented pass of K calls with an event
+    # between every stage (the events break the launch overlap, so these
+    # stages add up to more than the plain step)
+    for i in range(args.steps):
+        step_events(i)
+    torch.cuda.synchronize()
     stage_ms = {name: statistics.mean(ev[k].elapsed_time(ev[k + 1]) for ev in ev_sets)
                 for k, name in enumerate(STAGES)}
     step_each = [ev[0].elapsed_time(ev[len(STAGES)]) for ev in ev_sets]
@@ -273,7 +284,7 @@ def run_ours(args, rank, world, local_rank):
                    "global_batch": s.B * world, "seq_len": s.T, "meta_tokens": s.M, "d_model": s.d,
                    "heads": f"{s.Hq}q/{s.Hkv}kv x 64", "d_inner": s.di, "d_state": s.N, "rope_theta": s.rope_theta,
                    "activations": "fp16 (fp32 accumulate; delta/B/C/state/Y fp32)",
-                   "l2": "inputs larger than L2 (X~ 213 MB, projection 1.19 GB per step)",
+                   "l2": "inputs larger than L2 (X~ 213 MB, projection 1.19 GB per step); no flush",
                    "parallelism": f"dp{world} (independent batches, no collective)"},
         "layer_tflops": round(total_flops / (ms_max / 1e3) / 1e12, 1),
         "roofline_layer": {"bound": "tensor", "achieved_tflops": round(total_flops / (ms_max / 1e3) / 1e12, 1),
@@ -289,10 +300,11 @@ def run_ours(args, rank, world, local_rank):
                                       "fma": "fp32 lanes: 128 per clock per SM x 148 SMs x 2.032 GHz"}[
                                           kernels[dom]["bound"]]),
         "kernels": kernels,
+        # per-stage times from the instrumented pass (events between stages)
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        # each timed call alone (its first to its last stage event), beside the mean over the K steps above
-        "step_ms": {"median": round(statistics.median(step_each), 4), "min": round(min(step_each), 4),
-                    "max": round(max(step_each), 4)},
+        # each instrumented call (its first to its last stage event)
+        "instrumented_step_ms": {"median": round(statistics.median(step_each), 4), "min": round(min(step_each), 4),
+                                 "max": round(max(step_each), 4)},
         "clocks": clk,
         # per layer call: W_out, W_x (bf16 -> fp16 copies) and W_dt conversions, then in_proj,
         # attention, conv, x_proj, scan, fuse_norm, out_proj (the ncu launch list shows the same)
@@ -355,21 +367,42 @@ def load_traffic(kernel):
 
 
 def run_e2e(args, torch, hb, hl, dev, stream):
-    """Same prefill through the C ABI with host buffers: pinned X~ -> device,
-    layer, Y -> pinned host, every step."""
+    """The main prefill through the C ABI from host buffers: every step copies
+    X~ from pinned host memory, runs the layer and copies Y back to pinned host
+    memory.  The batch goes through in chunks of E2E_CHUNK sequences on three
+    streams, so the host-to-device copy of chunk i+1 and the device-to-host
+    copy of chunk i-1 overlap the layer call of chunk i."""
     s = synth.hymba15b_swa(rope_theta=10000.0)
     p = synth.make_layer_inputs(s, 7)
-    layer = hl.HymbaLayer(s, hl.params_to_device(p, s, dev))
+    sc = synth.with_(s, B=E2E_CHUNK)
+    layer = hl.HymbaLayer(sc, hl.params_to_device(p, sc, dev))
     Xh = torch.from_numpy(p["Xt"]).to(torch.bfloat16).pin_memory()
     Yh = torch.empty(s.B, s.L, s.d, dtype=torch.float32).pin_memory()
     Xd = torch.empty_like(Xh, device=dev)
     Yd = torch.empty(Yh.shape, dtype=torch.float32, device=dev)
     del p
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n_chunks = s.B // E2E_CHUNK
+    ev_in = [torch.cuda.Event() for _ in range(n_chunks)]
+    ev_done = [torch.cuda.Event() for _ in range(n_chunks)]
 
     def step():
-        Xd.copy_(Xh, non_blocking=True)
-        hb.hymba_layer_fwd(layer.desc, layer.weights, Xd, Yd, layer.ws, status=layer.status, stream=stream)
-        Yh.copy_(Yd, non_blocking=True)
+        s_in.wait_stream(stream)          # the previous step's reads of Xd are done
+        for c in range(n_chunks):
+            sl = slice(c * E2E_CHUNK, (c + 1) * E2E_CHUNK)
+            with torch.cuda.stream(s_in):
+                Xd[sl].copy_(Xh[sl], non_blocking=True)
+                ev_in[c].record(s_in)
+        for c in range(n_chunks):
+            sl = slice(c * E2E_CHUNK, (c + 1) * E2E_CHUNK)
+            stream.wait_event(ev_in[c])
+            hb.hymba_layer_fwd(layer.desc, layer.weights, Xd[sl], Yd[sl], layer.ws, status=layer.status,
+                               stream=stream)
+            ev_done[c].record(stream)
+            s_out.wait_event(ev_done[c])
+            with torch.cuda.stream(s_out):
+                Yh[sl].copy_(Yd[sl], non_blocking=True)
+        stream.wait_stream(s_out)         # the step ends when Y is on the host
 
     for _ in range(max(2, args.warmup)):
         step()
@@ -383,8 +416,13 @@ def run_e2e(args, torch, hb, hl, dev, stream):
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / n
-    return {"value": round(s.B * s.T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 3),
-            "h2d_bytes_per_step": Xh.numel() * 2, "d2h_bytes_per_step": Yh.numel() * 4}
+    out = {"value": round(s.B * s.T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 3),
+           "h2d_bytes_per_step": Xh.numel() * 2, "d2h_bytes_per_step": Yh.numel() * 4,
+           "pipeline": f"{n_chunks} chunks of {E2E_CHUNK} sequences; H2D, layer and D2H on three streams",
+           "status": layer.check_status()}
+    del layer, Xh, Yh, Xd, Yd
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_prefill_extra(args, torch, hb, hl, dev, stream, s, name):
@@ -488,25 +526,19 @@ def run_block(args, torch, hb, hl, dev, stream):
 
 
 def run_stack(args, torch, hb, hl, dev, stream):
+    """The 300M-ablation 4-layer stack, one hymba_stack_fwd call per step (the
+    fp32 stream and its bf16 copy for the next layer are written by each
+    layer's output projection; layer 2 reads layer 1's K/V)."""
     shapes = [synth.with_(s, rope_theta=10000.0) for s in synth.ablation300m_stack()]
     tok, layers = synth.make_stack_inputs(shapes, seed=3)
-    L = [hl.HymbaLayer(s, hl.params_to_device(p, s, dev), residual_mode=2)
-         for p, s in zip(layers, shapes)]
+    st = hl.HymbaStack(shapes, [hl.params_to_device(p, s, dev) for p, s in zip(layers, shapes)])
     s0 = shapes[0]
-    X0 = torch.from_numpy(tok["Xt"]).to(dev)
-    y = torch.empty_like(X0)
-    xb = torch.empty(X0.shape, dtype=torch.bfloat16, device=dev)
-    kd = hl.kv_dtype(s0)
-    kv = (torch.empty(s0.B, s0.L, s0.Hkv, s0.dh, device=dev, dtype=kd),
-          torch.empty(s0.B, s0.L, s0.Hkv, s0.dv, device=dev, dtype=kd))
-    kvs = hb.KV(kv[0].data_ptr(), kv[1].data_ptr())
+    X0 = hl.tokens_to_device(tok["Xt"], s0, dev)
+    y = torch.empty(s0.B, s0.L, s0.d, dtype=torch.float32, device=dev)
+    del tok, layers
 
     def step():
-        y.copy_(X0)
-        for i, (lay, s) in enumerate(zip(L, shapes)):
-            xb.copy_(y)
-            hb.hymba_layer_fwd(lay.desc, lay.weights, xb, y, lay.ws, kv_in=kvs if s.kv_shared else None,
-                               kv_out=kvs if i == 1 else None, status=lay.status, stream=stream)
+        hb.hymba_stack_fwd(st.descs, st.weights, X0, y, st.ws, status=st.status, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -526,10 +558,8 @@ def run_stack(args, torch, hb, hl, dev, stream):
         tot += fl["in_proj"] + fl["attention"] + fl["x_proj"] + fl["dt_proj"] + fl["out_proj"]
     out = {"workload": "300M-ablation 4-layer stack (global, SWA x3, layers 1->2 share K/V), batch 32 x (2048 + 128)",
            "value": round(s0.B * s0.T / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
-           "tflops": round(tot / (ms / 1e3) / 1e12, 1),
-           "note": "includes the fp32 residual copy and bf16 casts between layers",
-           "status": max(l.check_status() for l in L)}
-    del L, X0, y, xb, kv
+           "tflops": round(tot / (ms / 1e3) / 1e12, 1), "call": "hymba_stack_fwd", "status": st.check_status()}
+    del st, X0, y
     torch.cuda.empty_cache()
     return out
 
@@ -649,11 +679,24 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
 def cpu_baseline(args):
     T = args.cpu_sample_tokens
     toks, sec = oracle_sample(T, 11)
     n_dec, sec_dec = oracle_decode_sample(16, 12)
-    return {"value": round(toks / sec, 2), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+    return {"value": round(toks / sec, 2), "unit": "tokens/s", "cores": cpu_cores(), "cpu_model": cpu_model(),
+            "kind": "oracle",
             "sample": f"float64 NumPy oracle, 1 sequence x ({T} + 128 meta) tokens at the 1.5B SWA shapes, "
                       f"{sec:.1f} s",
             "decode": {"value": round(n_dec / sec_dec, 2), "unit": "tokens/s",
@@ -679,9 +722,39 @@ def run_reference(args, rank, world):
             "data": "synthetic (seeded)",
             "config": {"workload": "Hymba-1.5B-shaped SWA layer prefill (bounded sample: 1 sequence per step)",
                        "seq_len": T, "meta_tokens": 128, "parallelism": "host CPU"},
-            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": cpu_cores(), "cpu_model": cpu_model(),
+                             "kind": "oracle",
                              "sample": f"1 sequence x ({T} + 128 meta) tokens per step, float64 NumPy"},
             "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def relaunch_ranks(args_argv, n: int, backend_env: dict = None) -> int:
+    """--gpus N from a plain `python bench.py` (no torchrun around it): start
+    N ranks of this script under torch.distributed.run on this node, one per
+    GPU, rendezvous on 127.0.0.1, and return their exit status (rank 0 prints
+    the JSON line)."""
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *args_argv]
+    env = dict(os.environ)
+    env.update(backend_env or {})
+    return subprocess.call(cmd, env=env)
+
+
+def run_dry_cpu(args, rank, world):
+    """CPU stand-in of the multi-rank step for host-side tests (gloo): every
+    rank reports a fixed step time for its own batch; the job's time is the
+    slowest rank's, its throughput the tokens of all ranks."""
+    import torch.distributed as dist
+    ms_local = 10.0 + rank
+    ms_max, value = job_throughput(ms_local, 8 * 8192, world, "cpu")
+    if world > 1:
+        dist.barrier()
+    return {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "scaling": "weak", "dry_run": "cpu"}
 
 
 def main():
@@ -698,9 +771,12 @@ def main():
     ap.add_argument("--batch", type=int, default=8, help="sequences in the main prefill workload")
     ap.add_argument("--only-decode", action="store_true",
                     help="time only the decode step (used for profiler runs)")
+    ap.add_argument("--dry-run-cpu", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(relaunch_ranks(sys.argv[1:], args.gpus))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -708,6 +784,16 @@ def main():
         out = run_reference(args, rank, world)
         if out is not None:
             print(json.dumps(out), flush=True)
+        return
+    if args.dry_run_cpu:
+        import torch.distributed as dist
+        if world > 1:
+            dist.init_process_group("gloo")
+        out = run_dry_cpu(args, rank, world)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
         return
     if world > 1:
         import torch

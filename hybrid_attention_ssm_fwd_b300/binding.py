@@ -113,6 +113,11 @@ def lib() -> ctypes.CDLL:
     L.hymba_block_fwd.argtypes = [P(LayerDesc), P(BlockWeights), c_int32, c_void_p, c_void_p, c_size_t, c_void_p,
                                   c_void_p]
     L.hymba_block_fwd.restype = c_int32
+    L.hymba_stack_fwd_workspace.argtypes = [c_int32, P(LayerDesc)]
+    L.hymba_stack_fwd_workspace.restype = c_size_t
+    L.hymba_stack_fwd.argtypes = [c_int32, P(LayerDesc), P(LayerWeights), c_void_p, c_void_p, c_void_p, c_size_t,
+                                  c_void_p, c_void_p]
+    L.hymba_stack_fwd.restype = c_int32
     L.hymba_test_gemm.argtypes = [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p, c_int32,
                                   c_void_p, c_int32, c_void_p, c_void_p]
     L.hymba_test_gemm.restype = c_int32
@@ -266,6 +271,31 @@ def hymba_block_fwd(desc: LayerDesc, weights: BlockWeights, d_ff: int, x, ws, st
     rc = lib().hymba_block_fwd(ctypes.byref(desc), ctypes.byref(weights), d_ff, px, _arg(ws, "hymba_block_fwd ws"),
                                ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
     return _check(rc, "hymba_block_fwd") if check else rc
+
+
+def make_stack(descs, weights):
+    """ctypes arrays of layer descriptors and weight structs for hymba_stack_fwd."""
+    n = len(descs)
+    da = (LayerDesc * n)(*descs)
+    wa = (LayerWeights * n)(*weights)
+    return da, wa
+
+
+def stack_fwd_workspace(descs) -> int:
+    return lib().hymba_stack_fwd_workspace(len(descs), descs)
+
+
+def hymba_stack_fwd(descs, weights, x, y, ws, status=None, stream=None, check: bool = True) -> int:
+    """The residual stack over x (bf16 [B, L, d]) into y (fp32), see
+    include/hymba.h; descs/weights are the arrays make_stack returns."""
+    import torch
+    d0 = descs[0]
+    n = d0.batch * (d0.n_tokens + d0.n_meta) * d0.d_model
+    px = _arg(x, "hymba_stack_fwd x", torch.bfloat16, n)
+    py = _arg(y, "hymba_stack_fwd y", torch.float32, n)
+    rc = lib().hymba_stack_fwd(len(descs), descs, weights, px, py, _arg(ws, "hymba_stack_fwd ws"),
+                               ws.numel() * ws.element_size(), _ptr(status), _stream(stream))
+    return _check(rc, "hymba_stack_fwd") if check else rc
 
 
 def make_meta(m: Dict[str, "object"]) -> Meta:

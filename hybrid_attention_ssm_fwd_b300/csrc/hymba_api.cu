@@ -319,7 +319,8 @@ struct MetaCtx {
 
 hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const void* X, float* Y,
                       const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
-                      int32_t* status, Marks& mk, cudaStream_t st, const MetaCtx& mc = MetaCtx{}) {
+                      int32_t* status, Marks& mk, cudaStream_t st, const MetaCtx& mc = MetaCtx{},
+                      __nv_bfloat16* y_bf16 = nullptr) {
   const int sms = num_sms();
   const hymba_meta* mi = mc.in;
   const int rows = static_cast<int>(x.rows);
@@ -406,6 +407,8 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     p.resid = x.residual == 1 ? static_cast<const __nv_bfloat16*>(X) : nullptr;
     p.resid_f32 = x.residual == 2 ? Y : nullptr;
     p.ld_resid = x.d;
+    p.C2 = y_bf16;  // a stack's next layer input: Y rounded to bf16
+    p.ldc2 = x.d;
     TRY(gemm_tc(0, s, x.sw, at<__half>(ws, pl.wout), x.sw, EPI_F32, p, 0, 1, sms, st));
   }
   mk.mark();
@@ -870,6 +873,94 @@ hymba_status hymba_block_fwd(const hymba_layer_desc* d, const hymba_block_weight
     p.resid_f32 = xs;
     p.ld_resid = x.d;
     TRY(gemm_tc(0, h, d_ff, wdown, d_ff, EPI_F32, p, 0, 1, sms, st));
+  }
+  return HYMBA_OK;
+}
+
+// ---- residual stack ---------------------------------------------------------
+
+namespace {
+
+constexpr int kMaxStackLayers = 256;
+
+struct StackPlan {
+  size_t layer_ws, xb, kv_k, kv_v, total;
+};
+
+// Every layer on the bf16 path, one batch shape, residual 0 (the stack adds
+// the stream), no K/V sharing into layer 0.  dims[l] get residual 1 for layer
+// 0 (Y = X~ + layer) and 2 after (Y += layer, in place).
+hymba_status stack_dims(int32_t n, const hymba_layer_desc* d, Dims* dims, StackPlan* sp) {
+  if (n < 1 || n > kMaxStackLayers || !d) return HYMBA_ERR_INVALID;
+  StackPlan p{};
+  size_t kv_k = 0, kv_v = 0;
+  for (int l = 0; l < n; ++l) {
+    TRY(check_desc(&d[l], false, &dims[l]));
+    const Dims& x = dims[l];
+    if (d[l].residual != 0) return HYMBA_ERR_INVALID;
+    if (x.dtype != HYMBA_BF16) return HYMBA_ERR_UNSUPPORTED;
+    if (x.B != dims[0].B || x.L != dims[0].L || x.M != dims[0].M || x.d != dims[0].d) return HYMBA_ERR_INVALID;
+    if (x.kv_shared) {
+      if (l == 0) return HYMBA_ERR_INVALID;
+      const Dims& pr = dims[l - 1];
+      if (pr.Hkv != x.Hkv || pr.dh != x.dh || pr.dv != x.dv) return HYMBA_ERR_INVALID;
+      kv_k = std::max(kv_k, static_cast<size_t>(x.rows) * x.Hkv * x.dh * 2);
+      kv_v = std::max(kv_v, static_cast<size_t>(x.rows) * x.Hkv * x.dv * 2);
+    }
+    dims[l].residual = l == 0 ? 1 : 2;
+    p.layer_ws = std::max(p.layer_ws, plan_ws(dims[l], false).total);
+  }
+  size_t off = align_up(p.layer_ws, 256);
+  p.xb = off;
+  off = align_up(off + static_cast<size_t>(dims[0].rows) * dims[0].d * 2, 256);
+  p.kv_k = off;
+  off = align_up(off + kv_k, 256);
+  p.kv_v = off;
+  off = align_up(off + kv_v, 256);
+  p.total = off;
+  *sp = p;
+  return HYMBA_OK;
+}
+
+}  // namespace
+
+size_t hymba_stack_fwd_workspace(int32_t n_layers, const hymba_layer_desc* descs) {
+  if (n_layers < 1 || n_layers > kMaxStackLayers) return 0;
+  Dims dims[kMaxStackLayers];
+  StackPlan sp;
+  if (stack_dims(n_layers, descs, dims, &sp) != HYMBA_OK) return 0;
+  return sp.total;
+}
+
+hymba_status hymba_stack_fwd(int32_t n_layers, const hymba_layer_desc* descs, const hymba_layer_weights* weights,
+                             const void* x_in, float* y, void* ws, size_t ws_bytes, int32_t* dev_status,
+                             void* stream) {
+  if (n_layers < 1 || n_layers > kMaxStackLayers) return HYMBA_ERR_INVALID;
+  Dims dims[kMaxStackLayers];
+  StackPlan sp;
+  TRY(stack_dims(n_layers, descs, dims, &sp));
+  if (!weights || !x_in || !y || !ws) return HYMBA_ERR_INVALID;
+  for (int l = 0; l < n_layers; ++l) TRY(check_weights(&weights[l], dims[l]));
+  if (!aligned(x_in, 16) || !aligned(y, 16) || !aligned(ws, 256)) return HYMBA_ERR_INVALID;
+  if (ws_bytes < sp.total) return HYMBA_ERR_WORKSPACE;
+  const size_t stream_bytes = static_cast<size_t>(dims[0].rows) * dims[0].d;
+  const char* xb0 = static_cast<const char*>(x_in);
+  const char* yb0 = reinterpret_cast<const char*>(y);
+  if (xb0 < yb0 + stream_bytes * 4 && yb0 < xb0 + stream_bytes * 2) return HYMBA_ERR_INVALID;  // y may not overlap x
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  __nv_bfloat16* xb = at<__nv_bfloat16>(ws, sp.xb);
+  hymba_kv kv{at<void>(ws, sp.kv_k), at<void>(ws, sp.kv_v)};
+  for (int l = 0; l < n_layers; ++l) {
+    const Dims& x = dims[l];
+    const bool last = l + 1 == n_layers;
+    // export K/V when the next layer shares them (a shared layer's K/V are
+    // already in the buffer)
+    const bool export_kv = !last && dims[l + 1].kv_shared && !x.kv_shared;
+    Marks mk;
+    mk.st = st;
+    TRY(fwd_bf16(x, plan_ws(x, false), &weights[l], l == 0 ? x_in : xb, y, nullptr, x.kv_shared ? &kv : nullptr,
+                 export_kv ? &kv : nullptr, ws, dev_status, mk, st, MetaCtx{}, last ? nullptr : xb));
   }
   return HYMBA_OK;
 }

@@ -57,6 +57,21 @@ def alloc_cache(shape, cap: int, device="cuda", with_kv: bool = True) -> Dict[st
     return c
 
 
+def cache_row(cache: Dict[str, torch.Tensor], b: int) -> Dict[str, torch.Tensor]:
+    """Views of row b of a batch cache, for a batch-1 call: the per-sequence
+    tensors sliced at b (their data pointers offset by b rows), the meta K/V
+    shared.  A batch-1 prefill with this as cache_out admits a new sequence
+    into row b of a running batch."""
+    out = {k: cache[k][b:b + 1] for k in ("ssm_state", "conv_state", "pos") if k in cache}
+    for k in ("k_ring", "v_ring"):
+        if k in cache:
+            out[k] = cache[k][b:b + 1]
+    for k in ("k_meta", "v_meta"):
+        if k in cache:
+            out[k] = cache[k]
+    return out
+
+
 def cache_to_device(c: Dict[str, np.ndarray], shape, device="cuda") -> Dict[str, torch.Tensor]:
     dt = storage_dtype(shape)
     out = {}
@@ -196,6 +211,35 @@ class HymbaBlock:
         """x: [B, L, d] fp32 stream, updated in place and returned."""
         hb.hymba_block_fwd(self.desc, self.weights, self.d_ff, x, self.ws, status=self.status)
         return x
+
+    def check_status(self) -> int:
+        return int(self.status.item())
+
+
+class HymbaStack:
+    """A residual stack X_{l+1} = X_l + Y_l(bf16(X_l)) of hybrid-head layers
+    on one device, run by one hymba_stack_fwd call (a kv_shared layer reads
+    the previous layer's K/V)."""
+
+    def __init__(self, shapes, params, wait_limit_us: int = 0):
+        self.shapes = list(shapes)
+        self.params = list(params)
+        descs = [hb.make_desc(s, wait_limit_us, residual_mode=0) for s in self.shapes]
+        self.descs, self.weights = hb.make_stack(descs, [hb.make_weights(p) for p in self.params])
+        nbytes = hb.stack_fwd_workspace(self.descs)
+        if nbytes == 0:
+            raise hb.HymbaError(hb.HYMBA_ERR_INVALID, "stack workspace query")
+        dev = self.params[0]["W_in"].device
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def forward(self, x: torch.Tensor, y: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """x: [B, L, d] bf16; returns the fp32 stream after the last layer."""
+        s = self.shapes[0]
+        if y is None:
+            y = torch.empty(s.B, s.L, s.d, dtype=torch.float32, device=x.device)
+        hb.hymba_stack_fwd(self.descs, self.weights, x, y, self.ws, status=self.status)
+        return y
 
     def check_status(self) -> int:
         return int(self.status.item())

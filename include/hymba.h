@@ -291,6 +291,36 @@ HYMBA_API hymba_status hymba_block_fwd(const hymba_layer_desc* d, const hymba_bl
                                        float* x, void* ws, size_t ws_bytes, int32_t* dev_status,
                                        void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Residual stack of hybrid-head layers over one batch (the stacks of the
+ * Hymba page's 300M-parameter design roadmap, section 2 and Table 1;
+ * consecutive layers may share K/V, section 2.2):
+ *     X_{l+1} = X_l + Y_l( bf16(X_l) ),   X_0 = x
+ * The stream X_l is fp32; each layer reads it rounded to bf16 (its input
+ * type); a layer with desc.kv_shared reads the previous layer's post-RoPE
+ * K/V.  The Hymba pages describe no pre-norm or FFN for this stack.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of scratch memory hymba_stack_fwd needs (0 on invalid descs).      */
+HYMBA_API size_t hymba_stack_fwd_workspace(int32_t n_layers, const hymba_layer_desc* descs);
+
+/* Runs n_layers (1..256) layers back to back on `stream`.
+ *   descs    [n_layers] host array: HYMBA_BF16, the same batch, n_tokens,
+ *            n_meta and d_model in every layer; residual must be 0 (the
+ *            stack adds the stream itself); layer 0 may not be kv_shared,
+ *            and a kv_shared layer has its producer's n_kv_heads, head_dim
+ *            and v_head_dim.
+ *   weights  [n_layers] host array of device-pointer structs.
+ *   x        [B, L, d] device bf16: X_0 with the meta rows first.
+ *   y        [B, L, d] device fp32 (must not overlap x): the stream after
+ *            the last layer.
+ *   ws       device scratch, ws_bytes >= hymba_stack_fwd_workspace().
+ * Errors as hymba_layer_fwd, every descriptor validated before anything is
+ * launched.                                                                 */
+HYMBA_API hymba_status hymba_stack_fwd(int32_t n_layers, const hymba_layer_desc* descs,
+                                       const hymba_layer_weights* weights, const void* x, float* y, void* ws,
+                                       size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* Bytes of scratch memory hymba_layer_decode needs for `d` (0 on invalid). */
 HYMBA_API size_t hymba_layer_decode_workspace(const hymba_layer_desc* d);
 

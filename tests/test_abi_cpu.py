@@ -203,6 +203,34 @@ def test_block_workspace_and_argument_checks():
     assert rc == hb.HYMBA_ERR_WORKSPACE
 
 
+def test_stack_workspace_and_argument_checks():
+    """hymba_stack_fwd: descriptors validated before any launch (one batch
+    shape, residual 0, no sharing into layer 0, bf16 only), the workspace
+    covers the largest layer plus the bf16 stream and the shared K/V."""
+    shapes = synth.ablation300m_stack(B=2, T=100, M=16)
+    descs = [hb.make_desc(s, residual_mode=0) for s in shapes]
+    da, wa = hb.make_stack(descs, [_fake_weights() for _ in shapes])
+    n = hb.stack_fwd_workspace(da)
+    assert n > max(hb.layer_fwd_workspace(d) for d in descs)
+    L = hb.lib()
+    assert L.hymba_stack_fwd_workspace(0, da) == 0
+    bad = [hb.make_desc(s, residual_mode=0) for s in shapes]
+    bad[0].residual = 2
+    assert hb.stack_fwd_workspace(hb.make_stack(bad, [_fake_weights()] * 4)[0]) == 0
+    bad = [hb.make_desc(s, residual_mode=0) for s in shapes]
+    bad[1].batch = 3
+    assert hb.stack_fwd_workspace(hb.make_stack(bad, [_fake_weights()] * 4)[0]) == 0
+    bad = [hb.make_desc(s, residual_mode=0) for s in shapes[2:]]   # starts with the shared layer
+    assert hb.stack_fwd_workspace(hb.make_stack(bad, [_fake_weights()] * 2)[0]) == 0
+    bad = [hb.make_desc(synth.with_(s, dtype="f32"), residual_mode=0) for s in shapes]
+    assert hb.stack_fwd_workspace(hb.make_stack(bad, [_fake_weights()] * 4)[0]) == 0
+    x, y = 0x200000, 0x40000000
+    assert L.hymba_stack_fwd(4, da, wa, x, y, ctypes.c_void_p(0x100000), 16, None, None) == hb.HYMBA_ERR_WORKSPACE
+    assert L.hymba_stack_fwd(4, da, wa, x, x, ctypes.c_void_p(0x100000), 1 << 40, None, None) == hb.HYMBA_ERR_INVALID
+    assert L.hymba_stack_fwd(4, da, None, x, y, ctypes.c_void_p(0x100000), 1 << 40, None, None) == \
+        hb.HYMBA_ERR_INVALID
+
+
 def test_fusion_flag_values():
     assert hb.layer_fwd_workspace(_desc(fusion=1)) > hb.layer_fwd_workspace(_desc(fusion=0))   # s rows 2 di wide
     assert hb.layer_fwd_workspace(_desc(fusion=2)) == 0

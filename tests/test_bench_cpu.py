@@ -74,6 +74,11 @@ def test_stage_rooflines_dominant_kernel_and_scan_bounds():
     # four fp32 operations per state and row, against 128 lanes per SM: the same fraction
     assert kernels["scan_fma"]["frac"] == pytest.approx(kernels["scan"]["frac"], abs=1e-4)
     assert kernels["in_proj"]["frac"] == pytest.approx(1908.4e9 / 1.40e-3 / 1e12 / peaks["bf16_tflops"], rel=1e-3)
+    # x_proj against HBM: u (fp16) in, dt (fp16, R padded to 8) and B|C (fp32) out, W_x once:
+    # 66560 * (3200*2 + 104*2 + 32*4) + 132*3200*2 bytes
+    xb = rows * (s.di * 2 + 104 * 2 + 32 * 4) + 132 * s.di * 2
+    assert kernels["x_proj"]["bound"] == "hbm"
+    assert kernels["x_proj"]["frac"] == pytest.approx(xb / 0.13e-3 / 1e9 / peaks["hbm_gbs"], rel=1e-3)
     # the longest stage wins even when it is not the scan
     stage_ms["in_proj"] = 2.0
     assert bench.stage_rooflines(s, stage_ms, peaks)[1] == "in_proj"
@@ -85,5 +90,6 @@ def test_cpu_baseline_line():
     from types import SimpleNamespace
     cb = bench.cpu_baseline(SimpleNamespace(cpu_sample_tokens=64))
     assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["value"] > 0 and cb["cores"] >= 1
+    assert isinstance(cb["cpu_model"], str) and cb["cpu_model"]
     assert "64 + 128 meta" in cb["sample"]
     assert cb["decode"]["unit"] == "tokens/s" and cb["decode"]["value"] > 0

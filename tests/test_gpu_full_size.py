@@ -18,10 +18,10 @@ all of them, so both ends of the batch and of the sequence are covered.
   sequences (first, middle, last); pos of all.
 * 300M-ablation-shaped 4-layer stack (global, then three SWA layers; layers
   1 -> 2 share K/V), batch 32 x (2048 + 128): every row of the last sequence
-  after every layer, each layer fed the oracle's stream for that sequence
-  (the tolerance is per output; chained, the residual stream would carry
-  the sum of the layers' errors, which stays within the relative bound but
-  not the absolute one by layer 2).
+  after every layer, chained through the fp32 residual stream exactly as the
+  benchmark runs it (each layer reads the stream rounded to bf16).
+* The full residual block around the SWA layer (gated MLP, F = 3 d), batch
+  8 x (8192 + 128): sampled rows against the row-wise block oracle.
 """
 import numpy as np
 import pytest
@@ -80,12 +80,12 @@ def test_full_size_decode_batch128_sampled_sequences():
     assert np.all(c["pos"] == 8193)
 
 
-def test_full_size_stack_each_layer_last_sequence():
-    """Each layer of the stack on its own: before layer i the last sequence's
-    stream is set to the oracle's stream entering layer i (the other 31 keep
-    the GPU's), so the comparison after layer i measures that layer's error,
-    not the sum the residual stream carries from the layers before it.  The
-    K/V that layer 2 reuses come from the GPU's layer 1 on that same input."""
+def test_full_size_stack_chained_last_sequence():
+    """The 4-layer stack chained with no reset between layers: the stream
+    y (fp32) enters each layer rounded to bf16 and the layer adds into it
+    (residual mode 2); layer 2 reuses layer 1's exported K/V.  Every row of
+    the last sequence after every layer against the oracle's stack, which
+    rounds each layer's input the same way."""
     shapes = [synth.with_(s, rope_theta=10000.0) for s in synth.ablation300m_stack()]
     tok, layers = synth.make_stack_inputs(shapes, seed=3)
     b = shapes[0].B - 1
@@ -93,8 +93,6 @@ def test_full_size_stack_each_layer_last_sequence():
     y = torch.from_numpy(tok["Xt"].astype(np.float32)).cuda()
     kv = None
     for i, (p, s) in enumerate(zip(layers, shapes)):
-        if i > 0:
-            y[b] = torch.from_numpy(out["Y"][i - 1][0].astype(np.float32)).cuda()
         X = y.to(torch.bfloat16)
         layer = hl.HymbaLayer(s, hl.params_to_device(p, s), residual_mode=2)
         kv_out = None
@@ -109,3 +107,41 @@ def test_full_size_stack_each_layer_last_sequence():
         if kv_out is not None:
             kv = kv_out
         del layer, X
+
+
+def test_full_size_stack_call_last_sequence():
+    """The same stack through one hymba_stack_fwd call, as the benchmark
+    times it: the final stream of the last sequence, every row."""
+    shapes = [synth.with_(s, rope_theta=10000.0) for s in synth.ablation300m_stack()]
+    tok, layers = synth.make_stack_inputs(shapes, seed=3)
+    b = shapes[0].B - 1
+    out = ref.stack_fwd(layers, tok["Xt"][b:b + 1], [synth.with_(s, B=1) for s in shapes])
+    st = hl.HymbaStack(shapes, [hl.params_to_device(p, s) for p, s in zip(layers, shapes)])
+    y = st.forward(hl.tokens_to_device(tok["Xt"], shapes[0]))
+    torch.cuda.synchronize()
+    assert st.check_status() == 0
+    assert_bf16_close(y[b].cpu().numpy(), out["Y"][-1][0], f"stack call, batch 32 x 2K, sequence {b}")
+
+
+def test_full_size_block_sampled_rows():
+    """hymba_block_fwd over batch 8 x (8192 + 128) at the 1.5B shapes with
+    F = 3 d, as the benchmark runs it, against block_fwd_rows on sampled
+    rows of the first and last sequences."""
+    from oracle import block_ref as br
+    s = synth.hymba15b_swa(rope_theta=10000.0)
+    d_ff = 3 * s.d
+    tok, blocks = synth.make_block_inputs(s, d_ff, 4)
+    blk = hl.HymbaBlock(s, hl.block_params_to_device(blocks[0], s), d_ff)
+    x = torch.from_numpy(tok["Xt"]).cuda()
+    blk.forward(x)
+    torch.cuda.synchronize()
+    assert blk.check_status() == 0
+    y = x.cpu().numpy()
+    assert np.all(np.isfinite(y))
+    del blk, x
+    rows = _rows(s)
+    early = rows[rows <= s.M + 1025]
+    last = s.B - 1
+    assert_bf16_close(y[0, early], br.block_fwd_rows(blocks[0], tok["Xt"][:1], s, early)[0], "block, sequence 0")
+    assert_bf16_close(y[last, rows], br.block_fwd_rows(blocks[0], tok["Xt"][last:], s, rows)[0],
+                      f"block, sequence {last}")

@@ -96,6 +96,24 @@ def test_bf16_prefill_many_row_blocks():
     assert_bf16_close(y, yr, "1047 rows")
 
 
+@pytest.mark.parametrize("n_layers", [4, 3, 1])
+def test_bf16_stack_call_matches_oracle(n_layers):
+    """hymba_stack_fwd (global layer, window layer exporting K/V, window
+    layer reusing them, window layer) against the oracle's stack, which
+    rounds each layer's input to bf16 and adds the unrounded stream."""
+    shapes = synth.ablation300m_stack(B=2, T=200, M=16, d=128, Hq=4, Hkv=2, di=256)[:n_layers]
+    shapes = [synth.with_(s, window=(0 if i == 0 else 64), rope_theta=10000.0) for i, s in enumerate(shapes)]
+    tok, layers = synth.make_stack_inputs(shapes, seed=23)
+    out = ref.stack_fwd(layers, tok["Xt"], shapes)
+    st = hl.HymbaStack(shapes, [hl.params_to_device(p, s) for p, s in zip(layers, shapes)])
+    x = hl.tokens_to_device(tok["Xt"], shapes[0])
+    for rep in range(2):                  # the call leaves x intact: a second call gives the same stream
+        y = st.forward(x)
+        torch.cuda.synchronize()
+        assert st.check_status() == 0
+        assert_bf16_close(y.cpu().numpy(), out["Y"][-1], f"stack of {n_layers}, call {rep}")
+
+
 def test_bf16_beta_isolation():
     """beta2 = 0 leaves only the attention branch, beta1 = 0 only the SSM one."""
     s = small_bf16()

@@ -89,3 +89,24 @@ def test_reference_arm_runs_on_rank0_only(rank, expect_line):
         assert len(lines) == 1
         d = json.loads(lines[0])
         assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_bench_gpus_2_launches_two_ranks():
+    """`python bench.py --gpus 2` without torchrun around it starts two ranks
+    itself (torch.distributed.run on 127.0.0.1); with the CPU dry run they
+    meet over gloo, and rank 0 prints one line with n_gpus 2 and the slower
+    rank's step time."""
+    import json
+    env = dict(os.environ)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--dry-run-cpu",
+                        "--steps", "2", "--warmup", "3"], capture_output=True, text=True, timeout=240, env=env,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    assert out["n_gpus"] == 2
+    assert out["ms_per_step"] == 11.0                     # ranks report 10 + rank ms
+    assert out["value"] == pytest.approx(2 * 8 * 8192 / 11e-3, rel=1e-6)
