@@ -354,21 +354,9 @@ __global__ void __launch_bounds__(192, 1)
                 if (j < valid) v[j] += rr[j];
             }
             store_f32x32(reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col, v, valid);
-            if (p.C2) {  // the updated stream rounded to bf16: the next layer's input
-              __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C2) + static_cast<long long>(row) * p.ldc2 + col;
-#pragma unroll
-              for (int g = 0; g < 4; ++g) {
-                if (g * 8 < valid) {
-                  uint4 q;
-                  uint32_t* q32 = reinterpret_cast<uint32_t*>(&q);
-#pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(v[g * 8 + 2 * e], v[g * 8 + 2 * e + 1]);
-                    q32[e] = *reinterpret_cast<uint32_t*>(&h);
-                  }
-                  *reinterpret_cast<uint4*>(dst + g * 8) = q;
-                }
-              }
+            if (p.C2) {  // the updated stream rounded to fp16: the next layer's input
+              over |= any_over_half(v);
+              store_f16x32(reinterpret_cast<__half*>(p.C2) + static_cast<long long>(row) * p.ldc2 + col, v, valid);
             }
           } else if (EPI == EPI_GEGLU) {
             // exact GeLU, x Phi(x) with Phi from erff; 16 outputs per 32 columns

@@ -10,7 +10,7 @@ enum GemmEpi : int {
   EPI_F16 = 0,       // fp16 store (+ RoPE on columns < rope_cols, head_dim 64)
   EPI_XPROJ = 1,     // columns < R -> C2 fp16 (dt input); R..N-1 -> C fp32 at col-R
   EPI_SOFTPLUS = 2,  // C fp32 = softplus(acc + bias[col])
-  EPI_F32 = 3,       // C fp32 = acc (+ bf16 or fp32 residual); also C2 bf16 = the same value when C2 is set
+  EPI_F32 = 3,       // C fp32 = acc (+ bf16 or fp32 residual); also C2 fp16 = the same value when C2 is set
   EPI_PARTIAL = 4,   // C fp32 + split*M*ldc = acc (split-K partial sums)
   EPI_ATOMIC = 5,    // C fp32 += acc with vector atomics (split-K into a cleared or residual C)
   EPI_GEGLU = 6,     // columns (2j, 2j+1) = (gate j, up j): C fp16 [., N/2] = GeLU(gate) * up (N % 16 == 0)

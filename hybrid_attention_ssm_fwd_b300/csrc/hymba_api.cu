@@ -286,9 +286,11 @@ hymba_status convert_weights(const Dims& x, const Plan& pl, const hymba_layer_we
   return HYMBA_OK;
 }
 
+// X is bf16 against the bf16 W_in, or fp16 against an fp16 copy of W_in
+// (w_in_f16 set: a residual stack's later layers).
 hymba_status in_proj_bf16(const Dims& x, const void* X, const hymba_layer_weights* w, __half* proj, int rows,
                           const int32_t* pos, int pos_base, int rows_per_seq, int32_t* status, int sms,
-                          cudaStream_t st) {
+                          cudaStream_t st, const __half* w_in_f16 = nullptr) {
   GemmParams p = gp(rows, x.P_in, x.d, status, x.wait_ns);
   p.C = proj;
   p.ldc = x.P_in;
@@ -300,7 +302,10 @@ hymba_status in_proj_bf16(const Dims& x, const void* X, const hymba_layer_weight
   p.rows_per_seq = rows_per_seq;
   p.pos = pos;
   p.pos_base = pos_base;
-  TRY(gemm_tc(1, X, x.d, w->W_in, x.d, EPI_F16, p, 0, 1, sms, st));
+  if (w_in_f16)
+    TRY(gemm_tc(0, X, x.d, w_in_f16, x.d, EPI_F16, p, 0, 1, sms, st));
+  else
+    TRY(gemm_tc(1, X, x.d, w->W_in, x.d, EPI_F16, p, 0, 1, sms, st));
   if (x.theta > 0 && !fused_rope) {
     TRY(rope_simt<__half>(proj, x.P_in, rows, 0, x.Hq, x.dh, x.theta, rows_per_seq, pos, pos_base, st));
     if (!x.kv_shared)
@@ -317,10 +322,18 @@ struct MetaCtx {
   const hymba_meta* out = nullptr;
 };
 
+// A residual stack's plumbing: the layer reads X in fp16 against an fp16
+// copy of W_in (w_in_f16), and out_proj also writes the updated stream
+// rounded to fp16 (y_f16), the next layer's input.
+struct StackIO {
+  const __half* w_in_f16 = nullptr;
+  __half* y_f16 = nullptr;
+};
+
 hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* w, const void* X, float* Y,
                       const hymba_cache* cache_out, const hymba_kv* kv_in, const hymba_kv* kv_out, void* ws,
                       int32_t* status, Marks& mk, cudaStream_t st, const MetaCtx& mc = MetaCtx{},
-                      __nv_bfloat16* y_bf16 = nullptr) {
+                      const StackIO& sio = StackIO{}) {
   const int sms = num_sms();
   const hymba_meta* mi = mc.in;
   const int rows = static_cast<int>(x.rows);
@@ -336,7 +349,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
   TRY(convert_weights(x, pl, w, ws, st));
   mk.mark();
   // positions: logical (meta rows first), so real rows start at M when the meta rows are cached
-  TRY(in_proj_bf16(x, X, w, proj, rows, nullptr, mi ? x.M : 0, x.L, status, sms, st));
+  TRY(in_proj_bf16(x, X, w, proj, rows, nullptr, mi ? x.M : 0, x.L, status, sms, st, sio.w_in_f16));
   mk.mark();
 
   const __half* Kp = x.kv_shared ? static_cast<const __half*>(kv_in->k) : proj + x.k_col;
@@ -407,7 +420,7 @@ hymba_status fwd_bf16(const Dims& x, const Plan& pl, const hymba_layer_weights* 
     p.resid = x.residual == 1 ? static_cast<const __nv_bfloat16*>(X) : nullptr;
     p.resid_f32 = x.residual == 2 ? Y : nullptr;
     p.ld_resid = x.d;
-    p.C2 = y_bf16;  // a stack's next layer input: Y rounded to bf16
+    p.C2 = sio.y_f16;  // a stack's next layer input: the stream rounded to fp16
     p.ldc2 = x.d;
     TRY(gemm_tc(0, s, x.sw, at<__half>(ws, pl.wout), x.sw, EPI_F32, p, 0, 1, sms, st));
   }
@@ -884,7 +897,7 @@ namespace {
 constexpr int kMaxStackLayers = 256;
 
 struct StackPlan {
-  size_t layer_ws, xb, kv_k, kv_v, total;
+  size_t layer_ws, xs, w16, kv_k, kv_v, total;
 };
 
 // Every layer on the bf16 path, one batch shape, residual 0 (the stack adds
@@ -910,9 +923,13 @@ hymba_status stack_dims(int32_t n, const hymba_layer_desc* d, Dims* dims, StackP
     dims[l].residual = l == 0 ? 1 : 2;
     p.layer_ws = std::max(p.layer_ws, plan_ws(dims[l], false).total);
   }
+  size_t w16 = 0;
+  for (int l = 1; l < n; ++l) w16 = std::max(w16, static_cast<size_t>(dims[l].P_in) * dims[l].d * 2);
   size_t off = align_up(p.layer_ws, 256);
-  p.xb = off;
+  p.xs = off;
   off = align_up(off + static_cast<size_t>(dims[0].rows) * dims[0].d * 2, 256);
+  p.w16 = off;
+  off = align_up(off + w16, 256);
   p.kv_k = off;
   off = align_up(off + kv_k, 256);
   p.kv_v = off;
@@ -949,7 +966,8 @@ hymba_status hymba_stack_fwd(int32_t n_layers, const hymba_layer_desc* descs, co
   if (xb0 < yb0 + stream_bytes * 4 && yb0 < xb0 + stream_bytes * 2) return HYMBA_ERR_INVALID;  // y may not overlap x
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
-  __nv_bfloat16* xb = at<__nv_bfloat16>(ws, sp.xb);
+  __half* xs = at<__half>(ws, sp.xs);     // the stream rounded to fp16: layers 1.. read it
+  __half* w16 = at<__half>(ws, sp.w16);   // fp16 copy of the current layer's W_in
   hymba_kv kv{at<void>(ws, sp.kv_k), at<void>(ws, sp.kv_v)};
   for (int l = 0; l < n_layers; ++l) {
     const Dims& x = dims[l];
@@ -957,10 +975,17 @@ hymba_status hymba_stack_fwd(int32_t n_layers, const hymba_layer_desc* descs, co
     // export K/V when the next layer shares them (a shared layer's K/V are
     // already in the buffer)
     const bool export_kv = !last && dims[l + 1].kv_shared && !x.kv_shared;
+    StackIO sio;
+    sio.y_f16 = last ? nullptr : xs;
+    if (l > 0) {
+      TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(weights[l].W_in), x.d, w16, x.d, x.P_in,
+                                        x.d, st));
+      sio.w_in_f16 = w16;
+    }
     Marks mk;
     mk.st = st;
-    TRY(fwd_bf16(x, plan_ws(x, false), &weights[l], l == 0 ? x_in : xb, y, nullptr, x.kv_shared ? &kv : nullptr,
-                 export_kv ? &kv : nullptr, ws, dev_status, mk, st, MetaCtx{}, last ? nullptr : xb));
+    TRY(fwd_bf16(x, plan_ws(x, false), &weights[l], l == 0 ? x_in : xs, y, nullptr, x.kv_shared ? &kv : nullptr,
+                 export_kv ? &kv : nullptr, ws, dev_status, mk, st, MetaCtx{}, sio));
   }
   return HYMBA_OK;
 }

@@ -155,7 +155,11 @@ typedef struct hymba_cache {
   int32_t reserved;     /* must be 0                                         */
 } hymba_cache;
 
-/* Bytes of scratch memory hymba_layer_fwd needs for `d` (0 on invalid d).  */
+/* Bytes of scratch memory hymba_layer_fwd needs for `d` (0 on invalid d):
+ * the intermediates of eq. 3 of the Hymba page (section 2.1) -- the shared
+ * projection [Q|K|V|x|z], the conv output, [dt|B|C], both branch outputs
+ * and their normalised sum -- plus fp16 copies of W_out, W_x and W_dt.
+ * A pure function of the descriptor; launches nothing.                     */
 HYMBA_API size_t hymba_layer_fwd_workspace(const hymba_layer_desc* d);
 
 /* Prefill forward of one layer over X~ (Hymba page, section 2.1 eq. 3;
@@ -170,6 +174,15 @@ HYMBA_API size_t hymba_layer_fwd_workspace(const hymba_layer_desc* d);
  *            meta K/V, final SSM state, conv tail (last k-1 pre-conv x rows)
  *            and pos = T.  Requires cap >= window (SWA) or cap >= T (global).
  *            Not allowed with kv_shared except for its ssm/conv/pos fields.
+ *            Continuous batching: to admit a new sequence into row b of a
+ *            running batch's cache, prefill it alone (desc.batch = 1, its own
+ *            n_tokens) with cache_out pointing at row b -- k_ring + b*cap*Hkv*dh,
+ *            v_ring + b*cap*Hkv*dv, ssm_state + b*di*N, conv_state +
+ *            b*di*(k-1), pos + b elements -- and the batch's shared meta K/V
+ *            (rewritten with the same values: the meta rows are identical for
+ *            every sequence).  Rows are independent, so the other rows'
+ *            state is untouched and the next decode step runs them all, each
+ *            at its own pos.
  *   kv_in    non-NULL exactly when desc.kv_shared: the producer's K/V.
  *   kv_out   (may be NULL) receives this layer's post-RoPE K/V.
  *   ws       device scratch of ws_bytes >= hymba_layer_fwd_workspace(d),
@@ -295,10 +308,13 @@ HYMBA_API hymba_status hymba_block_fwd(const hymba_layer_desc* d, const hymba_bl
  * Residual stack of hybrid-head layers over one batch (the stacks of the
  * Hymba page's 300M-parameter design roadmap, section 2 and Table 1;
  * consecutive layers may share K/V, section 2.2):
- *     X_{l+1} = X_l + Y_l( bf16(X_l) ),   X_0 = x
- * The stream X_l is fp32; each layer reads it rounded to bf16 (its input
- * type); a layer with desc.kv_shared reads the previous layer's post-RoPE
- * K/V.  The Hymba pages describe no pre-norm or FFN for this stack.
+ *     X_{l+1} = X_l + Y_l(X_l),   X_0 = x
+ * The stream X_l is kept in fp32.  Layer 0 reads x (bf16); each later layer
+ * reads the stream rounded to fp16 (its matmul operand type; W_in is
+ * converted to fp16 for it, exact for every bf16 value in fp16's normal
+ * range).  A layer with desc.kv_shared reads the previous layer's post-RoPE
+ * K/V.  The Hymba pages describe no pre-norm or FFN for this stack.  Errors
+ * add HYMBA_ERR_RANGE (dev_status) if the stream leaves fp16's range.
  * ------------------------------------------------------------------------- */
 
 /* Bytes of scratch memory hymba_stack_fwd needs (0 on invalid descs).      */
@@ -321,10 +337,24 @@ HYMBA_API hymba_status hymba_stack_fwd(int32_t n_layers, const hymba_layer_desc*
                                        const hymba_layer_weights* weights, const void* x, float* y, void* ws,
                                        size_t ws_bytes, int32_t* dev_status, void* stream);
 
-/* Bytes of scratch memory hymba_layer_decode needs for `d` (0 on invalid). */
+/* Bytes of scratch memory hymba_layer_decode needs for `d` (0 on invalid):
+ * one row per sequence of the same intermediates as the prefill, the
+ * split-K partial sums of x_proj / out_proj and the key-split partials of
+ * the decode attention (the step of the Hymba page, sections 2.2-2.3, whose
+ * cost is the bytes it reads: "Griffin: Mixing Gated Linear Recurrences with
+ * Local Attention for Efficient Language Models", section 4.1, eq. 5).
+ * A pure function of the descriptor; launches nothing.                     */
 HYMBA_API size_t hymba_layer_decode_workspace(const hymba_layer_desc* d);
 
-/* One decode step for B sequences (desc.n_tokens must be 1).  The token of
+/* One decode step for B sequences (desc.n_tokens must be 1): eq. 3 of the
+ * Hymba page (section 2.1) for one new row per sequence, with the attention
+ * branch reading a window-bounded cache plus the meta-token K/V (sections 2.2
+ * and 2.3: SWA keeps only the last `window` tokens, the meta tokens act as a
+ * learned cache prefix; consecutive layers may share K/V) and the SSM branch
+ * advancing its carried state by one step of the recurrence.  Its time is the
+ * bytes it moves over the memory bandwidth ("Griffin: ...", section 4.1,
+ * eq. 5: decode is memory-bound, the cache and the weights are read once per
+ * step).  The token of
  * sequence b sits at absolute position M + pos[b]; its K/V go into slot
  * pos[b] % cap of `cache` (skipped for a kv_shared layer, which reads the
  * producer's `shared_cache`, already updated for this token); attention sees
@@ -386,7 +416,9 @@ HYMBA_API hymba_status hymba_layer_decode_events(const hymba_layer_desc* d, cons
                                                  int32_t* dev_status, void* const* events, int32_t n_events,
                                                  void* stream);
 
-/* Human-readable name of a status code (static storage).                    */
+/* Human-readable name of a status code (static storage, never NULL; unknown
+ * codes give "unknown hymba_status").  No counterpart in the paper: the
+ * error channel of this interface.                                          */
 HYMBA_API const char* hymba_status_str(hymba_status s);
 
 /* HYMBA_ABI_VERSION of the built library.                                   */

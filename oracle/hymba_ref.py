@@ -417,24 +417,22 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32).astype(F)
 
 
-def stack_fwd(layers, Xt: np.ndarray, shapes, round_inputs: bool = True) -> Dict[str, list]:
-    """Residual stack X_{l+1} = X_l + Y_l(X~_l) of hybrid-head layers (the
+def stack_fwd(layers, Xt: np.ndarray, shapes) -> Dict[str, list]:
+    """Residual stack X_{l+1} = X_l + Y_l(X_l) of hybrid-head layers (the
     Hymba pages describe no pre-norm or FFN for it); a kv_shared layer
     consumes the previous layer's post-RoPE K/V (section 2.2).
 
-    Reading: the stream X_l is kept at full precision (fp32 on the device,
-    float64 here) and each layer's input X~_l is the stream rounded to
-    bfloat16, the input type of a bf16 layer; the residual adds the unrounded
-    stream.  round_inputs=False feeds the stream unrounded (the fp32 path).
-    Every layer's own residual flag is ignored: the stack adds the stream.
+    Reading: the stream is carried at full precision and every layer reads
+    it unrounded (no rounding step is part of the definition; a device keeps
+    its own stream in fp32 and rounds only its matmul operands).  Every
+    layer's own residual flag is ignored: the stack adds the stream.
     Returns the stream after each layer.
     """
     X = np.asarray(Xt, F)
     outs, prev = [], None
     for p, s in zip(layers, shapes):
         kv = (prev["K"], prev["V"]) if s.kv_shared else None
-        Xin = round_bf16(X) if round_inputs else X
-        o = layer_fwd(p, Xin, s, kv_in=kv, residual=False)
+        o = layer_fwd(p, X, s, kv_in=kv, residual=False)
         X = X + o["Y"]
         outs.append(X)
         prev = o

@@ -17,9 +17,9 @@ all of them, so both ends of the batch and of the sequence are covered.
   the meta K/V: y, the SSM state and the ring slot written for three
   sequences (first, middle, last); pos of all.
 * 300M-ablation-shaped 4-layer stack (global, then three SWA layers; layers
-  1 -> 2 share K/V), batch 32 x (2048 + 128): every row of the last sequence
-  after every layer, chained through the fp32 residual stream exactly as the
-  benchmark runs it (each layer reads the stream rounded to bf16).
+  1 -> 2 share K/V), batch 32 x (2048 + 128), through hymba_stack_fwd as the
+  benchmark runs it: every row of the last sequence after 1, 2, 3 and 4
+  layers, chained through the fp32 residual stream.
 * The full residual block around the SWA layer (gated MLP, F = 3 d), batch
   8 x (8192 + 128): sampled rows against the row-wise block oracle.
 """
@@ -80,47 +80,23 @@ def test_full_size_decode_batch128_sampled_sequences():
     assert np.all(c["pos"] == 8193)
 
 
-def test_full_size_stack_chained_last_sequence():
-    """The 4-layer stack chained with no reset between layers: the stream
-    y (fp32) enters each layer rounded to bf16 and the layer adds into it
-    (residual mode 2); layer 2 reuses layer 1's exported K/V.  Every row of
-    the last sequence after every layer against the oracle's stack, which
-    rounds each layer's input the same way."""
+@pytest.mark.parametrize("n_layers", [1, 2, 3, 4])
+def test_full_size_stack_call_last_sequence(n_layers):
+    """The first n layers of the 4-layer stack through one hymba_stack_fwd
+    call each, as the benchmark runs it (n = 4): the fp32 stream after layer
+    n - 1, every row of the last sequence, chained with no reset, against the
+    oracle's stack (the stream at full precision)."""
     shapes = [synth.with_(s, rope_theta=10000.0) for s in synth.ablation300m_stack()]
     tok, layers = synth.make_stack_inputs(shapes, seed=3)
     b = shapes[0].B - 1
-    out = ref.stack_fwd(layers, tok["Xt"][b:b + 1], [synth.with_(s, B=1) for s in shapes])
-    y = torch.from_numpy(tok["Xt"].astype(np.float32)).cuda()
-    kv = None
-    for i, (p, s) in enumerate(zip(layers, shapes)):
-        X = y.to(torch.bfloat16)
-        layer = hl.HymbaLayer(s, hl.params_to_device(p, s), residual_mode=2)
-        kv_out = None
-        if i == 1:
-            kd = hl.kv_dtype(s)
-            kv_out = (torch.empty(s.B, s.L, s.Hkv, s.dh, device="cuda", dtype=kd),
-                      torch.empty(s.B, s.L, s.Hkv, s.dv, device="cuda", dtype=kd))
-        layer.forward(X, y=y, kv_in=kv if s.kv_shared else None, kv_out=kv_out)
-        torch.cuda.synchronize()
-        assert layer.check_status() == 0
-        assert_bf16_close(y[b].cpu().numpy(), out["Y"][i][0], f"stack batch 32 x 2K, layer {i}, sequence {b}")
-        if kv_out is not None:
-            kv = kv_out
-        del layer, X
-
-
-def test_full_size_stack_call_last_sequence():
-    """The same stack through one hymba_stack_fwd call, as the benchmark
-    times it: the final stream of the last sequence, every row."""
-    shapes = [synth.with_(s, rope_theta=10000.0) for s in synth.ablation300m_stack()]
-    tok, layers = synth.make_stack_inputs(shapes, seed=3)
-    b = shapes[0].B - 1
-    out = ref.stack_fwd(layers, tok["Xt"][b:b + 1], [synth.with_(s, B=1) for s in shapes])
-    st = hl.HymbaStack(shapes, [hl.params_to_device(p, s) for p, s in zip(layers, shapes)])
+    out = ref.stack_fwd(layers[:n_layers], tok["Xt"][b:b + 1], [synth.with_(s, B=1) for s in shapes[:n_layers]])
+    st = hl.HymbaStack(shapes[:n_layers], [hl.params_to_device(p, s) for p, s in zip(layers, shapes[:n_layers])])
     y = st.forward(hl.tokens_to_device(tok["Xt"], shapes[0]))
     torch.cuda.synchronize()
     assert st.check_status() == 0
-    assert_bf16_close(y[b].cpu().numpy(), out["Y"][-1][0], f"stack call, batch 32 x 2K, sequence {b}")
+    assert_bf16_close(y[b].cpu().numpy(), out["Y"][-1][0],
+                      f"stack call, batch 32 x 2K, after layer {n_layers - 1}, sequence {b}")
+    del st, y
 
 
 def test_full_size_block_sampled_rows():
