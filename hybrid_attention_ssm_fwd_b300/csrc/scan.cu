@@ -227,9 +227,11 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
           }
           const float4* Bp = reinterpret_cast<const float4*>(sBC + t * 2 * N + sub * NS);
           const float4* Cp = reinterpret_cast<const float4*>(sBC + t * 2 * N + N + sub * NS);
-          uint64_t y0[CPT], y1[CPT];
+          // one packed accumulator per channel: a single fma2 per state pair
+          // (two accumulators cost an extra add2 per channel and row)
+          uint64_t y0[CPT];
 #pragma unroll
-          for (int j = 0; j < CPT; ++j) y0[j] = y1[j] = pk2(0.f, 0.f);
+          for (int j = 0; j < CPT; ++j) y0[j] = pk2(0.f, 0.f);
 #pragma unroll
           for (int qq = 0; qq < NS / 4; ++qq) {
             const float4 bb = Bp[qq], cc = Cp[qq];
@@ -243,16 +245,13 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
                 const float2 ea = up2(mul2(pk2(dl[j], dl[j]), A2[j][p]));
                 const uint64_t av = pk2(ex2_approx(ea.x), ex2_approx(ea.y));
                 h2[j][p] = fma2(av, h2[j][p], mul2(pk2(dul[j], dul[j]), bp));
-                if (p2 == 0)
-                  y0[j] = fma2(cp, h2[j][p], y0[j]);
-                else
-                  y1[j] = fma2(cp, h2[j][p], y1[j]);
+                y0[j] = fma2(cp, h2[j][p], y0[j]);
               }
             }
           }
 #pragma unroll
           for (int j = 0; j < CPT; ++j) {
-            const float2 ys = up2(add2(y0[j], y1[j]));
+            const float2 ys = up2(y0[j]);
             yr[j][tr] = ys.x + ys.y;
           }
         }
