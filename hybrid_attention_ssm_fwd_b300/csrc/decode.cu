@@ -716,41 +716,89 @@ namespace {
 // The decode step's K/V ring append and conv step in one launch (same
 // arithmetic as kv_append_kernel and conv_step_kernel): elements
 // [0, B*di) are conv channels, the rest ring entries of the new token.
+// One decode step's conv step and ring append, one launch.  Conv: a thread
+// per (sequence, 4 adjacent channels) -- the 4 x (k-1) carried rows of the
+// group are contiguous in conv_state, so k = 4 moves them in three 16-byte
+// loads and stores (`vec`: k = 4 and 16-byte aligned conv_state / conv_w);
+// otherwise the scalar loop.  Append: a thread per
+// 8 consecutive K or V values of one sequence (16-byte loads and stores).
 __global__ void decode_prep_kernel(int B, int di, int k, const __half* __restrict__ proj, long long ldp, int x_col,
                                    int k_col, int v_col, int Hkv, int dh, int dv, int window, int cap,
                                    const int32_t* __restrict__ pos, __nv_bfloat16* __restrict__ k_ring,
                                    __nv_bfloat16* __restrict__ v_ring, const float* __restrict__ w,
                                    const float* __restrict__ bias, float* __restrict__ conv_state,
-                                   __half* __restrict__ u, long long ldu, int append) {
+                                   __half* __restrict__ u, long long ldu, int append, int vec) {
   pdl_wait();
   pdl_trigger();
-  const long long n_conv = static_cast<long long>(B) * di;
+  const int g4 = di / 4;                       // channel groups per sequence
+  const int n_conv = B * g4;
   const int wk = Hkv * dh, wv = Hkv * dv;
-  const long long n = n_conv + (append ? static_cast<long long>(B) * (wk + wv) : 0);
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+  const int kv8 = (wk + wv) / 8;               // 8-value groups per sequence
+  const int n = n_conv + (append ? B * kv8 : 0);
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += gridDim.x * blockDim.x) {
     if (idx < n_conv) {
-      const int b = static_cast<int>(idx / di), c = static_cast<int>(idx % di);
-      float* st = conv_state + idx * (k - 1);
-      const float xv = __half2float(proj[b * ldp + x_col + c]);
-      float acc = bias[c];
-      for (int j = 0; j < k - 1; ++j) acc = fmaf(w[c * k + j], st[j], acc);
-      acc = fmaf(w[c * k + k - 1], xv, acc);
-      for (int j = 0; j + 1 < k - 1; ++j) st[j] = st[j + 1];
-      if (k > 1) st[k - 2] = xv;
-      u[b * ldu + c] = __float2half_rn(acc / (1.0f + expf(-acc)));
+      const int b = idx / g4, c = (idx - b * g4) * 4;
+      const long long bc = static_cast<long long>(b) * di + c;
+      float* st = conv_state + bc * (k - 1);
+      const uint2 xr = *reinterpret_cast<const uint2*>(proj + b * ldp + x_col + c);
+      const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&xr.x));
+      const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&xr.y));
+      const float xv[4] = {x01.x, x01.y, x23.x, x23.y};
+      float acc[4] = {bias[c], bias[c + 1], bias[c + 2], bias[c + 3]};
+      if (vec) {
+        float4 s4[3];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) s4[i] = reinterpret_cast<const float4*>(st)[i];
+        const float* sv = reinterpret_cast<const float*>(s4);  // channel e: sv[3e..3e+2], oldest first
+        float nv[12];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 we = *reinterpret_cast<const float4*>(w + (c + e) * 4);
+          acc[e] = fmaf(we.x, sv[3 * e], fmaf(we.y, sv[3 * e + 1], fmaf(we.z, sv[3 * e + 2], fmaf(we.w, xv[e], acc[e]))));
+          nv[3 * e] = sv[3 * e + 1];
+          nv[3 * e + 1] = sv[3 * e + 2];
+          nv[3 * e + 2] = xv[e];
+        }
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+          reinterpret_cast<float4*>(st)[i] = make_float4(nv[4 * i], nv[4 * i + 1], nv[4 * i + 2], nv[4 * i + 3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float* se = st + e * (k - 1);
+          for (int j = 0; j < k - 1; ++j) acc[e] = fmaf(w[(c + e) * k + j], se[j], acc[e]);
+          acc[e] = fmaf(w[(c + e) * k + k - 1], xv[e], acc[e]);
+          for (int j = 0; j + 1 < k - 1; ++j) se[j] = se[j + 1];
+          if (k > 1) se[k - 2] = xv[e];
+        }
+      }
+      // silu(a) = a / (1 + 2^(-a log2 e))
+      uint2 o;
+      o.x = pack_half2(acc[0] * rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * acc[0])),
+                       acc[1] * rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * acc[1])));
+      o.y = pack_half2(acc[2] * rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * acc[2])),
+                       acc[3] * rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * acc[3])));
+      *reinterpret_cast<uint2*>(u + b * ldu + c) = o;
     } else {
-      const long long r = idx - n_conv;
-      const int b = static_cast<int>(r / (wk + wv)), c = static_cast<int>(r % (wk + wv));
+      const int r = idx - n_conv;
+      const int b = r / kv8, c = (r - b * kv8) * 8;
       const int p = pos[b];
       const int slot = window > 0 ? p % cap : p;
       if (slot < 0 || slot >= cap) continue;  // a full global cache: the token is not stored
-      if (c < wk)
-        k_ring[(static_cast<long long>(b) * cap + slot) * wk + c] =
-            __float2bfloat16_rn(__half2float(proj[b * ldp + k_col + c]));
-      else
-        v_ring[(static_cast<long long>(b) * cap + slot) * wv + (c - wk)] =
-            __float2bfloat16_rn(__half2float(proj[b * ldp + v_col + (c - wk)]));
+      const bool is_k = c < wk;
+      const uint4 src = *reinterpret_cast<const uint4*>(proj + b * ldp + (is_k ? k_col + c : v_col + c - wk));
+      const __half2* sh = reinterpret_cast<const __half2*>(&src);
+      uint4 dst;
+      uint32_t* d32 = reinterpret_cast<uint32_t*>(&dst);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(sh[e]);
+        __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+        d32[e] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      __nv_bfloat16* drow = is_k ? k_ring + (static_cast<long long>(b) * cap + slot) * wk + c
+                                 : v_ring + (static_cast<long long>(b) * cap + slot) * wv + (c - wk);
+      *reinterpret_cast<uint4*>(drow) = dst;
     }
   }
 }
@@ -761,11 +809,20 @@ hymba_status decode_prep(int B, int di, int k, const __half* proj, long long ldp
                          int Hkv, int dh, int dv, int window, int cap, const int32_t* pos, __nv_bfloat16* k_ring,
                          __nv_bfloat16* v_ring, const float* conv_w, const float* conv_b, float* conv_state,
                          __half* u, long long ldu, bool append, cudaStream_t st) {
-  const long long n = static_cast<long long>(B) * di + (append ? static_cast<long long>(B) * Hkv * (dh + dv) : 0);
+  // whole 4-channel / 8-value groups on 16-byte boundaries (the bf16 path's
+  // shape rules give them; the ring rows must be 16-byte aligned, as the
+  // decode attention's TMA maps need anyway)
+  if (di % 4 || (Hkv * dh) % 8 || (Hkv * dv) % 8 || ldp % 8 || ldu % 4 || x_col % 4 || k_col % 8 || v_col % 8)
+    return HYMBA_ERR_UNSUPPORTED;
+  if (append && ((reinterpret_cast<uintptr_t>(k_ring) & 15) || (reinterpret_cast<uintptr_t>(v_ring) & 15)))
+    return HYMBA_ERR_INVALID;
+  const int vec = k == 4 && !(reinterpret_cast<uintptr_t>(conv_state) & 15) && !(reinterpret_cast<uintptr_t>(conv_w) & 15);
+  const long long n = static_cast<long long>(B) * (di / 4) + (append ? static_cast<long long>(B) * Hkv * (dh + dv) / 8 : 0);
   if (n <= 0) return HYMBA_OK;
-  if (launch_pdl(decode_prep_kernel, dim3(static_cast<unsigned>(std::min<long long>((n + 255) / 256, 148 * 16))),
+  if (n > (1LL << 30)) return HYMBA_ERR_INVALID;
+  if (launch_pdl(decode_prep_kernel, dim3(static_cast<unsigned>(std::min<long long>((n + 255) / 256, 148 * 8))),
                  dim3(256), 0, st, B, di, k, proj, ldp, x_col, k_col, v_col, Hkv, dh, dv, window, cap, pos, k_ring,
-                 v_ring, conv_w, conv_b, conv_state, u, ldu, append ? 1 : 0) != cudaSuccess)
+                 v_ring, conv_w, conv_b, conv_state, u, ldu, append ? 1 : 0, vec) != cudaSuccess)
     return HYMBA_ERR_CUDA;
   return last_err();
 }
