@@ -20,6 +20,18 @@
 // Tiles are visited in row-major tile order (N fastest) by a static
 // round-robin over CTAs, so the CTAs resident at one time share a few A
 // row-blocks and the weight matrix stays in L2.  Every wait is bounded.
+//
+// CTA pairs (PAIR, many row blocks): a 2-CTA cluster computes a 256 x BN
+// tile with tcgen05.mma.cta_group::2, issued by the even CTA.  Each CTA
+// loads its own 128-row A block and its own half (BN/2 rows) of the B block
+// with plain TMA loads into its own shared memory, so a CTA pulls 128 + BN/2
+// operand rows per k-step from L2 instead of 128 + BN: at the large tiles the
+// single-CTA kernel is bound by L2-to-SM bandwidth (about 135 GB/s per SM
+// measured), which this halves for B.  The odd CTA's loads count their bytes
+// directly on the even CTA's stage barrier (.cta_group::2 tensor loads), whose
+// producer expects both CTAs' bytes; the even CTA's commits release the stage
+// and signal the accumulator in both CTAs; both CTAs' epilogues release the
+// accumulator on the even CTA's barrier.  No load is multicast.
 #include "gemm_tc.cuh"
 
 #include <atomic>
@@ -29,11 +41,14 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
+// widest tile run as CTA pairs (each CTA holds a 128 x BN accumulator pair in
+// its tensor memory, 2 BN columns)
+constexpr int kPairMaxBN = 256;
 constexpr int A_BYTES = BM * BK * 2;
 
-template <int BN>
+template <int BN, bool PAIR = false>
 struct GemmCfg {
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;  // this CTA's B rows
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int BUDGET = 220 * 1024 - 2048;
   static constexpr int S0 = BUDGET / STAGE;
@@ -46,6 +61,18 @@ struct GemmCfg {
 struct TileCoord {
   int m, n, kb0, kb1, split;
 };
+
+// tile pair t of a pair launch, for the CTA of cluster rank r: row block 2 mp + r
+HY_DEV TileCoord pair_coord(const GemmParams& p, int t, int r) {
+  TileCoord c;
+  const int mp = t / p.tiles_n;
+  c.n = t - mp * p.tiles_n;
+  c.m = 2 * mp + r;  // may be tiles_m (odd tiles_m): its rows load as zeros and are not stored
+  c.split = 0;
+  c.kb0 = 0;
+  c.kb1 = p.n_kb;
+  return c;
+}
 
 HY_DEV TileCoord tile_coord(const GemmParams& p, int t) {
   TileCoord c;
@@ -97,11 +124,11 @@ HY_DEV bool any_over_half(const float (&v)[32]) {
   return o;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p, const uint32_t idesc) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, PAIR>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -121,11 +148,13 @@ __global__ void __launch_bounds__(192, 1)
   auto tempty = [&](int a) { return smem_u32(&bars[2 * S + 2 + a]); };
   auto cvt = [&](int s) { return smem_u32(&bars[2 * S + 4 + s]); };
 
-  // tile walk: a static round-robin over the CTAs
-  const int t_first = static_cast<int>(blockIdx.x);
-  const int t_step = static_cast<int>(gridDim.x);
-  const int t_count = p.total_tiles;
-  auto coord = [&](int t) { return tile_coord(p, t); };
+  // tile walk: a static round-robin over the CTAs, or over the CTA pairs
+  const int rank = PAIR ? static_cast<int>(cluster_rank()) : 0;
+  const bool leader = rank == 0;
+  const int t_first = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int t_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int t_count = PAIR ? p.total_pairs : p.total_tiles;
+  auto coord = [&](int t) { return PAIR ? pair_coord(p, t, rank) : tile_coord(p, t); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -134,16 +163,22 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull(a), 1);
-      mbar_init(tempty(a), 4);
+      mbar_init(tempty(a), PAIR ? 8 : 4);  // pair: both CTAs' epilogue warps
     }
     for (int s = 0; s < S; ++s) mbar_init(cvt(s), 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (EPI == EPI_F16 && threadIdx.x < 32) rope_tab[threadIdx.x] = exp2f(threadIdx.x * p.rope_log2_step);
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    else
+      tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+  }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
   pdl_wait();  // only the setup above may overlap the preceding kernel
   pdl_trigger();
@@ -164,21 +199,34 @@ __global__ void __launch_bounds__(192, 1)
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
           if (!mbar_wait(empty(s), ph ^ 1, wc)) { ok = false; break; }
-          mbar_arrive_expect_tx(full(s), Cfg::STAGE);
-          tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full(s), kb * BK, c.m * BM);
-          tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full(s), kb * BK, c.n * BN);
+          if (!PAIR || leader) {
+            // a pair's even CTA expects both CTAs' bytes on its own barrier
+            mbar_arrive_expect_tx(full(s), PAIR ? 2 * Cfg::STAGE : Cfg::STAGE);
+            tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full(s), kb * BK, c.m * BM);
+            tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full(s), kb * BK, c.n * BN + rank * (BN / 2));
+          } else {
+            const uint32_t bar0 = mapa_shared(full(s), 0);
+            tma_load_2d_pair(smem_u32(sA + s * A_BYTES), &tmA, bar0, kb * BK, c.m * BM);
+            tma_load_2d_pair(smem_u32(sB + s * Cfg::B_BYTES), &tmB, bar0, kb * BK, c.n * BN + rank * (BN / 2));
+          }
           issued |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
         }
       }
-      if (!ok) {  // let the copies already in flight land before the CTA exits
+      // let the copies already in flight land before the CTA exits (a pair's
+      // odd CTA counts on the even CTA's barriers, whose drain covers them;
+      // the final cluster barrier keeps the odd CTA until then)
+      if (!ok && (!PAIR || leader)) {
         for (int s = 0; s < S; ++s)
           if (issued & (1u << s)) mbar_wait_drain(full(s), (last_par >> s) & 1, 1000000);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (PAIR && !leader) {
+      // the odd CTA issues no MMA: its tiles are loaded by its producer and
+      // consumed by the even CTA's MMAs
+    } else if (lane == 0) {
       uint32_t it = 0, committed = 0, last_par = 0, tcommitted = 0, tlast = 0;
       bool ok = true;
       int local = 0;
@@ -186,25 +234,36 @@ __global__ void __launch_bounds__(192, 1)
         const TileCoord c = coord(t);
         const int a = local & 1;
         const uint32_t u = (local >> 1) & 1;
-        if (!mbar_wait(tempty(a), u ^ 1, wc)) { ok = false; break; }
+        if (!(PAIR ? mbar_wait_cluster(tempty(a), u ^ 1, wc) : mbar_wait(tempty(a), u ^ 1, wc))) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem_base + a * BN;
         for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
-          if (!mbar_wait(p.cvt_b ? cvt(s) : full(s), ph, wc)) { ok = false; break; }
+          const bool got = PAIR ? mbar_wait_cluster(full(s), ph, wc) : mbar_wait(p.cvt_b ? cvt(s) : full(s), ph, wc);
+          if (!got) { ok = false; break; }
           tc_fence_after();
           const uint64_t da = sdesc_sw128(smem_u32(sA + s * A_BYTES), 16, 1024);
           const uint64_t db = sdesc_sw128(smem_u32(sB + s * Cfg::B_BYTES), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
-          tc_commit(empty(s));
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            if constexpr (PAIR)
+              tc_mma_f16_pair(d, da + 2 * kk, db + 2 * kk, idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
+            else
+              tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
+          }
+          if constexpr (PAIR)
+            tc_commit_pair(empty(s), 0x3);  // the stage is free in both CTAs
+          else
+            tc_commit(empty(s));
           committed |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
         }
         if (!ok) break;
-        tc_commit(tfull(a));
+        if constexpr (PAIR)
+          tc_commit_pair(tfull(a), 0x3);  // the accumulator is ready in both CTAs
+        else
+          tc_commit(tfull(a));
         tcommitted |= 1u << a;
         tlast = (tlast & ~(1u << a)) | (u << a);
       }
@@ -402,14 +461,25 @@ __global__ void __launch_bounds__(192, 1)
       if (over) set_status(p.status, HYMBA_ERR_RANGE);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty(a));
+      if (lane == 0) {
+        if (PAIR && !leader)
+          mbar_arrive_remote(mapa_shared(tempty(a), 0));  // the even CTA reuses this CTA's accumulator too
+        else
+          mbar_arrive(tempty(a));
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // no CTA leaves while its peer may still reach its memory
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
 }
 
 // Kernel attributes and occupancy figures belong to one device: the
@@ -417,11 +487,11 @@ __global__ void __launch_bounds__(192, 1)
 // set up on every call).
 constexpr int kMaxDevices = 64;
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, uint32_t idesc, int grid,
                        cudaStream_t st) {
-  using Cfg = GemmCfg<BN>;
-  auto kern = gemm_tc_kernel<BN, EPI>;
+  using Cfg = GemmCfg<BN, PAIR>;
+  auto kern = gemm_tc_kernel<BN, EPI, PAIR>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return HYMBA_ERR_CUDA;
   const bool cached = dev < kMaxDevices;
@@ -432,20 +502,51 @@ hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmP
       return HYMBA_ERR_CUDA;
     if (cached) attr_done[dev].store(true, std::memory_order_release);
   }
-  if (launch_pdl(kern, dim3(grid), dim3(192), Cfg::SMEM, st, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
+  if constexpr (!PAIR) {
+    if (launch_pdl(kern, dim3(grid), dim3(192), Cfg::SMEM, st, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
+    // persistent: no more pairs than can be resident at once, so no tile
+    // waits for a second wave
+    static std::atomic<int> max_clusters_dev[kMaxDevices];
+    int max_clusters = cached ? max_clusters_dev[dev].load(std::memory_order_relaxed) : 0;
+    if (max_clusters == 0) {
+      cfg.gridDim = dim3(2 * std::max(1, grid / 2), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return HYMBA_ERR_CUDA;
+      max_clusters = n;
+      if (cached) max_clusters_dev[dev].store(n, std::memory_order_relaxed);
+    }
+    const int clusters = std::max(1, std::min(std::min(grid / 2, max_clusters), p.total_pairs));
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }
 
-template <int EPI>
+template <int EPI, bool PAIR = false>
 hymba_status launch_epi(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                         uint32_t ab_fmt, int grid, cudaStream_t st) {
-  const uint32_t id = idesc_f16(BM, bn, ab_fmt, false, false);
+  const uint32_t id = idesc_f16(PAIR ? 2 * BM : BM, bn, ab_fmt, false, false);
   switch (bn) {
-    case 64: return launch_bn<64, EPI>(ta, tb, p, id, grid, st);
-    case 128: return launch_bn<128, EPI>(ta, tb, p, id, grid, st);
-    case 144: return launch_bn<144, EPI>(ta, tb, p, id, grid, st);
-    case 160: return launch_bn<160, EPI>(ta, tb, p, id, grid, st);
-    case 256: return launch_bn<256, EPI>(ta, tb, p, id, grid, st);
+    case 64: return launch_bn<64, EPI, PAIR>(ta, tb, p, id, grid, st);
+    case 128: return launch_bn<128, EPI, PAIR>(ta, tb, p, id, grid, st);
+    case 144: return launch_bn<144, EPI, PAIR>(ta, tb, p, id, grid, st);
+    case 160: return launch_bn<160, EPI, PAIR>(ta, tb, p, id, grid, st);
+    case 256: return launch_bn<256, EPI, PAIR>(ta, tb, p, id, grid, st);
     default: return HYMBA_ERR_UNSUPPORTED;
   }
 }
@@ -490,10 +591,13 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
     if (!encode_tmap(&ta, dt, 2, A, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
   }
   p.tiles_m = (p.M + BM - 1) / BM;
+  // CTA pairs (256-row tiles, each CTA loading half of B) once there are
+  // several row blocks; not for split-K or converted-B launches
+  const bool pair = splits <= 1 && !p.cvt_b && p.tiles_m >= 4 && num_sms >= 2 && bn <= kPairMaxBN;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
     const uint64_t str[1] = {static_cast<uint64_t>(ldb) * 2};
-    const uint32_t box[2] = {BK, static_cast<uint32_t>(bn)};
+    const uint32_t box[2] = {BK, static_cast<uint32_t>(pair ? bn / 2 : bn)};
     const CUtensorMapDataType dtb = p.cvt_b ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : dt;
     if (!encode_tmap(&tb, dtb, 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
   }
@@ -503,10 +607,21 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
   p.kb_per_split = (p.n_kb + splits - 1) / splits;
   p.splits = (p.n_kb + p.kb_per_split - 1) / p.kb_per_split;
   p.total_tiles = p.tiles_m * p.tiles_n * p.splits;
+  p.total_pairs = (p.tiles_m + 1) / 2 * p.tiles_n;
   if (p.splits > 1 && epi != EPI_PARTIAL && epi != EPI_ATOMIC) return HYMBA_ERR_INVALID;
   if (epi == EPI_GEGLU && (p.N % 16 || p.ldc % 8 || (reinterpret_cast<uintptr_t>(p.C) & 15))) return HYMBA_ERR_INVALID;
   const int grid = std::min(p.total_tiles, std::max(1, num_sms));
   const uint32_t fmt = ab_fmt == 1 ? 1u : 0u;
+  if (pair) {
+    switch (epi) {
+      case EPI_F16: return launch_epi<EPI_F16, true>(bn, ta, tb, p, fmt, num_sms, st);
+      case EPI_XPROJ: return launch_epi<EPI_XPROJ, true>(bn, ta, tb, p, fmt, num_sms, st);
+      case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS, true>(bn, ta, tb, p, fmt, num_sms, st);
+      case EPI_F32: return launch_epi<EPI_F32, true>(bn, ta, tb, p, fmt, num_sms, st);
+      case EPI_GEGLU: return launch_epi<EPI_GEGLU, true>(bn, ta, tb, p, fmt, num_sms, st);
+      default: return HYMBA_ERR_INVALID;
+    }
+  }
   switch (epi) {
     case EPI_F16: return launch_epi<EPI_F16>(bn, ta, tb, p, fmt, grid, st);
     case EPI_XPROJ: return launch_epi<EPI_XPROJ>(bn, ta, tb, p, fmt, grid, st);

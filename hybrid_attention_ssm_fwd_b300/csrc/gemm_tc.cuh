@@ -36,6 +36,7 @@ struct GemmParams {
   int32_t* status;
   uint64_t wait_ns;
   int cvt_b;  // B is bf16 in memory: converted to fp16 in shared memory before the MMA (A fp16)
+  int total_pairs;  // CTA-pair launch: 256-row tile pairs = ceil(tiles_m / 2) * tiles_n
 };
 
 // Launch C = A . B^T with the given epilogue.  ab_fmt: 0 fp16, 1 bf16.

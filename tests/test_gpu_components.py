@@ -16,9 +16,12 @@ F = np.float64
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 200, 100), (1000, 1600, 3200), (37, 8960, 1600),
                                    (4500, 144, 96), (128, 64, 8),
-                                   # 8+ row blocks run as 2-CTA cluster pairs; 9 and 17 blocks leave a
-                                   # padding tile in the last pair
-                                   (1115, 520, 200), (2100, 300, 64), (1921, 176, 72)])
+                                   (1115, 520, 200), (2100, 300, 64), (1921, 176, 72),
+                                   # 4+ row blocks and tiles at most 128 wide run as CTA pairs (256-row
+                                   # tiles on tcgen05.mma.cta_group::2); 5, 9 and 17 row blocks leave an
+                                   # empty half in the last pair; N not a multiple of the tile
+                                   (512, 128, 256), (600, 64, 1600), (1047, 384, 200), (2100, 120, 3200),
+                                   (1921, 96, 72)])
 @pytest.mark.parametrize("ab", [1, 2, 3])
 def test_gemm_tc_matches_fp64(M, N, K, ab):
     """ab 1: bf16 x bf16; 2: fp16 x fp16; 3: fp16 A against a bf16 B that the
