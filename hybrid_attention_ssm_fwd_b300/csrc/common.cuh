@@ -225,6 +225,15 @@ HY_DEV void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar_cl
       : "memory");
 }
 
+HY_DEV void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar_cluster, int32_t x, int32_t y,
+                             int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      : "memory");
+}
+
 // Arrive on an mbarrier of another CTA of the cluster (release, cluster scope).
 HY_DEV void mbar_arrive_remote(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");

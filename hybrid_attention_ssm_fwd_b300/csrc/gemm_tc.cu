@@ -46,10 +46,16 @@ constexpr int BK = 64;
 constexpr int kPairMaxBN = 256;
 constexpr int A_BYTES = BM * BK * 2;
 
-template <int BN, bool PAIR = false>
+// KC 64-column chunks of K per pipeline stage: with KC = 2 one 3-D tensor
+// load ([chunk][row][64]) brings both chunks of A and one both of B, halving
+// the copies a stage needs (one issuing thread sustains about one tensor copy
+// per 170-220 ns, longer than the MMAs of a 64-wide k-step at BN <= 160).
+template <int BN, bool PAIR = false, int KC = 1>
 struct GemmCfg {
-  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;  // this CTA's B rows
-  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int B_CHUNK = (PAIR ? BN / 2 : BN) * BK * 2;  // this CTA's B rows, one chunk
+  static constexpr int A_STAGE = KC * A_BYTES;
+  static constexpr int B_BYTES = KC * B_CHUNK;                    // this CTA's B rows, one stage
+  static constexpr int STAGE = A_STAGE + B_BYTES;
   static constexpr int BUDGET = 220 * 1024 - 2048;
   static constexpr int S0 = BUDGET / STAGE;
   static constexpr int STAGES = S0 > 8 ? 8 : S0;
@@ -124,16 +130,16 @@ HY_DEV bool any_over_half(const float (&v)[32]) {
   return o;
 }
 
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, bool PAIR, int KC>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p, const uint32_t idesc) {
-  using Cfg = GemmCfg<BN, PAIR>;
+  using Cfg = GemmCfg<BN, PAIR, KC>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + S * A_BYTES;
+  uint8_t* sB = smem + S * Cfg::A_STAGE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE);
   // bars: full[S], empty[S], tfull[2], tempty[2], cvt[S]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 4);
@@ -202,12 +208,22 @@ __global__ void __launch_bounds__(192, 1)
           if (!PAIR || leader) {
             // a pair's even CTA expects both CTAs' bytes on its own barrier
             mbar_arrive_expect_tx(full(s), PAIR ? 2 * Cfg::STAGE : Cfg::STAGE);
-            tma_load_2d(smem_u32(sA + s * A_BYTES), &tmA, full(s), kb * BK, c.m * BM);
-            tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full(s), kb * BK, c.n * BN + rank * (BN / 2));
+            if constexpr (KC == 1) {
+              tma_load_2d(smem_u32(sA + s * Cfg::A_STAGE), &tmA, full(s), kb * BK, c.m * BM);
+              tma_load_2d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full(s), kb * BK, c.n * BN + rank * (BN / 2));
+            } else {
+              tma_load_3d(smem_u32(sA + s * Cfg::A_STAGE), &tmA, full(s), 0, c.m * BM, kb * KC);
+              tma_load_3d(smem_u32(sB + s * Cfg::B_BYTES), &tmB, full(s), 0, c.n * BN + rank * (BN / 2), kb * KC);
+            }
           } else {
             const uint32_t bar0 = mapa_shared(full(s), 0);
-            tma_load_2d_pair(smem_u32(sA + s * A_BYTES), &tmA, bar0, kb * BK, c.m * BM);
-            tma_load_2d_pair(smem_u32(sB + s * Cfg::B_BYTES), &tmB, bar0, kb * BK, c.n * BN + rank * (BN / 2));
+            if constexpr (KC == 1) {
+              tma_load_2d_pair(smem_u32(sA + s * Cfg::A_STAGE), &tmA, bar0, kb * BK, c.m * BM);
+              tma_load_2d_pair(smem_u32(sB + s * Cfg::B_BYTES), &tmB, bar0, kb * BK, c.n * BN + rank * (BN / 2));
+            } else {
+              tma_load_3d_pair(smem_u32(sA + s * Cfg::A_STAGE), &tmA, bar0, 0, c.m * BM, kb * KC);
+              tma_load_3d_pair(smem_u32(sB + s * Cfg::B_BYTES), &tmB, bar0, 0, c.n * BN + rank * (BN / 2), kb * KC);
+            }
           }
           issued |= 1u << s;
           last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -243,14 +259,17 @@ __global__ void __launch_bounds__(192, 1)
           const bool got = PAIR ? mbar_wait_cluster(full(s), ph, wc) : mbar_wait(p.cvt_b ? cvt(s) : full(s), ph, wc);
           if (!got) { ok = false; break; }
           tc_fence_after();
-          const uint64_t da = sdesc_sw128(smem_u32(sA + s * A_BYTES), 16, 1024);
-          const uint64_t db = sdesc_sw128(smem_u32(sB + s * Cfg::B_BYTES), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
+          for (int kk = 0; kk < KC * BK / 16; ++kk) {
+            // chunk kk / 4 of the stage, 16-wide step kk % 4 within it
+            const uint64_t da = sdesc_sw128(smem_u32(sA + s * Cfg::A_STAGE + (kk / 4) * A_BYTES), 16, 1024) +
+                                2 * (kk % 4);
+            const uint64_t db = sdesc_sw128(smem_u32(sB + s * Cfg::B_BYTES + (kk / 4) * Cfg::B_CHUNK), 16, 1024) +
+                                2 * (kk % 4);
             if constexpr (PAIR)
-              tc_mma_f16_pair(d, da + 2 * kk, db + 2 * kk, idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
+              tc_mma_f16_pair(d, da, db, idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
             else
-              tc_mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
+              tc_mma_f16(d, da, db, idesc, (kb > c.kb0 || kk > 0) ? 1u : 0u);
           }
           if constexpr (PAIR)
             tc_commit_pair(empty(s), 0x3);  // the stage is free in both CTAs
@@ -487,11 +506,11 @@ __global__ void __launch_bounds__(192, 1)
 // set up on every call).
 constexpr int kMaxDevices = 64;
 
-template <int BN, int EPI, bool PAIR>
+template <int BN, int EPI, bool PAIR, int KC>
 hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, uint32_t idesc, int grid,
                        cudaStream_t st) {
-  using Cfg = GemmCfg<BN, PAIR>;
-  auto kern = gemm_tc_kernel<BN, EPI, PAIR>;
+  using Cfg = GemmCfg<BN, PAIR, KC>;
+  auto kern = gemm_tc_kernel<BN, EPI, PAIR, KC>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return HYMBA_ERR_CUDA;
   const bool cached = dev < kMaxDevices;
@@ -538,15 +557,24 @@ hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmP
 }
 
 template <int EPI, bool PAIR = false>
-hymba_status launch_epi(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+hymba_status launch_epi(int bn, int kc, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                         uint32_t ab_fmt, int grid, cudaStream_t st) {
   const uint32_t id = idesc_f16(PAIR ? 2 * BM : BM, bn, ab_fmt, false, false);
+  if (kc == 2) {
+    switch (bn) {
+      case 64: return launch_bn<64, EPI, PAIR, 2>(ta, tb, p, id, grid, st);
+      case 128: return launch_bn<128, EPI, PAIR, 2>(ta, tb, p, id, grid, st);
+      case 144: return launch_bn<144, EPI, PAIR, 2>(ta, tb, p, id, grid, st);
+      case 160: return launch_bn<160, EPI, PAIR, 2>(ta, tb, p, id, grid, st);
+      default: return HYMBA_ERR_UNSUPPORTED;
+    }
+  }
   switch (bn) {
-    case 64: return launch_bn<64, EPI, PAIR>(ta, tb, p, id, grid, st);
-    case 128: return launch_bn<128, EPI, PAIR>(ta, tb, p, id, grid, st);
-    case 144: return launch_bn<144, EPI, PAIR>(ta, tb, p, id, grid, st);
-    case 160: return launch_bn<160, EPI, PAIR>(ta, tb, p, id, grid, st);
-    case 256: return launch_bn<256, EPI, PAIR>(ta, tb, p, id, grid, st);
+    case 64: return launch_bn<64, EPI, PAIR, 1>(ta, tb, p, id, grid, st);
+    case 128: return launch_bn<128, EPI, PAIR, 1>(ta, tb, p, id, grid, st);
+    case 144: return launch_bn<144, EPI, PAIR, 1>(ta, tb, p, id, grid, st);
+    case 160: return launch_bn<160, EPI, PAIR, 1>(ta, tb, p, id, grid, st);
+    case 256: return launch_bn<256, EPI, PAIR, 1>(ta, tb, p, id, grid, st);
     default: return HYMBA_ERR_UNSUPPORTED;
   }
 }
@@ -583,8 +611,20 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
     return HYMBA_ERR_INVALID;
   if (bn == 0) bn = gemm_pick_bn(p.N, p.M <= BM);
   const CUtensorMapDataType dt = ab_fmt == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  // two 64-column chunks of K per stage (one 3-D copy of each operand) when
+  // the MMAs of one chunk are shorter than two copies: BN <= 160; the chunks
+  // must not run past K, so K % 64 == 0
+  // (split partial sums that a separate pass reduces keep one chunk per stage:
+  // their callers count the splits over 64-wide chunks)
+  const int kc = (p.K % BK == 0 && bn <= 160 && epi != EPI_PARTIAL) ? 2 : 1;
+  const int n_chunks = (p.K + BK - 1) / BK;
   CUtensorMap ta, tb;
-  {
+  if (kc == 2) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(BK), static_cast<uint64_t>(p.M), static_cast<uint64_t>(n_chunks)};
+    const uint64_t str[2] = {static_cast<uint64_t>(lda) * 2, BK * 2};
+    const uint32_t box[3] = {BK, BM, 2};
+    if (!encode_tmap(&ta, dt, 3, A, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
+  } else {
     const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
     const uint64_t str[1] = {static_cast<uint64_t>(lda) * 2};
     const uint32_t box[2] = {BK, BM};
@@ -595,14 +635,23 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
   // several row blocks; not for split-K or converted-B launches
   const bool pair = splits <= 1 && !p.cvt_b && p.tiles_m >= 4 && num_sms >= 2 && bn <= kPairMaxBN;
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
-    const uint64_t str[1] = {static_cast<uint64_t>(ldb) * 2};
-    const uint32_t box[2] = {BK, static_cast<uint32_t>(pair ? bn / 2 : bn)};
     const CUtensorMapDataType dtb = p.cvt_b ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : dt;
-    if (!encode_tmap(&tb, dtb, 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
+    const uint32_t rows_b = static_cast<uint32_t>(pair ? bn / 2 : bn);
+    if (kc == 2) {
+      const uint64_t dims[3] = {static_cast<uint64_t>(BK), static_cast<uint64_t>(p.N),
+                                static_cast<uint64_t>(n_chunks)};
+      const uint64_t str[2] = {static_cast<uint64_t>(ldb) * 2, BK * 2};
+      const uint32_t box[3] = {BK, rows_b, 2};
+      if (!encode_tmap(&tb, dtb, 3, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
+    } else {
+      const uint64_t dims[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
+      const uint64_t str[1] = {static_cast<uint64_t>(ldb) * 2};
+      const uint32_t box[2] = {BK, rows_b};
+      if (!encode_tmap(&tb, dtb, 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return HYMBA_ERR_CUDA;
+    }
   }
   p.tiles_n = (p.N + bn - 1) / bn;
-  p.n_kb = (p.K + BK - 1) / BK;
+  p.n_kb = (n_chunks + kc - 1) / kc;  // pipeline stages of K (kc chunks each)
   splits = std::max(1, std::min(splits, p.n_kb));
   p.kb_per_split = (p.n_kb + splits - 1) / splits;
   p.splits = (p.n_kb + p.kb_per_split - 1) / p.kb_per_split;
@@ -614,22 +663,22 @@ hymba_status gemm_tc(int ab_fmt, const void* A, long long lda, const void* B, lo
   const uint32_t fmt = ab_fmt == 1 ? 1u : 0u;
   if (pair) {
     switch (epi) {
-      case EPI_F16: return launch_epi<EPI_F16, true>(bn, ta, tb, p, fmt, num_sms, st);
-      case EPI_XPROJ: return launch_epi<EPI_XPROJ, true>(bn, ta, tb, p, fmt, num_sms, st);
-      case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS, true>(bn, ta, tb, p, fmt, num_sms, st);
-      case EPI_F32: return launch_epi<EPI_F32, true>(bn, ta, tb, p, fmt, num_sms, st);
-      case EPI_GEGLU: return launch_epi<EPI_GEGLU, true>(bn, ta, tb, p, fmt, num_sms, st);
+      case EPI_F16: return launch_epi<EPI_F16, true>(bn, kc, ta, tb, p, fmt, num_sms, st);
+      case EPI_XPROJ: return launch_epi<EPI_XPROJ, true>(bn, kc, ta, tb, p, fmt, num_sms, st);
+      case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS, true>(bn, kc, ta, tb, p, fmt, num_sms, st);
+      case EPI_F32: return launch_epi<EPI_F32, true>(bn, kc, ta, tb, p, fmt, num_sms, st);
+      case EPI_GEGLU: return launch_epi<EPI_GEGLU, true>(bn, kc, ta, tb, p, fmt, num_sms, st);
       default: return HYMBA_ERR_INVALID;
     }
   }
   switch (epi) {
-    case EPI_F16: return launch_epi<EPI_F16>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_XPROJ: return launch_epi<EPI_XPROJ>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_F32: return launch_epi<EPI_F32>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_PARTIAL: return launch_epi<EPI_PARTIAL>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_ATOMIC: return launch_epi<EPI_ATOMIC>(bn, ta, tb, p, fmt, grid, st);
-    case EPI_GEGLU: return launch_epi<EPI_GEGLU>(bn, ta, tb, p, fmt, grid, st);
+    case EPI_F16: return launch_epi<EPI_F16>(bn, kc, ta, tb, p, fmt, grid, st);
+    case EPI_XPROJ: return launch_epi<EPI_XPROJ>(bn, kc, ta, tb, p, fmt, grid, st);
+    case EPI_SOFTPLUS: return launch_epi<EPI_SOFTPLUS>(bn, kc, ta, tb, p, fmt, grid, st);
+    case EPI_F32: return launch_epi<EPI_F32>(bn, kc, ta, tb, p, fmt, grid, st);
+    case EPI_PARTIAL: return launch_epi<EPI_PARTIAL>(bn, kc, ta, tb, p, fmt, grid, st);
+    case EPI_ATOMIC: return launch_epi<EPI_ATOMIC>(bn, kc, ta, tb, p, fmt, grid, st);
+    case EPI_GEGLU: return launch_epi<EPI_GEGLU>(bn, kc, ta, tb, p, fmt, grid, st);
     default: return HYMBA_ERR_INVALID;
   }
 }
