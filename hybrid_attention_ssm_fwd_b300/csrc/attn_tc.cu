@@ -442,7 +442,7 @@ hymba_status launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMa
   auto kern = attn_tc_kernel<DV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<DV>::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
-  if (launch_pdl(kern, dim3(grid), dim3(NTHREADS), AttnCfg<DV>::SMEM, st, q, k, v, km, vm, p) != cudaSuccess)
+  if (launch_kernel(false, kern, dim3(grid), dim3(NTHREADS), AttnCfg<DV>::SMEM, st, q, k, v, km, vm, p) != cudaSuccess)
     return HYMBA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }

@@ -176,7 +176,7 @@ hymba_status launch_conv(const CUtensorMap& m, __half* u, long long ld_u, int B,
   const long long n_rt = static_cast<long long>(B) * ((L + CV_TT - 1) / CV_TT);
   const int per_ct = static_cast<int>(std::max(1LL, std::min(n_rt, (4LL * num_sms + n_ct - 1) / n_ct)));
   const int grid = n_ct * per_ct;
-  if (launch_pdl(kern, dim3(grid), dim3(CV_THREADS), Cfg::SMEM, st, m, u, ld_u, B, L, di, w, bias, tail, status,
+  if (launch_kernel(false, kern, dim3(grid), dim3(CV_THREADS), Cfg::SMEM, st, m, u, ld_u, B, L, di, w, bias, tail, status,
                  wait_ns) != cudaSuccess)
     return HYMBA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;

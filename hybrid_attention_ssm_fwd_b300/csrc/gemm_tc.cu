@@ -522,7 +522,8 @@ hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmP
     if (cached) attr_done[dev].store(true, std::memory_order_release);
   }
   if constexpr (!PAIR) {
-    if (launch_pdl(kern, dim3(grid), dim3(192), Cfg::SMEM, st, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
+    if (launch_kernel(p.pdl != 0, kern, dim3(grid), dim3(192), Cfg::SMEM, st, ta, tb, p, idesc) != cudaSuccess)
+      return HYMBA_ERR_CUDA;
   } else {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -550,7 +551,7 @@ hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmP
     }
     const int clusters = std::max(1, std::min(std::min(grid / 2, max_clusters), p.total_pairs));
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.numAttrs = 2;
+    cfg.numAttrs = p.pdl ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p, idesc) != cudaSuccess) return HYMBA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;

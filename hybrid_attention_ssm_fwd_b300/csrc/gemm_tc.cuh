@@ -37,6 +37,7 @@ struct GemmParams {
   uint64_t wait_ns;
   int cvt_b;  // B is bf16 in memory: converted to fp16 in shared memory before the MMA (A fp16)
   int total_pairs;  // CTA-pair launch: 256-row tile pairs = ceil(tiles_m / 2) * tiles_n
+  int pdl;          // 1: programmatic dependent launch (the decode step's GEMMs)
 };
 
 // Launch C = A . B^T with the given epilogue.  ab_fmt: 0 fp16, 1 bf16.

@@ -290,8 +290,9 @@ hymba_status convert_weights(const Dims& x, const Plan& pl, const hymba_layer_we
 // (w_in_f16 set: a residual stack's later layers).
 hymba_status in_proj_bf16(const Dims& x, const void* X, const hymba_layer_weights* w, __half* proj, int rows,
                           const int32_t* pos, int pos_base, int rows_per_seq, int32_t* status, int sms,
-                          cudaStream_t st, const __half* w_in_f16 = nullptr) {
+                          cudaStream_t st, const __half* w_in_f16 = nullptr, bool pdl = false) {
   GemmParams p = gp(rows, x.P_in, x.d, status, x.wait_ns);
+  p.pdl = pdl;
   p.C = proj;
   p.ldc = x.P_in;
   const bool fused_rope = x.theta > 0 && x.dh == 64;
@@ -534,7 +535,7 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
     TRY(copy2d<__nv_bfloat16, __half>(static_cast<const __nv_bfloat16*>(w->W_dt), x.R, at<__half>(ws, pl.wdt),
                                       x.Rp, x.di, x.R, st));
   mk.mark();
-  TRY(in_proj_bf16(x, Xn, w, proj, B, c->pos, x.M, 1, status, sms, st));
+  TRY(in_proj_bf16(x, Xn, w, proj, B, c->pos, x.M, 1, status, sms, st, nullptr, true));
   mk.mark();
   // the new token's K/V into the ring and the conv step, one launch
   TRY(decode_prep(B, x.di, x.k, proj, x.P_in, x.x_col, x.k_col, x.v_col, x.Hkv, x.dh, x.dv, x.W, c->cap, c->pos,
@@ -567,6 +568,7 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   {
     const int ldp = (x.xo + 15) / 16 * 16;
     GemmParams p = gp(B, x.xo, x.di, status, x.wait_ns);
+    p.pdl = 1;
     p.C = part;
     p.ldc = ldp;
     p.cvt_b = 1;
@@ -590,6 +592,7 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
                         c->pos, st));  // also advances pos
   } else {
     GemmParams p = gp(B, x.di, x.R, status, x.wait_ns);
+    p.pdl = 1;
     p.C = delta;
     p.ldc = x.di;
     p.bias = w->dt_bias;
@@ -603,6 +606,7 @@ hymba_status decode_bf16(const Dims& x, const Plan& pl, const hymba_layer_weight
   mk.mark();
   {
     GemmParams p = gp(B, x.d, x.sw, status, x.wait_ns);
+    p.pdl = 1;
     p.cvt_b = 1;
     if (x.residual != 1) {
       // split-K partials added straight into Y, which holds the fp32 residual

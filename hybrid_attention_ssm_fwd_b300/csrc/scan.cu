@@ -481,7 +481,7 @@ hymba_status launch_scan(int B, int L, int di, const CUtensorMap& mX, const __ha
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
     return HYMBA_ERR_CUDA;
   dim3 grid(di / CH, B);
-  if (launch_pdl(kern, grid, dim3(Cfg::NT), Cfg::SMEM, st, mX, mU, mZ, mBC, args) != cudaSuccess)
+  if (launch_kernel(false, kern, grid, dim3(Cfg::NT), Cfg::SMEM, st, mX, mU, mZ, mBC, args) != cudaSuccess)
     return HYMBA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? HYMBA_OK : HYMBA_ERR_CUDA;
 }

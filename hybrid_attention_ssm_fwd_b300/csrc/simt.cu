@@ -723,7 +723,7 @@ hymba_status fuse_norm(int rows, int di, const T* att, const T* g, const float* 
   // one warp per row wants many rows (a decode step's 128 rows would fill
   // 32 SMs): below that, one block per row
   if (vec_ok && di <= 32 * 8 * FW_V && rows >= 4 * 148 * 4) {
-    if (launch_pdl(cc ? fuse_norm_warp_kernel<true> : fuse_norm_warp_kernel<false>, dim3((rows + 3) / 4),
+    if (launch_kernel(false, cc ? fuse_norm_warp_kernel<true> : fuse_norm_warp_kernel<false>, dim3((rows + 3) / 4),
                    dim3(128), 0, st, rows, di, reinterpret_cast<const __half*>(att),
                    reinterpret_cast<const __half*>(g), beta1, beta2, eps, reinterpret_cast<__half*>(s)) !=
         cudaSuccess)
