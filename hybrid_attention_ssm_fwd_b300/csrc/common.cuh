@@ -39,6 +39,15 @@ HY_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Round the dynamic shared-memory base up to ALIGN bytes by pointer
+// arithmetic on the __shared__ array itself: a round trip through an integer
+// would hide the address space, and every C++ access through the result
+// would then compile to a generic load or store instead of a shared-memory one.
+template <int ALIGN>
+HY_DEV uint8_t* align_smem(uint8_t* base) {
+  return base + ((ALIGN - (smem_u32(base) & (ALIGN - 1))) & (ALIGN - 1));
+}
+
 HY_DEV void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(DA_WARPS * 32, 1)
   constexpr int NVB = DV / 64;        // V boxes per chunk
   constexpr int NOT = DV / 8;         // O n-tiles
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem<1024>(smem_raw);
   __shared__ __align__(8) uint64_t bars[DA_WARPS][DA_STAGES];
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

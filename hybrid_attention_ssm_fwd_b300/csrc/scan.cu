@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* smem = align_smem<128>(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   // full[SC_S] | du_full[2] | du_empty[2] | y_full[2] | y_empty[2]
   auto full = [&](int s) { return smem_u32(&bars[s]); };
