@@ -68,14 +68,25 @@ struct ScanCfg {
   static constexpr int X_BYTES = KS > 0 ? SC_T * KP * 2 : SC_T * CH * 4;
   static constexpr int U_BYTES = SC_T * CH * 2;
   static constexpr int BC_BYTES = SC_T * 2 * SC_N * 4;
-  static constexpr int OFF_U = X_BYTES;
-  static constexpr int OFF_Z = OFF_U + U_BYTES;
+  // The u tile lands first in its stage.  With 128-byte rows it is loaded
+  // with the 128-byte swizzle (16-byte chunk c of row r stored at chunk
+  // c ^ (r % 8)), so that the delta warps' column reads, eight rows at a
+  // time, fall in different banks; that needs 1024-byte aligned stages.
+  static constexpr bool SWZ_U = CH * 2 == 128;
+  static constexpr int STAGE_ALIGN = SWZ_U ? 1024 : 128;
+  static constexpr int OFF_U = 0;
+  static constexpr int OFF_X = U_BYTES;
+  static constexpr int OFF_Z = OFF_X + X_BYTES;
   static constexpr int OFF_BC = OFF_Z + U_BYTES;
   static constexpr int TX_BYTES = OFF_BC + BC_BYTES;  // bytes landing per stage
-  static constexpr int STAGE = (TX_BYTES + 127) / 128 * 128;
-  static constexpr int DU_STR = CH + 4;               // float2 per row of a (d, d*u) tile
+  static constexpr int STAGE = (TX_BYTES + STAGE_ALIGN - 1) / STAGE_ALIGN * STAGE_ALIGN;
+  // row strides of the (d, d*u) and C.h tiles, padded so that the delta
+  // warps' stores (eight rows x four column pairs) and the scan warps' row
+  // stores (rows SC_H / TPC apart) hit distinct banks
+  static constexpr int DU_STR = CH + 8;               // float2 per row of a (d, d*u) tile
   static constexpr int DU_BYTES = SC_T * DU_STR * 8;
-  static constexpr int Y_BYTES = SC_T * CH * 4;       // C.h [SC_T][CH] fp32
+  static constexpr int Y_STR = CH + 4;                // floats per row of a C.h tile
+  static constexpr int Y_BYTES = SC_T * Y_STR * 4;    // C.h [SC_T][Y_STR] fp32
   // W_dt mma fragments: in registers when three blocks of NT threads leave
   // 128 registers a thread, otherwise in shared memory
   static constexpr bool W_REG = NT <= 160;
@@ -85,7 +96,7 @@ struct ScanCfg {
   static constexpr int OFF_W = OFF_Y + 2 * Y_BYTES;
   static constexpr int OFF_BAR = OFF_W + W_BYTES;
   static constexpr int N_BAR = SC_S + 8;
-  static constexpr int SMEM = 128 + OFF_BAR + N_BAR * 8;
+  static constexpr int SMEM = STAGE_ALIGN + OFF_BAR + N_BAR * 8;
   static_assert(NWS >= 1 && CHD % 8 == 0 && CH % 8 == 0 && SC_H % TPC == 0 && SC_T % SC_H == 0 && (CPT == 1 || CPT == 2) &&
                     CH % CHW == 0,
                 "scan block shape");
@@ -142,7 +153,7 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align_smem<128>(smem_raw);
+  uint8_t* smem = align_smem<Cfg::STAGE_ALIGN>(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   // full[SC_S] | du_full[2] | du_empty[2] | y_full[2] | y_empty[2]
   auto full = [&](int s) { return smem_u32(&bars[s]); };
@@ -178,6 +189,10 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
   auto stage = [&](int k) { return smem + (k % SC_S) * Cfg::STAGE; };
   auto du_tile = [&](int k) { return reinterpret_cast<float2*>(smem + Cfg::OFF_DU + (k & 1) * Cfg::DU_BYTES); };
   auto y_tile = [&](int k) { return reinterpret_cast<float*>(smem + Cfg::OFF_Y + (k & 1) * Cfg::Y_BYTES); };
+  // element index of u[row][col] in a stage's u tile
+  auto u_at = [](int row, int col) {
+    return Cfg::SWZ_U ? row * CH + ((((col >> 3) ^ (row & 7)) << 3) | (col & 7)) : row * CH + col;
+  };
 
   if (warp < Cfg::NWS) {
     // ------------------------------------------------------------ scan warps
@@ -273,9 +288,9 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
         for (int r = 0; r < Cfg::RPL; ++r) {
           const int row = hh * SC_H + sub * Cfg::RPL + r;
           if constexpr (CPT == 2)
-            *reinterpret_cast<float2*>(y_p + row * CH) = make_float2(yr[0][r], yr[1][r]);
+            *reinterpret_cast<float2*>(y_p + row * Cfg::Y_STR) = make_float2(yr[0][r], yr[1][r]);
           else
-            y_p[row * CH] = yr[0][r];
+            y_p[row * Cfg::Y_STR] = yr[0][r];
         }
       }
       mbar_arrive(du_empty(i));
@@ -343,7 +358,7 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
         for (int nt = 0; nt < NTD; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-        const uint32_t abase = smem_u32(st) + ((lane & 15) * Cfg::KP + (lane >> 4) * 8) * 2;
+        const uint32_t abase = smem_u32(st + Cfg::OFF_X) + ((lane & 15) * Cfg::KP + (lane >> 4) * 8) * 2;
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           uint32_t af[4];
@@ -360,7 +375,7 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int row = grp + hh * 8;
-            const float2 uv = __half22float2(*reinterpret_cast<const __half2*>(sU + row * CH + col));
+            const float2 uv = __half22float2(*reinterpret_cast<const __half2*>(sU + u_at(row, col)));
             float d0 = softplus_scan(acc[nt][2 * hh] + bias_c[nt][0]);
             float d1 = softplus_scan(acc[nt][2 * hh + 1] + bias_c[nt][1]);
             if (row >= nt_rows) d0 = d1 = 0.f;
@@ -368,11 +383,11 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
           }
         }
       } else {
-        const float* sDl = reinterpret_cast<const float*>(st);
+        const float* sDl = reinterpret_cast<const float*>(st + Cfg::OFF_X);
         for (int idx = lane; idx < SC_T * Cfg::CHD; idx += 32) {
           const int row = idx / Cfg::CHD, col = dc0 + idx % Cfg::CHD;
           const float d = row < nt_rows ? sDl[row * CH + col] : 0.f;
-          du[row * Cfg::DU_STR + col] = make_float2(d, d * __half2float(sU[row * CH + col]));
+          du[row * Cfg::DU_STR + col] = make_float2(d, d * __half2float(sU[u_at(row, col)]));
         }
       }
       mbar_arrive(du_full(i));
@@ -390,7 +405,7 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
       const uint32_t bar = full(k % SC_S);
       const int r = static_cast<int>(row0) + k * SC_T;
       mbar_arrive_expect_tx(bar, Cfg::TX_BYTES);
-      tma_load_2d(smem_u32(st), &tmX, bar, KS > 0 ? 0 : c0, r);
+      tma_load_2d(smem_u32(st + Cfg::OFF_X), &tmX, bar, KS > 0 ? 0 : c0, r);
       tma_load_2d(smem_u32(st + Cfg::OFF_U), &tmU, bar, c0, r);
       tma_load_2d(smem_u32(st + Cfg::OFF_Z), &tmZ, bar, c0, r);
       tma_load_2d(smem_u32(st + Cfg::OFF_BC), &tmBC, bar, 0, r);
@@ -410,10 +425,10 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
       for (int it = lane; it < ITEMS; it += 32) {
         const int row = it / GPR;
         if (row >= nt_rows) break;
-        const float4 ya = *reinterpret_cast<const float4*>(yt + row * CH + gq * 8);
-        const float4 yb = *reinterpret_cast<const float4*>(yt + row * CH + gq * 8 + 4);
+        const float4 ya = *reinterpret_cast<const float4*>(yt + row * Cfg::Y_STR + gq * 8);
+        const float4 yb = *reinterpret_cast<const float4*>(yt + row * Cfg::Y_STR + gq * 8 + 4);
         const float y[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
-        const uint4 uv = *reinterpret_cast<const uint4*>(sU + row * CH + gq * 8);
+        const uint4 uv = *reinterpret_cast<const uint4*>(sU + u_at(row, gq * 8));
         const uint4 zv = *reinterpret_cast<const uint4*>(sZ + row * CH + gq * 8);
         const __half2* uh = reinterpret_cast<const __half2*>(&uv);
         const __half2* zh = reinterpret_cast<const __half2*>(&zv);
@@ -460,11 +475,11 @@ __global__ void wait_probe_kernel(uint64_t limit_ns, int32_t* status) {
 }
 
 bool map2(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, long long cols, long long rows,
-          long long ld, int box_c, int box_r) {
+          long long ld, int box_c, int box_r, bool swizzle128 = false) {
   const uint64_t dims[2] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows)};
   const uint64_t str[1] = {static_cast<uint64_t>(ld) * esize};
   const uint32_t box[2] = {static_cast<uint32_t>(box_c), static_cast<uint32_t>(box_r)};
-  return encode_tmap(m, dt, 2, base, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+  return encode_tmap(m, dt, 2, base, dims, str, box, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <int KS, int TPC, int CH, int CPT>
@@ -473,7 +488,7 @@ hymba_status launch_scan(int B, int L, int di, const CUtensorMap& mX, const __ha
   using Cfg = ScanCfg<KS, TPC, CH, CPT>;
   const long long rows = static_cast<long long>(B) * L;
   CUtensorMap mU, mZ, mBC;
-  if (!map2(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, u, di, rows, ld_u, CH, SC_T) ||
+  if (!map2(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, u, di, rows, ld_u, CH, SC_T, Cfg::SWZ_U) ||
       !map2(&mZ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, z, di, rows, ld_z, CH, SC_T) ||
       !map2(&mBC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, BC, 2 * SC_N, rows, 2 * SC_N, 2 * SC_N, SC_T))
     return HYMBA_ERR_CUDA;
