@@ -506,9 +506,9 @@ hymba_status launch_scan(int B, int L, int di, const CUtensorMap& mX, const __ha
 // sequence; fewer chains per thread mean more warps to hide the latency of
 // each step, while two channels per thread halve the shared-memory reads of
 // B_t / C_t.  Measured on B300 at d_inner 3200, L 8320 (scan alone):
-//   ~43 channels/SM:  (4,1) 0.57 ms, (4,2) 0.69, (2,1) 0.70, (2,2) 0.91
-//   ~86 channels/SM:  (4,2) 1.03 ms, (2,1) 1.12, (4,1) 1.13, (2,2) 1.31
-//   ~173 channels/SM: (2,2) 1.45 ms, (4,2) 1.49, (1,1) 1.51, (2,1) 1.64
+//   ~43 channels/SM:  (4,1) 0.49 ms, (2,1) 0.59, (4,2) 0.62, (1,1) 0.69, (2,2) 0.72
+//   ~86 channels/SM:  (2,1) 0.89 ms, (4,2) 0.92, (4,1) 1.05, (1,1) 1.12, (2,2) 1.14
+//   ~173 channels/SM: (2,2) 1.28 ms, (1,1) 1.28, (2,1) 1.30, (4,2) 1.33, (4,1) 1.80
 struct ScanLayout {
   int tpc, cpt;
 };
@@ -516,7 +516,7 @@ struct ScanLayout {
 ScanLayout pick_layout(int B, int di, int num_sms) {
   const long long per_sm = static_cast<long long>(B) * di / num_sms;
   if (per_sm >= 128) return {2, 2};
-  if (per_sm >= 64) return {4, 2};
+  if (per_sm >= 64) return {2, 1};
   return {4, 1};
 }
 
