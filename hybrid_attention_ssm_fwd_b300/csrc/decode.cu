@@ -328,8 +328,9 @@ __global__ void decode_attn_combine_kernel(int Hq, int dv, int nsplit, const flo
 //   delta = softplus(dt[b] . W_dt[c] + bias[c]),  h = exp(delta A) h + delta u B[b],
 //   y = C[b] . h + D u,  g = y silu(z);  the state is updated in place.
 // A block owns DS_CH channels x DS_SEQ sequences:
-//   0. every thread issues its loads of the state rows first (their HBM
-//      latency overlaps the rest), then dt (fp16) and W_dt (bf16 -> fp16,
+//   0. every thread issues its loads of the state rows first, before waiting
+//      for the preceding kernel (their HBM latency overlaps the rest and that
+//      kernel's tail), then dt (fp16) and W_dt (bf16 -> fp16,
 //      the same rounding as the prefill's weight conversion) are staged in
 //      shared memory with 8-byte vector loads, zero-padded to 16 columns;
 //   1. warps 0-3 compute delta for the block (16 sequences x 32 channels) on
@@ -373,6 +374,18 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
   const int c0 = blockIdx.x * DS_CH, b0 = blockIdx.y * DS_SEQ;
   const int tid = threadIdx.x;
   const int KP = (R + 15) / 16 * 16;  // padded dt rank
+  // ---- 0. state loads (phase-2 thread: quarter q of the rows j = tid/4 + 64 i)
+  constexpr int NJ = DS_SEQ * DS_CH / (DS_THREADS / 4);
+  const int q = tid & 3;
+  float4 hv[NJ];
+#pragma unroll
+  for (int i = 0; i < NJ; ++i) {
+    const int j = (tid >> 2) + i * (DS_THREADS / 4);
+    const int b = b0 + j / DS_CH, c = c0 + j % DS_CH;
+    hv[i] = (b < B && c < di)
+                ? reinterpret_cast<const float4*>(state + (static_cast<long long>(b) * di + c) * N)[q]
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   // W_dt rows: 8 threads per row, 4 values per 8-byte load; every load of a
   // thread is issued before the first is used (one round trip, not four)
   {
@@ -416,21 +429,11 @@ __global__ void __launch_bounds__(DS_THREADS, 3)
     sbias[tid] = c0 + tid < di ? dt_bias[c0 + tid] : 0.f;
     sD[tid] = c0 + tid < di ? D[c0 + tid] : 0.f;
   }
-  // everything above reads weights only; the rest reads what earlier kernels wrote
+  // everything above reads weights and the state only (no kernel of the
+  // step before this one writes the state, and all but the immediately
+  // preceding kernel have completed); the rest reads what they wrote
   pdl_wait();
   pdl_trigger();
-  // ---- 0. state loads (phase-2 thread: quarter q of the rows j = tid/4 + 64 i)
-  constexpr int NJ = DS_SEQ * DS_CH / (DS_THREADS / 4);
-  const int q = tid & 3;
-  float4 hv[NJ];
-#pragma unroll
-  for (int i = 0; i < NJ; ++i) {
-    const int j = (tid >> 2) + i * (DS_THREADS / 4);
-    const int b = b0 + j / DS_CH, c = c0 + j % DS_CH;
-    hv[i] = (b < B && c < di)
-                ? reinterpret_cast<const float4*>(state + (static_cast<long long>(b) * di + c) * N)[q]
-                : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   // dt rows: 16 threads per row, all loads issued first (the padding columns
   // past R are zeroed, never read); dt rounds to fp16 as in prefill
   {
