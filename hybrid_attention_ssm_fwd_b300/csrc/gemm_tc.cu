@@ -402,15 +402,43 @@ __global__ void __launch_bounds__(192, 1)
             store_f16x32(reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col, v,
                          valid);
           } else if (EPI == EPI_XPROJ) {
+            // groups of 8 columns: a whole dt group is one 16-byte fp16
+            // store, a whole [B | C] group two 16-byte fp32 stores; the group
+            // that straddles R and the ragged end go element by element
+            __half* drow = reinterpret_cast<__half*>(p.C2) + static_cast<long long>(row) * p.ldc2;
+            float* brow = reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc;  // column R
+            const bool vec_d = ((reinterpret_cast<uintptr_t>(p.C2) | static_cast<uintptr_t>(p.ldc2 * 2)) & 15) == 0;
+            const bool vec_b = ((reinterpret_cast<uintptr_t>(p.C) | static_cast<uintptr_t>(p.ldc * 4)) & 15) == 0 &&
+                               (p.xproj_R & 3) == 0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int cj = col + j;
-              if (j < valid) {
-                if (cj < p.xproj_R) {
-                  over |= !(fabsf(v[j]) <= kHalfMax);
-                  reinterpret_cast<__half*>(p.C2)[static_cast<long long>(row) * p.ldc2 + cj] = __float2half_rn(v[j]);
-                } else {
-                  reinterpret_cast<float*>(p.C)[static_cast<long long>(row) * p.ldc + (cj - p.xproj_R)] = v[j];
+            for (int g8 = 0; g8 < 4; ++g8) {
+              const int j0 = 8 * g8, c = col + j0;
+              if (j0 >= valid) break;
+              if (vec_d && c + 8 <= p.xproj_R) {
+                uint4 o;
+                o.x = pack_half2(v[j0], v[j0 + 1]);
+                o.y = pack_half2(v[j0 + 2], v[j0 + 3]);
+                o.z = pack_half2(v[j0 + 4], v[j0 + 5]);
+                o.w = pack_half2(v[j0 + 6], v[j0 + 7]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) over |= !(fabsf(v[j0 + e]) <= kHalfMax);
+                *reinterpret_cast<uint4*>(drow + c) = o;
+              } else if (vec_b && c >= p.xproj_R && j0 + 8 <= valid) {
+                float* bp = brow + (c - p.xproj_R);
+                *reinterpret_cast<float4*>(bp) = make_float4(v[j0], v[j0 + 1], v[j0 + 2], v[j0 + 3]);
+                *reinterpret_cast<float4*>(bp + 4) = make_float4(v[j0 + 4], v[j0 + 5], v[j0 + 6], v[j0 + 7]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int j = j0 + e, cj = c + e;
+                  if (j < valid) {
+                    if (cj < p.xproj_R) {
+                      over |= !(fabsf(v[j]) <= kHalfMax);
+                      drow[cj] = __float2half_rn(v[j]);
+                    } else {
+                      brow[cj - p.xproj_R] = v[j];
+                    }
+                  }
                 }
               }
             }
