@@ -38,7 +38,7 @@ from hybrid_attention_ssm_fwd_b300 import synth  # noqa: E402
 
 METRIC = "hybrid-head layer prefill tokens/s @8K bf16; decode tok/s; % of roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-E2E_CHUNK = 2
+E2E_CHUNK = 1
 STAGES = ["convert", "in_proj", "kv_export", "attention", "conv", "x_proj", "dt_proj", "scan", "fuse_norm",
           "out_proj", "cache"]
 
