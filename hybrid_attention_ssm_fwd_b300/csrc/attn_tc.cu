@@ -324,19 +324,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int c = 0; c < BKV / 32; ++c) tmem_ld32(lane_base + s_col + c * 32, sr[c]);
         tc_wait_ld();
-        // mask (raw scores; the positive scale is applied inside the exp2 below)
+        // mask (raw scores; the positive scale is applied inside the exp2 below).
+        // Decided for this warp's 32 rows: the causal bound (and the sequence
+        // end) cuts the tile unless every key precedes the warp's first row;
+        // the window cuts it unless the warp's last row still sees the
+        // tile's first non-meta key.  Most cut tiles are cut by one bound
+        // only, and take a one-comparison loop.
         const int k0 = tile_kt(U, t) * BKV;
-        const bool full_vis = (k0 + BKV - 1 <= U.q0) && (k0 + BKV <= p.L) &&
-                              (p.window == 0 || k0 + BKV <= p.M || (U.qv1 - 1) - max(k0, p.M) < p.window);
-        if (!full_vis) {
+        const int w_lo = U.q0 + q * 32, w_hi = min(w_lo + 31, p.L - 1);
+        const bool causal_ok = (k0 + BKV - 1 <= w_lo) && (k0 + BKV <= p.L);
+        const bool window_ok = p.window == 0 || k0 + BKV <= p.M || w_hi - max(k0, p.M) < p.window;
+        if (!(causal_ok && window_ok)) {
           // key e of this tile (j = k0 + e) is visible iff e <= hi and (e >= lo or e < ml)
           const int hi = min(i, p.L - 1) - k0;
           const int lo = p.window > 0 ? i - p.window + 1 - k0 : -BKV;
           const int ml = p.M - k0;
+          if (window_ok) {
 #pragma unroll
-          for (int e = 0; e < BKV; ++e) {
-            const bool vis = (e <= hi) && (e >= lo || e < ml);
-            sr[e >> 5][e & 31] = vis ? sr[e >> 5][e & 31] : 0xff800000u;  // -inf
+            for (int e = 0; e < BKV; ++e) sr[e >> 5][e & 31] = e <= hi ? sr[e >> 5][e & 31] : 0xff800000u;  // -inf
+          } else if (causal_ok && ml <= 0) {
+#pragma unroll
+            for (int e = 0; e < BKV; ++e) sr[e >> 5][e & 31] = e >= lo ? sr[e >> 5][e & 31] : 0xff800000u;
+          } else {
+#pragma unroll
+            for (int e = 0; e < BKV; ++e) {
+              const bool vis = (e <= hi) && (e >= lo || e < ml);
+              sr[e >> 5][e & 31] = vis ? sr[e >> 5][e & 31] : 0xff800000u;
+            }
           }
         }
         auto sv = [&](int e) { return __uint_as_float(sr[e >> 5][e & 31]); };
