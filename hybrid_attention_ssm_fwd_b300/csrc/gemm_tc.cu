@@ -109,6 +109,21 @@ HY_DEV void store_f16x32(__half* dst, const float (&v)[32], int valid) {
   }
 }
 
+// 16 fp32 values as fp16, the first `valid` (a multiple of 8) of them
+HY_DEV void store_f16x16(__half* dst, const float (&v)[16], int valid) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    if (g * 8 < valid) {
+      uint4 q;
+      q.x = pack_half2(v[g * 8 + 0], v[g * 8 + 1]);
+      q.y = pack_half2(v[g * 8 + 2], v[g * 8 + 3]);
+      q.z = pack_half2(v[g * 8 + 4], v[g * 8 + 5]);
+      q.w = pack_half2(v[g * 8 + 6], v[g * 8 + 7]);
+      *reinterpret_cast<uint4*>(dst + g * 8) = q;
+    }
+  }
+}
+
 // 32 fp32 values; `valid` leading columns are inside N.  Compile-time
 // indices only, so v stays in registers.
 HY_DEV void store_f32x32(float* dst, const float (&v)[32], int valid) {
@@ -342,36 +357,45 @@ __global__ void __launch_bounds__(192, 1)
       bool over = false;
 
       if (EPI == EPI_F16 && p.rope_cols > 0 && col_tile < p.rope_cols) {
-        // RoPE: 64-column heads, pair (i, i+32) rotated by pos * inv_freq[i]
+        // RoPE: 64-column heads, pair (i, i+32) rotated by pos * inv_freq[i].
+        // The angles depend on the row and i only, so each (sin, cos) is made
+        // once per row and tile, 16 frequencies at a time, and applied to
+        // every head of the tile.
         const int posn = p.pos_base + (p.pos ? p.pos[min(row, p.M - 1)] : (row % p.rows_per_seq));
-        for (int c0 = 0; c0 < BN; c0 += 64) {
-          const int col = col_tile + c0;
-          if (col >= p.N) break;
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tbase + c0, r0);
-          tmem_ld32(tbase + c0 + 32, r1);
-          tc_wait_ld();
-          float v0[32], v1[32];
+#pragma unroll 1
+        for (int jg = 0; jg < 2; ++jg) {
+          float sn[16], cs[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v0[j] = __uint_as_float(r0[j]);
-            v1[j] = __uint_as_float(r1[j]);
-          }
-          if (col < p.rope_cols) {
+          for (int j = 0; j < 16; ++j) sincosf(static_cast<float>(posn) * rope_tab[jg * 16 + j], &sn[j], &cs[j]);
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 64) {
+            const int col = col_tile + c0;
+            if (col >= p.N) break;
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tbase + c0 + jg * 16, r0);
+            tmem_ld16(tbase + c0 + 32 + jg * 16, r1);
+            tc_wait_ld();
+            float v0[16], v1[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              float sn, cs;
-              sincosf(static_cast<float>(posn) * rope_tab[j], &sn, &cs);
-              const float x1 = v0[j], x2 = v1[j];
-              v0[j] = x1 * cs - x2 * sn;
-              v1[j] = x2 * cs + x1 * sn;
+            for (int j = 0; j < 16; ++j) {
+              v0[j] = __uint_as_float(r0[j]);
+              v1[j] = __uint_as_float(r1[j]);
             }
-          }
-          over |= any_over_half(v0) | any_over_half(v1);
-          if (row_ok) {
-            __half* dst = reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col;
-            store_f16x32(dst, v0, p.N - col);
-            if (col + 32 < p.N) store_f16x32(dst + 32, v1, p.N - col - 32);
+            if (col < p.rope_cols) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float x1 = v0[j], x2 = v1[j];
+                v0[j] = x1 * cs[j] - x2 * sn[j];
+                v1[j] = x2 * cs[j] + x1 * sn[j];
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) over |= !(fabsf(v0[j]) <= kHalfMax) | !(fabsf(v1[j]) <= kHalfMax);
+            if (row_ok) {
+              __half* dst = reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col + jg * 16;
+              store_f16x16(dst, v0, p.N - col - jg * 16);
+              store_f16x16(dst + 32, v1, p.N - col - 32 - jg * 16);
+            }
           }
         }
       } else {
