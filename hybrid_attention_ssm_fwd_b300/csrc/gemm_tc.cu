@@ -635,13 +635,15 @@ hymba_status launch_epi(int bn, int kc, const CUtensorMap& ta, const CUtensorMap
 }  // namespace
 
 // Tile width: least padded N, each width weighted by its measured cost per
-// column relative to 256-wide tiles (narrower tiles issue more MMAs and
-// epilogues per FLOP: in_proj at 256 reached 0.80 of peak, out_proj at 160
-// 0.70), so a wide tile wins unless it pads N by more than a few percent.
+// column relative to 256-wide tiles (narrower tiles read more of A from L2
+// per FLOP and issue more MMAs and epilogues: in_proj at 256 reaches 0.93 of
+// the bf16 peak; out_proj, N = 1600, ran 0.474 ms at 160 against 0.465 ms at
+// 256 with 12% of the columns padding), so a wide tile wins unless it pads N
+// by more than about 15%.
 int gemm_pick_bn(int N, bool small_m) {
   if (small_m) return 64;
   static const int cand[] = {256, 160, 144, 128, 64};
-  static const int cost[] = {100, 108, 110, 112, 125};
+  static const int cost[] = {100, 118, 120, 122, 135};
   int best = 256;
   long long best_cost = 1LL << 60;
   for (int i = 0; i < 5; ++i) {
