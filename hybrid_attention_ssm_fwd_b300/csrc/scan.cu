@@ -140,8 +140,15 @@ HY_DEV float softplus_scan(float v) {
   return fmaxf(v, 0.f) + e * q;
 }
 
+// (y0 + D0 u0, y1 + D1 u1) gated by (z0, z1) on packed float pairs:
 // y * silu(z) = y * z / (1 + 2^(-z log2 e))
-HY_DEV float gate1(float y, float z) { return y * z * rcp_approx(1.0f + ex2_approx(-kLog2e * z)); }
+HY_DEV uint32_t gate2(uint64_t y, uint64_t Dp, uint64_t u, uint64_t z) {
+  const uint64_t yv = fma2(Dp, u, y);
+  const float2 t = up2(mul2(z, pk2(-kLog2e, -kLog2e)));
+  const float2 dd = up2(add2(pk2(ex2_approx(t.x), ex2_approx(t.y)), pk2(1.0f, 1.0f)));
+  const float2 o = up2(mul2(mul2(yv, z), pk2(rcp_approx(dd.x), rcp_approx(dd.y))));
+  return pack_half2(o.x, o.y);
+}
 
 template <int KS, int TPC, int CH, int CPT>
 __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
@@ -397,9 +404,9 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
     constexpr int GPR = CH / 8;             // 8-channel groups per row
     constexpr int ITEMS = SC_T * GPR;       // (row, group) items per chunk
     const int gq = lane % GPR;
-    float Dg[8];
+    uint64_t Dg[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) Dg[e] = a.D[c0 + gq * 8 + e];
+    for (int e = 0; e < 4; ++e) Dg[e] = pk2(a.D[c0 + gq * 8 + 2 * e], a.D[c0 + gq * 8 + 2 * e + 1]);
     auto issue = [&](int k) {
       uint8_t* st = stage(k);
       const uint32_t bar = full(k % SC_S);
@@ -427,7 +434,7 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
         if (row >= nt_rows) break;
         const float4 ya = *reinterpret_cast<const float4*>(yt + row * Cfg::Y_STR + gq * 8);
         const float4 yb = *reinterpret_cast<const float4*>(yt + row * Cfg::Y_STR + gq * 8 + 4);
-        const float y[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
+        const uint64_t y[4] = {pk2(ya.x, ya.y), pk2(ya.z, ya.w), pk2(yb.x, yb.y), pk2(yb.z, yb.w)};
         const uint4 uv = *reinterpret_cast<const uint4*>(sU + u_at(row, gq * 8));
         const uint4 zv = *reinterpret_cast<const uint4*>(sZ + row * CH + gq * 8);
         const __half2* uh = reinterpret_cast<const __half2*>(&uv);
@@ -436,8 +443,7 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 uf = __half22float2(uh[e]), zf = __half22float2(zh[e]);
-          o[e] = pack_half2(gate1(fmaf(Dg[2 * e], uf.x, y[2 * e]), zf.x),
-                            gate1(fmaf(Dg[2 * e + 1], uf.y, y[2 * e + 1]), zf.y));
+          o[e] = gate2(y[e], Dg[e], pk2(uf.x, uf.y), pk2(zf.x, zf.y));
         }
         *reinterpret_cast<uint4*>(a.g + (row0 + k * SC_T + row) * di + c0 + gq * 8) =
             make_uint4(o[0], o[1], o[2], o[3]);
