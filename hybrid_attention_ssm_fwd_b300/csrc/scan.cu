@@ -61,7 +61,6 @@ struct ScanCfg {
   static constexpr int W_GATE = NWS + ND;
   static constexpr int CHW = 32 * CPT / TPC;          // channels per scan warp
   static constexpr int NS = SC_N / TPC;               // states per scan thread
-  static constexpr int RPL = SC_H / TPC;              // rows of y a scan thread stores per SC_H rows
   static constexpr int CHD = CH / ND;                 // channels per delta warp
   static constexpr int NTD = CHD / 8;                 // mma n-tiles per delta warp
   static constexpr int KP = KS * 16;                  // padded dt rank
@@ -85,8 +84,15 @@ struct ScanCfg {
   // stores (rows SC_H / TPC apart) hit distinct banks
   static constexpr int DU_STR = CH + 8;               // float2 per row of a (d, d*u) tile
   static constexpr int DU_BYTES = SC_T * DU_STR * 8;
-  static constexpr int Y_STR = CH + 4;                // floats per row of a C.h tile
-  static constexpr int Y_BYTES = SC_T * Y_STR * 4;    // C.h [SC_T][Y_STR] fp32
+  // C.h leaves the scan warps either as TPC partials per row, added by the
+  // gate warp (two threads and two channels per thread), or summed across
+  // the TPC threads by shuffles (the other layouts, where the gate warp's
+  // share of the work is larger); measured both ways
+  static constexpr bool PARTIALS = TPC == 2 && CPT == 2;
+  static constexpr int NP = PARTIALS ? TPC : 1;        // partials stored per row
+  static constexpr int RPL = SC_H / TPC;              // rows a thread stores per SC_H rows (shuffled sums)
+  static constexpr int Y_STR = CH + 4;                // floats per (row, partial) of a C.h tile
+  static constexpr int Y_BYTES = SC_T * NP * Y_STR * 4;  // C.h [SC_T][NP][Y_STR] fp32
   // W_dt mma fragments: in registers when three blocks of NT threads leave
   // 128 registers a thread, otherwise in shared memory
   static constexpr bool W_REG = NT <= 160;
@@ -225,9 +231,10 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
       const float2* du_p = du_tile(k) + chl;
       const float* sBC = reinterpret_cast<const float*>(stage(k) + Cfg::OFF_BC);
       float* y_p = y_tile(k) + chl;
-      // C.h of SC_H rows stays in registers, then a transposing butterfly sums
-      // the TPC partials: no store inside the row loop, so the loads of later
-      // rows can be issued early
+      // C.h of SC_H rows stays in registers and is stored after them (no
+      // store inside the row loop, so the loads of later rows can be issued
+      // early): one partial per thread, or the TPC partials summed by a
+      // transposing butterfly of shuffles
 #pragma unroll
       for (int hh = 0; hh < SC_T / SC_H; ++hh) {
         float yr[CPT][SC_H];
@@ -277,27 +284,34 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
             yr[j][tr] = ys.x + ys.y;
           }
         }
-        // lane `sub` ends with the totals of rows sub*RPL .. sub*RPL + RPL - 1
-        // of these SC_H rows
+        if constexpr (Cfg::PARTIALS) {
 #pragma unroll
-        for (int o = TPC / 2, m = SC_H; o >= 1; o >>= 1, m >>= 1) {
-          const bool upper = (sub & o) != 0;
+          for (int r = 0; r < SC_H; ++r)
+            *reinterpret_cast<float2*>(y_p + ((hh * SC_H + r) * TPC + sub) * Cfg::Y_STR) =
+                make_float2(yr[0][r], yr[1][r]);
+        } else {
+          // lane `sub` ends with the totals of rows sub*RPL .. sub*RPL + RPL - 1
+          // of these SC_H rows
 #pragma unroll
-          for (int j = 0; j < CPT; ++j)
+          for (int o = TPC / 2, m = SC_H; o >= 1; o >>= 1, m >>= 1) {
+            const bool upper = (sub & o) != 0;
 #pragma unroll
-            for (int r = 0; r < m / 2; ++r) {
-              const float keep = upper ? yr[j][m / 2 + r] : yr[j][r];
-              const float send = upper ? yr[j][r] : yr[j][m / 2 + r];
-              yr[j][r] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-            }
-        }
+            for (int j = 0; j < CPT; ++j)
 #pragma unroll
-        for (int r = 0; r < Cfg::RPL; ++r) {
-          const int row = hh * SC_H + sub * Cfg::RPL + r;
-          if constexpr (CPT == 2)
-            *reinterpret_cast<float2*>(y_p + row * Cfg::Y_STR) = make_float2(yr[0][r], yr[1][r]);
-          else
-            y_p[row * Cfg::Y_STR] = yr[0][r];
+              for (int r = 0; r < m / 2; ++r) {
+                const float keep = upper ? yr[j][m / 2 + r] : yr[j][r];
+                const float send = upper ? yr[j][r] : yr[j][m / 2 + r];
+                yr[j][r] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+              }
+          }
+#pragma unroll
+          for (int r = 0; r < Cfg::RPL; ++r) {
+            const int row = hh * SC_H + sub * Cfg::RPL + r;
+            if constexpr (CPT == 2)
+              *reinterpret_cast<float2*>(y_p + row * Cfg::Y_STR) = make_float2(yr[0][r], yr[1][r]);
+            else
+              y_p[row * Cfg::Y_STR] = yr[0][r];
+          }
         }
       }
       mbar_arrive(du_empty(i));
@@ -432,8 +446,15 @@ __global__ void __launch_bounds__(ScanCfg<KS, TPC, CH, CPT>::NT, 3)
       for (int it = lane; it < ITEMS; it += 32) {
         const int row = it / GPR;
         if (row >= nt_rows) break;
-        const float4 ya = *reinterpret_cast<const float4*>(yt + row * Cfg::Y_STR + gq * 8);
-        const float4 yb = *reinterpret_cast<const float4*>(yt + row * Cfg::Y_STR + gq * 8 + 4);
+        const float* yrow = yt + row * Cfg::NP * Cfg::Y_STR + gq * 8;
+        float4 ya = *reinterpret_cast<const float4*>(yrow);
+        float4 yb = *reinterpret_cast<const float4*>(yrow + 4);
+        if constexpr (Cfg::PARTIALS) {  // C.h = partial 0 + partial 1
+          const float4 pa = *reinterpret_cast<const float4*>(yrow + Cfg::Y_STR);
+          const float4 pb = *reinterpret_cast<const float4*>(yrow + Cfg::Y_STR + 4);
+          ya = make_float4(ya.x + pa.x, ya.y + pa.y, ya.z + pa.z, ya.w + pa.w);
+          yb = make_float4(yb.x + pb.x, yb.y + pb.y, yb.z + pb.z, yb.w + pb.w);
+        }
         const uint64_t y[4] = {pk2(ya.x, ya.y), pk2(ya.z, ya.w), pk2(yb.x, yb.y), pk2(yb.z, yb.w)};
         const uint4 uv = *reinterpret_cast<const uint4*>(sU + u_at(row, gq * 8));
         const uint4 zv = *reinterpret_cast<const uint4*>(sZ + row * CH + gq * 8);
