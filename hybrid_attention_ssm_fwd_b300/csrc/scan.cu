@@ -24,8 +24,10 @@
 //   scan warps        the recurrence, fully unrolled over the chunk.  TPC
 //                     threads share one channel, each holding 16/TPC of its
 //                     states in registers for the whole sequence; their
-//                     partial C.h are summed with shuffles and stored per row;
-//   gate warp (1)     y = C.h + D*u, g = y*silu(z), eight channels of one row
+//                     partial C.h are stored per row (two threads and two
+//                     channels per thread) or first summed with shuffles;
+//   gate warp (1)     y = C.h + D*u (adding the stored partials), g =
+//                     y*silu(z) on packed float pairs, eight channels of one row
 //                     per lane and one 16-byte store to global memory; its
 //                     lane 0 also issues the TMA loads of the chunk's dt (or
 //                     delta), u, z and [B|C] tiles into an SC_S-stage ring,
