@@ -201,6 +201,25 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (PAIR) cluster_sync();  // the peer's barriers exist before any remote arrive
   tc_fence_after();
+  // In a programmatic launch (the decode step's GEMMs) the B operand is a
+  // weight no kernel of the step writes: the producer issues B of the first
+  // tile's first stages before waiting for the preceding kernel, so that
+  // the weight stream starts during that kernel's tail; A follows the wait.
+  int pre_b = 0;
+  if constexpr (!PAIR) {
+    if (p.pdl && warp == 0 && lane == 0 && t_first < t_count) {
+      const TileCoord c = coord(t_first);
+      pre_b = min(S, c.kb1 - c.kb0);
+      for (int j = 0; j < pre_b; ++j) {
+        const int kb = c.kb0 + j;
+        mbar_arrive_expect_tx(full(j), Cfg::STAGE);
+        if constexpr (KC == 1)
+          tma_load_2d(smem_u32(sB + j * Cfg::B_BYTES), &tmB, full(j), kb * BK, c.n * BN);
+        else
+          tma_load_3d(smem_u32(sB + j * Cfg::B_BYTES), &tmB, full(j), 0, c.n * BN, kb * KC);
+      }
+    }
+  }
   pdl_wait();  // only the setup above may overlap the preceding kernel
   pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
@@ -219,6 +238,16 @@ __global__ void __launch_bounds__(192, 1)
         for (int kb = c.kb0; kb < c.kb1; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
+          if (static_cast<int>(it) < pre_b) {
+            // B of this stage is on its way (issued before the wait): A only
+            if constexpr (KC == 1)
+              tma_load_2d(smem_u32(sA + s * Cfg::A_STAGE), &tmA, full(s), kb * BK, c.m * BM);
+            else
+              tma_load_3d(smem_u32(sA + s * Cfg::A_STAGE), &tmA, full(s), 0, c.m * BM, kb * KC);
+            issued |= 1u << s;
+            last_par = (last_par & ~(1u << s)) | (ph << s);
+            continue;
+          }
           if (!mbar_wait(empty(s), ph ^ 1, wc)) { ok = false; break; }
           if (!PAIR || leader) {
             // a pair's even CTA expects both CTAs' bytes on its own barrier

@@ -339,10 +339,26 @@ __global__ void __launch_bounds__(256) fuse_norm_vec_kernel(int di, const __half
                                                             const float* __restrict__ beta1,
                                                             const float* __restrict__ beta2, float eps,
                                                             __half* __restrict__ s) {
-  pdl_wait();
-  pdl_trigger();
   const long long row = blockIdx.x;
   const int nch = di / 8;
+  // the weights do not depend on the preceding kernel: load them before
+  // waiting for it
+  float4 b1v[FN_MAXC][2], b2v[FN_MAXC][2];
+  if (!CONCAT) {
+#pragma unroll
+    for (int q = 0; q < FN_MAXC; ++q) {
+      const int ch = threadIdx.x + q * 256;
+      if (ch < nch) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          b1v[q][h] = *reinterpret_cast<const float4*>(beta1 + ch * 8 + 4 * h);
+          b2v[q][h] = *reinterpret_cast<const float4*>(beta2 + ch * 8 + 4 * h);
+        }
+      }
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
   const uint4* a4 = reinterpret_cast<const uint4*>(att + row * di);
   const uint4* g4 = reinterpret_cast<const uint4*>(g + row * di);
   uint4 av[FN_MAXC], gv[FN_MAXC];
@@ -390,10 +406,7 @@ __global__ void __launch_bounds__(256) fuse_norm_vec_kernel(int di, const __half
     } else if (!CONCAT && ch < nch) {
       const __half2* ah = reinterpret_cast<const __half2*>(&av[q]);
       const __half2* gh = reinterpret_cast<const __half2*>(&gv[q]);
-      const float4 b1a = *reinterpret_cast<const float4*>(beta1 + ch * 8);
-      const float4 b1b = *reinterpret_cast<const float4*>(beta1 + ch * 8 + 4);
-      const float4 b2a = *reinterpret_cast<const float4*>(beta2 + ch * 8);
-      const float4 b2b = *reinterpret_cast<const float4*>(beta2 + ch * 8 + 4);
+      const float4 b1a = b1v[q][0], b1b = b1v[q][1], b2a = b2v[q][0], b2b = b2v[q][1];
       const float bb1[8] = {b1a.x, b1a.y, b1a.z, b1a.w, b1b.x, b1b.y, b1b.z, b1b.w};
       const float bb2[8] = {b2a.x, b2a.y, b2a.z, b2a.w, b2b.x, b2b.y, b2b.z, b2b.w};
       uint32_t o[4];
