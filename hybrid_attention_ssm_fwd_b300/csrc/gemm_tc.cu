@@ -50,19 +50,81 @@ constexpr int A_BYTES = BM * BK * 2;
 // load ([chunk][row][64]) brings both chunks of A and one both of B, halving
 // the copies a stage needs (one issuing thread sustains about one tensor copy
 // per 170-220 ns, longer than the MMAs of a 64-wide k-step at BN <= 160).
-template <int BN, bool PAIR = false, int KC = 1>
+// STG: bytes of the epilogue warps' store-staging tiles (see store_rows_*).
+template <int BN, bool PAIR = false, int KC = 1, int STG = 0>
 struct GemmCfg {
   static constexpr int B_CHUNK = (PAIR ? BN / 2 : BN) * BK * 2;  // this CTA's B rows, one chunk
   static constexpr int A_STAGE = KC * A_BYTES;
   static constexpr int B_BYTES = KC * B_CHUNK;                    // this CTA's B rows, one stage
   static constexpr int STAGE = A_STAGE + B_BYTES;
-  static constexpr int BUDGET = 220 * 1024 - 2048;
+  static constexpr int BUDGET = 220 * 1024 - 2048 - STG;
   static constexpr int S0 = BUDGET / STAGE;
   static constexpr int STAGES = S0 > 8 ? 8 : S0;
   static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                         : (2 * BN <= 256) ? 256 : 512;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + 512;
+  static constexpr int OFF_STG = STAGES * STAGE + 512;
+  static constexpr int SMEM = 1024 + OFF_STG + STG;
 };
+
+// Row-per-thread results stored through a per-warp shared-memory tile: each
+// lane writes its row's 32 values, then the warp stores whole 64- or 128-byte
+// row pieces, several rows per instruction, instead of 32 rows' 16-byte
+// pieces per instruction.  Row strides padded by 16 bytes against bank
+// conflicts.
+constexpr int STG_F16_STR = 32 * 2 + 16, STG_F32_STR = 32 * 4 + 16;
+template <int EPI>
+constexpr int epi_stg_bytes() {
+  return EPI == 0 ? 4 * 32 * STG_F16_STR : EPI == 3 ? 4 * 32 * STG_F32_STR : 0;  // EPI_F16, EPI_F32
+}
+
+// fp16 [32 rows][32 columns]: lane l holds row row0 + l; `valid` (a multiple
+// of 8) leading columns are inside N; rows at or past M are not stored
+HY_DEV void store_rows_f16(uint8_t* stg, __half* C, long long ldc, int row0, int M, int col, int valid,
+                           const float (&v)[32], int lane) {
+  uint8_t* my = stg + lane * STG_F16_STR;
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    *reinterpret_cast<uint4*>(my + 16 * g) =
+        make_uint4(pack_half2(v[8 * g], v[8 * g + 1]), pack_half2(v[8 * g + 2], v[8 * g + 3]),
+                   pack_half2(v[8 * g + 4], v[8 * g + 5]), pack_half2(v[8 * g + 6], v[8 * g + 7]));
+  __syncwarp();
+  const int ch = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = (lane >> 2) + 8 * i;
+    const uint4 q = *reinterpret_cast<const uint4*>(stg + r * STG_F16_STR + 16 * ch);
+    if (row0 + r < M && 8 * ch < valid)
+      *reinterpret_cast<uint4*>(C + static_cast<long long>(row0 + r) * ldc + col + 8 * ch) = q;
+  }
+  __syncwarp();
+}
+
+// fp32 [32 rows][32 columns], as store_rows_f16 (any `valid`; C and ldc on
+// 16-byte boundaries)
+HY_DEV void store_rows_f32(uint8_t* stg, float* C, long long ldc, int row0, int M, int col, int valid,
+                           const float (&v)[32], int lane) {
+  uint8_t* my = stg + lane * STG_F32_STR;
+#pragma unroll
+  for (int g = 0; g < 8; ++g)
+    *reinterpret_cast<float4*>(my + 16 * g) = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+  __syncwarp();
+  const int ch = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = (lane >> 3) + 4 * i;
+    const float4 q = *reinterpret_cast<const float4*>(stg + r * STG_F32_STR + 16 * ch);
+    float* dst = C + static_cast<long long>(row0 + r) * ldc + col + 4 * ch;
+    if (row0 + r < M) {
+      if (4 * ch + 4 <= valid) {
+        *reinterpret_cast<float4*>(dst) = q;
+      } else if (4 * ch < valid) {
+        const float e4[4] = {q.x, q.y, q.z, q.w};
+        for (int e = 0; e < valid - 4 * ch; ++e) dst[e] = e4[e];
+      }
+    }
+  }
+  __syncwarp();
+}
 
 struct TileCoord {
   int m, n, kb0, kb1, split;
@@ -149,7 +211,7 @@ template <int BN, int EPI, bool PAIR, int KC>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p, const uint32_t idesc) {
-  using Cfg = GemmCfg<BN, PAIR, KC>;
+  using Cfg = GemmCfg<BN, PAIR, KC, epi_stg_bytes<EPI>()>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem<1024>(smem_raw);
@@ -449,11 +511,20 @@ __global__ void __launch_bounds__(192, 1)
             for (int j = 16; j < 32; ++j) v[j] = 0.f;
           }
           const int valid = min(nv, p.N - col);
+          if (EPI == EPI_F16) {  // all lanes: the store goes through the warp's staging tile
+            if (row_ok) over |= any_over_half(v);
+            store_rows_f16(smem + Cfg::OFF_STG + q * 32 * STG_F16_STR, reinterpret_cast<__half*>(p.C), p.ldc,
+                           c.m * BM + q * 32, p.M, col, valid, v, lane);
+            continue;
+          }
+          if (EPI == EPI_F32 && !p.resid && !p.resid_f32 && !p.C2 &&
+              ((reinterpret_cast<uintptr_t>(p.C) | static_cast<uintptr_t>(p.ldc * 4)) & 15) == 0) {
+            store_rows_f32(smem + Cfg::OFF_STG + q * 32 * STG_F32_STR, reinterpret_cast<float*>(p.C), p.ldc,
+                           c.m * BM + q * 32, p.M, col, valid, v, lane);
+            continue;
+          }
           if (!row_ok) continue;
           if (EPI == EPI_F16) {
-            over |= any_over_half(v);
-            store_f16x32(reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col, v,
-                         valid);
           } else if (EPI == EPI_XPROJ) {
             // groups of 8 columns: a whole dt group is one 16-byte fp16
             // store, a whole [B | C] group two 16-byte fp32 stores; the group
@@ -590,7 +661,7 @@ constexpr int kMaxDevices = 64;
 template <int BN, int EPI, bool PAIR, int KC>
 hymba_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, uint32_t idesc, int grid,
                        cudaStream_t st) {
-  using Cfg = GemmCfg<BN, PAIR, KC>;
+  using Cfg = GemmCfg<BN, PAIR, KC, epi_stg_bytes<EPI>()>;
   auto kern = gemm_tc_kernel<BN, EPI, PAIR, KC>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return HYMBA_ERR_CUDA;
