@@ -99,6 +99,27 @@ HY_DEV void store_rows_f16(uint8_t* stg, __half* C, long long ldc, int row0, int
   __syncwarp();
 }
 
+// fp16 [32 rows][16 columns], as store_rows_f16 (`valid` a multiple of 8)
+HY_DEV void store_rows_f16x16(uint8_t* stg, __half* C, long long ldc, int row0, int M, int col, int valid,
+                              const float (&v)[16], int lane) {
+  uint8_t* my = stg + lane * STG_F16_STR;
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+    *reinterpret_cast<uint4*>(my + 16 * g) =
+        make_uint4(pack_half2(v[8 * g], v[8 * g + 1]), pack_half2(v[8 * g + 2], v[8 * g + 3]),
+                   pack_half2(v[8 * g + 4], v[8 * g + 5]), pack_half2(v[8 * g + 6], v[8 * g + 7]));
+  __syncwarp();
+  const int ch = lane & 1;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = (lane >> 1) + 16 * i;
+    const uint4 q = *reinterpret_cast<const uint4*>(stg + r * STG_F16_STR + 16 * ch);
+    if (row0 + r < M && 8 * ch < valid)
+      *reinterpret_cast<uint4*>(C + static_cast<long long>(row0 + r) * ldc + col + 8 * ch) = q;
+  }
+  __syncwarp();
+}
+
 // fp32 [32 rows][32 columns], as store_rows_f16 (any `valid`; C and ldc on
 // 16-byte boundaries)
 HY_DEV void store_rows_f32(uint8_t* stg, float* C, long long ldc, int row0, int M, int col, int valid,
@@ -160,21 +181,6 @@ HY_DEV void store_f16x32(__half* dst, const float (&v)[32], int valid) {
   // valid = number of leading columns inside N (multiple of 8 or >= 32)
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    if (g * 8 < valid) {
-      uint4 q;
-      q.x = pack_half2(v[g * 8 + 0], v[g * 8 + 1]);
-      q.y = pack_half2(v[g * 8 + 2], v[g * 8 + 3]);
-      q.z = pack_half2(v[g * 8 + 4], v[g * 8 + 5]);
-      q.w = pack_half2(v[g * 8 + 6], v[g * 8 + 7]);
-      *reinterpret_cast<uint4*>(dst + g * 8) = q;
-    }
-  }
-}
-
-// 16 fp32 values as fp16, the first `valid` (a multiple of 8) of them
-HY_DEV void store_f16x16(__half* dst, const float (&v)[16], int valid) {
-#pragma unroll
-  for (int g = 0; g < 2; ++g) {
     if (g * 8 < valid) {
       uint4 q;
       q.x = pack_half2(v[g * 8 + 0], v[g * 8 + 1]);
@@ -482,11 +488,12 @@ __global__ void __launch_bounds__(192, 1)
             }
 #pragma unroll
             for (int j = 0; j < 16; ++j) over |= !(fabsf(v0[j]) <= kHalfMax) | !(fabsf(v1[j]) <= kHalfMax);
-            if (row_ok) {
-              __half* dst = reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col + jg * 16;
-              store_f16x16(dst, v0, p.N - col - jg * 16);
-              store_f16x16(dst + 32, v1, p.N - col - 32 - jg * 16);
-            }
+            // all lanes: the stores go through the warp's staging tile
+            uint8_t* stg = smem + Cfg::OFF_STG + q * 32 * STG_F16_STR;
+            __half* out = reinterpret_cast<__half*>(p.C);
+            store_rows_f16x16(stg, out, p.ldc, c.m * BM + q * 32, p.M, col + jg * 16, p.N - col - jg * 16, v0, lane);
+            store_rows_f16x16(stg, out, p.ldc, c.m * BM + q * 32, p.M, col + 32 + jg * 16, p.N - col - 32 - jg * 16,
+                              v1, lane);
           }
         }
       } else {
