@@ -74,7 +74,7 @@ struct GemmCfg {
 constexpr int STG_F16_STR = 32 * 2 + 16, STG_F32_STR = 32 * 4 + 16;
 template <int EPI>
 constexpr int epi_stg_bytes() {
-  return EPI == 0 ? 4 * 32 * STG_F16_STR : EPI == 3 ? 4 * 32 * STG_F32_STR : 0;  // EPI_F16, EPI_F32
+  return EPI == 0 || EPI == 6 ? 4 * 32 * STG_F16_STR : EPI == 3 ? 4 * 32 * STG_F32_STR : 0;  // EPI_F16, EPI_GEGLU, EPI_F32
 }
 
 // fp16 [32 rows][32 columns]: lane l holds row row0 + l; `valid` (a multiple
@@ -120,31 +120,71 @@ HY_DEV void store_rows_f16x16(uint8_t* stg, __half* C, long long ldc, int row0, 
   __syncwarp();
 }
 
-// fp32 [32 rows][32 columns], as store_rows_f16 (any `valid`; C and ldc on
-// 16-byte boundaries)
-HY_DEV void store_rows_f32(uint8_t* stg, float* C, long long ldc, int row0, int M, int col, int valid,
-                           const float (&v)[32], int lane) {
+// fp32 [32 rows][32 columns], as store_rows_f16 (any `valid`), plus at most
+// one residual (bf16 rb or fp32 rf, may alias C) read and an optional fp16
+// copy C2 written in the same row pieces.  All eight residual pieces of a
+// lane are loaded before its first store (a residual aliasing C would
+// otherwise order each load behind the previous store).  C, ldc and rf on
+// 16-byte boundaries, rb and C2 on 8-byte ones.  Returns whether a value of
+// the fp16 copy is out of fp16 range.
+HY_DEV bool store_rows_f32(uint8_t* stg, float* C, long long ldc, int row0, int M, int col, int valid,
+                           const float (&v)[32], int lane, const __nv_bfloat16* rb, const float* rf, long long ldr,
+                           __half* C2, long long ldc2) {
   uint8_t* my = stg + lane * STG_F32_STR;
 #pragma unroll
   for (int g = 0; g < 8; ++g)
     *reinterpret_cast<float4*>(my + 16 * g) = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
   __syncwarp();
   const int ch = lane & 7;
+  const int c = col + 4 * ch;
+  const bool full = 4 * ch + 4 <= valid;  // this lane's piece lies inside N
+  float4 a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const long long row = row0 + (lane >> 3) + 4 * i;
+    a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < M && full) {
+      if (rf) {
+        a[i] = *reinterpret_cast<const float4*>(rf + row * ldr + c);
+      } else if (rb) {
+        const uint2 w = *reinterpret_cast<const uint2*>(rb + row * ldr + c);
+        const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+        const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+        a[i] = make_float4(a0.x, a0.y, a1.x, a1.y);
+      }
+    }
+  }
+  bool over = false;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = (lane >> 3) + 4 * i;
-    const float4 q = *reinterpret_cast<const float4*>(stg + r * STG_F32_STR + 16 * ch);
-    float* dst = C + static_cast<long long>(row0 + r) * ldc + col + 4 * ch;
-    if (row0 + r < M) {
-      if (4 * ch + 4 <= valid) {
-        *reinterpret_cast<float4*>(dst) = q;
-      } else if (4 * ch < valid) {
-        const float e4[4] = {q.x, q.y, q.z, q.w};
-        for (int e = 0; e < valid - 4 * ch; ++e) dst[e] = e4[e];
+    const long long row = row0 + r;
+    if (row >= M || 4 * ch >= valid) continue;
+    float4 q = *reinterpret_cast<const float4*>(stg + r * STG_F32_STR + 16 * ch);
+    if (full) {
+      q = make_float4(q.x + a[i].x, q.y + a[i].y, q.z + a[i].z, q.w + a[i].w);
+      *reinterpret_cast<float4*>(C + row * ldc + c) = q;
+      if (C2) {
+        over |= !(fabsf(q.x) <= kHalfMax) | !(fabsf(q.y) <= kHalfMax) | !(fabsf(q.z) <= kHalfMax) |
+                !(fabsf(q.w) <= kHalfMax);
+        *reinterpret_cast<uint2*>(C2 + row * ldc2 + c) = make_uint2(pack_half2(q.x, q.y), pack_half2(q.z, q.w));
+      }
+    } else {
+      const float e4[4] = {q.x, q.y, q.z, q.w};
+      for (int e = 0; e < valid - 4 * ch; ++e) {
+        float t = e4[e];
+        if (rf) t += rf[row * ldr + c + e];
+        else if (rb) t += __bfloat162float(rb[row * ldr + c + e]);
+        C[row * ldc + c + e] = t;
+        if (C2) {
+          over |= !(fabsf(t) <= kHalfMax);
+          C2[row * ldc2 + c + e] = __float2half_rn(t);
+        }
       }
     }
   }
   __syncwarp();
+  return over;
 }
 
 struct TileCoord {
@@ -410,6 +450,15 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
     const int ct = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+    // fp32 results, residual and fp16 copy in whole row pieces when every
+    // pointer and leading dimension allows the vector accesses
+    const bool f32_staged =
+        EPI == EPI_F32 && ((reinterpret_cast<uintptr_t>(p.C) | static_cast<uintptr_t>(p.ldc * 4)) & 15) == 0 &&
+        ((reinterpret_cast<uintptr_t>(p.resid_f32) | static_cast<uintptr_t>(p.resid_f32 ? p.ld_resid * 4 : 0)) & 15) ==
+            0 &&
+        ((reinterpret_cast<uintptr_t>(p.resid) | static_cast<uintptr_t>(p.resid ? p.ld_resid * 2 : 0)) & 7) == 0 &&
+        ((reinterpret_cast<uintptr_t>(p.C2) | static_cast<uintptr_t>(p.C2 ? p.ldc2 * 2 : 0)) & 7) == 0 &&
+        !(p.resid && p.resid_f32);
     int local = 0;
     uint32_t cit = 0;  // k-block counter of the conversion (follows the producer's)
     bool cok = true;
@@ -524,10 +573,24 @@ __global__ void __launch_bounds__(192, 1)
                            c.m * BM + q * 32, p.M, col, valid, v, lane);
             continue;
           }
-          if (EPI == EPI_F32 && !p.resid && !p.resid_f32 && !p.C2 &&
-              ((reinterpret_cast<uintptr_t>(p.C) | static_cast<uintptr_t>(p.ldc * 4)) & 15) == 0) {
-            store_rows_f32(smem + Cfg::OFF_STG + q * 32 * STG_F32_STR, reinterpret_cast<float*>(p.C), p.ldc,
-                           c.m * BM + q * 32, p.M, col, valid, v, lane);
+          if (EPI == EPI_F32 && f32_staged) {
+            over |= store_rows_f32(smem + Cfg::OFF_STG + q * 32 * STG_F32_STR, reinterpret_cast<float*>(p.C), p.ldc,
+                                   c.m * BM + q * 32, p.M, col, valid, v, lane, p.resid, p.resid_f32, p.ld_resid,
+                                   reinterpret_cast<__half*>(p.C2), p.ldc2);
+            continue;
+          }
+          if (EPI == EPI_GEGLU) {
+            // exact GeLU, x Phi(x) with Phi from erff; 16 outputs per 32
+            // columns, stored through the staging tile
+            float o[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float gt = v[2 * e], up = v[2 * e + 1];
+              o[e] = 0.5f * gt * (1.0f + erff(gt * 0.7071067811865476f)) * up;
+              if (row_ok) over |= !(fabsf(o[e]) <= kHalfMax);
+            }
+            store_rows_f16x16(smem + Cfg::OFF_STG + q * 32 * STG_F16_STR, reinterpret_cast<__half*>(p.C), p.ldc,
+                              c.m * BM + q * 32, p.M, col / 2, valid / 2, o, lane);
             continue;
           }
           if (!row_ok) continue;
@@ -594,27 +657,6 @@ __global__ void __launch_bounds__(192, 1)
             if (p.C2) {  // the updated stream rounded to fp16: the next layer's input
               over |= any_over_half(v);
               store_f16x32(reinterpret_cast<__half*>(p.C2) + static_cast<long long>(row) * p.ldc2 + col, v, valid);
-            }
-          } else if (EPI == EPI_GEGLU) {
-            // exact GeLU, x Phi(x) with Phi from erff; 16 outputs per 32 columns
-            float o[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float gt = v[2 * e], up = v[2 * e + 1];
-              o[e] = 0.5f * gt * (1.0f + erff(gt * 0.7071067811865476f)) * up;
-              over |= !(fabsf(o[e]) <= kHalfMax);
-            }
-            __half* dst = reinterpret_cast<__half*>(p.C) + static_cast<long long>(row) * p.ldc + col / 2;
-#pragma unroll
-            for (int gg = 0; gg < 2; ++gg) {
-              if (gg * 8 < valid / 2) {
-                uint4 q;
-                q.x = pack_half2(o[gg * 8 + 0], o[gg * 8 + 1]);
-                q.y = pack_half2(o[gg * 8 + 2], o[gg * 8 + 3]);
-                q.z = pack_half2(o[gg * 8 + 4], o[gg * 8 + 5]);
-                q.w = pack_half2(o[gg * 8 + 6], o[gg * 8 + 7]);
-                *reinterpret_cast<uint4*>(dst + gg * 8) = q;
-              }
             }
           } else if (EPI == EPI_ATOMIC) {
             float* dst = reinterpret_cast<float*>(p.C) + static_cast<long long>(row) * p.ldc + col;
