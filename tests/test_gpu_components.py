@@ -50,6 +50,33 @@ def test_gemm_tc_matches_fp64(M, N, K, ab):
     assert err <= 1e-5 * max(1.0, ref_c.abs().max().item()) * math.sqrt(K / 64), err
 
 
+@pytest.mark.parametrize("M,N,K,ldc", [(300, 37, 64, 40), (1047, 45, 200, 48), (520, 203, 96, 208),
+                                       (129, 3, 64, 4), (2100, 61, 72, 64)])
+def test_gemm_tc_ragged_columns_in_padded_rows(M, N, K, ldc):
+    """fp32 results whose last 32-column piece holds a number of columns that
+    is not a multiple of four, in rows padded to a 16-byte stride: the staged
+    store writes whole 4-column pieces and the tail element by element, and
+    never the padding (left NaN)."""
+    g = torch.Generator().manual_seed(M + 31 * N + K)
+    A = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    B = (0.05 * torch.randn(N, K, generator=g)).to(torch.bfloat16)
+    Cp = torch.full((M, ldc), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Kp = (K + 7) // 8 * 8
+    Ad = torch.zeros(M, Kp, dtype=torch.bfloat16, device="cuda")
+    Bd = torch.zeros(N, Kp, dtype=torch.bfloat16, device="cuda")
+    Ad[:, :K] = A.cuda()
+    Bd[:, :K] = B.cuda()
+    assert hb.hymba_test_gemm(Ad[:, :K], Bd[:, :K], Cp[:, :N], 1, status=st) == 0
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    got = Cp.cpu().double()
+    ref_c = A.double() @ B.double().T
+    err = (got[:, :N] - ref_c).abs().max().item()
+    assert err <= 1e-5 * max(1.0, ref_c.abs().max().item()) * math.sqrt(K / 64), err
+    assert torch.isnan(got[:, N:]).all()
+
+
 def _scan_inputs(B, L, di, N, seed, u0=None, d0=None, b0=None, c0=None):
     rng = np.random.default_rng(seed)
     u = rng.standard_normal((B, L, di)) if u0 is None else np.full((B, L, di), u0)
